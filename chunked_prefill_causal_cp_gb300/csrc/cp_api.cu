@@ -1,0 +1,314 @@
+// cp_api.cu -- the C ABI: argument checks, tensor-map setup and the launches
+// behind cp_kv_append, cp_prefill_chunk_attn, cp_mixed_step and
+// cp_workspace_size.  Every argument is checked before anything is enqueued.
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "cp_internal.h"
+
+using namespace cp;
+
+namespace {
+
+int esize_of(int dtype) { return dtype == CP_F32 ? 4 : 2; }
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int check_desc(const cp_layer_desc* d, bool need_batch) {
+  if (d == nullptr) return CP_ERR_INVALID_ARG;
+  if (d->dtype != CP_F32 && d->dtype != CP_BF16 && d->dtype != CP_F16) return CP_ERR_INVALID_ARG;
+  if (need_batch && d->batch <= 0) return CP_ERR_INVALID_ARG;
+  if (d->num_q_heads <= 0 || d->num_kv_heads <= 0) return CP_ERR_INVALID_ARG;
+  if (d->num_q_heads % d->num_kv_heads != 0) return CP_ERR_INVALID_ARG;
+  if (d->head_dim != 64 && d->head_dim != 128) return CP_ERR_UNSUPPORTED;
+  if (!(d->scale >= 0.f) || std::isinf(d->scale)) return CP_ERR_INVALID_ARG;
+  switch (d->kind) {
+    case CP_CACHE_CONTIG:
+    case CP_CACHE_ROLLING:
+      if (d->capacity <= 0) return CP_ERR_INVALID_ARG;
+      break;
+    case CP_CACHE_PAGED:
+      if (d->page_size != 16 && d->page_size != 32 && d->page_size != 64 && d->page_size != 128)
+        return CP_ERR_UNSUPPORTED;
+      if (d->num_pages <= 0 || d->max_blocks <= 0) return CP_ERR_INVALID_ARG;
+      break;
+    default:
+      return CP_ERR_INVALID_ARG;
+  }
+  return CP_OK;
+}
+
+// Upper bound of positions a sequence may reach in this layout.
+int64_t layout_limit(const cp_layer_desc* d) {
+  if (d->kind == CP_CACHE_CONTIG) return d->capacity;
+  if (d->kind == CP_CACHE_PAGED) return (int64_t)d->max_blocks * d->page_size;
+  return INT32_MAX;  // rolling: positions grow without bound, slots wrap
+}
+
+CacheView make_cache(const cp_layer_desc* d, const int32_t* block_table) {
+  CacheView c;
+  c.kind = d->kind;
+  c.capacity = d->capacity;
+  c.page_size = d->page_size;
+  c.num_pages = d->num_pages;
+  c.max_blocks = d->max_blocks;
+  c.block_table = block_table;
+  return c;
+}
+
+float scale_log2(const cp_layer_desc* d) {
+  const double sc = d->scale > 0.f ? (double)d->scale : 1.0 / std::sqrt((double)d->head_dim);
+  return (float)(sc * 1.4426950408889634);  // log2(e)
+}
+
+int64_t max_splits_for(int32_t max_ctx) { return ((int64_t)max_ctx + kDecodeSplit - 1) / kDecodeSplit; }
+
+int64_t decode_ws_bytes(const cp_layer_desc* d, int32_t max_ctx, int32_t num_seqs) {
+  const int64_t ms = max_splits_for(max_ctx);
+  return (int64_t)num_seqs * d->num_q_heads * ms * (d->head_dim + 2) * (int64_t)sizeof(float);
+}
+
+// ---- tensor maps (driver entry point fetched through the runtime)
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// 3-D tensor of 16-bit elements: dims {d0 (contiguous), d1, d2}, 128-byte
+// swizzled boxes; out-of-range box elements read as zero.
+bool encode_3d(CUtensorMap* m, int dtype, const void* base, uint64_t d0, uint64_t d1, uint64_t d2,
+               uint32_t b0, uint32_t b1, uint32_t b2) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[3] = {d0, d1, d2};
+  const cuuint64_t strides[2] = {d0 * 2, d0 * d1 * 2};
+  const cuuint32_t box[3] = {b0, b1, b2};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  const CUtensorMapDataType ty =
+      dtype == CP_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  return fn(m, ty, 3, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Tensor maps of the tensor-core path: Q/out rows [rows_total, Hq, D] in
+// boxes of (64 dims, G heads, 128/G tokens); K/V in boxes of 128 keys
+// (contiguous / rolling) or one page (paged) by 64 dims.
+bool make_tc_maps(const cp_layer_desc* d, const void* q, int64_t rows_total, const void* k, const void* v,
+                  int batch, CUtensorMap* tq, CUtensorMap* tk, CUtensorMap* tv) {
+  const int G = d->num_q_heads / d->num_kv_heads;
+  const uint64_t D = d->head_dim;
+  if (!encode_3d(tq, d->dtype, q, D, d->num_q_heads, (uint64_t)rows_total, 64, G, kTcBlockM / G)) return false;
+  if (d->kind == CP_CACHE_PAGED) {
+    const uint64_t planes = (uint64_t)d->num_pages * d->num_kv_heads;
+    return encode_3d(tk, d->dtype, k, D, d->page_size, planes, 64, d->page_size, 1) &&
+           encode_3d(tv, d->dtype, v, D, d->page_size, planes, 64, d->page_size, 1);
+  }
+  const uint64_t planes = (uint64_t)batch * d->num_kv_heads;
+  return encode_3d(tk, d->dtype, k, D, d->capacity, planes, 64, kTcBlockN, 1) &&
+         encode_3d(tv, d->dtype, v, D, d->capacity, planes, 64, kTcBlockN, 1);
+}
+
+int launch_result(cudaError_t e) { return e == cudaSuccess ? CP_OK : CP_ERR_CUDA; }
+
+// Attention over every sequence of `rows`, routed by dtype and row count.
+int run_attention(const cp_layer_desc* d, const AttnArgs& base, int64_t rows_total, int rows_max_per_seq,
+                  const void* k, const void* v, int batch_for_maps, void* workspace, size_t ws_bytes,
+                  cudaStream_t st) {
+  const int G = d->num_q_heads / d->num_kv_heads;
+  AttnArgs a = base;
+  if (d->dtype == CP_F32) {
+    a.min_rows = 1;
+    return launch_result(launch_attn_f32(a, rows_max_per_seq, st));
+  }
+  const bool decode_ok = decode_supported(d->head_dim, G, d->dtype) && d->kind != CP_CACHE_ROLLING;
+  if (!attn_tc_supported(d->head_dim, G, d->dtype)) return CP_ERR_UNSUPPORTED;
+  const bool any_multi = rows_max_per_seq > 1;
+  const bool any_single = base.rows.rows_uniform == 0 || base.rows.rows_uniform == 1;
+  if (decode_ok && any_single) {
+    const int64_t need = decode_ws_bytes(d, a.max_ctx, a.rows.num_seqs);
+    if (workspace == nullptr || (int64_t)ws_bytes < need) return CP_ERR_WORKSPACE;
+    AttnArgs dec = a;
+    dec.part_o = static_cast<float*>(workspace);
+    dec.max_splits = (int)max_splits_for(a.max_ctx);
+    dec.part_ml = dec.part_o + (int64_t)a.rows.num_seqs * d->num_q_heads * dec.max_splits * d->head_dim;
+    const int r = launch_result(launch_decode(dec, d->dtype, st));
+    if (r != CP_OK) return r;
+  }
+  if (any_multi || !decode_ok) {
+    a.min_rows = decode_ok ? 2 : 1;
+    CUtensorMap tq, tk, tv;
+    if (!make_tc_maps(d, a.q, rows_total, k, v, batch_for_maps, &tq, &tk, &tv)) return CP_ERR_CUDA;
+    const int rpt = kTcBlockM / G;
+    int64_t tiles;
+    if (a.rows.rows_uniform > 0)
+      tiles = (int64_t)a.rows.num_seqs * ((a.rows.rows_uniform + rpt - 1) / rpt);
+    else
+      tiles = (rows_total + rpt - 1) / rpt + a.rows.num_seqs;
+    if (tiles > INT32_MAX) return CP_ERR_UNSUPPORTED;
+    return launch_result(launch_attn_tc(a, d->dtype, tq, tk, tv, (int)tiles, st));
+  }
+  return CP_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t cp_workspace_size(const cp_layer_desc* desc, int32_t max_rows, int32_t max_ctx, int32_t num_seqs) {
+  if (check_desc(desc, false) != CP_OK || max_rows < 0 || max_ctx < 0 || num_seqs < 0) return 0;
+  (void)max_rows;
+  return (size_t)decode_ws_bytes(desc, max_ctx, num_seqs);
+}
+
+int cp_kv_append(const cp_layer_desc* desc, const void* k_new, const void* v_new, int32_t rows, void* k_cache,
+                 void* v_cache, const int32_t* seqlens_k, const int32_t* block_table, int32_t max_past,
+                 int32_t* dev_status, void* stream) {
+  int r = check_desc(desc, true);
+  if (r != CP_OK) return r;
+  if (rows < 0 || max_past < 0) return CP_ERR_INVALID_ARG;
+  if (rows == 0) return CP_OK;
+  if (!k_new || !v_new || !k_cache || !v_cache || !seqlens_k) return CP_ERR_INVALID_ARG;
+  if (desc->kind == CP_CACHE_PAGED && !block_table) return CP_ERR_INVALID_ARG;
+  if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(k_cache) || !aligned16(v_cache))
+    return CP_ERR_INVALID_ARG;
+  if (desc->kind == CP_CACHE_ROLLING) {
+    if (rows > desc->capacity) return CP_ERR_CAPACITY;
+  } else if ((int64_t)max_past + rows > layout_limit(desc)) {
+    return CP_ERR_CAPACITY;
+  }
+  if ((int64_t)desc->batch * rows > INT32_MAX) return CP_ERR_UNSUPPORTED;
+  AppendArgs a;
+  a.hkv = desc->num_kv_heads;
+  a.d = desc->head_dim;
+  a.esize = esize_of(desc->dtype);
+  a.rows = SeqRows{desc->batch, rows, nullptr};
+  a.cache = make_cache(desc, block_table);
+  a.past = seqlens_k;
+  a.max_ctx = (int)std::min<int64_t>((int64_t)max_past + rows, INT32_MAX);
+  a.k_new = k_new;
+  a.v_new = v_new;
+  a.k_cache = k_cache;
+  a.v_cache = v_cache;
+  a.status = dev_status;
+  return launch_result(launch_kv_append(a, desc->batch * rows, static_cast<cudaStream_t>(stream)));
+}
+
+int cp_prefill_chunk_attn(const cp_layer_desc* desc, const void* q, const void* k_cache, const void* v_cache,
+                          int32_t* seqlens_k, const int32_t* block_table, const int32_t* left_pad,
+                          int32_t rows_padded, int32_t real_rows, int32_t max_past, void* out, void* workspace,
+                          size_t workspace_bytes, int32_t commit, int32_t* dev_status, void* stream) {
+  int r = check_desc(desc, true);
+  if (r != CP_OK) return r;
+  if (rows_padded <= 0 || real_rows <= 0 || real_rows > rows_padded || max_past < 0) return CP_ERR_INVALID_ARG;
+  if (!q || !k_cache || !v_cache || !seqlens_k || !out) return CP_ERR_INVALID_ARG;
+  if (desc->kind == CP_CACHE_PAGED && !block_table) return CP_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out)) return CP_ERR_INVALID_ARG;
+  if (desc->kind == CP_CACHE_ROLLING) {
+    if (real_rows != rows_padded) return CP_ERR_INVALID_ARG;
+    if (rows_padded > desc->capacity) return CP_ERR_CAPACITY;
+  } else if ((int64_t)max_past + rows_padded > layout_limit(desc)) {
+    return CP_ERR_CAPACITY;
+  }
+  const int64_t rows_total = (int64_t)desc->batch * rows_padded;
+  if (rows_total > INT32_MAX || (int64_t)max_past + rows_padded > INT32_MAX) return CP_ERR_UNSUPPORTED;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  AttnArgs a;
+  std::memset(&a, 0, sizeof(a));
+  a.hq = desc->num_q_heads;
+  a.hkv = desc->num_kv_heads;
+  a.d = desc->head_dim;
+  a.group = a.hq / a.hkv;
+  a.scale_log2 = scale_log2(desc);
+  a.rows = SeqRows{desc->batch, rows_padded, nullptr};
+  a.cache = make_cache(desc, block_table);
+  a.past = seqlens_k;
+  a.left_pad = desc->kind == CP_CACHE_ROLLING ? left_pad : nullptr;
+  a.max_ctx = max_past + rows_padded;
+  a.q = q;
+  a.k = k_cache;
+  a.v = v_cache;
+  a.out = out;
+  a.status = dev_status;
+  r = run_attention(desc, a, rows_total, rows_padded, k_cache, v_cache, desc->batch, workspace, workspace_bytes, st);
+  if (r != CP_OK) return r;
+  if (commit) return launch_result(launch_commit(seqlens_k, a.rows, real_rows, st));
+  return CP_OK;
+}
+
+int cp_mixed_step(const cp_layer_desc* desc, const void* q, const void* k_new, const void* v_new, void* k_pages,
+                  void* v_pages, const int32_t* block_table, const int32_t* cu_rows, int32_t* past_len,
+                  int32_t num_seqs, int32_t total_rows, int32_t max_ctx, void* out, void* workspace,
+                  size_t workspace_bytes, int32_t* dev_status, void* stream) {
+  int r = check_desc(desc, false);
+  if (r != CP_OK) return r;
+  if (desc->kind != CP_CACHE_PAGED) return CP_ERR_UNSUPPORTED;
+  if (num_seqs <= 0 || total_rows < 0 || max_ctx <= 0) return CP_ERR_INVALID_ARG;
+  if (total_rows == 0) return CP_OK;
+  if (!q || !k_new || !v_new || !k_pages || !v_pages || !block_table || !cu_rows || !past_len || !out)
+    return CP_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k_new) || !aligned16(v_new) || !aligned16(k_pages) || !aligned16(v_pages) ||
+      !aligned16(out))
+    return CP_ERR_INVALID_ARG;
+  if ((int64_t)max_ctx > layout_limit(desc)) return CP_ERR_CAPACITY;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const SeqRows rows{num_seqs, 0, cu_rows};
+  const CacheView cache = make_cache(desc, block_table);
+
+  AppendArgs ap;
+  ap.hkv = desc->num_kv_heads;
+  ap.d = desc->head_dim;
+  ap.esize = esize_of(desc->dtype);
+  ap.rows = rows;
+  ap.cache = cache;
+  ap.past = past_len;
+  ap.max_ctx = max_ctx;
+  ap.k_new = k_new;
+  ap.v_new = v_new;
+  ap.k_cache = k_pages;
+  ap.v_cache = v_pages;
+  ap.status = dev_status;
+  r = launch_result(launch_kv_append(ap, total_rows, st));
+  if (r != CP_OK) return r;
+
+  AttnArgs a;
+  std::memset(&a, 0, sizeof(a));
+  a.hq = desc->num_q_heads;
+  a.hkv = desc->num_kv_heads;
+  a.d = desc->head_dim;
+  a.group = a.hq / a.hkv;
+  a.scale_log2 = scale_log2(desc);
+  a.rows = rows;
+  a.cache = cache;
+  a.past = past_len;
+  a.max_ctx = max_ctx;
+  a.q = q;
+  a.k = k_pages;
+  a.v = v_pages;
+  a.out = out;
+  a.status = dev_status;
+  r = run_attention(desc, a, total_rows, total_rows, k_pages, v_pages, 0, workspace, workspace_bytes, st);
+  if (r != CP_OK) return r;
+  return launch_result(launch_commit(past_len, rows, -1, st));
+}
+
+}  // extern "C"

@@ -1,0 +1,92 @@
+// cp_internal.h -- argument blocks shared between the C-ABI layer
+// (cp_api.cu) and the kernel translation units.  Plain data only; every
+// pointer is a device pointer unless marked otherwise.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "../../include/cp_api.h"
+
+namespace cp {
+
+// Keys per split of the memory-bound decode path.  Fixed, so a row's result
+// never depends on how many other rows share the launch.
+constexpr int kDecodeSplit = 512;
+
+// How query rows map onto sequences.
+struct SeqRows {
+  int num_seqs;
+  int rows_uniform;      // > 0: sequence s owns rows [s*rows_uniform, (s+1)*rows_uniform)
+  const int* cu_rows;    // else: sequence s owns rows [cu_rows[s], cu_rows[s+1])
+};
+
+__host__ __device__ inline int seq_row0(const SeqRows& r, int s) {
+  return r.rows_uniform > 0 ? s * r.rows_uniform : r.cu_rows[s];
+}
+__host__ __device__ inline int seq_rows(const SeqRows& r, int s) {
+  return r.rows_uniform > 0 ? r.rows_uniform : r.cu_rows[s + 1] - r.cu_rows[s];
+}
+
+// Where a sequence's K/V live.
+struct CacheView {
+  int kind;          // cp_cache_kind
+  int capacity;      // CONTIG / ROLLING slots per (sequence, KV head)
+  int page_size;     // PAGED
+  int num_pages;     // PAGED
+  int max_blocks;    // PAGED
+  const int* block_table;  // PAGED [num_seqs, max_blocks]
+};
+
+// Arguments of the attention kernels (tensor-core, SIMT fp32, decode).
+struct AttnArgs {
+  int hq, hkv, d, group;   // group = hq / hkv query heads per KV head
+  float scale_log2;        // softmax scale * log2(e)
+  SeqRows rows;
+  CacheView cache;
+  const int* past;         // [num_seqs] positions cached before this call's rows
+  const int* left_pad;     // ROLLING [num_seqs] or nullptr
+  int max_ctx;             // host bound: past + rows <= max_ctx (checked in kernel)
+  int min_rows;            // sequences with fewer rows are skipped (routed elsewhere)
+  const void* q;           // [rows_total, hq, d]
+  const void* k;           // cache / pool base (SIMT and decode kernels)
+  const void* v;
+  void* out;               // [rows_total, hq, d]
+  float* part_o;           // decode split partials [num_seqs, hq, max_splits, d]
+  float* part_ml;          // [num_seqs, hq, max_splits, 2] (max, sum) in log2 domain
+  int max_splits;
+  int* status;             // optional CP_DEV_* bits
+};
+
+struct AppendArgs {
+  int hkv, d, esize;       // esize: bytes per element
+  SeqRows rows;
+  CacheView cache;
+  const int* past;
+  int max_ctx;
+  const void* k_new;       // [rows_total, hkv, d]
+  const void* v_new;
+  void* k_cache;
+  void* v_cache;
+  int* status;
+};
+
+// ---- launchers (return cudaGetLastError() after the launch) ----
+cudaError_t launch_kv_append(const AppendArgs& a, int rows_total, cudaStream_t st);
+cudaError_t launch_commit(int* lens, const SeqRows& rows, int add_uniform, cudaStream_t st);
+cudaError_t launch_attn_f32(const AttnArgs& a, int rows_bound, cudaStream_t st);
+cudaError_t launch_attn_tc(const AttnArgs& a, int dtype, const CUtensorMap& tq, const CUtensorMap& tk,
+                           const CUtensorMap& tv, int tiles_bound, cudaStream_t st);
+cudaError_t launch_decode(const AttnArgs& a, int dtype, cudaStream_t st);
+
+// Tensor-core path tiling (shared with the host so it can size grids and
+// tensor-map boxes).
+constexpr int kTcBlockM = 128;   // packed (token, head) rows per CTA
+constexpr int kTcBlockN = 128;   // keys per KV tile
+bool attn_tc_supported(int d, int group, int dtype);
+bool decode_supported(int d, int group, int dtype);
+
+}  // namespace cp

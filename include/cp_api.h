@@ -1,0 +1,240 @@
+/*
+ * cp_api.h -- C ABI of the GB300 chunked-prefill causal attention library
+ * (libcp.so, built for sm_103a).
+ *
+ * Sources cited below:
+ *   [Wiki]     ONNX GenAI Wiki, "Chunked Prefill".
+ *   [Horizon]  Horizon developer blog, "【大模型】Chunk Prefill——把一次算不动的事拆成多次".
+ *   [Glossary] Ultralytics glossary, "Chunked Prefill".
+ *
+ * Conventions shared by every entry point:
+ *   - Pointers named as device pointers must point to GPU memory of the
+ *     current device; the caller allocates and owns every buffer.  The
+ *     library allocates nothing and keeps no state between calls, so calls on
+ *     different streams are independent.  "host" pointers are read before the
+ *     call returns.
+ *   - Layouts are dense row-major with the last dimension contiguous:
+ *       q, out           [B, R, Hq, D]   (cp_prefill_chunk_attn)
+ *                        [T, Hq, D]      (cp_mixed_step)
+ *       k_new, v_new     [B, R, Hkv, D]  (cp_kv_append), [T, Hkv, D] (mixed)
+ *       contiguous cache [B, Hkv, capacity, D]
+ *       rolling cache    [B, Hkv, capacity, D]
+ *       paged pool       [num_pages, Hkv, page_size, D]
+ *       block_table      int32 [B or S, max_blocks], page ids of each sequence
+ *     Element type is cp_layer_desc.dtype for all of q, k, v, caches and out.
+ *     Device pointers must be 16-byte aligned.
+ *   - All work is enqueued asynchronously on `stream` (a cudaStream_t; NULL =
+ *     the legacy default stream).
+ *   - Errors: every argument is checked on the host before anything is
+ *     enqueued; on a bad argument the call returns a negative cp_status and
+ *     launches nothing.  CP_ERR_CUDA is returned if a launch reports an error.
+ *     Values that live on the device (seqlens_k, past_len, block table
+ *     entries) are checked by the kernels against the host bounds given in
+ *     the call: an out-of-range value is never dereferenced -- the affected
+ *     rows are skipped and, if `dev_status` is not NULL, a CP_DEV_* bit is
+ *     OR-ed into *dev_status (an int32 in device memory the caller zeroes and
+ *     reads back after synchronizing).  No kernel asserts or traps; every
+ *     wait inside a kernel is bounded and reports CP_DEV_TIMEOUT.
+ */
+#ifndef CP_API_H
+#define CP_API_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define CP_ABI_VERSION 1
+
+typedef enum {
+  CP_OK = 0,
+  CP_ERR_INVALID_ARG = -1, /* malformed argument (null, negative, misaligned, ...) */
+  CP_ERR_UNSUPPORTED = -2, /* well-formed but outside what the kernels implement  */
+  CP_ERR_CAPACITY = -3,    /* rows would not fit in the cache / pages / table      */
+  CP_ERR_CUDA = -4,        /* a CUDA launch or query failed                         */
+  CP_ERR_WORKSPACE = -5    /* workspace missing or smaller than cp_workspace_size   */
+} cp_status;
+
+/* Bits OR-ed into *dev_status by kernels. */
+#define CP_DEV_BOUNDS 1  /* a device-side length or page id was out of range   */
+#define CP_DEV_TIMEOUT 2 /* a bounded wait inside a kernel gave up             */
+
+typedef enum { CP_F32 = 0, CP_BF16 = 1, CP_F16 = 2 } cp_dtype;
+
+/* Cache layouts.
+ * CONTIG : fixed physical capacity, slot = absolute position ([Wiki] 一.3: the
+ *          past K/V stay bound at physical capacity; the valid length travels
+ *          separately in seqlens_k).
+ * ROLLING: right-aligned window of the newest `capacity` positions ([Horizon]
+ *          2-4).  Position a lives in slot a mod capacity, so the window's
+ *          rotation is implied by seqlens_k and needs no separate state.
+ * PAGED  : fixed-size pages listed in a block table ([Glossary] "Related
+ *          techniques", PagedAttention). */
+typedef enum { CP_CACHE_CONTIG = 0, CP_CACHE_ROLLING = 1, CP_CACHE_PAGED = 2 } cp_cache_kind;
+
+typedef struct {
+  int32_t dtype;        /* cp_dtype                                            */
+  int32_t batch;        /* B, sequences in a cp_kv_append / prefill call        */
+  int32_t num_q_heads;  /* Hq                                                   */
+  int32_t num_kv_heads; /* Hkv; Hq % Hkv == 0 (GroupQueryAttention, [Wiki] 一.3) */
+  int32_t head_dim;     /* D: 64 or 128                                         */
+  int32_t kind;         /* cp_cache_kind                                        */
+  int32_t capacity;     /* CONTIG/ROLLING: slots per (sequence, KV head)        */
+  int32_t page_size;    /* PAGED: tokens per page (16, 32, 64 or 128)           */
+  int32_t num_pages;    /* PAGED: pages in the pool                             */
+  int32_t max_blocks;   /* PAGED: columns of block_table                        */
+  float scale;          /* softmax scale; 0 selects 1/sqrt(head_dim)            */
+} cp_layer_desc;
+
+/* cp_kv_append -- write a chunk's new K/V rows into the cache.
+ *
+ * [Wiki] 一.1: chunk k writes its own positions and never revisits or
+ * rewrites an earlier slot.  [Horizon] 3: in rolling mode the new rows replace
+ * the oldest ones.  [Glossary]: in paged mode a sequence's cache grows page by
+ * page.
+ *   k_new, v_new  device [B, rows, Hkv, D]
+ *   rows          rows per sequence (the padded width R when padding is used)
+ *   k_cache, v_cache  device cache of desc->kind (layouts above)
+ *   seqlens_k     device int32 [B]: valid length = absolute position of row 0.
+ *                 Not modified (cp_prefill_chunk_attn commits it).
+ *   block_table   device int32 [B, max_blocks] (PAGED only, else NULL)
+ *   max_past      host bound on every seqlens_k[b]; CONTIG needs
+ *                 max_past + rows <= capacity, ROLLING needs rows <= capacity,
+ *                 PAGED needs max_past + rows <= max_blocks * page_size.
+ * Row t of sequence b goes to absolute position seqlens_k[b] + t:
+ * CONTIG slot = position; ROLLING slot = position mod capacity; PAGED page =
+ * block_table[b][position / page_size], offset position % page_size.
+ * Bit-exact copy; nothing else in the cache is touched. */
+int cp_kv_append(const cp_layer_desc* desc, const void* k_new, const void* v_new,
+                 int32_t rows, void* k_cache, void* v_cache, const int32_t* seqlens_k,
+                 const int32_t* block_table, int32_t max_past, int32_t* dev_status,
+                 void* stream);
+
+/* cp_prefill_chunk_attn -- causal attention of one chunk of query rows.
+ *
+ * Row i of sequence b is the query at absolute position p = seqlens_k[b] + i
+ * and attends to every cached key before the chunk plus its own causal
+ * triangle: keys at positions [0, p] ([Wiki] 一.2; [Glossary] "How chunked
+ * prefill works": the chunk mask is the lower triangle shifted by the chunk
+ * start).  The chunk's K/V must already be in the cache (cp_kv_append).
+ *   O[b,i,h] = sum_j softmax_j(scale * q[b,i,h] . k_j) v_j over visible j,
+ *   KV head of query head h = h / (Hq / Hkv).
+ * ROLLING ([Horizon] 3-4): the cache holds the newest `capacity` positions;
+ * key position a is visible iff a >= left_pad[b], a >= 0, a is still in the
+ * window and a <= p.  (The page adds -32768 to masked scores; for a row with
+ * at least one visible key that weight underflows to exactly 0, so excluding
+ * the slot gives the same result.  A row with no visible key -- a left-pad
+ * query -- gets output 0.)
+ *   q, out        device [B, rows_padded, Hq, D]; pad rows' outputs are
+ *                 written but unspecified ([Wiki] 四: results are cut back to
+ *                 the real rows)
+ *   seqlens_k     device int32 [B]; if commit != 0 it is advanced by real_rows
+ *                 after the attention ([Wiki] 四: rewind to past + real rows;
+ *                 the pad rows' K/V stay beyond it until the next chunk
+ *                 overwrites them)
+ *   left_pad      device int32 [B] (ROLLING, may be NULL = 0), else NULL
+ *   rows_padded   R, rows per sequence in q/out (query-width ladder tier)
+ *   real_rows     r <= R; ROLLING requires r == R (a pad row would evict a
+ *                 live slot)
+ *   max_past      host bound on seqlens_k[b] (same rule as cp_kv_append)
+ *   workspace     device scratch of at least
+ *                 cp_workspace_size(desc, B * R, max_past + R, B) bytes
+ *                 (may be NULL when that size is 0) */
+int cp_prefill_chunk_attn(const cp_layer_desc* desc, const void* q, const void* k_cache,
+                          const void* v_cache, int32_t* seqlens_k, const int32_t* block_table,
+                          const int32_t* left_pad, int32_t rows_padded, int32_t real_rows,
+                          int32_t max_past, void* out, void* workspace, size_t workspace_bytes,
+                          int32_t commit, int32_t* dev_status, void* stream);
+
+/* cp_mixed_step -- one token-budget step over a paged cache.
+ *
+ * [Glossary] "How chunked prefill works": a step holds one row for every
+ * running decode plus chunks of waiting prompts; mixing them uses the compute
+ * that decode rows leave idle.  The call appends every row's K/V into its
+ * sequence's pages, then computes causal attention for every row (decode rows
+ * -- sequences with one row -- on a memory-bound split-KV path, prompt chunks on
+ * the tensor-core path), then advances past_len[s] by the sequence's rows.
+ *   desc->kind must be CP_CACHE_PAGED; desc->batch is ignored.
+ *   q, out        device [T, Hq, D];  k_new, v_new device [T, Hkv, D]
+ *   k_pages, v_pages  device pools [num_pages, Hkv, page_size, D]
+ *   block_table   device int32 [num_seqs, max_blocks]
+ *   cu_rows       device int32 [num_seqs + 1]: rows of sequence s are
+ *                 [cu_rows[s], cu_rows[s+1]); cu_rows[num_seqs] == T
+ *   past_len      device int32 [num_seqs]: positions already cached
+ *   max_ctx       host bound on past_len[s] + rows of s (<= max_blocks*page_size)
+ *   workspace     >= cp_workspace_size(desc, T, max_ctx, num_seqs) bytes */
+int cp_mixed_step(const cp_layer_desc* desc, const void* q, const void* k_new,
+                  const void* v_new, void* k_pages, void* v_pages, const int32_t* block_table,
+                  const int32_t* cu_rows, int32_t* past_len, int32_t num_seqs,
+                  int32_t total_rows, int32_t max_ctx, void* out, void* workspace,
+                  size_t workspace_bytes, int32_t* dev_status, void* stream);
+
+/* cp_workspace_size -- bytes of device scratch the two attention calls need
+ * for up to `max_rows` query rows, contexts of up to `max_ctx` keys and
+ * `num_seqs` sequences (split-KV partial results and the work list). */
+size_t cp_workspace_size(const cp_layer_desc* desc, int32_t max_rows, int32_t max_ctx,
+                         int32_t num_seqs);
+
+/* ---- host-side integer helpers (no GPU work) ---- */
+
+/* cp_chunk_plan -- chunk sizes of an n_tokens prompt at width `chunk`
+ * ([Wiki] 三: every chunk is `chunk` wide except the last, which takes the
+ * remainder).  Writes up to `cap` sizes to host `sizes` and returns the
+ * number of chunks (which may exceed cap), or a negative cp_status. */
+int32_t cp_chunk_plan(int32_t n_tokens, int32_t chunk, int32_t* sizes, int32_t cap);
+
+/* cp_query_ladder -- the query-width tiers of chunk width `chunk` ([Wiki] 四
+ * and 六: three evenly spaced tiers whose step ceil(chunk/3) is rounded up
+ * so the top tier is exactly `chunk`; {171,342,512} for 512).  Writes the
+ * distinct tiers (1 to 3) to host `tiers[3]` and returns their count. */
+int32_t cp_query_ladder(int32_t chunk, int32_t* tiers);
+
+/* cp_query_width -- smallest tier >= real_rows (1 <= real_rows <= chunk), or a
+ * negative cp_status. */
+int32_t cp_query_width(int32_t real_rows, int32_t chunk);
+
+/* cp_aligned_length -- n_real rounded up to a multiple of the chunk size c
+ * ([Horizon] 5: the prompt is left-padded to a multiple of chunk_size). */
+int32_t cp_aligned_length(int32_t n_real, int32_t c);
+
+/* cp_rolling_mask -- materialise the per-chunk additive mask [c, C] of
+ * [Horizon] 4 into host `out` (row-major floats): row i is the query at
+ * absolute position chunk_idx*c + i, slot j holds position
+ * (chunk_idx+1)*c - C + j; the entry is 0 when that position exists, is not
+ * a left-pad position and is not in the future, else -32768.  The kernels
+ * never materialise it; it is here for tests and callers that want the
+ * tensor.  Returns CP_OK or a negative cp_status. */
+int cp_rolling_mask(int32_t c, int32_t C, int32_t chunk_idx, int32_t left_pad, float* out);
+
+/* One entry of a token-budget plan.  Decode rows have start == -1, rows == 1. */
+typedef struct {
+  int32_t step;  /* step index, from 0                                     */
+  int32_t seq;   /* running decodes 0..n_running-1, prompt i = n_running+i */
+  int32_t start; /* first prompt token of the chunk, -1 for a decode row   */
+  int32_t rows;  /* rows of this entry in the step                         */
+} cp_sched_entry;
+
+/* cp_schedule -- token-budget step plan ([Glossary] "How chunked prefill
+ * works"): each step gives one row to every running decode first, then fills
+ * the remaining budget with chunks of the waiting prompts in arrival order; a
+ * prompt that does not fit continues next step and decodes from the step
+ * after its last chunk.  Entries of a step are ordered decodes first (by seq
+ * id), then prompt chunks.  Writes up to `cap` entries to host `out` and
+ * returns the total entry count (may exceed cap), or a negative cp_status
+ * (CP_ERR_INVALID_ARG if the budget leaves no room for prompt tokens). */
+int32_t cp_schedule(int32_t budget, int32_t n_running, const int32_t* prompt_lens,
+                    int32_t n_prompts, cp_sched_entry* out, int32_t cap);
+
+/* cp_status_string -- static text for a cp_status value. */
+const char* cp_status_string(int32_t status);
+
+/* cp_abi_version -- CP_ABI_VERSION of the built library. */
+int32_t cp_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* CP_API_H */

@@ -1,0 +1,209 @@
+"""GPU parity of the token-budget mixed step over a paged cache (decode rows
+on the split-KV path, prompt chunks on the tensor-core path) against the
+oracle, plus batch invariance."""
+import numpy as np
+import pytest
+import torch
+
+import chunked_prefill_causal_cp_gb300 as cp
+import oracle
+import synth_inputs as SI
+from gpu_util import BF16_TOL, f64
+
+pytestmark = pytest.mark.gpu
+
+HQ, HKV, D, PAGE = 32, 8, 128, 16
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a GPU")
+    from chunked_prefill_causal_cp_gb300 import _build
+    _build.build()
+
+
+class Paged:
+    """GPU pools + an oracle copy of the same pools."""
+
+    def __init__(self, mb: SI.MixedBatch, with_oracle=True, dtype=torch.bfloat16):
+        self.mb = mb
+        self.dtype = dtype
+        self.desc = cp.layer_desc(dtype, 0, HQ, HKV, D, cp.CP_CACHE_PAGED, page_size=mb.page_size,
+                                  num_pages=mb.num_pages, max_blocks=mb.max_blocks)
+        self.k = torch.full((mb.num_pages, HKV, mb.page_size, D), float("nan"), dtype=dtype, device="cuda")
+        self.v = torch.full_like(self.k, float("nan"))
+        self.table = mb.block_table.cuda()
+        self.ok = np.full(tuple(self.k.shape), np.nan) if with_oracle else None
+        self.ov = np.full(tuple(self.k.shape), np.nan) if with_oracle else None
+        self.status = torch.zeros(1, dtype=torch.int32, device="cuda")
+
+    def prefill_history(self, s, kv_k, kv_v):
+        """Write positions [0, n) of sequence s directly (test set-up)."""
+        n = kv_k.shape[0]
+        a = torch.arange(n)
+        pages = self.mb.block_table[s, a // PAGE].long()
+        self.k[pages, :, a % PAGE] = kv_k.to("cuda", self.dtype)
+        self.v[pages, :, a % PAGE] = kv_v.to("cuda", self.dtype)
+        if self.ok is not None:
+            self.ok[pages.numpy(), :, (a % PAGE).numpy()] = f64(kv_k.to(self.dtype))
+            self.ov[pages.numpy(), :, (a % PAGE).numpy()] = f64(kv_v.to(self.dtype))
+
+    def step(self, seqs, rows, past, q, kn, vn, max_ctx):
+        S = len(seqs)
+        cu = torch.tensor(np.concatenate([[0], np.cumsum(rows)]), dtype=torch.int32, device="cuda")
+        pl = torch.tensor(past, dtype=torch.int32, device="cuda")
+        bt = self.table[torch.tensor(seqs, device="cuda")].contiguous()
+        T = int(sum(rows))
+        out = torch.empty(T, HQ, D, dtype=self.dtype, device="cuda")
+        ws = torch.empty(cp.cp_workspace_size(self.desc, T, max_ctx, S), dtype=torch.uint8, device="cuda")
+        cp.cp_mixed_step(self.desc, q, kn, vn, self.k, self.v, bt, cu, pl, S, T, max_ctx, out, ws,
+                         dev_status=self.status)
+        return out, pl
+
+
+def _schedule_steps(budget, n_dec, prompts):
+    steps = {}
+    for st, seq, start, r in cp.cp_schedule(budget, n_dec, prompts):
+        steps.setdefault(st, []).append((seq, start, r))
+    return [steps[i] for i in sorted(steps)]
+
+
+def test_mixed_steps_reduced_full_check():
+    """8 decodes with contexts at page and split edges plus 2 prompts, budget
+    256: every step's every row matches the oracle's mixed step, the pools
+    match the oracle's bit for bit, and past lengths advance by the rows."""
+    ctx = [1, 2, 16, 17, 511, 512, 513, 700]
+    prompts = [600, 450]
+    mb = SI.mixed_batch(n_decode=len(ctx), ctx_lo=1, ctx_hi=2, n_prompt=2, prompt_len=600, decode_tail=64, seed=21)
+    mb.decode_ctx = ctx
+    need = [-(-(n + 64) // PAGE) for n in ctx + prompts]
+    mb.max_blocks = max(need)
+    mb.num_pages = sum(need)
+    g = torch.Generator().manual_seed(21)
+    perm = torch.randperm(mb.num_pages, generator=g)
+    mb.block_table = torch.full((len(need), mb.max_blocks), -1, dtype=torch.int32)
+    off = 0
+    for s, nb in enumerate(need):
+        mb.block_table[s, :nb] = perm[off:off + nb].to(torch.int32)
+        off += nb
+    P = Paged(mb)
+    pos = [c - 1 for c in ctx] + [0, 0]
+    for s, c in enumerate(ctx):
+        P.prefill_history(s, SI.normal((c - 1, HKV, D), 100 + s), SI.normal((c - 1, HKV, D), 200 + s))
+    pq = [SI.gqa_prompt(n, seed=30 + i) for i, n in enumerate(prompts)]
+    nd = len(ctx)
+    for si, entries in enumerate(_schedule_steps(256, nd, prompts)):
+        seqs, rows, qs, ks, vs = [], [], [], [], []
+        for seq, start, r in entries:
+            seqs.append(seq)
+            rows.append(r)
+            if start < 0:  # a decode row: fresh token
+                t = SI.gqa_prompt(1, seed=1000 * si + seq)
+                qs.append(t[0]); ks.append(t[1]); vs.append(t[2])
+            else:
+                q_, k_, v_ = pq[seq - nd]
+                qs.append(q_[start:start + r]); ks.append(k_[start:start + r]); vs.append(v_[start:start + r])
+        q = torch.cat(qs); kn = torch.cat(ks); vn = torch.cat(vs)
+        past = [pos[s] for s in seqs]
+        max_ctx = max(p + r for p, r in zip(past, rows))
+        out, pl = P.step(seqs, rows, past, q.cuda(), kn.cuda(), vn.cuda(), max_ctx)
+        torch.cuda.synchronize()
+        ref, P.ok, P.ov, newp = oracle.mixed_step(f64(q), f64(kn), f64(vn), P.ok, P.ov,
+                                                  mb.block_table[seqs].numpy(), rows, past)
+        err = np.abs(f64(out) - ref).max()
+        assert err < BF16_TOL, (si, err)
+        assert pl.tolist() == newp
+        for s, p in zip(seqs, newp):
+            pos[s] = p
+    assert int(P.status.item()) == 0
+    got_k = f64(P.k)
+    mask = ~np.isnan(P.ok)
+    assert np.array_equal(got_k[mask], P.ok[mask])
+    assert np.isnan(got_k[~mask]).all()
+
+
+def test_mixed_step_batch_invariance():
+    """A request's rows are bit-identical whether it runs in a full mixed step
+    or alone (fixed split length, tiles aligned to each sequence's start)."""
+    ctx = [900, 37, 2000]
+    mb = SI.mixed_batch(n_decode=3, ctx_lo=1, ctx_hi=2, n_prompt=1, prompt_len=700, seed=22)
+    need = [-(-(n + 64) // PAGE) for n in ctx + [700]]
+    mb.max_blocks, mb.num_pages = max(need), sum(need)
+    mb.block_table = torch.full((4, mb.max_blocks), -1, dtype=torch.int32)
+    perm = torch.randperm(mb.num_pages, generator=torch.Generator().manual_seed(5))
+    off = 0
+    for s, nb in enumerate(need):
+        mb.block_table[s, :nb] = perm[off:off + nb].to(torch.int32)
+        off += nb
+    P = Paged(mb, with_oracle=False)
+    for s, c in enumerate(ctx):
+        P.prefill_history(s, SI.normal((c - 1, HKV, D), 300 + s), SI.normal((c - 1, HKV, D), 400 + s))
+    qp, kp, vp = SI.gqa_prompt(700, seed=44)
+    dq, dk, dv = SI.gqa_prompt(3, seed=45)
+    q = torch.cat([dq, qp[:300]]).cuda()
+    kn = torch.cat([dk, kp[:300]]).cuda()
+    vn = torch.cat([dv, vp[:300]]).cuda()
+    k0, v0 = P.k.clone(), P.v.clone()
+    full, _ = P.step([0, 1, 2, 3], [1, 1, 1, 300], [c - 1 for c in ctx] + [0], q, kn, vn, 2000)
+    torch.cuda.synchronize()
+    for sel, rows_sel in [([1], slice(1, 2)), ([3], slice(3, 303)), ([2, 3], slice(2, 303))]:
+        P.k.copy_(k0); P.v.copy_(v0)
+        rows = [1 if s < 3 else 300 for s in sel]
+        past = [(ctx[s] - 1) if s < 3 else 0 for s in sel]
+        alone, _ = P.step(sel, rows, past, q[rows_sel].contiguous(), kn[rows_sel].contiguous(),
+                          vn[rows_sel].contiguous(), 2000)
+        torch.cuda.synchronize()
+        assert torch.equal(alone, full[rows_sel]), sel
+    assert int(P.status.item()) == 0
+
+
+def test_mixed_step_full_size_first_step():
+    """The mixed-step workload at full size: 64 decodes with contexts
+    U{512..8192} in 16-token pages plus the first 8128-row chunk of a
+    20000-token prompt (budget 8192).  All 64 decode rows and 64 sampled
+    prompt rows match the oracle one by one."""
+    mb = SI.mixed_batch()
+    P = Paged(mb, with_oracle=False)
+    hist = []
+    for s, c in enumerate(mb.decode_ctx):
+        hk, hv = SI.normal((c - 1, HKV, D), 500 + s), SI.normal((c - 1, HKV, D), 600 + s)
+        P.prefill_history(s, hk, hv)
+        hist.append((hk, hv))
+    entries = _schedule_steps(8192, 64, mb.prompt_lens)[0]
+    assert entries[-1] == (64, 0, 8128)
+    qp, kp, vp = SI.gqa_prompt(8128, seed=50)
+    dq, dk, dv = SI.gqa_prompt(64, seed=51)
+    seqs = list(range(65))
+    rows = [1] * 64 + [8128]
+    past = [c - 1 for c in mb.decode_ctx] + [0]
+    q = torch.cat([dq, qp]).cuda(); kn = torch.cat([dk, kp]).cuda(); vn = torch.cat([dv, vp]).cuda()
+    out, pl = P.step(seqs, rows, past, q, kn, vn, max(8192, 8128))
+    torch.cuda.synchronize()
+    assert int(P.status.item()) == 0
+    assert pl.tolist() == [p + r for p, r in zip(past, rows)]
+    o = f64(out)
+    worst = 0.0
+    for s in range(64):
+        ks = np.concatenate([f64(hist[s][0].to(torch.bfloat16)), f64(dk[s:s + 1])])
+        vs = np.concatenate([f64(hist[s][1].to(torch.bfloat16)), f64(dv[s:s + 1])])
+        ref = oracle.attention_row(f64(dq[s]), ks, vs, past[s])
+        worst = max(worst, np.abs(o[s] - ref).max())
+    rng = np.random.default_rng(1)
+    kk, vv, qq = f64(kp), f64(vp), f64(qp)
+    for p in [0, 1, 127, 128, 8127] + list(rng.integers(0, 8128, 59)):
+        ref = oracle.attention_row(qq[p], kk, vv, int(p))
+        worst = max(worst, np.abs(o[64 + p] - ref).max())
+    assert worst < BF16_TOL, worst
+
+
+def test_bad_page_id_is_reported_not_read():
+    """A block-table entry outside the pool is never dereferenced; the step
+    flags CP_DEV_BOUNDS in the device status word."""
+    mb = SI.mixed_batch(n_decode=2, ctx_lo=40, ctx_hi=40, n_prompt=1, prompt_len=64, seed=23)
+    P = Paged(mb, with_oracle=False)
+    P.table[0, 1] = mb.num_pages + 5  # page of positions 16..31 of sequence 0
+    q, kn, vn = SI.gqa_prompt(2 + 64, seed=46)
+    out, _ = P.step([0, 1, 2], [1, 1, 64], [39, 39, 0], q.cuda(), kn.cuda(), vn.cuda(), 64)
+    torch.cuda.synchronize()
+    assert int(P.status.item()) & cp.CP_DEV_BOUNDS

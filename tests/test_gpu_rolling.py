@@ -1,0 +1,77 @@
+"""GPU parity of the right-aligned rolling cache path (fp16, 16 heads x 128,
+C = 1024, c = 256) against the oracle's literal cat/slice cache and additive
+-32768 mask."""
+import numpy as np
+import pytest
+import torch
+
+import chunked_prefill_causal_cp_gb300 as cp
+import oracle
+import synth_inputs as SI
+from gpu_util import BF16_TOL, f64
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a GPU")
+    from chunked_prefill_causal_cp_gb300 import _build
+    _build.build()
+
+
+def _run_rolling(n_real, c, C, H, d, dtype, seed):
+    L = cp.cp_aligned_length(n_real, c)
+    lp = L - n_real
+    q, k, v = SI.rolling_prompt(L, seed=seed, heads=H, dim=d, dtype=dtype)
+    desc = cp.layer_desc(dtype, 1, H, H, d, cp.CP_CACHE_ROLLING, capacity=C)
+    kc = torch.full((1, H, C, d), float("nan"), dtype=dtype, device="cuda")
+    vc = torch.full_like(kc, float("nan"))
+    lens = torch.zeros(1, dtype=torch.int32, device="cuda")
+    left = torch.tensor([lp], dtype=torch.int32, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = torch.empty(L, H, d, dtype=dtype, device="cuda")
+    qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
+    ref_out, snaps = oracle.rolling_prefill(f64(q), f64(k), f64(v), c, C, lp)
+    for ci in range(L // c):
+        sl = slice(ci * c, (ci + 1) * c)
+        cp.cp_kv_append(desc, kd[None, sl], vd[None, sl], c, kc, vc, lens, ci * c, dev_status=status)
+        cp.cp_prefill_chunk_attn(desc, qd[None, sl], kc, vc, lens, c, c, ci * c, out[None, sl], None,
+                                 commit=True, left_pad=left, dev_status=status)
+        torch.cuda.synchronize()
+        # De-rotate: logical slot j holds position a = n - C + j, stored at a mod C.
+        n = (ci + 1) * c
+        ok_k, ok_v = snaps[ci]
+        j = np.arange(C)
+        a = n - C + j
+        keep = a >= 0
+        phys = torch.from_numpy(a[keep] % C)
+        assert torch.equal(kc[0, :, phys].cpu().double(), torch.from_numpy(ok_k[:, keep])), ci
+        assert torch.equal(vc[0, :, phys].cpu().double(), torch.from_numpy(ok_v[:, keep])), ci
+    assert int(status.item()) == 0 and int(lens.item()) == L
+    got = f64(out)
+    err = np.abs(got[lp:] - ref_out[lp:]).max()
+    assert err < BF16_TOL, err
+    # Left-pad query rows see no key: their value is unpinned, only finite.
+    assert np.isfinite(got).all()
+    return got, ref_out, lp, q, k, v
+
+
+def test_rolling_sliding_window_2048():
+    """L = 2048 > C = 1024 (2000 real tokens, 48 left-pad): from chunk 4 on the
+    oldest KV is forgotten (sliding-window regime)."""
+    _run_rolling(2000, 256, 1024, 16, 128, torch.float16, seed=3)
+
+
+def test_rolling_no_overflow_768_equals_plain_prefill():
+    """L = 768 <= C (700 real tokens, 68 left-pad): the result equals ordinary
+    causal prefill over the 700 real tokens."""
+    got, _, lp, q, k, v = _run_rolling(700, 256, 1024, 16, 128, torch.float16, seed=3)
+    plain = oracle.causal_attention(f64(q[lp:]), f64(k[lp:]), f64(v[lp:]))
+    assert np.abs(got[lp:] - plain).max() < BF16_TOL
+
+
+def test_rolling_small_ragged():
+    """A cache that is not a multiple of the 128-key tile, bf16, head_dim 64."""
+    _run_rolling(300, 48, 176, 4, 64, torch.bfloat16, seed=11)
