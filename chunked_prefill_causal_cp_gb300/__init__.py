@@ -68,6 +68,7 @@ def lib():
         L = ctypes.CDLL(LIB_PATH)
         P = c_void_p
         L.cp_kv_append.argtypes = [POINTER(LayerDesc), P, P, c_int32, P, P, P, P, c_int32, P, P]
+        L.cp_pad_chunk.argtypes = [POINTER(LayerDesc), P, P, P, c_int32, c_int32, P]
         L.cp_prefill_chunk_attn.argtypes = [POINTER(LayerDesc), P, P, P, P, P, P, c_int32, c_int32,
                                             c_int32, P, P, c_size_t, c_int32, P, P]
         L.cp_mixed_step.argtypes = [POINTER(LayerDesc), P, P, P, P, P, P, P, P, c_int32, c_int32,
@@ -82,7 +83,7 @@ def lib():
         L.cp_schedule.argtypes = [c_int32, c_int32, POINTER(c_int32), c_int32, POINTER(SchedEntry), c_int32]
         L.cp_status_string.argtypes = [c_int32]
         L.cp_status_string.restype = ctypes.c_char_p
-        for name in ("cp_kv_append", "cp_prefill_chunk_attn", "cp_mixed_step", "cp_chunk_plan",
+        for name in ("cp_kv_append", "cp_pad_chunk", "cp_prefill_chunk_attn", "cp_mixed_step", "cp_chunk_plan",
                      "cp_query_ladder", "cp_query_width", "cp_aligned_length", "cp_rolling_mask",
                      "cp_schedule", "cp_abi_version"):
             getattr(L, name).restype = c_int32
@@ -125,6 +126,12 @@ def cp_kv_append(desc, k_new, v_new, rows, k_cache, v_cache, seqlens_k, max_past
                            _ptr(v_cache), _ptr(seqlens_k), _ptr(block_table), max_past,
                            _ptr(dev_status), _stream(stream, k_new))
     _check(s, "cp_kv_append")
+
+
+def cp_pad_chunk(desc, q, k_new, v_new, real_rows, rows_padded, stream=None):
+    s = lib().cp_pad_chunk(ctypes.byref(desc), _ptr(q), _ptr(k_new), _ptr(v_new), real_rows, rows_padded,
+                           _stream(stream, q, k_new, v_new))
+    _check(s, "cp_pad_chunk")
 
 
 def cp_prefill_chunk_attn(desc, q, k_cache, v_cache, seqlens_k, rows_padded, real_rows, max_past,

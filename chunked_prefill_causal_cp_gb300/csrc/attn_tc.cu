@@ -6,33 +6,48 @@
 // triangle -- over a cache at fixed physical capacity, a paged pool, or a
 // right-aligned rolling window ([Horizon] 3-4).
 //
-// Tiling.  One CTA computes one 128-row M tile.  GroupQueryAttention packs the
-// G = Hq/Hkv query heads of one KV head into the tile: 128/G consecutive
-// tokens x G heads, row m <-> (token m / G, head m % G), so every K/V tile
-// loaded into shared memory serves all heads of the group.  K/V tiles hold
-// 128 keys and start at absolute key 0, so tile boundaries never depend on
-// the chunk's width (padded and unpadded runs see the same tiles); tiles past
-// the tile's last query position are never loaded (causal tile skip).
+// Work decomposition.  GroupQueryAttention packs the G = Hq/Hkv query heads of
+// one KV head into 128-row Q tiles: 128/G consecutive tokens x G heads, row
+// m <-> (token m / G, head m % G), so every K/V tile serves all heads of the
+// group.  A cluster of two CTAs owns a pair of Q tiles (256 rows); both CTAs
+// hold both Q tiles, and the KV tiles (128 keys, starting at absolute key 0)
+// are split between them by parity: rank 0 takes tiles 0, 2, 4, ..., rank 1
+// tiles 1, 3, 5, ....  Each CTA thus multiplies every K/V tile it loads into
+// 256 query rows -- the shared-memory fill rate from L2 (about 30 bytes per
+// clock per SM on this part) would otherwise cap the tensor pipe -- while a
+// chunk still spreads over as many SMs as it has 128-row tiles.  Tile
+// boundaries and the parity split depend only on absolute positions, so a
+// padded and an unpadded run of the same rows do identical arithmetic; tiles
+// past the pair's last query position are never loaded (causal tile skip).
 //
-// Warp roles (192 threads):
-//   warp 0      TMA producer: Q once, then K and V tiles into a 2-stage ring.
-//   warp 1      TMEM allocator and MMA issuer (one elected lane):
-//               S = Q K^T  (A = Q, B = K, both K-major, from shared memory),
-//               O += P V   (A = P from TMEM, B = V MN-major from shared memory).
-//   warps 2-5   softmax: thread m owns row m (TMEM lane m).  It reads the
-//               S row from TMEM, masks by absolute position, keeps the running
-//               max / sum in the log2 domain, writes P (16-bit) over the S
-//               columns it came from, rescales its O row in TMEM when the max
-//               grows, and finally normalises O and stores it.
-// TMEM (512 columns): S0 [0,128), S1 [128,256), O [256, 256+D).  Two S
-// buffers let the tensor core compute S_{j+1} while softmax works on S_j.
+// Warp roles (320 threads per CTA):
+//   warp 0      TMA producer: both Q tiles once, then this CTA's K and V tiles
+//               in a 2-stage ring, one stage = one K tile + one V tile (paged
+//               caches: one box per page).
+//   warp 1      TMEM allocator and MMA issuer (one elected lane).  Per KV tile:
+//               S0 = Q0 K^T, S1 = Q1 K^T (A, B K-major in shared memory);
+//               O0 += P0 V, O1 += P1 V (A = P in TMEM, B = V MN-major).
+//   warps 2-5   softmax group 0 (Q tile 0);  warps 6-9  softmax group 1 (Q tile 1).
+// TMEM (512 columns): group w uses [256w, 256w+128) for S/P, [256w+128, +D) for O.
+// Thread m of a group owns row m (TMEM lane m): it reads its S row, masks by
+// absolute position, exponentiates in the log2 domain against a running max,
+// writes P (16-bit) over the S columns, and rescales its O row only when its
+// own max has grown by more than kRescaleLog2 (a row-local decision).
 //
-// Shared memory (128-byte swizzle, what TMA writes and the MMA descriptors
-// read): Q [D/64][128 rows][128 B]; K and V [2 stages][D/64][128 rows][128 B].
+// Ordering: the MMA warp issues S_w(i+1) after O_w += P_w(i) V(i), and tcgen05
+// operations from one thread complete in issue order, so when group w sees
+// S_w(i+1) complete, its P V of tile i has completed too: O_w is then safe to
+// rescale and P_w(i+1) may overwrite P_w(i).
+//
+// Merge: each CTA's partial (max, sum, unnormalised O) per row is combined in
+// a fixed order (even-tile half first): rank r finishes the rows of Q tile r,
+// receiving the peer's partial for those rows through distributed shared
+// memory.
 //
 // Keys beyond the written length inside the last tile may hold stale or
 // poisoned bytes; their scores are masked and the MMA warp zeroes those V rows
 // before P V, so 0 * garbage never reaches O.
+#include <atomic>
 #include <cmath>
 #include <cstdint>
 #include <type_traits>
@@ -46,32 +61,34 @@
 namespace cp {
 namespace {
 
-constexpr int kThreads = 192;
+constexpr int kThreads = 320;
 constexpr int kStages = 2;
 constexpr uint32_t kBlockBytes = 128 * 128;  // [128 rows][64 x 16-bit] = 16 KB
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColS0 = 0, kColS1 = 128, kColO = 256;
+constexpr float kRescaleLog2 = 8.0f;         // O is rescaled when the max grows by > 2^8
 
 struct __align__(8) TcBarriers {
   uint64_t q_full;
-  uint64_t k_full[kStages], k_empty[kStages];
-  uint64_t v_full[kStages], v_empty[kStages];
+  uint64_t kv_full[kStages], kv_empty[kStages];  // a stage holds one K tile and one V tile
   uint64_t s_full[2], p_ready[2];
-  uint64_t o_done;
-  uint64_t drain;
+  uint64_t o_final;
   uint32_t tmem_base;
   int abort;
+  float peer_m[128];  // the peer CTA's partial max / sum for this CTA's rows
+  float peer_l[128];
 };
 
 template <int D>
 struct TcSmem {
   static constexpr int DB = D / 64;
-  static constexpr uint32_t q_off = 0;
-  static constexpr uint32_t k_off = q_off + DB * kBlockBytes;
-  static constexpr uint32_t v_off = k_off + kStages * DB * kBlockBytes;
+  static constexpr uint32_t q_off = 0;                                   // 2 Q tiles
+  static constexpr uint32_t k_off = q_off + 2 * DB * kBlockBytes;        // K stages
+  static constexpr uint32_t v_off = k_off + kStages * DB * kBlockBytes;  // V stages
   static constexpr uint32_t bar_off = v_off + kStages * DB * kBlockBytes;
   static constexpr uint32_t bytes = bar_off + sizeof(TcBarriers);
   static constexpr uint32_t alloc = bytes + 1024;  // slack for 1024-byte alignment
+  // After the main loop the K stages hold the peer's partial O rows [128][D] fp32.
+  static_assert(kStages * DB * kBlockBytes >= 128u * D * 4u, "merge buffer does not fit");
 };
 
 template <typename T>
@@ -87,27 +104,28 @@ __device__ __forceinline__ uint32_t pack2<__half>(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
-// Which (sequence, first token) this CTA owns.  Within a sequence the tiles are
-// handed out last-first, so the tiles with the most keys start earliest.
-__device__ __forceinline__ bool find_tile(const AttnArgs& a, int rpt, int w, int& s, int& t0) {
+// Which (sequence, first token) a cluster owns; a pair covers 2*rpt tokens.
+// Within a sequence the pairs are handed out last-first, so the pairs with
+// the most keys start earliest.
+__device__ __forceinline__ bool find_pair(const AttnArgs& a, int ppt, int w, int& s, int& t0) {
   if (a.rows.rows_uniform > 0) {
-    const int nt = (a.rows.rows_uniform + rpt - 1) / rpt;
-    const int tile = nt - 1 - w / a.rows.num_seqs;
+    const int np = (a.rows.rows_uniform + ppt - 1) / ppt;
+    const int pair = np - 1 - w / a.rows.num_seqs;
     s = w % a.rows.num_seqs;
-    if (tile < 0) return false;
-    t0 = tile * rpt;
+    if (pair < 0) return false;
+    t0 = pair * ppt;
     return true;
   }
   for (int q = 0; q < a.rows.num_seqs; ++q) {
     const int r = seq_rows(a.rows, q);
     if (r < a.min_rows) continue;
-    const int nt = (r + rpt - 1) / rpt;
-    if (w < nt) {
+    const int np = (r + ppt - 1) / ppt;
+    if (w < np) {
       s = q;
-      t0 = (nt - 1 - w) * rpt;
+      t0 = (np - 1 - w) * ppt;
       return true;
     }
-    w -= nt;
+    w -= np;
   }
   return false;
 }
@@ -131,43 +149,43 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = a.group;
-  const int rpt = kTcBlockM / G;
+  const int rpt = kTcBlockM / G;  // tokens per Q tile
   const int g = blockIdx.y;
+  const int rank = (int)cluster_ctarank();
 
-  // ---- this CTA's tile (uniform across the CTA; exits before any setup)
+  // ---- this cluster's pair (same for both CTAs; exits before any setup)
   int s, t0;
-  if (!find_tile(a, rpt, blockIdx.x, s, t0)) return;
+  if (!find_pair(a, 2 * rpt, blockIdx.x >> 1, s, t0)) return;
   const int rows = seq_rows(a.rows, s);
   const int past = a.past[s];
   const int n = past + rows;  // positions written, including this call's rows
   if (past < 0 || n > a.max_ctx) {
-    if (a.status && threadIdx.x == 0) atomicOr(a.status, CP_DEV_BOUNDS);
+    if (a.status && threadIdx.x == 0 && rank == 0) atomicOr(a.status, CP_DEV_BOUNDS);
     return;
   }
   const int row0 = seq_row0(a.rows, s);
-  const int t_end = min(t0 + rpt, rows);
+  const int t_end = min(t0 + 2 * rpt, rows);
   const bool rolling = a.cache.kind == CP_CACHE_ROLLING;
+  const bool paged = a.cache.kind == CP_CACHE_PAGED;
   const int cap = a.cache.capacity;
   // Key indices walked: absolute positions [0, nkeys) (contiguous / paged) or
   // physical ring slots [0, nkeys) (rolling).
   const int nkeys = rolling ? min(n, cap) : past + t_end;
   const int n_valid = rolling ? nkeys : n;  // key indices holding written data
   const int ntiles = (nkeys + kTcBlockN - 1) / kTcBlockN;
+  const int nmine = ntiles > rank ? (ntiles - rank + 1) / 2 : 0;  // this CTA's KV tiles: rank + 2i
 
   if (threadIdx.x == 0) {
     mbar_init(&bar->q_full, 1);
     for (int i = 0; i < kStages; ++i) {
-      mbar_init(&bar->k_full[i], 1);
-      mbar_init(&bar->k_empty[i], 1);
-      mbar_init(&bar->v_full[i], 1);
-      mbar_init(&bar->v_empty[i], 1);
+      mbar_init(&bar->kv_full[i], 1);
+      mbar_init(&bar->kv_empty[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bar->s_full[i], 1);
       mbar_init(&bar->p_ready[i], 128);
     }
-    mbar_init(&bar->o_done, 1);
-    mbar_init(&bar->drain, 1);
+    mbar_init(&bar->o_final, 1);
     bar->abort = 0;
     fence_barrier_init();
   }
@@ -183,172 +201,172 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == 0) {
     // ================================================================ producer
-    if (lane == 0 && ntiles > 0) {
+    if (lane == 0 && nmine > 0) {
       tma_prefetch_desc(&tm_q);
       tma_prefetch_desc(&tm_k);
       tma_prefetch_desc(&tm_v);
-      mbar_arrive_expect_tx(&bar->q_full, DB * kBlockBytes);
-      for (int db = 0; db < DB; ++db)
-        tma_load_3d(sQ + db * kBlockBytes, &tm_q, &bar->q_full, db * 64, g * G, row0 + t0);
-      const int ps = a.cache.page_size;
-      int last_issued = -1;
-      for (int j = 0; j < ntiles; ++j) {
-        const int st = j & 1;
-        const uint32_t ph = (j >> 1) & 1;
-        const int j0 = j * kTcBlockN;
-        for (int which = 0; which < 2; ++which) {  // 0: K, 1: V
-          uint64_t* full = which ? &bar->v_full[st] : &bar->k_full[st];
-          uint64_t* empty = which ? &bar->v_empty[st] : &bar->k_empty[st];
-          const CUtensorMap* map = which ? &tm_v : &tm_k;
-          uint8_t* dst = (which ? sV : sK) + st * DB * kBlockBytes;
-          if (!mbar_wait(empty, ph ^ 1, abort_flag, a.status)) break;
-          if (a.cache.kind != CP_CACHE_PAGED) {
-            mbar_arrive_expect_tx(full, DB * kBlockBytes);
-            for (int db = 0; db < DB; ++db)
-              tma_load_3d(dst + db * kBlockBytes, map, full, db * 64, j0, s * a.hkv + g);
-          } else {
-            // One box of `ps` rows per page that holds at least one written key.
-            const int npg = kTcBlockN / ps;
-            int pages[kTcBlockN / 16];
-            int cnt = 0;
-            for (int pi = 0; pi < npg; ++pi) {
-              const int key = j0 + pi * ps;
-              int page = -1;
-              if (key < n_valid) {
-                const int blk = key / ps;
-                if (blk < a.cache.max_blocks) page = a.cache.block_table[(long long)s * a.cache.max_blocks + blk];
-                if (page < 0 || page >= a.cache.num_pages) {
-                  if (a.status) atomicOr(a.status, CP_DEV_BOUNDS);
-                  page = -1;
-                }
-              }
-              pages[pi] = page;
-              cnt += page >= 0;
-            }
-            mbar_arrive_expect_tx(full, (uint32_t)cnt * DB * ps * 128u);
-            for (int pi = 0; pi < npg; ++pi) {
-              if (pages[pi] < 0) continue;
-              for (int db = 0; db < DB; ++db)
-                tma_load_3d(dst + db * kBlockBytes + pi * ps * 128, map, full, db * 64, 0,
-                            pages[pi] * a.hkv + g);
-            }
+      mbar_arrive_expect_tx(&bar->q_full, 2 * DB * kBlockBytes);
+      for (int w = 0; w < 2; ++w)
+        for (int db = 0; db < DB; ++db)
+          tma_load_3d(sQ + (w * DB + db) * kBlockBytes, &tm_q, &bar->q_full, db * 64, g * G, row0 + t0 + w * rpt);
+    }
+    const int ps = a.cache.page_size;
+    const int npg = paged ? kTcBlockN / ps : 0;
+    // One stage = the K tile and the V tile of one KV tile, signalled together.
+    int issued = -1;
+    for (int i = 0; i < nmine; ++i) {
+      const int st = i & 1;
+      const uint32_t ph = (i >> 1) & 1;
+      const int j0 = (rank + 2 * i) * kTcBlockN;
+      int my_page = -1;  // paged: lane l looks up the page of keys [j0 + l*ps, ...)
+      if (paged && lane < npg) {
+        const int key = j0 + lane * ps;
+        if (key < n_valid) {
+          const int blk = key / ps;
+          if (blk < a.cache.max_blocks) my_page = a.cache.block_table[(long long)s * a.cache.max_blocks + blk];
+          if (my_page < 0 || my_page >= a.cache.num_pages) {
+            if (a.status) atomicOr(a.status, CP_DEV_BOUNDS);
+            my_page = -1;
           }
         }
-        if (*abort_flag) break;
-        last_issued = j;
       }
-      if (*abort_flag) {
-        // Let copies already in flight land before the CTA's shared memory is released.
-        volatile int zero = 0;
-        for (int t = last_issued - 1; t <= last_issued; ++t) {
-          if (t < 0) continue;
-          mbar_wait(&bar->k_full[t & 1], (t >> 1) & 1, &zero, nullptr);
-          mbar_wait(&bar->v_full[t & 1], (t >> 1) & 1, &zero, nullptr);
+      const uint32_t page_mask = paged ? __ballot_sync(0xffffffffu, my_page >= 0) : 0u;
+      bool ok = true;
+      if (lane == 0) ok = mbar_wait(&bar->kv_empty[st], ph ^ 1, abort_flag, a.status);
+      if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+      uint64_t* full = &bar->kv_full[st];
+      uint8_t* dk = sK + st * DB * kBlockBytes;
+      uint8_t* dv = sV + st * DB * kBlockBytes;
+      if (!paged) {
+        if (lane == 0) {
+          mbar_arrive_expect_tx(full, 2 * DB * kBlockBytes);
+          for (int db = 0; db < DB; ++db) {
+            tma_load_3d(dk + db * kBlockBytes, &tm_k, full, db * 64, j0, s * a.hkv + g);
+            tma_load_3d(dv + db * kBlockBytes, &tm_v, full, db * 64, j0, s * a.hkv + g);
+          }
+        }
+      } else {
+        if (lane == 0) mbar_arrive_expect_tx(full, 2u * (uint32_t)__popc(page_mask) * DB * ps * 128u);
+        __syncwarp();
+        for (int pi = 0; pi < npg; ++pi) {
+          const int page = __shfl_sync(0xffffffffu, my_page, pi);
+          if (lane == 0 && page >= 0)
+            for (int db = 0; db < DB; ++db) {
+              tma_load_3d(dk + db * kBlockBytes + pi * ps * 128, &tm_k, full, db * 64, 0, page * a.hkv + g);
+              tma_load_3d(dv + db * kBlockBytes + pi * ps * 128, &tm_v, full, db * 64, 0, page * a.hkv + g);
+            }
         }
       }
+      issued = i;
+    }
+    if (lane == 0 && *abort_flag) {
+      // Let copies already in flight land before the CTA's shared memory is released.
+      volatile int zero = 0;
+      for (int t = issued - 1; t <= issued; ++t)
+        if (t >= 0) mbar_wait(&bar->kv_full[t & 1], (t >> 1) & 1, &zero, nullptr);
     }
   } else if (warp == 1) {
     // ================================================================ MMA issuer
-    bool ok = ntiles > 0 && warp_wait(&bar->q_full, 0, abort_flag, a.status);
-    auto issue_qk = [&](int j) -> bool {
-      const int st = j & 1;
-      if (!warp_wait(&bar->k_full[st], (j >> 1) & 1, abort_flag, a.status)) return false;
-      tc_fence_after();
-      if (lane == 0) {
-        const uint32_t d_tmem = tmem + (st ? kColS1 : kColS0);
-        const uint32_t q_base = smem_u32(sQ);
-        const uint32_t k_base = smem_u32(sK + st * DB * kBlockBytes);
+    // Lane 0 alone polls and issues; a tcgen05.mma holds its thread for most
+    // of its own execution time, so the loop keeps work between MMAs minimal:
+    // per KV tile three waits (P0, K/V of the next tile, P1) and three commits.
+    if (lane == 0) {
+      auto wait = [&](uint64_t* b, uint32_t parity) { return mbar_wait(b, parity, abort_flag, a.status); };
+      constexpr uint64_t kTileStep = (DB * kBlockBytes) >> 4;
+      const uint64_t q_desc0 = make_sdesc_sw128(smem_u32(sQ), 16, 1024);
+      const uint64_t k_desc0 = make_sdesc_sw128(smem_u32(sK), 16, 1024);
+      const uint64_t v_desc0 = make_sdesc_sw128(smem_u32(sV), kBlockBytes, 1024);
+      auto issue_qk = [&](int w, int i) {  // S_w = Q_w K_i^T
+        const uint64_t q_desc = q_desc0 + w * kTileStep;
+        const uint64_t k_desc = k_desc0 + (i & 1) * kTileStep;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * kBlockBytes + (kk & 3) * 32;
-          mma_ss(d_tmem, make_sdesc_sw128(q_base + off, 16, 1024), make_sdesc_sw128(k_base + off, 16, 1024),
-                 kIdescQK, kk > 0);
+          const uint64_t off = ((kk >> 2) * kBlockBytes + (kk & 3) * 32) >> 4;
+          mma_ss(tmem + 256u * w, q_desc + off, k_desc + off, kIdescQK, kk > 0);
         }
-        mma_commit(&bar->s_full[st]);
-        mma_commit(&bar->k_empty[st]);
-      }
-      __syncwarp();
-      return true;
-    };
-    if (ok) ok = issue_qk(0);
-    if (ok && ntiles > 1) ok = issue_qk(1);
-    for (int j = 0; ok && j < ntiles; ++j) {
-      const int st = j & 1;
-      const uint32_t ph = (j >> 1) & 1;
-      if (!warp_wait(&bar->p_ready[st], ph, abort_flag, a.status)) break;
-      if (!warp_wait(&bar->v_full[st], ph, abort_flag, a.status)) break;
-      tc_fence_after();
-      uint8_t* v_stage = sV + st * DB * kBlockBytes;
-      if (j == ntiles - 1) {
-        const int tail = n_valid - j * kTcBlockN;  // rows >= tail hold no written key
-        if (tail < kTcBlockN) {
-          for (int db = 0; db < DB; ++db) {
-            uint4* p = reinterpret_cast<uint4*>(v_stage + db * kBlockBytes + tail * 128);
-            const int nvec = (kTcBlockN - tail) * 128 / 16;
-            for (int i = lane; i < nvec; i += 32) p[i] = make_uint4(0, 0, 0, 0);
-          }
-          fence_proxy_async_smem();
-        }
-        __syncwarp();
-      }
-      if (lane == 0) {
-        const uint32_t p_tmem = tmem + (st ? kColS1 : kColS0);
-        const uint32_t v_base = smem_u32(v_stage);
+        mma_commit(&bar->s_full[w]);
+      };
+      auto issue_pv = [&](int w, int i) {  // O_w += P_w V_i
+        const uint64_t v_desc = v_desc0 + (i & 1) * kTileStep;
 #pragma unroll
         for (int kk = 0; kk < kTcBlockN / 16; ++kk)
-          mma_ts(tmem + kColO, p_tmem + kk * 8, make_sdesc_sw128(v_base + kk * 2048, kBlockBytes, 1024),
-                 kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
-        mma_commit(&bar->o_done);
-        mma_commit(&bar->v_empty[st]);
+          mma_ts(tmem + 256u * w + 128u, tmem + 256u * w + kk * 8, v_desc + ((kk * 2048) >> 4), kIdescPV,
+                 (i > 0 || kk > 0) ? 1u : 0u);
+      };
+      bool ok = nmine > 0 && wait(&bar->q_full, 0) && wait(&bar->kv_full[0], 0);
+      if (ok) {
+        tc_fence_after();
+        issue_qk(0, 0);
+        issue_qk(1, 0);
       }
-      __syncwarp();
-      if (j + 2 < ntiles) ok = issue_qk(j + 2);
-    }
-    // Make sure every MMA this warp issued has finished before TMEM is freed.
-    if (lane == 0 && ntiles > 0) mma_commit(&bar->drain);
-    __syncwarp();
-    if (ntiles > 0) {
+      for (int i = 0; ok && i < nmine; ++i) {
+        const bool more = i + 1 < nmine;
+        if (!wait(&bar->p_ready[0], i & 1)) break;
+        if (rank + 2 * i == ntiles - 1) {  // last KV tile: zero V rows past the written keys
+          const int tail = n_valid - (ntiles - 1) * kTcBlockN;
+          if (tail < kTcBlockN) {
+            uint8_t* v_stage = sV + (i & 1) * DB * kBlockBytes;
+            for (int db = 0; db < DB; ++db) {
+              uint4* p = reinterpret_cast<uint4*>(v_stage + db * kBlockBytes + tail * 128);
+              const int nvec = (kTcBlockN - tail) * 128 / 16;
+              for (int e = 0; e < nvec; ++e) p[e] = make_uint4(0, 0, 0, 0);
+            }
+            fence_proxy_async_smem();
+          }
+        }
+        tc_fence_after();
+        issue_pv(0, i);
+        if (more) {
+          if (!wait(&bar->kv_full[(i + 1) & 1], ((i + 1) >> 1) & 1)) break;
+          issue_qk(0, i + 1);
+        }
+        if (!wait(&bar->p_ready[1], i & 1)) break;
+        tc_fence_after();
+        issue_pv(1, i);
+        mma_commit(&bar->kv_empty[i & 1]);
+        if (more) issue_qk(1, i + 1);
+      }
+      // o_final: every MMA issued has completed (epilogue and TMEM release wait on it).
+      mma_commit(&bar->o_final);
       volatile int zero = 0;  // wait even after an abort: MMAs may still be in flight
-      warp_wait(&bar->drain, 0, &zero, a.status);
+      mbar_wait(&bar->o_final, 0, &zero, a.status);
     }
-  } else {
-    // ================================================================ softmax
-    const int quarter = warp & 3;            // TMEM lanes [32*quarter, +32)
-    const int mrow = quarter * 32 + lane;    // this thread's row of the tile
-    const int tok = t0 + mrow / G;
-    const int head = g * G + mrow % G;
-    const bool row_ok = tok < t_end;
+    __syncwarp();
+  }
+
+  // ================================================================ softmax groups
+  const bool is_softmax = warp >= 2;
+  const int grp = (warp - 2) >> 2;          // Q tile of this group
+  const int quarter = warp & 3;             // TMEM lanes [32*quarter, +32)
+  const int mrow = quarter * 32 + lane;     // this thread's row of its Q tile
+  const int tok = t0 + grp * rpt + mrow / G;
+  const int head = g * G + mrow % G;
+  const bool row_ok = tok < t_end;
+  const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+  const uint32_t s_col = tmem + lane_off + 256u * grp;
+  const uint32_t o_col = s_col + 128u;
+  float m_run = -INFINITY;  // max used for exponentiation (log2 domain)
+  float l_run = 0.f;
+  bool alive = true;
+  if (is_softmax) {
     const int p_row = row_ok ? past + tok : -1;  // absolute query position
-    const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
     const int lo = rolling ? max(a.left_pad ? a.left_pad[s] : 0, 0) : 0;
-    // Rolling: slot -> absolute position (see cp_kv.cuh), split at slot r.
+    // Rolling: slot -> absolute position (see cp_kv.cuh), split at slot r_slot.
     const int r_slot = n > 0 ? (n - 1) % cap : 0;
     const int base_hi = n - 1 - r_slot;
     const float sl2 = a.scale_log2;
-
-    float m_run = -INFINITY, l_run = 0.f;
-    bool alive = true;
-    for (int j = 0; j < ntiles; ++j) {
-      const int st = j & 1;
-      if (!warp_wait(&bar->s_full[st], (j >> 1) & 1, abort_flag, a.status)) { alive = false; break; }
+    for (int i = 0; i < nmine; ++i) {
+      if (!warp_wait(&bar->s_full[grp], i & 1, abort_flag, a.status)) { alive = false; break; }
       tc_fence_after();
-      const uint32_t s_col = lane_base + (st ? kColS1 : kColS0);
       uint32_t sv[128];
       tmem_ld32(s_col + 0, &sv[0]);
       tmem_ld32(s_col + 32, &sv[32]);
       tmem_ld32(s_col + 64, &sv[64]);
       tmem_ld32(s_col + 96, &sv[96]);
       tmem_wait_ld();
-      const int j0 = j * kTcBlockN;
+      const int j0 = (rank + 2 * i) * kTcBlockN;
       float mx = -INFINITY;
-      if (!rolling && j0 + kTcBlockN - 1 <= p_row) {
-#pragma unroll
-        for (int c = 0; c < 128; ++c) {
-          const float x = __uint_as_float(sv[c]) * sl2;
-          sv[c] = __float_as_uint(x);
-          mx = fmaxf(mx, x);
-        }
-      } else {
+      if (!(!rolling && j0 + kTcBlockN - 1 <= p_row)) {  // not fully visible: mask first
 #pragma unroll
         for (int c = 0; c < 128; ++c) {
           const int key = j0 + c;
@@ -359,71 +377,128 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int pos = key + base_hi - (key > r_slot ? cap : 0);
             vis = key < nkeys && pos >= lo && pos <= p_row;
           }
-          const float x = vis ? __uint_as_float(sv[c]) * sl2 : -INFINITY;
-          sv[c] = __float_as_uint(x);
-          mx = fmaxf(mx, x);
+          if (!vis) sv[c] = __float_as_uint(-INFINITY);
         }
       }
-      const float m_new = fmaxf(m_run, mx);
-      const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
-      const float alpha = (m_run == -INFINITY) ? (m_new == -INFINITY ? 1.f : 0.f) : ex2_approx(m_run - m_new);
-      float psum = 0.f;
+      {
+        float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+        for (int c = 0; c < 128; c += 8) {
+          m4[0] = fmax3(m4[0], __uint_as_float(sv[c + 0]), __uint_as_float(sv[c + 1]));
+          m4[1] = fmax3(m4[1], __uint_as_float(sv[c + 2]), __uint_as_float(sv[c + 3]));
+          m4[2] = fmax3(m4[2], __uint_as_float(sv[c + 4]), __uint_as_float(sv[c + 5]));
+          m4[3] = fmax3(m4[3], __uint_as_float(sv[c + 6]), __uint_as_float(sv[c + 7]));
+        }
+        mx = fmaxf(fmax3(m4[0], m4[1], m4[2]), m4[3]);
+      }
+      const float mx2 = mx * sl2;  // scale > 0, so the max commutes with it
+      const bool grow = mx2 > m_run + kRescaleLog2 || (m_run == -INFINITY && mx2 != -INFINITY);
+      const float m_new = grow ? mx2 : m_run;
+      const float alpha = grow ? (m_run == -INFINITY ? 0.f : ex2_approx(m_run - m_new)) : 1.f;
+      const float neg_m = (m_new == -INFINITY) ? 0.f : -m_new;
+      float ps4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int c = 0; c < 64; ++c) {
-        const float p0 = ex2_approx(__uint_as_float(sv[2 * c]) - m_use);
-        const float p1 = ex2_approx(__uint_as_float(sv[2 * c + 1]) - m_use);
-        psum += p0 + p1;
+        float x0 = __uint_as_float(sv[2 * c]), x1 = __uint_as_float(sv[2 * c + 1]);
+        ffma2(x0, x1, sl2, neg_m);
+        const float p0 = ex2_approx(x0);
+        const float p1 = ex2_approx(x1);
+        fadd2(ps4[2 * (c & 1)], ps4[2 * (c & 1) + 1], p0, p1);
         sv[c] = pack2<T>(p0, p1);
       }
+      const float psum = (ps4[0] + ps4[1]) + (ps4[2] + ps4[3]);
       l_run = l_run * alpha + psum;
       m_run = m_new;
       tmem_st32(s_col + 0, &sv[0]);
       tmem_st32(s_col + 32, &sv[32]);
+      // O holds P V of this group's earlier tiles (complete: see the ordering
+      // note above).  Rows whose max grew rescale it; the others multiply by 1.
+      if (i > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t ov[32];
+          tmem_ld32(o_col + 32 * c, ov);
+          tmem_wait_ld();
+#pragma unroll
+          for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
+          tmem_st32(o_col + 32 * c, ov);
+        }
+      }
       tmem_wait_st();
-      if (j > 0) {
-        // O holds P V of tiles < j; rescale it before P_j V_j is added.
-        if (!warp_wait(&bar->o_done, (j - 1) & 1, abort_flag, a.status)) { alive = false; break; }
-        tc_fence_after();
-        if (__any_sync(0xffffffffu, alpha != 1.f)) {
-#pragma unroll
-          for (int c = 0; c < D / 32; ++c) {
-            uint32_t ov[32];
-            tmem_ld32(lane_base + kColO + 32 * c, ov);
-            tmem_wait_ld();
-#pragma unroll
-            for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
-            tmem_st32(lane_base + kColO + 32 * c, ov);
-          }
-          tmem_wait_st();
-        }
-      }
       tc_fence_before();
-      mbar_arrive(&bar->p_ready[st]);
+      mbar_arrive(&bar->p_ready[grp]);
     }
-    // ---- epilogue: O / l -> out
-    if (alive && ntiles > 0 && warp_wait(&bar->o_done, (ntiles - 1) & 1, abort_flag, a.status)) {
-      tc_fence_after();
-      const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
-      T* out = static_cast<T*>(a.out) + ((long long)(row0 + tok) * a.hq + head) * D;
+  }
+
+  // ================================================================ merge across the pair
+  // Every warp of both CTAs takes part in the two cluster barriers.
+  volatile int zero = 0;
+  const bool done = (!is_softmax || warp_wait(&bar->o_final, 0, &zero, a.status)) && alive;
+  tc_fence_before();
+  cluster_sync_all();  // #1: both CTAs are past their main loops
+  tc_fence_after();
+  const bool have_o = nmine > 0;  // this CTA wrote O (else its TMEM O is unset: send zeros)
+  if (is_softmax && grp != rank) {
+    // Rows of Q tile (1 - rank) are finished by the peer: send this CTA's partial.
+    const uint32_t peer = (uint32_t)(1 - rank);
+    const uint32_t pm = mapa_shared(smem_u32(&bar->peer_m[mrow]), peer);
+    const uint32_t pl = mapa_shared(smem_u32(&bar->peer_l[mrow]), peer);
+    st_cluster_f32(pm, have_o ? m_run : -INFINITY);
+    st_cluster_f32(pl, have_o ? l_run : 0.f);
+    const uint32_t po = mapa_shared(smem_u32(sK + (uint32_t)mrow * D * 4u), peer);
 #pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
-        uint32_t ov[32];
-        tmem_ld32(lane_base + kColO + 32 * c, ov);
+    for (int c = 0; c < D / 32; ++c) {
+      uint32_t ov[32];
+      if (have_o) {
+        tmem_ld32(o_col + 32 * c, ov);
         tmem_wait_ld();
-        if (row_ok) {
-          uint32_t pk[16];
+      } else {
 #pragma unroll
-          for (int e = 0; e < 16; ++e)
-            pk[e] = pack2<T>(__uint_as_float(ov[2 * e]) * inv, __uint_as_float(ov[2 * e + 1]) * inv);
-          uint4* dst = reinterpret_cast<uint4*>(out + 32 * c);
-#pragma unroll
-          for (int e = 0; e < 4; ++e) dst[e] = make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
-        }
+        for (int e = 0; e < 32; ++e) ov[e] = 0u;
       }
-    } else if (ntiles == 0 && row_ok) {
-      // No key visible at all (e.g. a rolling left-pad query): output 0.
-      T* out = static_cast<T*>(a.out) + ((long long)(row0 + tok) * a.hq + head) * D;
-      for (int e = 0; e < D; ++e) out[e] = T(0.f);
+#pragma unroll
+      for (int e = 0; e < 8; ++e)
+        st_cluster_v4(po + (uint32_t)(c * 32 + 4 * e) * 4u, ov[4 * e], ov[4 * e + 1], ov[4 * e + 2], ov[4 * e + 3]);
+    }
+  }
+  cluster_sync_all();  // #2: the peer's partial for this CTA's rows is in place
+  if (is_softmax && grp == rank) {
+    // Fixed order: the even-tile half (rank 0's partial) first.
+    const float* peer_o = reinterpret_cast<const float*>(sK + (uint32_t)mrow * D * 4u);
+    const float m_own = have_o ? m_run : -INFINITY, l_own = have_o ? l_run : 0.f;
+    const float m_peer = bar->peer_m[mrow], l_peer = bar->peer_l[mrow];
+    const float mA = rank == 0 ? m_own : m_peer, lA = rank == 0 ? l_own : l_peer;
+    const float mB = rank == 0 ? m_peer : m_own, lB = rank == 0 ? l_peer : l_own;
+    const float mm = fmaxf(mA, mB);
+    const float wA = (mA == -INFINITY) ? 0.f : ex2_approx(mA - mm);
+    const float wB = (mB == -INFINITY) ? 0.f : ex2_approx(mB - mm);
+    const float lsum = lA * wA + lB * wB;
+    const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
+    T* out = static_cast<T*>(a.out) + ((long long)(row0 + tok) * a.hq + head) * D;
+#pragma unroll
+    for (int c = 0; c < D / 32; ++c) {
+      uint32_t ov[32];
+      if (have_o) {
+        tmem_ld32(o_col + 32 * c, ov);
+        tmem_wait_ld();
+      } else {
+#pragma unroll
+        for (int e = 0; e < 32; ++e) ov[e] = 0u;
+      }
+      if (done && row_ok) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          const float own0 = __uint_as_float(ov[2 * e]), own1 = __uint_as_float(ov[2 * e + 1]);
+          const float pr0 = peer_o[c * 32 + 2 * e], pr1 = peer_o[c * 32 + 2 * e + 1];
+          const float x0 = rank == 0 ? own0 * wA + pr0 * wB : pr0 * wA + own0 * wB;
+          const float x1 = rank == 0 ? own1 * wA + pr1 * wB : pr1 * wA + own1 * wB;
+          pk[e] = pack2<T>(x0 * inv, x1 * inv);
+        }
+        uint4* dst = reinterpret_cast<uint4*>(out + 32 * c);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) dst[e] = make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
+      }
     }
   }
 
@@ -437,14 +512,37 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 template <typename T, int D>
 cudaError_t launch_t(const AttnArgs& a, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                     int tiles_bound, cudaStream_t st) {
+                     int pairs_bound, cudaStream_t st) {
   // D = 64 would fit two CTAs per SM, but each CTA takes all 512 TMEM
   // columns; ask for enough shared memory to keep it at one CTA per SM.
   const uint32_t smem = TcSmem<D>::alloc < 120u * 1024u ? 120u * 1024u : TcSmem<D>::alloc;
-  cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel<T, D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  // Raise the dynamic shared-memory limit once per device (it is a per-device
+  // function attribute), so later calls -- including ones being captured into
+  // a CUDA graph -- only launch.
+  static std::atomic<uint64_t> ready_mask{0};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  dim3 grid(tiles_bound, a.hkv);
-  attn_tc_kernel<T, D><<<grid, kThreads, smem, st>>>(tq, tk, tv, a);
+  const uint64_t bit = 1ull << (dev & 63);
+  if (!(ready_mask.load(std::memory_order_acquire) & bit)) {
+    e = cudaFuncSetAttribute(attn_tc_kernel<T, D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    ready_mask.fetch_or(bit, std::memory_order_release);
+  }
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.gridDim = dim3(2 * pairs_bound, a.hkv);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, attn_tc_kernel<T, D>, tq, tk, tv, a);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
@@ -455,14 +553,15 @@ bool attn_tc_supported(int d, int group, int dtype) {
          (dtype == CP_BF16 || dtype == CP_F16);
 }
 
+// pairs_bound: number of 2*128-row Q-tile pairs to cover (one 2-CTA cluster each).
 cudaError_t launch_attn_tc(const AttnArgs& a, int dtype, const CUtensorMap& tq, const CUtensorMap& tk,
-                           const CUtensorMap& tv, int tiles_bound, cudaStream_t st) {
-  if (tiles_bound <= 0) return cudaSuccess;
+                           const CUtensorMap& tv, int pairs_bound, cudaStream_t st) {
+  if (pairs_bound <= 0) return cudaSuccess;
   if (dtype == CP_BF16)
-    return a.d == 64 ? launch_t<__nv_bfloat16, 64>(a, tq, tk, tv, tiles_bound, st)
-                     : launch_t<__nv_bfloat16, 128>(a, tq, tk, tv, tiles_bound, st);
-  return a.d == 64 ? launch_t<__half, 64>(a, tq, tk, tv, tiles_bound, st)
-                   : launch_t<__half, 128>(a, tq, tk, tv, tiles_bound, st);
+    return a.d == 64 ? launch_t<__nv_bfloat16, 64>(a, tq, tk, tv, pairs_bound, st)
+                     : launch_t<__nv_bfloat16, 128>(a, tq, tk, tv, pairs_bound, st);
+  return a.d == 64 ? launch_t<__half, 64>(a, tq, tk, tv, pairs_bound, st)
+                   : launch_t<__half, 128>(a, tq, tk, tv, pairs_bound, st);
 }
 
 }  // namespace cp

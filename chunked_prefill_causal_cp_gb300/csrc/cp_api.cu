@@ -158,14 +158,14 @@ int run_attention(const cp_layer_desc* d, const AttnArgs& base, int64_t rows_tot
     a.min_rows = decode_ok ? 2 : 1;
     CUtensorMap tq, tk, tv;
     if (!make_tc_maps(d, a.q, rows_total, k, v, batch_for_maps, &tq, &tk, &tv)) return CP_ERR_CUDA;
-    const int rpt = kTcBlockM / G;
-    int64_t tiles;
+    const int ppt = 2 * (kTcBlockM / G);  // tokens per pair of 128-row Q tiles
+    int64_t pairs;
     if (a.rows.rows_uniform > 0)
-      tiles = (int64_t)a.rows.num_seqs * ((a.rows.rows_uniform + rpt - 1) / rpt);
+      pairs = (int64_t)a.rows.num_seqs * ((a.rows.rows_uniform + ppt - 1) / ppt);
     else
-      tiles = (rows_total + rpt - 1) / rpt + a.rows.num_seqs;
-    if (tiles > INT32_MAX) return CP_ERR_UNSUPPORTED;
-    return launch_result(launch_attn_tc(a, d->dtype, tq, tk, tv, (int)tiles, st));
+      pairs = (rows_total + ppt - 1) / ppt + a.rows.num_seqs;
+    if (2 * pairs > INT32_MAX) return CP_ERR_UNSUPPORTED;
+    return launch_result(launch_attn_tc(a, d->dtype, tq, tk, tv, (int)pairs, st));
   }
   return CP_OK;
 }
@@ -211,6 +211,26 @@ int cp_kv_append(const cp_layer_desc* desc, const void* k_new, const void* v_new
   a.v_cache = v_cache;
   a.status = dev_status;
   return launch_result(launch_kv_append(a, desc->batch * rows, static_cast<cudaStream_t>(stream)));
+}
+
+int cp_pad_chunk(const cp_layer_desc* desc, void* q, void* k_new, void* v_new, int32_t real_rows,
+                 int32_t rows_padded, void* stream) {
+  int r = check_desc(desc, true);
+  if (r != CP_OK) return r;
+  if (real_rows <= 0 || rows_padded < real_rows) return CP_ERR_INVALID_ARG;
+  if ((q && !aligned16(q)) || (k_new && !aligned16(k_new)) || (v_new && !aligned16(v_new))) return CP_ERR_INVALID_ARG;
+  if ((int64_t)desc->batch * rows_padded > INT32_MAX) return CP_ERR_UNSUPPORTED;
+  if (rows_padded == real_rows) return CP_OK;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int es = esize_of(desc->dtype);
+  const int qb = desc->num_q_heads * desc->head_dim * es;
+  const int kb = desc->num_kv_heads * desc->head_dim * es;
+  if (q && (r = launch_result(launch_pad_rows(q, desc->batch, rows_padded, real_rows, qb, st))) != CP_OK) return r;
+  if (k_new && (r = launch_result(launch_pad_rows(k_new, desc->batch, rows_padded, real_rows, kb, st))) != CP_OK)
+    return r;
+  if (v_new && (r = launch_result(launch_pad_rows(v_new, desc->batch, rows_padded, real_rows, kb, st))) != CP_OK)
+    return r;
+  return CP_OK;
 }
 
 int cp_prefill_chunk_attn(const cp_layer_desc* desc, const void* q, const void* k_cache, const void* v_cache,

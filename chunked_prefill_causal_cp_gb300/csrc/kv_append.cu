@@ -66,6 +66,22 @@ __global__ void kv_append_kernel(const AppendArgs a, int rows_total) {
   *reinterpret_cast<uint4*>(static_cast<char*>(a.v_cache) + dst_b) = vv;
 }
 
+// Rows [real_rows, rows_padded) of each sequence become copies of row
+// real_rows - 1 ([Wiki] 四: pad rows repeat the last real token).
+__global__ void pad_rows_kernel(char* base, int batch, int rows_padded, int real_rows, int row_bytes) {
+  const int vecs = row_bytes / 16;
+  const int pad = rows_padded - real_rows;
+  const long long gid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (gid >= (long long)batch * pad * vecs) return;
+  const int vec = (int)(gid % vecs);
+  const long long r = gid / vecs;
+  const int b = (int)(r / pad);
+  const int t = real_rows + (int)(r % pad);
+  const char* src = base + ((long long)b * rows_padded + real_rows - 1) * row_bytes;
+  char* dst = base + ((long long)b * rows_padded + t) * row_bytes;
+  reinterpret_cast<uint4*>(dst)[vec] = reinterpret_cast<const uint4*>(src)[vec];
+}
+
 __global__ void commit_kernel(int* lens, const SeqRows rows, int add_uniform) {
   const int s = blockIdx.x * blockDim.x + threadIdx.x;
   if (s >= rows.num_seqs) return;
@@ -81,6 +97,15 @@ cudaError_t launch_kv_append(const AppendArgs& a, int rows_total, cudaStream_t s
   const int block = 256;
   const long long grid = (threads + block - 1) / block;
   kv_append_kernel<<<(unsigned)grid, block, 0, st>>>(a, rows_total);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_pad_rows(void* base, int batch, int rows_padded, int real_rows, int row_bytes, cudaStream_t st) {
+  const long long threads = (long long)batch * (rows_padded - real_rows) * (row_bytes / 16);
+  if (threads <= 0) return cudaSuccess;
+  const int block = 256;
+  pad_rows_kernel<<<(unsigned)((threads + block - 1) / block), block, 0, st>>>(static_cast<char*>(base), batch,
+                                                                              rows_padded, real_rows, row_bytes);
   return cudaGetLastError();
 }
 

@@ -112,6 +112,18 @@ int cp_kv_append(const cp_layer_desc* desc, const void* k_new, const void* v_new
                  const int32_t* block_table, int32_t max_past, int32_t* dev_status,
                  void* stream);
 
+/* cp_pad_chunk -- widen a chunk in place to its query-width tier.
+ *
+ * [Wiki] 四: the rows of a forward are rounded up to a ladder tier and the
+ * extra rows repeat the last real token; every per-token input of shape
+ * [1, rows, ...] is widened the same way.  For each sequence b, rows
+ * [real_rows, rows_padded) of q [B, rows_padded, Hq, D] and of k_new, v_new
+ * [B, rows_padded, Hkv, D] (device) are overwritten with copies of row
+ * real_rows - 1; rows below real_rows are not touched.  Any of the three
+ * pointers may be NULL to skip that tensor.  Bit-exact copy. */
+int cp_pad_chunk(const cp_layer_desc* desc, void* q, void* k_new, void* v_new, int32_t real_rows,
+                 int32_t rows_padded, void* stream);
+
 /* cp_prefill_chunk_attn -- causal attention of one chunk of query rows.
  *
  * Row i of sequence b is the query at absolute position p = seqlens_k[b] + i
