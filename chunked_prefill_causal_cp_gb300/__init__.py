@@ -73,6 +73,11 @@ def lib():
                                             c_int32, P, P, c_size_t, c_int32, P, P]
         L.cp_mixed_step.argtypes = [POINTER(LayerDesc), P, P, P, P, P, P, P, P, c_int32, c_int32,
                                     c_int32, P, P, c_size_t, P, P]
+        L.cp_mixed_step_noalloc.argtypes = [POINTER(LayerDesc), P, P, P, P, P, P, P, P, c_int32, c_int32,
+                                            c_int32, P, P, P]
+        L.cp_mixed_step_noalloc.restype = c_int32
+        L.cp_noalloc_scratch_bytes.argtypes = []
+        L.cp_noalloc_scratch_bytes.restype = c_size_t
         L.cp_workspace_size.argtypes = [POINTER(LayerDesc), c_int32, c_int32, c_int32]
         L.cp_workspace_size.restype = c_size_t
         L.cp_chunk_plan.argtypes = [c_int32, c_int32, POINTER(c_int32), c_int32]
@@ -153,6 +158,21 @@ def cp_mixed_step(desc, q, k_new, v_new, k_pages, v_pages, block_table, cu_rows,
                             total_rows, max_ctx, _ptr(out), _ptr(workspace), ws_bytes,
                             _ptr(dev_status), _stream(stream, q))
     _check(s, "cp_mixed_step")
+
+
+def cp_mixed_step_noalloc(desc, q, k_new, v_new, k_pages, v_pages, block_table, cu_rows, past_len,
+                          num_seqs, total_rows, max_ctx, out, dev_status=None, stream=None):
+    """cp_mixed_step without a workspace: the split-KV scratch is a fixed array
+    inside the library (see include/cp_api.h for its limit and sharing rules)."""
+    s = lib().cp_mixed_step_noalloc(ctypes.byref(desc), _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_pages),
+                                    _ptr(v_pages), _ptr(block_table), _ptr(cu_rows), _ptr(past_len),
+                                    num_seqs, total_rows, max_ctx, _ptr(out), _ptr(dev_status),
+                                    _stream(stream, q))
+    _check(s, "cp_mixed_step_noalloc")
+
+
+def cp_noalloc_scratch_bytes() -> int:
+    return int(lib().cp_noalloc_scratch_bytes())
 
 
 def cp_workspace_size(desc, max_rows, max_ctx, num_seqs) -> int:

@@ -183,6 +183,41 @@ int cp_mixed_step(const cp_layer_desc* desc, const void* q, const void* k_new,
                   int32_t total_rows, int32_t max_ctx, void* out, void* workspace,
                   size_t workspace_bytes, int32_t* dev_status, void* stream);
 
+/* cp_mixed_step_noalloc -- cp_mixed_step for callers that cannot allocate.
+ *
+ * The pages have no counterpart to this entry point; it is a convenience of
+ * this library's interface.  Some callers cannot allocate device memory or hand
+ * the library a workspace: serving engines that reserve all device memory up
+ * front and forbid allocation on the request path, plugins that receive only
+ * input and output tensors from a host framework that owns every allocation,
+ * and code running where cudaMalloc is not allowed (for example inside a
+ * stream callback).  This is cp_mixed_step with its split-KV scratch taken from
+ * a fixed array of cp_noalloc_scratch_bytes() bytes (8 MiB) compiled into the
+ * library; every GPU that loads the library holds that array until the
+ * process exits.  It allocates nothing: no cudaMalloc, cudaFree or allocating
+ * library routine.
+ *   Arguments and results are those of cp_mixed_step, without the workspace.
+ *   A step whose cp_workspace_size(desc, total_rows, max_ctx, num_seqs)
+ *   exceeds the array is refused with CP_ERR_WORKSPACE before anything is
+ *   enqueued.
+ *   The first call on a device looks up the array's device address (once per
+ *   device, with that device current); make that first call before any stream
+ *   capture on that device.
+ *   Every call uses the same array, which keeps the last call's contents (the
+ *   kernels write every entry before reading it, so nothing needs clearing).
+ *   Calls whose work overlaps on the GPU -- on different streams or from
+ *   different host threads -- race on the array; the caller must serialise
+ *   them. */
+int cp_mixed_step_noalloc(const cp_layer_desc* desc, const void* q, const void* k_new,
+                          const void* v_new, void* k_pages, void* v_pages,
+                          const int32_t* block_table, const int32_t* cu_rows, int32_t* past_len,
+                          int32_t num_seqs, int32_t total_rows, int32_t max_ctx, void* out,
+                          int32_t* dev_status, void* stream);
+
+/* cp_noalloc_scratch_bytes -- size of the fixed scratch array used by
+ * cp_mixed_step_noalloc (no GPU work). */
+size_t cp_noalloc_scratch_bytes(void);
+
 /* cp_workspace_size -- bytes of device scratch the two attention calls need
  * for up to `max_rows` query rows, contexts of up to `max_ctx` keys and
  * `num_seqs` sequences (split-KV partial results and the work list). */
