@@ -87,8 +87,11 @@ struct TcSmem {
   static constexpr uint32_t bar_off = v_off + kStages * DB * kBlockBytes;
   static constexpr uint32_t bytes = bar_off + sizeof(TcBarriers);
   static constexpr uint32_t alloc = bytes + 1024;  // slack for 1024-byte alignment
-  // After the main loop the K stages hold the peer's partial O rows [128][D] fp32.
-  static_assert(kStages * DB * kBlockBytes >= 128u * D * 4u, "merge buffer does not fit");
+  // After the main loop the K and V stages hold the peer's partial O rows:
+  // [128][kMergeStride] fp32, padded so a quarter-warp's row accesses cover all
+  // shared-memory banks.
+  static constexpr uint32_t kMergeStride = D + 4;
+  static_assert(2 * kStages * DB * kBlockBytes >= 128u * kMergeStride * 4u, "merge buffer does not fit");
 };
 
 template <typename T>
@@ -174,6 +177,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int n_valid = rolling ? nkeys : n;  // key indices holding written data
   const int ntiles = (nkeys + kTcBlockN - 1) / kTcBlockN;
   const int nmine = ntiles > rank ? (ntiles - rank + 1) / 2 : 0;  // this CTA's KV tiles: rank + 2i
+  const bool q1 = t0 + rpt < rows;  // Q tile 1 holds at least one row (else it is skipped)
 
   if (threadIdx.x == 0) {
     mbar_init(&bar->q_full, 1);
@@ -205,8 +209,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_desc(&tm_q);
       tma_prefetch_desc(&tm_k);
       tma_prefetch_desc(&tm_v);
-      mbar_arrive_expect_tx(&bar->q_full, 2 * DB * kBlockBytes);
-      for (int w = 0; w < 2; ++w)
+      mbar_arrive_expect_tx(&bar->q_full, (q1 ? 2 : 1) * DB * kBlockBytes);
+      for (int w = 0; w < (q1 ? 2 : 1); ++w)
         for (int db = 0; db < DB; ++db)
           tma_load_3d(sQ + (w * DB + db) * kBlockBytes, &tm_q, &bar->q_full, db * 64, g * G, row0 + t0 + w * rpt);
     }
@@ -297,7 +301,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (ok) {
         tc_fence_after();
         issue_qk(0, 0);
-        issue_qk(1, 0);
+        if (q1) issue_qk(1, 0);
       }
       for (int i = 0; ok && i < nmine; ++i) {
         const bool more = i + 1 < nmine;
@@ -320,11 +324,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!wait(&bar->kv_full[(i + 1) & 1], ((i + 1) >> 1) & 1)) break;
           issue_qk(0, i + 1);
         }
-        if (!wait(&bar->p_ready[1], i & 1)) break;
-        tc_fence_after();
-        issue_pv(1, i);
+        if (q1) {
+          if (!wait(&bar->p_ready[1], i & 1)) break;
+          tc_fence_after();
+          issue_pv(1, i);
+        }
         mma_commit(&bar->kv_empty[i & 1]);
-        if (more) issue_qk(1, i + 1);
+        if (more && q1) issue_qk(1, i + 1);
       }
       // o_final: every MMA issued has completed (epilogue and TMEM release wait on it).
       mma_commit(&bar->o_final);
@@ -348,7 +354,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   float m_run = -INFINITY;  // max used for exponentiation (log2 domain)
   float l_run = 0.f;
   bool alive = true;
-  if (is_softmax) {
+  if (is_softmax && (grp == 0 || q1)) {
     const int p_row = row_ok ? past + tok : -1;  // absolute query position
     const int lo = rolling ? max(a.left_pad ? a.left_pad[s] : 0, 0) : 0;
     // Rolling: slot -> absolute position (see cp_kv.cuh), split at slot r_slot.
@@ -438,14 +444,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   cluster_sync_all();  // #1: both CTAs are past their main loops
   tc_fence_after();
   const bool have_o = nmine > 0;  // this CTA wrote O (else its TMEM O is unset: send zeros)
-  if (is_softmax && grp != rank) {
+  constexpr uint32_t kStride = L::kMergeStride;
+  if (is_softmax && grp != rank && (grp == 0 || q1)) {
     // Rows of Q tile (1 - rank) are finished by the peer: send this CTA's partial.
     const uint32_t peer = (uint32_t)(1 - rank);
     const uint32_t pm = mapa_shared(smem_u32(&bar->peer_m[mrow]), peer);
     const uint32_t pl = mapa_shared(smem_u32(&bar->peer_l[mrow]), peer);
     st_cluster_f32(pm, have_o ? m_run : -INFINITY);
     st_cluster_f32(pl, have_o ? l_run : 0.f);
-    const uint32_t po = mapa_shared(smem_u32(sK + (uint32_t)mrow * D * 4u), peer);
+    const uint32_t po = mapa_shared(smem_u32(sK + (uint32_t)mrow * kStride * 4u), peer);
 #pragma unroll
     for (int c = 0; c < D / 32; ++c) {
       uint32_t ov[32];
@@ -462,9 +469,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
   cluster_sync_all();  // #2: the peer's partial for this CTA's rows is in place
-  if (is_softmax && grp == rank) {
+  if (is_softmax && grp == rank && (grp == 0 || q1)) {
     // Fixed order: the even-tile half (rank 0's partial) first.
-    const float* peer_o = reinterpret_cast<const float*>(sK + (uint32_t)mrow * D * 4u);
+    const float* peer_o = reinterpret_cast<const float*>(sK + (uint32_t)mrow * kStride * 4u);
     const float m_own = have_o ? m_run : -INFINITY, l_own = have_o ? l_run : 0.f;
     const float m_peer = bar->peer_m[mrow], l_peer = bar->peer_l[mrow];
     const float mA = rank == 0 ? m_own : m_peer, lA = rank == 0 ? l_own : l_peer;
@@ -490,7 +497,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
           const float own0 = __uint_as_float(ov[2 * e]), own1 = __uint_as_float(ov[2 * e + 1]);
-          const float pr0 = peer_o[c * 32 + 2 * e], pr1 = peer_o[c * 32 + 2 * e + 1];
+          const float2 pr = *reinterpret_cast<const float2*>(peer_o + c * 32 + 2 * e);
+          const float pr0 = pr.x, pr1 = pr.y;
           const float x0 = rank == 0 ? own0 * wA + pr0 * wB : pr0 * wA + own0 * wB;
           const float x1 = rank == 0 ? own1 * wA + pr1 * wB : pr1 * wA + own1 * wB;
           pk[e] = pack2<T>(x0 * inv, x1 * inv);
