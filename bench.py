@@ -83,13 +83,23 @@ def barrier(world):
 
 
 def max_over_ranks(x, world):
+    """The largest value of x over all ranks (the slowest rank's time)."""
     if world == 1:
         return x
     import torch
     import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def job_throughput(local_ms, units_per_step, steps, world):
+    """Whole-job throughput of `world` replicas: every rank processes
+    `units_per_step` units per step, the job takes as long as the slowest rank.
+    Returns (max_ms_over_ranks, units per second over all ranks)."""
+    total_ms = max_over_ranks(local_ms, world)
+    return total_ms, world * units_per_step * steps / (total_ms / 1e3)
 
 
 # --------------------------------------------------------------------------- clocks
@@ -366,9 +376,8 @@ def run_native(args):
     clk = clocks.stop()
     torch.cuda.synchronize()
     barrier(world)
-    total_ms = max_over_ranks(sum(times), world)
+    total_ms, value = job_throughput(sum(times), wl.tokens, args.steps, world)
     ms_per_step = total_ms / args.steps
-    value = world * wl.tokens * args.steps / (total_ms / 1e3)
 
     # ---- kernel-level timing of the attention kernel (per chunk, same state as in the step)
     reps = 20
@@ -399,8 +408,7 @@ def run_native(args):
         e2e_step()
     torch.cuda.synchronize()
     e2e_times = time_steps(e2e_step, flush, e2e_steps, torch)
-    e2e_total = max_over_ranks(sum(e2e_times), world)
-    e2e_value = world * wl.tokens * e2e_steps / (e2e_total / 1e3)
+    _, e2e_value = job_throughput(sum(e2e_times), wl.tokens, e2e_steps, world)
     if int(wl.status.item()) != 0:
         raise RuntimeError(f"device status {int(wl.status.item())}")
 
