@@ -156,12 +156,20 @@ def test_query_padding_ladder(idx):
         assert np.abs(oo[p] - oracle.attention_row(qq[p], kk, vv, int(p))).max() < BF16_TOL
 
 
-def test_decode_row_through_prefill_call():
-    """A one-row chunk (a decode step) over a long contiguous context takes the
-    split-KV path and matches the oracle."""
-    n = 3000
-    q, k, v = SI.gqa_prompt(n, seed=9)
-    cache = Contig(torch.bfloat16, 32, 8, 128, cap=4096)
+@pytest.mark.parametrize("n,hq,hkv,d,dtype", [
+    (3000, 32, 8, 128, torch.bfloat16),  # GQA 4, several 512-key splits and a ragged last one
+    (1, 32, 8, 128, torch.bfloat16),     # first token: the row sees only itself
+    (1537, 16, 2, 128, torch.bfloat16),  # GQA 8, one key past a split boundary
+    (700, 8, 4, 64, torch.float16),      # GQA 2, head_dim 64
+    (512, 8, 8, 64, torch.float16),      # MHA, exactly one split
+    (900, 16, 1, 64, torch.bfloat16),    # GQA 16 (goes to the tensor-core kernel)
+])
+def test_decode_row_through_prefill_call(n, hq, hkv, d, dtype):
+    """A one-row chunk (a decode step) over a contiguous context takes the
+    split-KV path (the tensor-core path for groups wider than 8) and matches
+    the oracle."""
+    q, k, v = SI.gqa_prompt(n, seed=9 + n, hq=hq, hkv=hkv, dim=d, dtype=dtype)
+    cache = Contig(dtype, hq, hkv, d, cap=((n + 127) // 128 + 1) * 128)
     cache.k[0, :, :n - 1] = k[:n - 1].permute(1, 0, 2).cuda()
     cache.v[0, :, :n - 1] = v[:n - 1].permute(1, 0, 2).cuda()
     cache.lens.fill_(n - 1)
@@ -169,6 +177,7 @@ def test_decode_row_through_prefill_call():
     torch.cuda.synchronize()
     ref = oracle.attention_row(f64(q[n - 1]), f64(k), f64(v), n - 1)
     assert np.abs(f64(out[0, 0]) - ref).max() < BF16_TOL
+    assert torch.equal(cache.k[0, :, :n].cpu(), k.permute(1, 0, 2))
     assert int(cache.status.item()) == 0
 
 
