@@ -109,7 +109,11 @@ __device__ __forceinline__ uint32_t pack2<__half>(float lo, float hi) {
 
 // Which (sequence, first token) a cluster owns; a pair covers 2*rpt tokens.
 // Within a sequence the pairs are handed out last-first, so the pairs with
-// the most keys start earliest.
+// the most keys start earliest.  Every warp of the CTA calls this with all
+// lanes: for ragged rows each warp scans the sequences 32 at a time (one
+// coalesced round of loads per 32 sequences, a shuffle prefix sum of their
+// pair counts), so the lookup costs a few memory latencies, not one per
+// sequence.
 __device__ __forceinline__ bool find_pair(const AttnArgs& a, int ppt, int w, int& s, int& t0) {
   if (a.rows.rows_uniform > 0) {
     const int np = (a.rows.rows_uniform + ppt - 1) / ppt;
@@ -119,16 +123,30 @@ __device__ __forceinline__ bool find_pair(const AttnArgs& a, int ppt, int w, int
     t0 = pair * ppt;
     return true;
   }
-  for (int q = 0; q < a.rows.num_seqs; ++q) {
-    const int r = seq_rows(a.rows, q);
-    if (r < a.min_rows) continue;
-    const int np = (r + ppt - 1) / ppt;
-    if (w < np) {
-      s = q;
-      t0 = (np - 1 - w) * ppt;
+  const int lane = threadIdx.x & 31;
+  for (int q0 = 0; q0 < a.rows.num_seqs; q0 += 32) {
+    const int q = q0 + lane;
+    int np = 0;
+    if (q < a.rows.num_seqs) {
+      const int r = seq_rows(a.rows, q);
+      np = r < a.min_rows ? 0 : (r + ppt - 1) / ppt;
+    }
+    int inc = np;  // inclusive prefix sum over the lanes
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, inc, o);
+      if (lane >= o) inc += v;
+    }
+    const int tot = __shfl_sync(0xffffffffu, inc, 31);
+    if (w < tot) {
+      const int L = __ffs(__ballot_sync(0xffffffffu, inc > w)) - 1;
+      const int before = __shfl_sync(0xffffffffu, inc - np, L);
+      const int npl = __shfl_sync(0xffffffffu, np, L);
+      s = q0 + L;
+      t0 = (npl - 1 - (w - before)) * ppt;
       return true;
     }
-    w -= np;
+    w -= tot;
   }
   return false;
 }

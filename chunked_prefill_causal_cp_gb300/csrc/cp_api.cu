@@ -68,9 +68,13 @@ float scale_log2(const cp_layer_desc* d) {
 
 int64_t max_splits_for(int32_t max_ctx) { return ((int64_t)max_ctx + kDecodeSplit - 1) / kDecodeSplit; }
 
+// Decode workspace: the persistent grid's work counter (its own 256 bytes),
+// then the split partials (output rows, then max and sum).
+constexpr int64_t kDecodeCounterBytes = 256;
+
 int64_t decode_ws_bytes(const cp_layer_desc* d, int32_t max_ctx, int32_t num_seqs) {
   const int64_t ms = max_splits_for(max_ctx);
-  return (int64_t)num_seqs * d->num_q_heads * ms * (d->head_dim + 2) * (int64_t)sizeof(float);
+  return kDecodeCounterBytes + (int64_t)num_seqs * d->num_q_heads * ms * (d->head_dim + 2) * (int64_t)sizeof(float);
 }
 
 // ---- tensor maps (driver entry point fetched through the runtime)
@@ -148,10 +152,11 @@ int run_attention(const cp_layer_desc* d, const AttnArgs& base, int64_t rows_tot
     const int64_t need = decode_ws_bytes(d, a.max_ctx, a.rows.num_seqs);
     if (workspace == nullptr || (int64_t)ws_bytes < need) return CP_ERR_WORKSPACE;
     AttnArgs dec = a;
-    dec.part_o = static_cast<float*>(workspace);
+    int* counter = static_cast<int*>(workspace);
+    dec.part_o = reinterpret_cast<float*>(static_cast<char*>(workspace) + kDecodeCounterBytes);
     dec.max_splits = (int)max_splits_for(a.max_ctx);
     dec.part_ml = dec.part_o + (int64_t)a.rows.num_seqs * d->num_q_heads * dec.max_splits * d->head_dim;
-    const int r = launch_result(launch_decode(dec, d->dtype, st));
+    const int r = launch_result(launch_decode(dec, d->dtype, counter, st));
     if (r != CP_OK) return r;
   }
   if (any_multi || !decode_ok) {
@@ -271,7 +276,7 @@ int cp_prefill_chunk_attn(const cp_layer_desc* desc, const void* q, const void* 
   a.status = dev_status;
   r = run_attention(desc, a, rows_total, rows_padded, k_cache, v_cache, desc->batch, workspace, workspace_bytes, st);
   if (r != CP_OK) return r;
-  if (commit) return launch_result(launch_commit(seqlens_k, a.rows, real_rows, st));
+  if (commit) return launch_result(launch_commit(seqlens_k, a.rows, real_rows, nullptr, st));
   return CP_OK;
 }
 
@@ -326,9 +331,14 @@ int cp_mixed_step(const cp_layer_desc* desc, const void* q, const void* k_new, c
   a.v = v_pages;
   a.out = out;
   a.status = dev_status;
-  r = run_attention(desc, a, total_rows, total_rows, k_pages, v_pages, 0, workspace, workspace_bytes, st);
+  // Every listed sequence has at least one row, so none has more than
+  // total_rows - num_seqs + 1; with one row each the tensor-core path has no
+  // work and is not launched.
+  const int64_t max_rows_per_seq = total_rows >= num_seqs ? (int64_t)total_rows - num_seqs + 1 : total_rows;
+  r = run_attention(desc, a, total_rows, (int)max_rows_per_seq, k_pages, v_pages, 0, workspace, workspace_bytes,
+                    st);
   if (r != CP_OK) return r;
-  return launch_result(launch_commit(past_len, rows, -1, st));
+  return launch_result(launch_commit(past_len, rows, -1, dev_status, st));
 }
 
 }  // extern "C"

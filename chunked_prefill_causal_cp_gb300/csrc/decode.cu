@@ -31,9 +31,11 @@
 namespace cp {
 namespace {
 
-constexpr int kDecConsumers = 4;            // consumer warps per CTA (plus one producer warp)
-constexpr int kDecStageKeys = 32;           // K or V rows per ring stage
-constexpr int kDecRingBytes = 48 * 1024;    // ring of stages: 6 stages at D = 128, 12 at D = 64
+constexpr int kDecConsumers = 8;     // consumer warps per CTA (plus one producer warp)
+constexpr int kDecCtasPerSm = 2;     // resident CTAs per SM of the persistent grid
+constexpr int kDecStageBytes = 8192; // one ring stage: 32 rows at D = 128, 64 at D = 64
+constexpr int kDecStages = 9;        // ring depth
+constexpr int kDecSlots = 3;         // resolved items held ahead of the consumers
 
 template <typename T>
 __device__ __forceinline__ T from_float(float x);
@@ -66,23 +68,42 @@ __device__ __forceinline__ void ffma2v(float2& a, float2 b, float2 c) {
 // Shared-memory plan of decode_split_kernel<T, D, H>.
 template <int D, int H>
 struct DecSmem {
-  static constexpr int kRow = D * 2;                       // bytes of one K or V row
-  static constexpr int kStageBytes = kDecStageKeys * kRow;
-  static constexpr int kStages = kDecRingBytes / kStageBytes;
-  static constexpr int ring = 0;
-  static constexpr int full = ring + kDecRingBytes;        // uint64 [kStages]
-  static constexpr int empty = full + 8 * kStages;         // uint64 [kStages]
-  static constexpr int off = empty + 8 * kStages;          // long long [kDecodeSplit]
-  static constexpr int sc = off + 8 * kDecodeSplit;        // float [H][kDecodeSplit]
-  static constexpr int ml = sc + 4 * H * kDecodeSplit;     // float [2][H]
-  static constexpr int flags = ml + 8 * H;                 // int abort, bad
-  static constexpr int bytes = flags + 16;
-  static_assert(kDecConsumers * H * D * 4 <= kDecRingBytes, "reduction buffer aliases the ring");
+  static constexpr int kRow = D * 2;                        // bytes of one K or V row
+  static constexpr int kStageRows = kDecStageBytes / kRow;  // 32 (D = 128) or 64 (D = 64)
+  static constexpr int ring = 0;                                      // [kDecStages][kDecStageBytes]
+  static constexpr int q = ring + kDecStages * kDecStageBytes;        // 16-bit [kDecSlots][H][D]
+  static constexpr int rows = q + kDecSlots * H * D * 2;              // uint32 [kDecSlots][kDecodeSplit]
+  static constexpr int pages = rows + kDecSlots * 4 * kDecodeSplit;   // int [kDecodeSplit + 1] (resolver)
+  static constexpr int sc = pages + 4 * (kDecodeSplit + 4);           // float [H][kDecodeSplit]
+  static constexpr int red = sc + 4 * H * kDecodeSplit;               // float [kDecConsumers][H][D]
+  static constexpr int bars = red + 4 * kDecConsumers * H * D;        // uint64 full, empty, ready, freed
+  static constexpr int items = bars + 8 * (2 * kDecStages + 2 * kDecSlots);  // int [kDecSlots][2]
+  static constexpr int misc = items + 8 * kDecSlots;                  // int bad[kDecSlots], abort
+  static constexpr int ml = misc + 4 * (kDecSlots + 1);               // float m[H], l[H]
+  static constexpr int bytes = ml + 8 * H;
+  static_assert(kDecCtasPerSm * (bytes + 1024) <= 228 * 1024, "two CTAs per SM");
 };
+
+// Row index (in rows of D elements) of an invalid key: never copied.
+constexpr uint32_t kNoRow = 0xffffffffu;
 
 __device__ __forceinline__ void consumers_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kDecConsumers * 32) : "memory"); }
 
-// Row j of a staged tile, as the two 16-byte chunks c0 = sub and c1 = sub + LPK.
+// Named barrier over the consumer warps that also ORs a predicate across them.
+__device__ __forceinline__ bool consumers_sync_or(bool p) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred pi, po;\n\t"
+      "setp.ne.u32 pi, %1, 0;\n\t"
+      "bar.red.or.pred po, 1, %2, pi;\n\t"
+      "selp.u32 %0, 1, 0, po;\n\t}"
+      : "=r"(r)
+      : "r"((uint32_t)p), "n"(kDecConsumers * 32)
+      : "memory");
+  return r != 0;
+}
+
+// Row of a staged tile, as the two 16-byte chunks c0 = sub and c1 = sub + LPK.
 __device__ __forceinline__ void lds_row(const unsigned char* row, int sub, int lpk, uint32_t (&w)[8]) {
   const uint4 a = *reinterpret_cast<const uint4*>(row + sub * 16);
   const uint4 b = *reinterpret_cast<const uint4*>(row + (sub + lpk) * 16);
@@ -90,217 +111,346 @@ __device__ __forceinline__ void lds_row(const unsigned char* row, int sub, int l
   w[4] = b.x; w[5] = b.y; w[6] = b.z; w[7] = b.w;
 }
 
-// One CTA per (split of kDecodeSplit keys, H query heads of one KV group,
-// sequence).  Warp kDecConsumers is the producer: it resolves the split's key
-// rows to cache offsets once, then streams the split's K rows and then its V
-// rows through a ring of kDecStageKeys-row stages with bulk copies (one copy
-// per run of contiguous rows: a whole stage for a contiguous cache, one page
-// per copy for a paged one), so the bytes in flight are bounded by shared
-// memory, not by registers.  Warps 0..kDecConsumers-1 consume: a group of
-// LPK = D/16 lanes takes one row, 16 elements per lane (chunks sub and
-// sub+LPK, so a quarter-warp reads 128 contiguous bytes), with packed fp32x2
-// FMAs; scores go to shared memory, the split's max and sum are taken in the
-// log2 domain, then the V stages are consumed and the unnormalised partial
-// output written.
-template <typename T, int D, int H>
-__global__ void __launch_bounds__((kDecConsumers + 1) * 32) decode_split_kernel(const AttnArgs a) {
-  using L = DecSmem<D, H>;
-  constexpr int LPK = D / 16;                 // lanes per row
-  constexpr int KPW = 32 / LPK;               // rows per warp per pass
-  constexpr int KPP = kDecConsumers * KPW;    // rows per pass
-  constexpr int PASSES = kDecStageKeys / KPP;
-  constexpr int NST = L::kStages;
-  static_assert(kDecStageKeys % KPP == 0 && kDecStageKeys == 32, "one producer lane per staged row");
-  extern __shared__ __align__(128) unsigned char smem[];
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::full);
-  uint64_t* empty = reinterpret_cast<uint64_t*>(smem + L::empty);
-  long long* s_off = reinterpret_cast<long long*>(smem + L::off);
-  float (*sc)[kDecodeSplit] = reinterpret_cast<float (*)[kDecodeSplit]>(smem + L::sc);
-  float* s_m = reinterpret_cast<float*>(smem + L::ml);
-  float* s_l = s_m + H;
-  volatile int* s_abort = reinterpret_cast<volatile int*>(smem + L::flags);
-  volatile int* s_bad = s_abort + 1;
+// A work item: one split of kDecodeSplit keys, for H query heads of one KV
+// group of one decode sequence.  Ids run sequence-major, then split, then
+// head block, so the H-head blocks of one split are neighbours (a group of 8
+// heads takes two blocks that read the same rows close together in time, the
+// second mostly from L2), and a sequence's empty splits (those past its
+// length) are the tail of its id range, which a claim skips in one step.
+struct DecItem {
+  int s, split, hb, nk;
+};
 
-  const int split = blockIdx.x, hb = blockIdx.y, s = blockIdx.z;
-  if (seq_rows(a.rows, s) != 1) return;
-  const int past = a.past[s];
+__device__ __forceinline__ void dec_ids(const AttnArgs& a, int id, int nhb, DecItem& it) {
+  it.hb = id % nhb;
+  it.split = (id / nhb) % a.max_splits;
+  it.s = (id / nhb) / a.max_splits;
+}
+
+__device__ __forceinline__ bool dec_item(const AttnArgs& a, int id, int nhb, DecItem& it) {
+  dec_ids(a, id, nhb, it);
+  if (seq_rows(a.rows, it.s) != 1) return false;
+  const int past = a.past[it.s];
   const int n = past + 1;
   if (past < 0 || n > a.max_ctx) {
-    if (a.status && threadIdx.x == 0 && split == 0 && hb == 0) atomicOr(a.status, CP_DEV_BOUNDS);
-    return;
+    if (a.status && it.split == 0 && it.hb == 0) atomicOr(a.status, CP_DEV_BOUNDS);
+    return false;
   }
-  const int k0 = split * kDecodeSplit;
-  if (k0 >= n) return;
-  const int nk = min(n - k0, kDecodeSplit);
-  const int nt = (nk + kDecStageKeys - 1) / kDecStageKeys;  // stages per phase
-  const int h0 = hb * H;                                    // first query head
-  const int g = h0 / a.group;                               // its KV head
+  const int k0 = it.split * kDecodeSplit;
+  if (k0 >= n) return false;
+  it.nk = min(n - k0, kDecodeSplit);
+  return true;
+}
 
+// Persistent split-KV decode: kDecCtasPerSm CTAs per SM, each with
+// kDecConsumers consumer warps, an issuer warp and a resolver warp.
+//
+// The resolver claims work items from a device counter (lane 0, one atomic
+// per claim, the next claim issued ahead; a claim that lands on a sequence's
+// empty tail moves the counter to the next sequence), reads the sequence's
+// length and page table, and writes the item's row indices into one of
+// kDecSlots item slots, up to kDecSlots items ahead of the consumers, so the
+// latency of those reads is off the copy path.  The issuer streams each
+// resolved item's q heads, then its K rows, then its V rows through a ring of
+// kDecStages stages with bulk copies: one copy per run of contiguous rows (a
+// whole stage for a contiguous cache, one page per copy for a paged one).  It
+// runs across item boundaries without a gap, so the ring stays full and the
+// bytes in flight are bounded by shared memory, not registers.  After the last
+// item both pass a sentinel that ends the consumers.
+//
+// In the K phase the consumers take a row per group of LPK = D/16 lanes, 16
+// elements per lane (chunks sub and sub + LPK, so a quarter-warp reads 128
+// contiguous bytes), with packed fp32x2 FMAs; scores go to shared memory, the
+// split's max and sum are taken in the log2 domain, the V stages are
+// accumulated with D/8 lanes per row (half the accumulator registers),
+// warps' partial sums are added in a fixed order and the unnormalised partial
+// output is written for the combine kernel.
+template <typename T, int D, int H>
+__global__ void __launch_bounds__((kDecConsumers + 2) * 32, kDecCtasPerSm)
+    decode_split_kernel(const AttnArgs a, int* counter) {
+  using L = DecSmem<D, H>;
+  constexpr int LPK = D / 16;               // lanes per row (K phase)
+  constexpr int KPW = 32 / LPK;             // rows per warp per stage
+  constexpr int SR = L::kStageRows;
+  constexpr int NST = kDecStages;
+  constexpr int NSL = kDecSlots;
+  static_assert(kDecConsumers * KPW == SR, "one pass of the consumers covers a stage");
+  static_assert(SR % 32 == 0, "the issuer covers a stage in rounds of 32 rows");
+  constexpr int LPV = D / 8;                // lanes per row in the V phase
+  constexpr int RPW = 32 / LPV;             // rows per warp per V pass
+  constexpr int VPASS = SR / (kDecConsumers * RPW);
+  static_assert(VPASS * kDecConsumers * RPW == SR, "V passes cover a stage");
+  extern __shared__ __align__(128) unsigned char smem[];
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::bars);
+  uint64_t* empty = full + NST;
+  uint64_t* ready = empty + NST;
+  uint64_t* freed = ready + NSL;
+  int* s_items = reinterpret_cast<int*>(smem + L::items);
+  int* s_bad = reinterpret_cast<int*>(smem + L::misc);
+  volatile int* s_abort = s_bad + NSL;
+  float* s_m = reinterpret_cast<float*>(smem + L::ml);
+  float* s_l = s_m + H;
+
+  const int nhb = a.hq / H;
+  const int total = a.max_splits * a.rows.num_seqs * nhb;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     for (int i = 0; i < NST; ++i) {
       mbar_init(&full[i], 1);
       mbar_init(&empty[i], kDecConsumers);
     }
+    for (int i = 0; i < NSL; ++i) {
+      mbar_init(&ready[i], 1);
+      mbar_init(&freed[i], kDecConsumers);
+    }
     *s_abort = 0;
-    *s_bad = 0;
     fence_barrier_init();
   }
   __syncthreads();
 
-  if (warp == kDecConsumers) {
-    // ------------------------------------------------ producer warp
-    bool bad = false;
-    for (int kk = lane; kk < nk; kk += 32) {
-      const long long off = key_offset(a.cache, a.hkv, D, s, g, k0 + kk);
-      s_off[kk] = off;
-      bad |= off < 0;
-    }
-    if (__any_sync(0xffffffffu, bad)) {
+  if (warp == kDecConsumers + 1) {
+    // ------------------------------------------------ resolver warp
+    int* s_pg = reinterpret_cast<int*>(smem + L::pages);
+    int next = lane == 0 ? atomicAdd(counter, 1) : 0;
+    for (int j = 0;; ++j) {
+      const int sl = j % NSL;
+      DecItem it;
+      int id;
+      for (;;) {
+        id = __shfl_sync(0xffffffffu, next, 0);
+        if (id >= total) break;
+        if (lane == 0) next = atomicAdd(counter, 1);
+        if (dec_item(a, id, nhb, it)) break;
+        // Every later id of this sequence is empty too: move the counter past them.
+        if (lane == 0) atomicMax(counter, (it.s + 1) * a.max_splits * nhb);
+      }
+      if (j >= NSL && !warp_wait(&freed[sl], ((j - NSL) / NSL) & 1, s_abort, a.status)) return;
+      if (id >= total) {  // sentinel
+        if (lane == 0) {
+          s_items[sl * 2] = -1;
+          mbar_arrive(&ready[sl]);
+        }
+        return;
+      }
+      const int g = (it.hb * H) / a.group, k0 = it.split * kDecodeSplit;
+      uint32_t* rows = reinterpret_cast<uint32_t*>(smem + L::rows) + sl * kDecodeSplit;
+      bool bad = false;
+      if (a.cache.kind == CP_CACHE_PAGED) {
+        // The item's page ids first (one load per page, all in flight together),
+        // then each row from its page.
+        const int ps = a.cache.page_size;
+        const int b0 = k0 / ps, nb = (k0 + it.nk - 1) / ps - b0 + 1;
+        for (int b = lane; b < nb; b += 32) {
+          const int blk = b0 + b;
+          int pg = -1;
+          if (blk < a.cache.max_blocks) pg = a.cache.block_table[(long long)it.s * a.cache.max_blocks + blk];
+          s_pg[b] = (pg >= 0 && pg < a.cache.num_pages) ? pg : -1;
+        }
+        __syncwarp();
+        for (int kk = lane; kk < it.nk; kk += 32) {
+          const int jj = k0 + kk;
+          const int pg = s_pg[jj / ps - b0];
+          rows[kk] = pg < 0 ? kNoRow : (uint32_t)(((long long)pg * a.hkv + g) * ps + jj % ps);
+          bad |= pg < 0;
+        }
+        __syncwarp();
+      } else {
+        const uint32_t base = (uint32_t)(((long long)it.s * a.hkv + g) * a.cache.capacity + k0);
+        for (int kk = lane; kk < it.nk; kk += 32) rows[kk] = base + kk;
+      }
+      bad = __any_sync(0xffffffffu, bad);
       if (lane == 0) {
-        *s_bad = 1;
-        if (a.status) atomicOr(a.status, CP_DEV_BOUNDS);
+        s_bad[sl] = bad ? 1 : 0;
+        if (bad && a.status) atomicOr(a.status, CP_DEV_BOUNDS);
+        s_items[sl * 2] = id;
+        s_items[sl * 2 + 1] = it.nk;
       }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&ready[sl]);
     }
-    __syncwarp();
-    const unsigned char* base[2] = {static_cast<const unsigned char*>(a.k), static_cast<const unsigned char*>(a.v)};
-    int issued = 0;
-    for (int t = 0; t < 2 * nt; ++t) {
-      const int st = t % NST, use = t / NST;
-      if (use > 0 && !warp_wait(&empty[st], (use - 1) & 1, s_abort, a.status)) break;
-      const int tl = t < nt ? t : t - nt;
-      const int kk = tl * kDecStageKeys + lane;
-      const long long off = kk < nk ? s_off[kk] : -1;
-      const bool valid = off >= 0;
-      const long long prev = __shfl_up_sync(0xffffffffu, off, 1);
-      const bool start = valid && (lane == 0 || prev < 0 || off != prev + D);
-      const uint32_t brk = __ballot_sync(0xffffffffu, start || !valid);
-      const uint32_t nvalid = __popc(__ballot_sync(0xffffffffu, valid));
-      if (lane == 0) mbar_expect_tx(&full[st], nvalid * L::kRow);
-      __syncwarp();
-      if (start) {
-        const uint32_t later = lane == 31 ? 0u : (brk >> (lane + 1));
-        const int len = later ? __ffs(later) : 32 - lane;
-        bulk_load(smem + L::ring + st * L::kStageBytes + lane * L::kRow,
-                  base[t < nt ? 0 : 1] + off * (long long)sizeof(T), len * L::kRow, &full[st]);
+  }
+
+  if (warp == kDecConsumers) {
+    // ------------------------------------------------ issuer warp
+    const unsigned char* kbase = static_cast<const unsigned char*>(a.k);
+    const unsigned char* vbase = static_cast<const unsigned char*>(a.v);
+    int t = 0;  // stages issued
+    for (int j = 0;; ++j) {
+      const int sl = j % NSL;
+      if (!warp_wait(&ready[sl], (j / NSL) & 1, s_abort, a.status)) break;
+      const int id = s_items[sl * 2];
+      if (id < 0) {  // sentinel stage: ends the consumers
+        const int st = t % NST, use = t / NST;
+        if (use > 0 && !warp_wait(&empty[st], (use - 1) & 1, s_abort, a.status)) break;
+        if (lane == 0) mbar_arrive(&full[st]);
+        ++t;
+        break;
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&full[st]);
-      issued = t + 1;
+      DecItem it;
+      dec_ids(a, id, nhb, it);
+      it.nk = s_items[sl * 2 + 1];
+      const uint32_t* rows = reinterpret_cast<const uint32_t*>(smem + L::rows) + sl * kDecodeSplit;
+      const int ntl = (it.nk + SR - 1) / SR;
+      bool alive = true;
+      for (int tt = 0; tt < 2 * ntl; ++tt, ++t) {
+        const int st = t % NST, use = t / NST;
+        if (use > 0 && !warp_wait(&empty[st], (use - 1) & 1, s_abort, a.status)) {
+          alive = false;
+          break;
+        }
+        const int tl = tt < ntl ? tt : tt - ntl;
+        const unsigned char* base = tt < ntl ? kbase : vbase;
+        unsigned char* stage = smem + L::ring + st * kDecStageBytes;
+#pragma unroll
+        for (int rd = 0; rd < SR / 32; ++rd) {
+          const int r = rd * 32 + lane;
+          const int kk = tl * SR + r;
+          const uint32_t row = kk < it.nk ? rows[kk] : kNoRow;
+          const bool valid = row != kNoRow;
+          const uint32_t prev = __shfl_up_sync(0xffffffffu, row, 1);
+          const bool start = valid && (lane == 0 || prev == kNoRow || row != prev + 1);
+          const uint32_t brk = __ballot_sync(0xffffffffu, start || !valid);
+          const uint32_t nvalid = __popc(__ballot_sync(0xffffffffu, valid));
+          if (lane == 0 && nvalid) mbar_expect_tx(&full[st], nvalid * L::kRow);
+          __syncwarp();
+          if (start) {
+            const uint32_t later = lane == 31 ? 0u : (brk >> (lane + 1));
+            const int len = later ? __ffs(later) : 32 - lane;
+            bulk_load(stage + r * L::kRow, base + (long long)row * L::kRow, len * L::kRow, &full[st]);
+          }
+        }
+        if (tt == 0 && lane == 0) {  // the item's q heads ride on its first stage
+          const T* q = static_cast<const T*>(a.q) + ((long long)seq_row0(a.rows, it.s) * a.hq + it.hb * H) * D;
+          mbar_expect_tx(&full[st], H * D * 2);
+          bulk_load(smem + L::q + sl * H * D * 2, q, H * D * 2, &full[st]);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&full[st]);
+      }
+      if (!alive) break;
     }
     // Let every issued copy land before the CTA can exit.
     if (lane == 0) {
-      for (int t = issued - NST < 0 ? 0 : issued - NST; t < issued; ++t)
-        if (!mbar_wait_drain(&full[t % NST], (t / NST) & 1) && a.status) atomicOr(a.status, CP_DEV_TIMEOUT);
+      for (int u = t - NST < 0 ? 0 : t - NST; u < t; ++u)
+        if (!mbar_wait_drain(&full[u % NST], (u / NST) & 1) && a.status) atomicOr(a.status, CP_DEV_TIMEOUT);
     }
     return;
   }
+  if (warp > kDecConsumers) return;
 
   // -------------------------------------------------- consumer warps
   const int sub = lane % LPK;
-  const int slot = warp * KPW + lane / LPK;
+  const int r = warp * KPW + lane / LPK;  // this lane's row within a stage (K phase)
+  const int subv = lane % LPV;
+  const int rv = warp * RPW + lane / LPV;  // this lane's row within a V pass
+  float (*sc)[kDecodeSplit] = reinterpret_cast<float (*)[kDecodeSplit]>(smem + L::sc);
+  float (*red)[H][D] = reinterpret_cast<float (*)[H][D]>(smem + L::red);
   bool ok = true;
+  int t = 0;
+  for (int j = 0;; ++j) {
+    const int sl = j % NSL;
+    ok = ok && warp_wait(&full[t % NST], (t / NST) & 1, s_abort, a.status);
+    const int id = ok ? s_items[sl * 2] : -1;
+    if (consumers_sync_or(!ok || id < 0)) break;
+    DecItem it;
+    dec_ids(a, id, nhb, it);
+    it.nk = s_items[sl * 2 + 1];
+    const int ntl = (it.nk + SR - 1) / SR;
+    const uint32_t* rows = reinterpret_cast<const uint32_t*>(smem + L::rows) + sl * kDecodeSplit;
+    const bool bad = s_bad[sl] != 0;
 
-  // q slices (chunks sub, sub + LPK) of the H heads, scaled into the log2 domain.
-  float2 qv[H][8];
-  {
-    const T* q = static_cast<const T*>(a.q) + ((long long)seq_row0(a.rows, s) * a.hq + h0) * D;
+    // q slices (chunks sub, sub + LPK) of the H heads, scaled into the log2 domain.
+    float2 qv[H][8];
+    {
+      const unsigned char* qs = smem + L::q + sl * H * D * 2;
 #pragma unroll
-    for (int h = 0; h < H; ++h) {
-      const uint4 r0 = *reinterpret_cast<const uint4*>(q + h * D + sub * 8);
-      const uint4 r1 = *reinterpret_cast<const uint4*>(q + h * D + (sub + LPK) * 8);
-      const uint32_t w[8] = {r0.x, r0.y, r0.z, r0.w, r1.x, r1.y, r1.z, r1.w};
-#pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        const float2 f = unpack2<T>(w[e]);
-        qv[h][e] = make_float2(f.x * a.scale_log2, f.y * a.scale_log2);
-      }
-    }
-  }
-
-  // ---- scores over the K stages
-  for (int t = 0; t < nt; ++t) {
-    const int st = t % NST;
-    ok = ok && warp_wait(&full[st], (t / NST) & 1, s_abort, a.status);
-    if (ok) {
-      const bool bad = *s_bad != 0;
-      const unsigned char* stage = smem + L::ring + st * L::kStageBytes;
-#pragma unroll
-      for (int p = 0; p < PASSES; ++p) {
-        const int r = p * KPP + slot;
-        const int kk = t * kDecStageKeys + r;
+      for (int h = 0; h < H; ++h) {
         uint32_t w[8];
-        lds_row(stage + r * L::kRow, sub, LPK, w);
-        float2 acc[H];
-#pragma unroll
-        for (int h = 0; h < H; ++h) acc[h] = make_float2(0.f, 0.f);
+        lds_row(qs + h * D * 2, sub, LPK, w);
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
-          const float2 kf = unpack2<T>(w[e]);
-#pragma unroll
-          for (int h = 0; h < H; ++h) ffma2v(acc[h], qv[h][e], kf);
+          const float2 f = unpack2<T>(w[e]);
+          qv[h][e] = make_float2(f.x * a.scale_log2, f.y * a.scale_log2);
         }
+      }
+    }
+
+    // ---- scores over the K stages
+    for (int tl = 0; tl < ntl; ++tl, ++t) {
+      const int st = t % NST;
+      if (tl > 0) ok = ok && warp_wait(&full[st], (t / NST) & 1, s_abort, a.status);
+      if (!ok) continue;
+      const int kk = tl * SR + r;
+      uint32_t w[8];
+      lds_row(smem + L::ring + st * kDecStageBytes + r * L::kRow, sub, LPK, w);
+      float2 acc[H];
 #pragma unroll
-        for (int h = 0; h < H; ++h) {
-          float v = acc[h].x + acc[h].y;
+      for (int h = 0; h < H; ++h) acc[h] = make_float2(0.f, 0.f);
 #pragma unroll
-          for (int o = LPK / 2; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-          if (sub == 0 && kk < nk) sc[h][kk] = (bad && s_off[kk] < 0) ? -INFINITY : v;
-        }
+      for (int e = 0; e < 8; ++e) {
+        const float2 kf = unpack2<T>(w[e]);
+#pragma unroll
+        for (int h = 0; h < H; ++h) ffma2v(acc[h], qv[h][e], kf);
+      }
+#pragma unroll
+      for (int h = 0; h < H; ++h) {
+        float v = acc[h].x + acc[h].y;
+#pragma unroll
+        for (int o = LPK / 2; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+        if (sub == 0 && kk < it.nk) sc[h][kk] = (bad && rows[kk] == kNoRow) ? -INFINITY : v;
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[st]);
     }
-  }
-  consumers_sync();
+    consumers_sync();
 
-  // ---- split max / sum per query head (log2 domain)
-  if (ok) {
-    for (int h = warp; h < H; h += kDecConsumers) {
-      float m = -INFINITY;
-      for (int kk = lane; kk < nk; kk += 32) m = fmaxf(m, sc[h][kk]);
+    // ---- split max / sum per query head (log2 domain)
+    if (ok) {
+      for (int h = warp; h < H; h += kDecConsumers) {
+        float m = -INFINITY;
+        for (int kk = lane; kk < it.nk; kk += 32) m = fmaxf(m, sc[h][kk]);
 #pragma unroll
-      for (int o = 16; o; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-      float l = 0.f;
-      for (int kk = lane; kk < nk; kk += 32) {
-        const float pr = (m == -INFINITY) ? 0.f : ex2_approx(sc[h][kk] - m);
-        sc[h][kk] = pr;
-        l += pr;
-      }
+        for (int o = 16; o; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+        float l = 0.f;
+        for (int kk = lane; kk < it.nk; kk += 32) {
+          const float pr = (m == -INFINITY) ? 0.f : ex2_approx(sc[h][kk] - m);
+          sc[h][kk] = pr;
+          l += pr;
+        }
 #pragma unroll
-      for (int o = 16; o; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
-      if (lane == 0) {
-        s_m[h] = m;
-        s_l[h] = l;
+        for (int o = 16; o; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
+        if (lane == 0) {
+          s_m[h] = m;
+          s_l[h] = l;
+        }
       }
     }
-  }
-  consumers_sync();
+    consumers_sync();
 
-  // ---- p . V over the V stages
-  float2 acc[H][8];
+    // ---- p . V over the V stages: a group of LPV = D/8 lanes per row, one
+    // 16-byte chunk per lane, so a quarter-warp again reads 128 contiguous bytes.
+    float2 acc[H][4];
 #pragma unroll
-  for (int h = 0; h < H; ++h)
+    for (int h = 0; h < H; ++h)
 #pragma unroll
-    for (int e = 0; e < 8; ++e) acc[h][e] = make_float2(0.f, 0.f);
-  for (int t = 0; t < nt; ++t) {
-    const int st = (nt + t) % NST;
-    ok = ok && warp_wait(&full[st], ((nt + t) / NST) & 1, s_abort, a.status);
-    if (ok) {
-      const bool bad = *s_bad != 0;
-      const unsigned char* stage = smem + L::ring + st * L::kStageBytes;
+      for (int e = 0; e < 4; ++e) acc[h][e] = make_float2(0.f, 0.f);
+    for (int tl = 0; tl < ntl; ++tl, ++t) {
+      const int st = t % NST;
+      ok = ok && warp_wait(&full[st], (t / NST) & 1, s_abort, a.status);
+      if (!ok) continue;
+      const unsigned char* stage = smem + L::ring + st * kDecStageBytes;
 #pragma unroll
-      for (int p = 0; p < PASSES; ++p) {
-        const int r = p * KPP + slot;
-        const int kk = t * kDecStageKeys + r;
-        if (kk < nk && !(bad && s_off[kk] < 0)) {
-          uint32_t w[8];
-          lds_row(stage + r * L::kRow, sub, LPK, w);
+      for (int p = 0; p < VPASS; ++p) {
+        const int row = p * kDecConsumers * RPW + rv;
+        const int kk = tl * SR + row;
+        if (kk < it.nk && !(bad && rows[kk] == kNoRow)) {
+          const uint4 c = *reinterpret_cast<const uint4*>(stage + row * L::kRow + subv * 16);
+          const uint32_t w[4] = {c.x, c.y, c.z, c.w};
           float2 pp[H];
 #pragma unroll
           for (int h = 0; h < H; ++h) pp[h] = make_float2(sc[h][kk], sc[h][kk]);
 #pragma unroll
-          for (int e = 0; e < 8; ++e) {
+          for (int e = 0; e < 4; ++e) {
             const float2 vf = unpack2<T>(w[e]);
 #pragma unroll
             for (int h = 0; h < H; ++h) ffma2v(acc[h][e], pp[h], vf);
@@ -310,44 +460,40 @@ __global__ void __launch_bounds__((kDecConsumers + 1) * 32) decode_split_kernel(
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[st]);
     }
-  }
-  // Sum the KPW row slots of the warp (lanes with the same `sub`).
-#pragma unroll
-  for (int h = 0; h < H; ++h)
-#pragma unroll
-    for (int e = 0; e < 8; ++e)
-#pragma unroll
-      for (int o = LPK; o < 32; o <<= 1) {
-        acc[h][e].x += __shfl_xor_sync(0xffffffffu, acc[h][e].x, o);
-        acc[h][e].y += __shfl_xor_sync(0xffffffffu, acc[h][e].y, o);
-      }
-  consumers_sync();  // every warp is done with the ring, which now holds the reduction
-  float (*red)[H][D] = reinterpret_cast<float (*)[H][D]>(smem + L::ring);
-  if (lane < LPK) {
+    // Sum the RPW row slots of the warp (lanes with the same `subv`).
 #pragma unroll
     for (int h = 0; h < H; ++h)
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        red[warp][h][sub * 8 + 2 * e] = acc[h][e].x;
-        red[warp][h][sub * 8 + 2 * e + 1] = acc[h][e].y;
-        red[warp][h][(sub + LPK) * 8 + 2 * e] = acc[h][e + 4].x;
-        red[warp][h][(sub + LPK) * 8 + 2 * e + 1] = acc[h][e + 4].y;
-      }
-  }
-  consumers_sync();
-  if (!ok || *s_abort) return;
-  const long long part_base = ((long long)s * a.hq + h0) * a.max_splits;
-  for (int i = threadIdx.x; i < H * D; i += kDecConsumers * 32) {
-    const int h = i / D, dd = i % D;
-    float v = 0.f;
+      for (int e = 0; e < 4; ++e)
 #pragma unroll
-    for (int w = 0; w < kDecConsumers; ++w) v += red[w][h][dd];
-    a.part_o[((part_base + (long long)h * a.max_splits) + split) * D + dd] = v;
-  }
-  if (threadIdx.x < H) {
-    const long long idx = (part_base + (long long)threadIdx.x * a.max_splits) + split;
-    a.part_ml[idx * 2 + 0] = s_m[threadIdx.x];
-    a.part_ml[idx * 2 + 1] = s_l[threadIdx.x];
+        for (int o = LPV; o < 32; o <<= 1) {
+          acc[h][e].x += __shfl_xor_sync(0xffffffffu, acc[h][e].x, o);
+          acc[h][e].y += __shfl_xor_sync(0xffffffffu, acc[h][e].y, o);
+        }
+    if (lane < LPV) {
+#pragma unroll
+      for (int h = 0; h < H; ++h)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) *reinterpret_cast<float2*>(&red[warp][h][subv * 8 + 2 * e]) = acc[h][e];
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&freed[sl]);  // done with this item's slot: q and row indices
+    consumers_sync();
+    if (!ok) continue;
+    const int h0 = it.hb * H;
+    const long long part_base = ((long long)it.s * a.hq + h0) * a.max_splits;
+    for (int i = threadIdx.x; i < H * D; i += kDecConsumers * 32) {
+      const int h = i / D, dd = i % D;
+      float v = 0.f;
+#pragma unroll
+      for (int w = 0; w < kDecConsumers; ++w) v += red[w][h][dd];
+      a.part_o[((part_base + (long long)h * a.max_splits) + it.split) * D + dd] = v;
+    }
+    if (threadIdx.x < H) {
+      const long long idx = (part_base + (long long)threadIdx.x * a.max_splits) + it.split;
+      a.part_ml[idx * 2 + 0] = s_m[threadIdx.x];
+      a.part_ml[idx * 2 + 1] = s_l[threadIdx.x];
+    }
   }
 }
 
@@ -375,7 +521,7 @@ __global__ void __launch_bounds__(D) decode_combine_kernel(const AttnArgs a) {
 }
 
 template <typename T, int D, int H>
-cudaError_t launch_decode_t(const AttnArgs& a, cudaStream_t st) {
+cudaError_t launch_decode_t(const AttnArgs& a, int* counter, cudaStream_t st) {
   constexpr int smem = DecSmem<D, H>::bytes;
   // The dynamic shared-memory limit is a per-device function attribute: raise
   // it once per device, so later calls (including ones being captured into a
@@ -390,8 +536,20 @@ cudaError_t launch_decode_t(const AttnArgs& a, cudaStream_t st) {
     if (e != cudaSuccess) return e;
     ready_mask.fetch_or(bit, std::memory_order_release);
   }
-  dim3 grid(a.max_splits, a.hq / H, a.rows.num_seqs);
-  decode_split_kernel<T, D, H><<<grid, (kDecConsumers + 1) * 32, smem, st>>>(a);
+  int sms = 0;
+  e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  const long long items = (long long)a.max_splits * a.rows.num_seqs * (a.hq / H);
+  if (items >= (1ll << 31) - (1ll << 20)) return cudaErrorInvalidValue;
+  // Row indices are 32-bit: the cache must hold fewer than 2^32 - 1 rows.
+  const long long cache_rows = a.cache.kind == CP_CACHE_PAGED
+                                   ? (long long)a.cache.num_pages * a.hkv * a.cache.page_size
+                                   : (long long)a.rows.num_seqs * a.hkv * a.cache.capacity;
+  if (cache_rows >= (long long)kNoRow) return cudaErrorInvalidValue;
+  const int grid = (int)(items < (long long)sms * kDecCtasPerSm ? items : (long long)sms * kDecCtasPerSm);
+  e = cudaMemsetAsync(counter, 0, sizeof(int), st);
+  if (e != cudaSuccess) return e;
+  decode_split_kernel<T, D, H><<<grid, (kDecConsumers + 2) * 32, smem, st>>>(a, counter);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   decode_combine_kernel<T, D><<<dim3(a.rows.num_seqs, a.hq), D, 0, st>>>(a);
@@ -401,12 +559,12 @@ cudaError_t launch_decode_t(const AttnArgs& a, cudaStream_t st) {
 // Query heads per CTA: the whole GQA group up to 4 (a group of 8 takes two
 // CTAs, which read the same K/V rows, the second mostly from L2).
 template <typename T, int D>
-cudaError_t launch_decode_d(const AttnArgs& a, cudaStream_t st) {
+cudaError_t launch_decode_d(const AttnArgs& a, int* counter, cudaStream_t st) {
   switch (a.group) {
-    case 1: return launch_decode_t<T, D, 1>(a, st);
-    case 2: return launch_decode_t<T, D, 2>(a, st);
+    case 1: return launch_decode_t<T, D, 1>(a, counter, st);
+    case 2: return launch_decode_t<T, D, 2>(a, counter, st);
     case 4:
-    case 8: return launch_decode_t<T, D, 4>(a, st);
+    case 8: return launch_decode_t<T, D, 4>(a, counter, st);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -418,11 +576,11 @@ bool decode_supported(int d, int group, int dtype) {
          (dtype == CP_BF16 || dtype == CP_F16);
 }
 
-cudaError_t launch_decode(const AttnArgs& a, int dtype, cudaStream_t st) {
+cudaError_t launch_decode(const AttnArgs& a, int dtype, int* counter, cudaStream_t st) {
   if (a.rows.num_seqs == 0 || a.max_splits == 0) return cudaSuccess;
-  if (dtype == CP_BF16) return a.d == 64 ? launch_decode_d<__nv_bfloat16, 64>(a, st)
-                                         : launch_decode_d<__nv_bfloat16, 128>(a, st);
-  return a.d == 64 ? launch_decode_d<__half, 64>(a, st) : launch_decode_d<__half, 128>(a, st);
+  if (dtype == CP_BF16) return a.d == 64 ? launch_decode_d<__nv_bfloat16, 64>(a, counter, st)
+                                         : launch_decode_d<__nv_bfloat16, 128>(a, counter, st);
+  return a.d == 64 ? launch_decode_d<__half, 64>(a, counter, st) : launch_decode_d<__half, 128>(a, counter, st);
 }
 
 }  // namespace cp

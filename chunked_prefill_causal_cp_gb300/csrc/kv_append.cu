@@ -82,10 +82,15 @@ __global__ void pad_rows_kernel(char* base, int batch, int rows_padded, int real
   reinterpret_cast<uint4*>(dst)[vec] = reinterpret_cast<const uint4*>(src)[vec];
 }
 
-__global__ void commit_kernel(int* lens, const SeqRows rows, int add_uniform) {
+// Advances each sequence's length by its rows (or by add_uniform); with
+// `status`, a sequence with no rows is reported (a mixed step lists only
+// sequences that have rows in it).
+__global__ void commit_kernel(int* lens, const SeqRows rows, int add_uniform, int* status) {
   const int s = blockIdx.x * blockDim.x + threadIdx.x;
   if (s >= rows.num_seqs) return;
-  lens[s] += add_uniform >= 0 ? add_uniform : seq_rows(rows, s);
+  const int r = add_uniform >= 0 ? add_uniform : seq_rows(rows, s);
+  if (status && r < 1) atomicOr(status, CP_DEV_BOUNDS);
+  lens[s] += r;
 }
 
 }  // namespace
@@ -111,10 +116,10 @@ cudaError_t launch_pad_rows(void* base, int batch, int rows_padded, int real_row
 
 // add_uniform >= 0 adds that count to every sequence; -1 adds each
 // sequence's own row count.
-cudaError_t launch_commit(int* lens, const SeqRows& rows, int add_uniform, cudaStream_t st) {
+cudaError_t launch_commit(int* lens, const SeqRows& rows, int add_uniform, int* status, cudaStream_t st) {
   if (rows.num_seqs == 0) return cudaSuccess;
   const int block = 128;
-  commit_kernel<<<(rows.num_seqs + block - 1) / block, block, 0, st>>>(lens, rows, add_uniform);
+  commit_kernel<<<(rows.num_seqs + block - 1) / block, block, 0, st>>>(lens, rows, add_uniform, status);
   return cudaGetLastError();
 }
 

@@ -173,7 +173,11 @@ int cp_prefill_chunk_attn(const cp_layer_desc* desc, const void* q, const void* 
  *   k_pages, v_pages  device pools [num_pages, Hkv, page_size, D]
  *   block_table   device int32 [num_seqs, max_blocks]
  *   cu_rows       device int32 [num_seqs + 1]: rows of sequence s are
- *                 [cu_rows[s], cu_rows[s+1]); cu_rows[num_seqs] == T
+ *                 [cu_rows[s], cu_rows[s+1]); cu_rows[num_seqs] == T.  Every
+ *                 listed sequence has at least one row (a sequence with no
+ *                 rows in this step is left out of the call); the host relies
+ *                 on it to bound rows per sequence by T - num_seqs + 1, and a
+ *                 sequence with no rows sets CP_DEV_BOUNDS in *dev_status
  *   past_len      device int32 [num_seqs]: positions already cached
  *   max_ctx       host bound on past_len[s] + rows of s (<= max_blocks*page_size)
  *   workspace     >= cp_workspace_size(desc, T, max_ctx, num_seqs) bytes */
@@ -203,8 +207,9 @@ int cp_mixed_step(const cp_layer_desc* desc, const void* q, const void* k_new,
  *   The first call on a device looks up the array's device address (once per
  *   device, with that device current); make that first call before any stream
  *   capture on that device.
- *   Every call uses the same array, which keeps the last call's contents (the
- *   kernels write every entry before reading it, so nothing needs clearing).
+ *   Every call uses the same array, which keeps the last call's contents:
+ *   each call clears the work counter at its start (an asynchronous memset on
+ *   the call's stream) and writes every other entry before reading it.
  *   Calls whose work overlaps on the GPU -- on different streams or from
  *   different host threads -- race on the array; the caller must serialise
  *   them. */

@@ -207,3 +207,61 @@ def test_bad_page_id_is_reported_not_read():
     out, _ = P.step([0, 1, 2], [1, 1, 64], [39, 39, 0], q.cuda(), kn.cuda(), vn.cuda(), 64)
     torch.cuda.synchronize()
     assert int(P.status.item()) & cp.CP_DEV_BOUNDS
+
+
+def _decode_only_batch(ctx, seed):
+    mb = SI.mixed_batch(n_decode=len(ctx), ctx_lo=1, ctx_hi=2, n_prompt=1, prompt_len=64, decode_tail=64,
+                        seed=seed)
+    mb.decode_ctx = list(ctx)
+    need = [-(-(n + 64) // PAGE) for n in ctx]
+    mb.max_blocks, mb.num_pages = max(need), sum(need)
+    perm = torch.randperm(mb.num_pages, generator=torch.Generator().manual_seed(seed))
+    mb.block_table = torch.full((len(need), mb.max_blocks), -1, dtype=torch.int32)
+    off = 0
+    for s, nb in enumerate(need):
+        mb.block_table[s, :nb] = perm[off:off + nb].to(torch.int32)
+        off += nb
+    return mb
+
+
+def test_all_decode_steps_match_oracle():
+    """Steps made only of decode rows (one row per sequence: the tensor-core
+    path is not launched) at contexts on page and 512-key split edges, two
+    steps in a row: every row matches the oracle's mixed step and the pools
+    match it bit for bit."""
+    ctx = [1, 2, 16, 511, 512, 513, 1024, 1025, 3000, 77]
+    mb = _decode_only_batch(ctx, seed=24)
+    P = Paged(mb)
+    for s, c in enumerate(ctx):
+        P.prefill_history(s, SI.normal((c - 1, HKV, D), 700 + s), SI.normal((c - 1, HKV, D), 800 + s))
+    seqs = list(range(len(ctx)))
+    rows = [1] * len(ctx)
+    past = [c - 1 for c in ctx]
+    for step in range(2):
+        q, kn, vn = SI.gqa_prompt(len(ctx), seed=60 + step)
+        out, pl = P.step(seqs, rows, past, q.cuda(), kn.cuda(), vn.cuda(), max(past) + 1)
+        torch.cuda.synchronize()
+        ref, P.ok, P.ov, newp = oracle.mixed_step(f64(q), f64(kn), f64(vn), P.ok, P.ov,
+                                                  mb.block_table[seqs].numpy(), rows, past)
+        err = np.abs(f64(out) - ref).max()
+        assert err < BF16_TOL, (step, err)
+        assert pl.tolist() == newp
+        past = newp
+    assert int(P.status.item()) == 0
+    got_k = f64(P.k)
+    mask = ~np.isnan(P.ok)
+    assert np.array_equal(got_k[mask], P.ok[mask])
+
+
+def test_sequence_without_rows_is_reported():
+    """A mixed step lists only sequences with rows; a listed sequence with no
+    rows is reported in the device status word."""
+    ctx = [40, 300, 90]
+    mb = _decode_only_batch(ctx, seed=25)
+    P = Paged(mb, with_oracle=False)
+    for s, c in enumerate(ctx):
+        P.prefill_history(s, SI.normal((c - 1, HKV, D), 900 + s), SI.normal((c - 1, HKV, D), 950 + s))
+    q, kn, vn = SI.gqa_prompt(3, seed=62)
+    P.step([0, 1, 2], [0, 2, 1], [39, 299, 89], q.cuda(), kn.cuda(), vn.cuda(), 301)
+    torch.cuda.synchronize()
+    assert int(P.status.item()) & cp.CP_DEV_BOUNDS
