@@ -31,10 +31,10 @@
 namespace cp {
 namespace {
 
-constexpr int kDecConsumers = 8;     // consumer warps per CTA (plus one producer warp)
-constexpr int kDecCtasPerSm = 2;     // resident CTAs per SM of the persistent grid
+constexpr int kDecConsumers = 4;     // consumer warps per CTA (plus an issuer and a resolver warp)
+constexpr int kDecCtasPerSm = 3;     // resident CTAs per SM of the persistent grid
 constexpr int kDecStageBytes = 8192; // one ring stage: 32 rows at D = 128, 64 at D = 64
-constexpr int kDecStages = 9;        // ring depth
+constexpr int kDecStages = 5;        // ring depth
 constexpr int kDecSlots = 3;         // resolved items held ahead of the consumers
 
 template <typename T>
@@ -79,8 +79,8 @@ struct DecSmem {
   static constexpr int bars = red + 4 * kDecConsumers * H * D;        // uint64 full, empty, ready, freed
   static constexpr int items = bars + 8 * (2 * kDecStages + 2 * kDecSlots);  // int [kDecSlots][2]
   static constexpr int misc = items + 8 * kDecSlots;                  // int bad[kDecSlots], abort
-  static constexpr int ml = misc + 4 * (kDecSlots + 1);               // float m[H], l[H]
-  static constexpr int bytes = ml + 8 * H;
+  static constexpr int ml = misc + 4 * (kDecSlots + 1);               // float max[kDecConsumers][H], sum[..][H]
+  static constexpr int bytes = ml + 8 * kDecConsumers * H;
   static_assert(kDecCtasPerSm * (bytes + 1024) <= 228 * 1024, "two CTAs per SM");
 };
 
@@ -174,7 +174,9 @@ __global__ void __launch_bounds__((kDecConsumers + 2) * 32, kDecCtasPerSm)
   constexpr int SR = L::kStageRows;
   constexpr int NST = kDecStages;
   constexpr int NSL = kDecSlots;
-  static_assert(kDecConsumers * KPW == SR, "one pass of the consumers covers a stage");
+  constexpr int KPP = kDecConsumers * KPW;  // rows per K pass of all consumers
+  constexpr int KPASS = SR / KPP;
+  static_assert(KPASS * KPP == SR, "K passes cover a stage");
   static_assert(SR % 32 == 0, "the issuer covers a stage in rounds of 32 rows");
   constexpr int LPV = D / 8;                // lanes per row in the V phase
   constexpr int RPW = 32 / LPV;             // rows per warp per V pass
@@ -188,8 +190,8 @@ __global__ void __launch_bounds__((kDecConsumers + 2) * 32, kDecCtasPerSm)
   int* s_items = reinterpret_cast<int*>(smem + L::items);
   int* s_bad = reinterpret_cast<int*>(smem + L::misc);
   volatile int* s_abort = s_bad + NSL;
-  float* s_m = reinterpret_cast<float*>(smem + L::ml);
-  float* s_l = s_m + H;
+  float (*s_wmax)[H] = reinterpret_cast<float (*)[H]>(smem + L::ml);            // per warp, per head
+  float (*s_psum)[H] = reinterpret_cast<float (*)[H]>(smem + L::ml + 4 * kDecConsumers * H);
 
   const int nhb = a.hq / H;
   const int total = a.max_splits * a.rows.num_seqs * nhb;
@@ -341,6 +343,15 @@ __global__ void __launch_bounds__((kDecConsumers + 2) * 32, kDecCtasPerSm)
   // -------------------------------------------------- consumer warps
   const int sub = lane % LPK;
   const int r = warp * KPW + lane / LPK;  // this lane's row within a stage (K phase)
+  // The LPK lanes of a row reduce their H partial dot products by halving:
+  // at each xor level a lane keeps half of the heads it holds and adds its
+  // partner's half, so after log2(LPK) levels lane `sub` holds the full dot
+  // product of head hb (lanes sub and sub ^ 1 ... hold the same head).
+  int hb = 0;
+#pragma unroll
+  for (int lvl = 0; (LPK >> (lvl + 1)) >= 1; ++lvl)
+    if ((H >> lvl) > 1 && (lane & (LPK >> (lvl + 1)))) hb += (H >> lvl) / 2;
+  constexpr int kHeadLanes = LPK / H;     // lanes of a row holding the same head
   const int subv = lane % LPV;
   const int rv = warp * RPW + lane / LPV;  // this lane's row within a V pass
   float (*sc)[kDecodeSplit] = reinterpret_cast<float (*)[kDecodeSplit]>(smem + L::sc);
@@ -376,13 +387,16 @@ __global__ void __launch_bounds__((kDecConsumers + 2) * 32, kDecCtasPerSm)
     }
 
     // ---- scores over the K stages
+    float mx = -INFINITY;  // running max of this lane's head over its rows
     for (int tl = 0; tl < ntl; ++tl, ++t) {
       const int st = t % NST;
       if (tl > 0) ok = ok && warp_wait(&full[st], (t / NST) & 1, s_abort, a.status);
       if (!ok) continue;
-      const int kk = tl * SR + r;
+#pragma unroll
+      for (int kp = 0; kp < KPASS; ++kp) {
+      const int kk = tl * SR + kp * KPP + r;
       uint32_t w[8];
-      lds_row(smem + L::ring + st * kDecStageBytes + r * L::kRow, sub, LPK, w);
+      lds_row(smem + L::ring + st * kDecStageBytes + (kp * KPP + r) * L::kRow, sub, LPK, w);
       float2 acc[H];
 #pragma unroll
       for (int h = 0; h < H; ++h) acc[h] = make_float2(0.f, 0.f);
@@ -392,38 +406,58 @@ __global__ void __launch_bounds__((kDecConsumers + 2) * 32, kDecCtasPerSm)
 #pragma unroll
         for (int h = 0; h < H; ++h) ffma2v(acc[h], qv[h][e], kf);
       }
+      float v[H];
 #pragma unroll
-      for (int h = 0; h < H; ++h) {
-        float v = acc[h].x + acc[h].y;
+      for (int h = 0; h < H; ++h) v[h] = acc[h].x + acc[h].y;
 #pragma unroll
-        for (int o = LPK / 2; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-        if (sub == 0 && kk < it.nk) sc[h][kk] = (bad && rows[kk] == kNoRow) ? -INFINITY : v;
+      for (int lvl = 0; (LPK >> (lvl + 1)) >= 1; ++lvl) {
+        const int o = LPK >> (lvl + 1);
+        constexpr int kMaxH = H;
+        const int nh = kMaxH >> lvl;
+        if (nh > 1) {
+          const bool up = (lane & o) != 0;
+#pragma unroll
+          for (int i = 0; i < nh / 2; ++i) {
+            const float send = up ? v[i] : v[i + nh / 2];
+            const float keep = up ? v[i + nh / 2] : v[i];
+            v[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+          }
+        } else {
+          v[0] += __shfl_xor_sync(0xffffffffu, v[0], o);
+        }
+      }
+      if (kk < it.nk) {
+        const float sv = (bad && rows[kk] == kNoRow) ? -INFINITY : v[0];
+        if (sub % kHeadLanes == 0) sc[hb][kk] = sv;
+        mx = fmaxf(mx, sv);
+      }
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[st]);
     }
+    // The warp's max per head: lanes holding the same head across the row groups.
+#pragma unroll
+    for (int o = LPK; o < 32; o <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    if (lane < LPK && sub % kHeadLanes == 0) s_wmax[warp][hb] = mx;
     consumers_sync();
 
-    // ---- split max / sum per query head (log2 domain)
+    // ---- split max / sum per query head (log2 domain): kDecConsumers / H
+    // warps per head, each over an interleaved share of the split's keys.
+    constexpr int WPH = kDecConsumers / H;
     if (ok) {
-      for (int h = warp; h < H; h += kDecConsumers) {
-        float m = -INFINITY;
-        for (int kk = lane; kk < it.nk; kk += 32) m = fmaxf(m, sc[h][kk]);
+      const int h = warp % H, part = warp / H;
+      float m = -INFINITY;
 #pragma unroll
-        for (int o = 16; o; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-        float l = 0.f;
-        for (int kk = lane; kk < it.nk; kk += 32) {
-          const float pr = (m == -INFINITY) ? 0.f : ex2_approx(sc[h][kk] - m);
-          sc[h][kk] = pr;
-          l += pr;
-        }
-#pragma unroll
-        for (int o = 16; o; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
-        if (lane == 0) {
-          s_m[h] = m;
-          s_l[h] = l;
-        }
+      for (int w = 0; w < kDecConsumers; ++w) m = fmaxf(m, s_wmax[w][h]);
+      float l = 0.f;
+      for (int kk = part * 32 + lane; kk < it.nk; kk += 32 * WPH) {
+        const float pr = (m == -INFINITY) ? 0.f : ex2_approx(sc[h][kk] - m);
+        sc[h][kk] = pr;
+        l += pr;
       }
+#pragma unroll
+      for (int o = 16; o; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
+      if (lane == 0) s_psum[part][h] = l;
     }
     consumers_sync();
 
@@ -490,9 +524,15 @@ __global__ void __launch_bounds__((kDecConsumers + 2) * 32, kDecCtasPerSm)
       a.part_o[((part_base + (long long)h * a.max_splits) + it.split) * D + dd] = v;
     }
     if (threadIdx.x < H) {
-      const long long idx = (part_base + (long long)threadIdx.x * a.max_splits) + it.split;
-      a.part_ml[idx * 2 + 0] = s_m[threadIdx.x];
-      a.part_ml[idx * 2 + 1] = s_l[threadIdx.x];
+      const int h = threadIdx.x;
+      float m = -INFINITY, l = 0.f;
+#pragma unroll
+      for (int w = 0; w < kDecConsumers; ++w) m = fmaxf(m, s_wmax[w][h]);
+#pragma unroll
+      for (int p = 0; p < WPH; ++p) l += s_psum[p][h];
+      const long long idx = (part_base + (long long)h * a.max_splits) + it.split;
+      a.part_ml[idx * 2 + 0] = m;
+      a.part_ml[idx * 2 + 1] = l;
     }
   }
 }
