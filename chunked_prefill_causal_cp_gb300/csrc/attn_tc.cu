@@ -40,9 +40,14 @@
 // rescale and P_w(i+1) may overwrite P_w(i).
 //
 // Merge: each CTA's partial (max, sum, unnormalised O) per row is combined in
-// a fixed order (even-tile half first): rank r finishes the rows of Q tile r,
-// receiving the peer's partial for those rows through distributed shared
-// memory.
+// a fixed order (even-tile half first): rank r finishes the rows of Q tile r.
+// Once a CTA's own MMAs are complete it tells its peer (a remote mbarrier
+// arrive) that its K/V stages may receive; the peer's group for the other Q
+// tile stages its partial O rows in its own K stages (16-byte chunks XOR-
+// swizzled by row, so the row-per-thread stores are conflict-free) and sends
+// them with one bulk shared-to-shared copy, completed on the receiver's
+// mbarrier.  The receiver combines, writes the finished 16-bit rows into its
+// Q buffer in the TMA layout and stores the tile with a TMA tensor store.
 //
 // Keys beyond the written length inside the last tile may hold stale or
 // poisoned bytes; their scores are masked and the MMA warp zeroes those V rows
@@ -67,15 +72,17 @@ constexpr uint32_t kBlockBytes = 128 * 128;  // [128 rows][64 x 16-bit] = 16 KB
 constexpr uint32_t kTmemCols = 512;
 constexpr float kRescaleLog2 = 8.0f;         // O is rescaled when the max grows by > 2^8
 
-struct __align__(8) TcBarriers {
+struct __align__(16) TcBarriers {
   uint64_t q_full;
   uint64_t kv_full[kStages], kv_empty[kStages];  // a stage holds one K tile and one V tile
   uint64_t s_full[2], p_ready[2];
   uint64_t o_final;
+  uint64_t merge_full;  // the peer's partial for this CTA's rows has landed
+  uint64_t peer_free;   // the peer's K/V stages may receive this CTA's partial
   uint32_t tmem_base;
   int abort;
-  float peer_m[128];  // the peer CTA's partial max / sum for this CTA's rows
-  float peer_l[128];
+  __align__(16) float peer_ml[256];  // the peer's partial max [0, 128) and sum [128, 256) for this CTA's rows
+  __align__(16) float out_ml[256];   // this CTA's partial max / sum for the peer's rows (sent)
 };
 
 template <int D>
@@ -87,12 +94,19 @@ struct TcSmem {
   static constexpr uint32_t bar_off = v_off + kStages * DB * kBlockBytes;
   static constexpr uint32_t bytes = bar_off + sizeof(TcBarriers);
   static constexpr uint32_t alloc = bytes + 1024;  // slack for 1024-byte alignment
-  // After the main loop the K and V stages hold the peer's partial O rows:
-  // [128][kMergeStride] fp32, padded so a quarter-warp's row accesses cover all
-  // shared-memory banks.
-  static constexpr uint32_t kMergeStride = D + 4;
-  static_assert(2 * kStages * DB * kBlockBytes >= 128u * kMergeStride * 4u, "merge buffer does not fit");
+  // After the main loop the K stages hold this CTA's outgoing partial O rows
+  // and the V stages the peer's incoming ones: [128][D] fp32 each.
+  static constexpr uint32_t kMergeBytes = 128u * D * 4u;
+  static_assert(kStages * DB * kBlockBytes == kMergeBytes, "a merge buffer is exactly the K (or V) stages");
 };
+
+// Byte offset of 16-byte chunk q of row m in a [128][D] fp32 merge buffer:
+// chunks are XOR-swizzled by (m mod 8), so the 8 rows a quarter-warp touches
+// at once fall on distinct banks.
+template <int D>
+__device__ __forceinline__ uint32_t merge_off(int m, int q) {
+  return (uint32_t)m * (D * 4) + (uint32_t)((q ^ (m & 7)) * 16);
+}
 
 template <typename T>
 __device__ __forceinline__ uint32_t pack2(float lo, float hi);
@@ -154,7 +168,8 @@ __device__ __forceinline__ bool find_pair(const AttnArgs& a, int ppt, int w, int
 template <typename T, int D>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                   const __grid_constant__ CUtensorMap tm_v, const AttnArgs a) {
+                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
+                   const AttnArgs a) {
   using L = TcSmem<D>;
   constexpr int DB = L::DB;
   constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
@@ -196,6 +211,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int ntiles = (nkeys + kTcBlockN - 1) / kTcBlockN;
   const int nmine = ntiles > rank ? (ntiles - rank + 1) / 2 : 0;  // this CTA's KV tiles: rank + 2i
   const bool q1 = t0 + rpt < rows;  // Q tile 1 holds at least one row (else it is skipped)
+  const bool own_tile = rank == 0 || q1;   // Q tile `rank` (finished here) has rows
+  const bool peer_tile = rank == 1 || q1;  // Q tile `1 - rank` (finished by the peer) has rows
+  const uint32_t peer = (uint32_t)(1 - rank);
 
   if (threadIdx.x == 0) {
     mbar_init(&bar->q_full, 1);
@@ -208,8 +226,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bar->p_ready[i], 128);
     }
     mbar_init(&bar->o_final, 1);
+    mbar_init(&bar->merge_full, 1);
+    mbar_init(&bar->peer_free, 1);
     bar->abort = 0;
     fence_barrier_init();
+    if (own_tile) mbar_arrive_expect_tx(&bar->merge_full, L::kMergeBytes + 256u * 4u);
   }
   if (warp == 1) {
     tmem_alloc(&bar->tmem_base, kTmemCols);
@@ -218,6 +239,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  cluster_arrive();  // barrier inits are visible cluster-wide before any remote access (waited below)
   const uint32_t tmem = bar->tmem_base;
   volatile int* abort_flag = &bar->abort;
 
@@ -455,22 +477,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 
   // ================================================================ merge across the pair
-  // Every warp of both CTAs takes part in the two cluster barriers.
   volatile int zero = 0;
   const bool done = (!is_softmax || warp_wait(&bar->o_final, 0, &zero, a.status)) && alive;
-  tc_fence_before();
-  cluster_sync_all();  // #1: both CTAs are past their main loops
   tc_fence_after();
+  __syncwarp();
+  cluster_wait();  // the peer's barriers are initialised
   const bool have_o = nmine > 0;  // this CTA wrote O (else its TMEM O is unset: send zeros)
-  constexpr uint32_t kStride = L::kMergeStride;
-  if (is_softmax && grp != rank && (grp == 0 || q1)) {
-    // Rows of Q tile (1 - rank) are finished by the peer: send this CTA's partial.
-    const uint32_t peer = (uint32_t)(1 - rank);
-    const uint32_t pm = mapa_shared(smem_u32(&bar->peer_m[mrow]), peer);
-    const uint32_t pl = mapa_shared(smem_u32(&bar->peer_l[mrow]), peer);
-    st_cluster_f32(pm, have_o ? m_run : -INFINITY);
-    st_cluster_f32(pl, have_o ? l_run : 0.f);
-    const uint32_t po = mapa_shared(smem_u32(sK + (uint32_t)mrow * kStride * 4u), peer);
+  if (warp == 1 && lane == 0 && own_tile) {
+    // This CTA's MMAs are complete (the issuer waited o_final): its K/V stages are free.
+    mbar_arrive_remote(mapa_shared(smem_u32(&bar->peer_free), peer));
+  }
+  if (is_softmax && grp != rank && peer_tile) {
+    // Rows of Q tile (1 - rank) are finished by the peer: stage and send this CTA's partial.
 #pragma unroll
     for (int c = 0; c < D / 32; ++c) {
       uint32_t ov[32];
@@ -483,15 +501,24 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
 #pragma unroll
       for (int e = 0; e < 8; ++e)
-        st_cluster_v4(po + (uint32_t)(c * 32 + 4 * e) * 4u, ov[4 * e], ov[4 * e + 1], ov[4 * e + 2], ov[4 * e + 3]);
+        *reinterpret_cast<uint4*>(sK + merge_off<D>(mrow, c * 8 + e)) =
+            make_uint4(ov[4 * e], ov[4 * e + 1], ov[4 * e + 2], ov[4 * e + 3]);
+    }
+    bar->out_ml[mrow] = have_o ? m_run : -INFINITY;
+    bar->out_ml[128 + mrow] = have_o ? l_run : 0.f;
+    fence_proxy_async_smem();  // the bulk copy reads these through the async proxy
+    asm volatile("bar.sync 1, 128;" ::: "memory");
+    if (mrow == 0 && mbar_wait_cluster(&bar->peer_free, 0, a.status)) {
+      const uint32_t rbar = mapa_shared(smem_u32(&bar->merge_full), peer);
+      bulk_copy_to_peer(mapa_shared(smem_u32(sV), peer), sK, L::kMergeBytes, rbar);
+      bulk_copy_to_peer(mapa_shared(smem_u32(bar->peer_ml), peer), bar->out_ml, 256u * 4u, rbar);
     }
   }
-  cluster_sync_all();  // #2: the peer's partial for this CTA's rows is in place
-  if (is_softmax && grp == rank && (grp == 0 || q1)) {
+  if (is_softmax && grp == rank && own_tile) {
     // Fixed order: the even-tile half (rank 0's partial) first.
-    const float* peer_o = reinterpret_cast<const float*>(sK + (uint32_t)mrow * kStride * 4u);
+    const bool got = mbar_wait_cluster(&bar->merge_full, 0, a.status);
     const float m_own = have_o ? m_run : -INFINITY, l_own = have_o ? l_run : 0.f;
-    const float m_peer = bar->peer_m[mrow], l_peer = bar->peer_l[mrow];
+    const float m_peer = bar->peer_ml[mrow], l_peer = bar->peer_ml[128 + mrow];
     const float mA = rank == 0 ? m_own : m_peer, lA = rank == 0 ? l_own : l_peer;
     const float mB = rank == 0 ? m_peer : m_own, lB = rank == 0 ? l_peer : l_own;
     const float mm = fmaxf(mA, mB);
@@ -499,6 +526,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float wB = (mB == -INFINITY) ? 0.f : ex2_approx(mB - mm);
     const float lsum = lA * wA + lB * wB;
     const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
+    // A tile whose rows all belong to this sequence leaves through a TMA store
+    // from the (now unused) Q buffer; a ragged tile row by row.
+    const int tile_tok0 = t0 + rank * rpt;
+    const bool full_tile = tile_tok0 + rpt <= t_end;
+    uint8_t* sOut = sQ + rank * DB * kBlockBytes;
     T* out = static_cast<T*>(a.out) + ((long long)(row0 + tok) * a.hq + head) * D;
 #pragma unroll
     for (int c = 0; c < D / 32; ++c) {
@@ -510,26 +542,50 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int e = 0; e < 32; ++e) ov[e] = 0u;
       }
-      if (done && row_ok) {
-        uint32_t pk[16];
+      uint32_t pk[16];
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          const float own0 = __uint_as_float(ov[2 * e]), own1 = __uint_as_float(ov[2 * e + 1]);
-          const float2 pr = *reinterpret_cast<const float2*>(peer_o + c * 32 + 2 * e);
-          const float pr0 = pr.x, pr1 = pr.y;
-          const float x0 = rank == 0 ? own0 * wA + pr0 * wB : pr0 * wA + own0 * wB;
-          const float x1 = rank == 0 ? own1 * wA + pr1 * wB : pr1 * wA + own1 * wB;
-          pk[e] = pack2<T>(x0 * inv, x1 * inv);
+      for (int e = 0; e < 8; ++e) {
+        const float4 pr = *reinterpret_cast<const float4*>(sV + merge_off<D>(mrow, c * 8 + e));
+        const float own[4] = {__uint_as_float(ov[4 * e]), __uint_as_float(ov[4 * e + 1]),
+                              __uint_as_float(ov[4 * e + 2]), __uint_as_float(ov[4 * e + 3])};
+        const float prv[4] = {pr.x, pr.y, pr.z, pr.w};
+        float x[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) x[u] = rank == 0 ? own[u] * wA + prv[u] * wB : prv[u] * wA + own[u] * wB;
+        pk[2 * e] = pack2<T>(x[0] * inv, x[1] * inv);
+        pk[2 * e + 1] = pack2<T>(x[2] * inv, x[3] * inv);
+      }
+      if (full_tile) {
+        // Columns [32c, 32c + 32) are 16-byte chunks 4(c%2) .. 4(c%2)+3 of box c/2 (128B swizzle).
+        uint8_t* box = sOut + (c >> 1) * kBlockBytes + mrow * 128;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int chunk = (c & 1) * 4 + e;
+          *reinterpret_cast<uint4*>(box + ((chunk ^ (mrow & 7)) * 16)) =
+              make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
         }
+      } else if (done && got && row_ok) {
         uint4* dst = reinterpret_cast<uint4*>(out + 32 * c);
 #pragma unroll
         for (int e = 0; e < 4; ++e) dst[e] = make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
       }
     }
+    if (full_tile) {
+      fence_proxy_async_smem();  // the TMA store reads the tile through the async proxy
+      asm volatile("bar.sync 2, 128;" ::: "memory");
+      if (mrow == 0 && done && got) {
+        for (int db = 0; db < DB; ++db)
+          tma_store_3d(&tm_o, sOut + db * kBlockBytes, db * 64, g * G, row0 + tile_tok0);
+        bulk_commit_group();
+        bulk_wait_all();
+      }
+    }
   }
 
+  // Both CTAs leave together: the copies each sent into the other have landed
+  // and been read before either CTA's shared memory is released.
   tc_fence_before();
-  __syncthreads();
+  cluster_sync_all();
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
@@ -538,7 +594,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 template <typename T, int D>
 cudaError_t launch_t(const AttnArgs& a, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                     int pairs_bound, cudaStream_t st) {
+                     const CUtensorMap& to, int pairs_bound, cudaStream_t st) {
   // D = 64 would fit two CTAs per SM, but each CTA takes all 512 TMEM
   // columns; ask for enough shared memory to keep it at one CTA per SM.
   const uint32_t smem = TcSmem<D>::alloc < 120u * 1024u ? 120u * 1024u : TcSmem<D>::alloc;
@@ -567,7 +623,7 @@ cudaError_t launch_t(const AttnArgs& a, const CUtensorMap& tq, const CUtensorMap
   cfg.stream = st;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, attn_tc_kernel<T, D>, tq, tk, tv, a);
+  e = cudaLaunchKernelEx(&cfg, attn_tc_kernel<T, D>, tq, tk, tv, to, a);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
@@ -580,14 +636,15 @@ bool attn_tc_supported(int d, int group, int dtype) {
 }
 
 // pairs_bound: number of 2*128-row Q-tile pairs to cover (one 2-CTA cluster each).
+// to: the output [rows, Hq, D] with the same box as tq (finished tiles are TMA-stored).
 cudaError_t launch_attn_tc(const AttnArgs& a, int dtype, const CUtensorMap& tq, const CUtensorMap& tk,
-                           const CUtensorMap& tv, int pairs_bound, cudaStream_t st) {
+                           const CUtensorMap& tv, const CUtensorMap& to, int pairs_bound, cudaStream_t st) {
   if (pairs_bound <= 0) return cudaSuccess;
   if (dtype == CP_BF16)
-    return a.d == 64 ? launch_t<__nv_bfloat16, 64>(a, tq, tk, tv, pairs_bound, st)
-                     : launch_t<__nv_bfloat16, 128>(a, tq, tk, tv, pairs_bound, st);
-  return a.d == 64 ? launch_t<__half, 64>(a, tq, tk, tv, pairs_bound, st)
-                   : launch_t<__half, 128>(a, tq, tk, tv, pairs_bound, st);
+    return a.d == 64 ? launch_t<__nv_bfloat16, 64>(a, tq, tk, tv, to, pairs_bound, st)
+                     : launch_t<__nv_bfloat16, 128>(a, tq, tk, tv, to, pairs_bound, st);
+  return a.d == 64 ? launch_t<__half, 64>(a, tq, tk, tv, to, pairs_bound, st)
+                   : launch_t<__half, 128>(a, tq, tk, tv, to, pairs_bound, st);
 }
 
 }  // namespace cp

@@ -117,11 +117,12 @@ bool encode_3d(CUtensorMap* m, int dtype, const void* base, uint64_t d0, uint64_
 // Tensor maps of the tensor-core path: Q/out rows [rows_total, Hq, D] in
 // boxes of (64 dims, G heads, 128/G tokens); K/V in boxes of 128 keys
 // (contiguous / rolling) or one page (paged) by 64 dims.
-bool make_tc_maps(const cp_layer_desc* d, const void* q, int64_t rows_total, const void* k, const void* v,
-                  int batch, CUtensorMap* tq, CUtensorMap* tk, CUtensorMap* tv) {
+bool make_tc_maps(const cp_layer_desc* d, const void* q, const void* out, int64_t rows_total, const void* k,
+                  const void* v, int batch, CUtensorMap* tq, CUtensorMap* to, CUtensorMap* tk, CUtensorMap* tv) {
   const int G = d->num_q_heads / d->num_kv_heads;
   const uint64_t D = d->head_dim;
   if (!encode_3d(tq, d->dtype, q, D, d->num_q_heads, (uint64_t)rows_total, 64, G, kTcBlockM / G)) return false;
+  if (!encode_3d(to, d->dtype, out, D, d->num_q_heads, (uint64_t)rows_total, 64, G, kTcBlockM / G)) return false;
   if (d->kind == CP_CACHE_PAGED) {
     const uint64_t planes = (uint64_t)d->num_pages * d->num_kv_heads;
     return encode_3d(tk, d->dtype, k, D, d->page_size, planes, 64, d->page_size, 1) &&
@@ -161,8 +162,8 @@ int run_attention(const cp_layer_desc* d, const AttnArgs& base, int64_t rows_tot
   }
   if (any_multi || !decode_ok) {
     a.min_rows = decode_ok ? 2 : 1;
-    CUtensorMap tq, tk, tv;
-    if (!make_tc_maps(d, a.q, rows_total, k, v, batch_for_maps, &tq, &tk, &tv)) return CP_ERR_CUDA;
+    CUtensorMap tq, to, tk, tv;
+    if (!make_tc_maps(d, a.q, a.out, rows_total, k, v, batch_for_maps, &tq, &to, &tk, &tv)) return CP_ERR_CUDA;
     const int ppt = 2 * (kTcBlockM / G);  // tokens per pair of 128-row Q tiles
     int64_t pairs;
     if (a.rows.rows_uniform > 0)
@@ -170,7 +171,7 @@ int run_attention(const cp_layer_desc* d, const AttnArgs& base, int64_t rows_tot
     else
       pairs = (rows_total + ppt - 1) / ppt + a.rows.num_seqs;
     if (2 * pairs > INT32_MAX) return CP_ERR_UNSUPPORTED;
-    return launch_result(launch_attn_tc(a, d->dtype, tq, tk, tv, (int)pairs, st));
+    return launch_result(launch_attn_tc(a, d->dtype, tq, tk, tv, to, (int)pairs, st));
   }
   return CP_OK;
 }
