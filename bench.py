@@ -16,8 +16,7 @@ public calls; L2 is flushed (512 MiB write) between timed steps.
 Prints one JSON line (rank 0).  ``--impl reference`` times the CPU oracle
 (test infrastructure, float64 numpy) on a bounded sample of the same
 workload instead.  Other workloads (decode rows, mixed step) print the same
-kind of line with their own metric; they are used for the numbers quoted in
-DESIGN.md.
+kind of line with their own metric.
 """
 from __future__ import annotations
 

@@ -25,7 +25,7 @@ Sources, cited by page title and section:
               budget scheduler and the one-layer equivalence example);
               "Related techniques" (PagedAttention).
 
-Readings taken where the pages are silent (each also listed in the design doc):
+Readings taken where the pages are silent:
   * softmax scale 1/sqrt(head_dim) (the glossary example uses the attention
     routine's default scale);
   * GQA groups are contiguous: query head h reads KV head h // (Hq / Hkv);
