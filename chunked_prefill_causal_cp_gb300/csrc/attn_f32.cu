@@ -29,6 +29,8 @@ __global__ void __launch_bounds__(256) attn_f32_kernel(const AttnArgs a) {
   __shared__ float vs[kKeysPerTile][D];
   __shared__ float qs[kRowsPerCta][D];
 
+  pdl_launch_dependents();
+  pdl_wait();
   const int s = blockIdx.z;
   const int h = blockIdx.y;
   const int g = h / a.group;
@@ -122,11 +124,8 @@ __global__ void __launch_bounds__(256) attn_f32_kernel(const AttnArgs a) {
 cudaError_t launch_attn_f32(const AttnArgs& a, int rows_bound, cudaStream_t st) {
   dim3 grid((rows_bound + kRowsPerCta - 1) / kRowsPerCta, a.hq, a.rows.num_seqs);
   if (grid.x == 0 || grid.z == 0) return cudaSuccess;
-  if (a.d == 64)
-    attn_f32_kernel<64><<<grid, 256, 0, st>>>(a);
-  else
-    attn_f32_kernel<128><<<grid, 256, 0, st>>>(a);
-  return cudaGetLastError();
+  if (a.d == 64) return launch_pdl(attn_f32_kernel<64>, grid, dim3(256), 0, st, a);
+  return launch_pdl(attn_f32_kernel<128>, grid, dim3(256), 0, st, a);
 }
 
 }  // namespace cp

@@ -183,38 +183,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* sV = smem + L::v_off;
   TcBarriers* bar = reinterpret_cast<TcBarriers*>(smem + L::bar_off);
 
+  pdl_launch_dependents();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = a.group;
   const int rpt = kTcBlockM / G;  // tokens per Q tile
   const int g = blockIdx.y;
   const int rank = (int)cluster_ctarank();
 
-  // ---- this cluster's pair (same for both CTAs; exits before any setup)
-  int s, t0;
-  if (!find_pair(a, 2 * rpt, blockIdx.x >> 1, s, t0)) return;
-  const int rows = seq_rows(a.rows, s);
-  const int past = a.past[s];
-  const int n = past + rows;  // positions written, including this call's rows
-  if (past < 0 || n > a.max_ctx) {
-    if (a.status && threadIdx.x == 0 && rank == 0) atomicOr(a.status, CP_DEV_BOUNDS);
-    return;
-  }
-  const int row0 = seq_row0(a.rows, s);
-  const int t_end = min(t0 + 2 * rpt, rows);
-  const bool rolling = a.cache.kind == CP_CACHE_ROLLING;
-  const bool paged = a.cache.kind == CP_CACHE_PAGED;
-  const int cap = a.cache.capacity;
-  // Key indices walked: absolute positions [0, nkeys) (contiguous / paged) or
-  // physical ring slots [0, nkeys) (rolling).
-  const int nkeys = rolling ? min(n, cap) : past + t_end;
-  const int n_valid = rolling ? nkeys : n;  // key indices holding written data
-  const int ntiles = (nkeys + kTcBlockN - 1) / kTcBlockN;
-  const int nmine = ntiles > rank ? (ntiles - rank + 1) / 2 : 0;  // this CTA's KV tiles: rank + 2i
-  const bool q1 = t0 + rpt < rows;  // Q tile 1 holds at least one row (else it is skipped)
-  const bool own_tile = rank == 0 || q1;   // Q tile `rank` (finished here) has rows
-  const bool peer_tile = rank == 1 || q1;  // Q tile `1 - rank` (finished by the peer) has rows
-  const uint32_t peer = (uint32_t)(1 - rank);
-
+  // ---- set-up that reads no global memory: it may overlap the previous kernel
   if (threadIdx.x == 0) {
     mbar_init(&bar->q_full, 1);
     for (int i = 0; i < kStages; ++i) {
@@ -230,7 +206,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&bar->peer_free, 1);
     bar->abort = 0;
     fence_barrier_init();
-    if (own_tile) mbar_arrive_expect_tx(&bar->merge_full, L::kMergeBytes + 256u * 4u);
+    tma_prefetch_desc(&tm_q);
+    tma_prefetch_desc(&tm_k);
+    tma_prefetch_desc(&tm_v);
+    tma_prefetch_desc(&tm_o);
   }
   if (warp == 1) {
     tmem_alloc(&bar->tmem_base, kTmemCols);
@@ -242,13 +221,50 @@ __global__ void __launch_bounds__(kThreads, 1)
   cluster_arrive();  // barrier inits are visible cluster-wide before any remote access (waited below)
   const uint32_t tmem = bar->tmem_base;
   volatile int* abort_flag = &bar->abort;
+  pdl_wait();  // everything below reads what earlier kernels wrote
+
+  // ---- this cluster's pair (the same for both CTAs, so both leave together)
+  int s = 0, t0 = 0, rows = 0, past = 0;
+  bool have_pair = find_pair(a, 2 * rpt, blockIdx.x >> 1, s, t0);
+  if (have_pair) {
+    rows = seq_rows(a.rows, s);
+    past = a.past[s];
+    if (past < 0 || past + rows > a.max_ctx) {
+      if (a.status && threadIdx.x == 0 && rank == 0) atomicOr(a.status, CP_DEV_BOUNDS);
+      have_pair = false;
+    }
+  }
+  if (!have_pair) {
+    cluster_wait();
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+      tc_fence_after();
+      tmem_dealloc(tmem, kTmemCols);
+    }
+    return;
+  }
+  const int n = past + rows;  // positions written, including this call's rows
+  const int row0 = seq_row0(a.rows, s);
+  const int t_end = min(t0 + 2 * rpt, rows);
+  const bool rolling = a.cache.kind == CP_CACHE_ROLLING;
+  const bool paged = a.cache.kind == CP_CACHE_PAGED;
+  const int cap = a.cache.capacity;
+  // Key indices walked: absolute positions [0, nkeys) (contiguous / paged) or
+  // physical ring slots [0, nkeys) (rolling).
+  const int nkeys = rolling ? min(n, cap) : past + t_end;
+  const int n_valid = rolling ? nkeys : n;  // key indices holding written data
+  const int ntiles = (nkeys + kTcBlockN - 1) / kTcBlockN;
+  const int nmine = ntiles > rank ? (ntiles - rank + 1) / 2 : 0;  // this CTA's KV tiles: rank + 2i
+  const bool q1 = t0 + rpt < rows;  // Q tile 1 holds at least one row (else it is skipped)
+  const bool own_tile = rank == 0 || q1;   // Q tile `rank` (finished here) has rows
+  const bool peer_tile = rank == 1 || q1;  // Q tile `1 - rank` (finished by the peer) has rows
+  const uint32_t peer = (uint32_t)(1 - rank);
+  if (threadIdx.x == 0 && own_tile) mbar_arrive_expect_tx(&bar->merge_full, L::kMergeBytes + 256u * 4u);
 
   if (warp == 0) {
     // ================================================================ producer
     if (lane == 0 && nmine > 0) {
-      tma_prefetch_desc(&tm_q);
-      tma_prefetch_desc(&tm_k);
-      tma_prefetch_desc(&tm_v);
       mbar_arrive_expect_tx(&bar->q_full, (q1 ? 2 : 1) * DB * kBlockBytes);
       for (int w = 0; w < (q1 ? 2 : 1); ++w)
         for (int db = 0; db < DB; ++db)
@@ -612,17 +628,20 @@ cudaError_t launch_t(const AttnArgs& a, const CUtensorMap& tq, const CUtensorMap
     ready_mask.fetch_or(bit, std::memory_order_release);
   }
   cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 2;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  // Programmatic dependent launch: set-up overlaps the previous kernel (see launch_pdl).
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.gridDim = dim3(2 * pairs_bound, a.hkv);
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   e = cudaLaunchKernelEx(&cfg, attn_tc_kernel<T, D>, tq, tk, tv, to, a);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();

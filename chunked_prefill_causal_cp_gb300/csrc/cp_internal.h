@@ -5,6 +5,7 @@
 
 #include <cstddef>
 #include <cstdint>
+#include <utility>
 
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -73,6 +74,38 @@ struct AppendArgs {
   void* v_cache;
   int* status;
 };
+
+// Launches `kernel` with programmatic dependent launch allowed: the grid may
+// be scheduled while the previous kernel in the stream is still running.
+// Every kernel of this library triggers its dependents on entry and waits
+// for the previous grid (griddepcontrol.wait) before it touches global
+// memory, so only set-up that reads no global memory (barrier init, TMEM
+// allocation) overlaps the previous kernel's tail.
+#ifdef __CUDACC__
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                       Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
+// Device side of programmatic dependent launch.
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+#endif
 
 // ---- launchers (return cudaGetLastError() after the launch) ----
 cudaError_t launch_kv_append(const AppendArgs& a, int rows_total, cudaStream_t st);

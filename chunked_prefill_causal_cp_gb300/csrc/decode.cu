@@ -193,6 +193,7 @@ __global__ void __launch_bounds__((kDecConsumers + 2) * 32, kDecCtasPerSm)
   float (*s_wmax)[H] = reinterpret_cast<float (*)[H]>(smem + L::ml);            // per warp, per head
   float (*s_psum)[H] = reinterpret_cast<float (*)[H]>(smem + L::ml + 4 * kDecConsumers * H);
 
+  pdl_launch_dependents();
   const int nhb = a.hq / H;
   const int total = a.max_splits * a.rows.num_seqs * nhb;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -209,6 +210,7 @@ __global__ void __launch_bounds__((kDecConsumers + 2) * 32, kDecCtasPerSm)
     fence_barrier_init();
   }
   __syncthreads();
+  pdl_wait();  // everything below reads what earlier kernels wrote
 
   if (warp == kDecConsumers + 1) {
     // ------------------------------------------------ resolver warp
@@ -539,6 +541,8 @@ __global__ void __launch_bounds__((kDecConsumers + 2) * 32, kDecCtasPerSm)
 
 template <typename T, int D>
 __global__ void __launch_bounds__(D) decode_combine_kernel(const AttnArgs a) {
+  pdl_launch_dependents();
+  pdl_wait();
   const int s = blockIdx.x, h = blockIdx.y, dd = threadIdx.x;
   if (seq_rows(a.rows, s) != 1) return;
   const int past = a.past[s];
@@ -589,11 +593,9 @@ cudaError_t launch_decode_t(const AttnArgs& a, int* counter, cudaStream_t st) {
   const int grid = (int)(items < (long long)sms * kDecCtasPerSm ? items : (long long)sms * kDecCtasPerSm);
   e = cudaMemsetAsync(counter, 0, sizeof(int), st);
   if (e != cudaSuccess) return e;
-  decode_split_kernel<T, D, H><<<grid, (kDecConsumers + 2) * 32, smem, st>>>(a, counter);
-  e = cudaGetLastError();
+  e = launch_pdl(decode_split_kernel<T, D, H>, dim3(grid), dim3((kDecConsumers + 2) * 32), smem, st, a, counter);
   if (e != cudaSuccess) return e;
-  decode_combine_kernel<T, D><<<dim3(a.rows.num_seqs, a.hq), D, 0, st>>>(a);
-  return cudaGetLastError();
+  return launch_pdl(decode_combine_kernel<T, D>, dim3(a.rows.num_seqs, a.hq), dim3(D), 0, st, a);
 }
 
 // Query heads per CTA: the whole GQA group up to 4 (a group of 8 takes two

@@ -44,6 +44,8 @@ __device__ __forceinline__ long long slot_offset(const CacheView& c, int hkv, in
 }
 
 __global__ void kv_append_kernel(const AppendArgs a, int rows_total) {
+  pdl_launch_dependents();
+  pdl_wait();
   const int vec_per_row = a.d * a.esize / 16;           // 16-byte vectors per row
   const long long gid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   const long long row = gid / vec_per_row;              // (token, head) row
@@ -69,6 +71,8 @@ __global__ void kv_append_kernel(const AppendArgs a, int rows_total) {
 // Rows [real_rows, rows_padded) of each sequence become copies of row
 // real_rows - 1 ([Wiki] 四: pad rows repeat the last real token).
 __global__ void pad_rows_kernel(char* base, int batch, int rows_padded, int real_rows, int row_bytes) {
+  pdl_launch_dependents();
+  pdl_wait();
   const int vecs = row_bytes / 16;
   const int pad = rows_padded - real_rows;
   const long long gid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
@@ -86,6 +90,8 @@ __global__ void pad_rows_kernel(char* base, int batch, int rows_padded, int real
 // `status`, a sequence with no rows is reported (a mixed step lists only
 // sequences that have rows in it).
 __global__ void commit_kernel(int* lens, const SeqRows rows, int add_uniform, int* status) {
+  pdl_launch_dependents();
+  pdl_wait();
   const int s = blockIdx.x * blockDim.x + threadIdx.x;
   if (s >= rows.num_seqs) return;
   const int r = add_uniform >= 0 ? add_uniform : seq_rows(rows, s);
@@ -101,17 +107,15 @@ cudaError_t launch_kv_append(const AppendArgs& a, int rows_total, cudaStream_t s
   if (threads == 0) return cudaSuccess;
   const int block = 256;
   const long long grid = (threads + block - 1) / block;
-  kv_append_kernel<<<(unsigned)grid, block, 0, st>>>(a, rows_total);
-  return cudaGetLastError();
+  return launch_pdl(kv_append_kernel, dim3((unsigned)grid), dim3(block), 0, st, a, rows_total);
 }
 
 cudaError_t launch_pad_rows(void* base, int batch, int rows_padded, int real_rows, int row_bytes, cudaStream_t st) {
   const long long threads = (long long)batch * (rows_padded - real_rows) * (row_bytes / 16);
   if (threads <= 0) return cudaSuccess;
   const int block = 256;
-  pad_rows_kernel<<<(unsigned)((threads + block - 1) / block), block, 0, st>>>(static_cast<char*>(base), batch,
-                                                                              rows_padded, real_rows, row_bytes);
-  return cudaGetLastError();
+  return launch_pdl(pad_rows_kernel, dim3((unsigned)((threads + block - 1) / block)), dim3(block), 0, st,
+                    static_cast<char*>(base), batch, rows_padded, real_rows, row_bytes);
 }
 
 // add_uniform >= 0 adds that count to every sequence; -1 adds each
@@ -119,8 +123,8 @@ cudaError_t launch_pad_rows(void* base, int batch, int rows_padded, int real_row
 cudaError_t launch_commit(int* lens, const SeqRows& rows, int add_uniform, int* status, cudaStream_t st) {
   if (rows.num_seqs == 0) return cudaSuccess;
   const int block = 128;
-  commit_kernel<<<(rows.num_seqs + block - 1) / block, block, 0, st>>>(lens, rows, add_uniform, status);
-  return cudaGetLastError();
+  return launch_pdl(commit_kernel, dim3((rows.num_seqs + block - 1) / block), dim3(block), 0, st, lens, rows,
+                    add_uniform, status);
 }
 
 }  // namespace cp
