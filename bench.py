@@ -2,7 +2,7 @@
 """Benchmark of the chunked-prefill causal attention hot path on one GB300.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
-                    [--workload gqa_prefill|decode|mixed] [--no-pad]
+                    [--workload gqa_prefill|decode|mixed|rolling|fp32] [--no-pad]
 
 Default workload (the one the headline metric is quoted on): one GQA layer,
 32 query / 8 KV heads, head_dim 128, bf16, a 4000-token prompt prefilled in
@@ -44,7 +44,7 @@ def parse_args():
     p.add_argument("--steps", type=int, default=3000)
     p.add_argument("--warmup", type=int, default=20)
     p.add_argument("--impl", default="native", choices=["native", "reference"])
-    p.add_argument("--workload", default="gqa_prefill", choices=["gqa_prefill", "decode", "mixed"])
+    p.add_argument("--workload", default="gqa_prefill", choices=["gqa_prefill", "decode", "mixed", "rolling", "fp32"])
     p.add_argument("--no-pad", action="store_true", help="do not widen chunks to the query-width ladder")
     p.add_argument("--cpu-seconds", type=float, default=12.0, help="CPU-baseline sample budget")
     p.add_argument("--skip-cpu", action="store_true")
@@ -350,6 +350,8 @@ def run_native(args):
     import chunked_prefill_causal_cp_gb300 as cp
     cp.lib()
     pk, pk_src = peaks()
+    if args.workload in ("rolling", "fp32"):
+        return run_chunk_loop(args, rank, world, dev, pk, pk_src)
     if args.workload != "gqa_prefill":
         return run_paged(args, rank, world, dev, pk, pk_src)
 
@@ -501,6 +503,123 @@ class PagedStep:
         self.past.copy_(self.past0)
         self.cp.cp_mixed_step(self.desc, self.q, self.kn, self.vn, self.kp, self.vp, self.bt, self.cu, self.past,
                               self.S, self.T, self.max_ctx, self.out, self.ws, dev_status=self.status)
+
+
+def rolling_visible_pairs(L, c, C, left_pad):
+    """Visible (query, key) pairs of the rolling workload, real query rows only:
+    chunk k row i is position p = k*c + i; logical slot j holds position
+    a = (k+1)*c - C + j, visible iff a >= 0, a >= left_pad and a <= p."""
+    total = 0
+    for k in range(L // c):
+        lo = max(0, (k + 1) * c - C, left_pad)
+        for i in range(c):
+            p = k * c + i
+            if p >= left_pad:
+                total += max(0, p - lo + 1)
+    return total
+
+
+class ChunkLoop:
+    """Chunk-by-chunk prefill of one prompt through the public calls, for the
+    rolling-cache workload (fp16 MHA 16 x 128, window 1024, chunk 256, aligned
+    lengths 2048 and 768 with 48 and 68 left-pad rows) and the fp32 example
+    (1000 tokens, 8 heads x 64, chunk 256)."""
+
+    def __init__(self, dev, mode):
+        import torch
+        import chunked_prefill_causal_cp_gb300 as cp
+        import synth_inputs as SI
+
+        self.cp, self.torch, self.mode = cp, torch, mode
+        self.runs = []
+        if mode == "rolling":
+            H, d, c, C = 16, 128, 256, 1024
+            for n_real in (2000, 700):
+                L = cp.cp_aligned_length(n_real, c)
+                q, k, v = SI.rolling_prompt(L, seed=3, heads=H, dim=d)
+                self.runs.append(dict(kind=cp.CP_CACHE_ROLLING, H=H, Hkv=H, d=d, W=c, cap=C, L=L, lp=L - n_real,
+                                      q=q, k=k, v=v, dtype=torch.float16,
+                                      pairs=rolling_visible_pairs(L, c, C, L - n_real)))
+        else:
+            q, k, v = SI.fp32_sdpa_example()
+            N, W = q.shape[0], 256
+            self.runs.append(dict(kind=cp.CP_CACHE_CONTIG, H=q.shape[1], Hkv=k.shape[1], d=q.shape[2], W=W,
+                                  cap=N, L=N, lp=0, q=q, k=k, v=v, dtype=torch.float32,
+                                  pairs=visible_pairs(0, N)))
+        self.status = torch.zeros(1, dtype=torch.int32, device=dev)
+        for r in self.runs:
+            r["desc"] = cp.layer_desc(r["dtype"], 1, r["H"], r["Hkv"], r["d"], r["kind"], capacity=r["cap"])
+            r["qd"], r["kd"], r["vd"] = (t.to(dev, r["dtype"]) for t in (r["q"], r["k"], r["v"]))
+            r["kc"] = torch.zeros(1, r["Hkv"], r["cap"], r["d"], dtype=r["dtype"], device=dev)
+            r["vc"] = torch.zeros_like(r["kc"])
+            r["lens"] = torch.zeros(1, dtype=torch.int32, device=dev)
+            r["left"] = torch.tensor([r["lp"]], dtype=torch.int32, device=dev)
+            r["out"] = torch.empty(r["L"], r["H"], r["d"], dtype=r["dtype"], device=dev)
+            r["sizes"] = cp.cp_chunk_plan(r["L"], r["W"])
+        self.tokens = sum(r["L"] - r["lp"] for r in self.runs)
+        self.flops = sum(4 * r["d"] * r["H"] * r["pairs"] for r in self.runs)
+        self.launches = sum(3 * len(r["sizes"]) for r in self.runs)
+
+    def step(self):
+        cp = self.cp
+        for r in self.runs:
+            r["lens"].zero_()
+            rolling = r["kind"] == cp.CP_CACHE_ROLLING
+            past = 0
+            for w in r["sizes"]:
+                sl = slice(past, past + w)
+                cp.cp_kv_append(r["desc"], r["kd"][None, sl], r["vd"][None, sl], w, r["kc"], r["vc"], r["lens"],
+                                past, dev_status=self.status)
+                cp.cp_prefill_chunk_attn(r["desc"], r["qd"][None, sl], r["kc"], r["vc"], r["lens"], w, w, past,
+                                         r["out"][None, sl], None, commit=True,
+                                         left_pad=r["left"] if rolling else None, dev_status=self.status)
+                past += w
+
+    def config(self):
+        if self.mode == "rolling":
+            return {"workload": "rolling_fp16_mha16_d128_window1024_chunk256_len2048+768",
+                    "aligned_lengths": [r["L"] for r in self.runs], "left_pad": [r["lp"] for r in self.runs],
+                    "visible_pairs": [r["pairs"] for r in self.runs],
+                    "l2": "flushed between timed steps (512 MiB write)", "cuda_graph": True}
+        return {"workload": "fp32_mha8_d64_prompt1000_chunk256", "visible_pairs": self.runs[0]["pairs"],
+                "l2": "flushed between timed steps (512 MiB write)", "cuda_graph": True}
+
+
+def run_chunk_loop(args, rank, world, dev, pk, pk_src):
+    import torch
+    wl = ChunkLoop(dev, args.workload)
+    s = torch.cuda.Stream(dev)
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        for _ in range(2):
+            wl.step()
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        wl.step()
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    for _ in range(max(args.warmup, 3)):
+        g.replay()
+    torch.cuda.synchronize()
+    clocks = ClockSampler()
+    clocks.start()
+    times = time_steps(g.replay, flush, args.steps, torch)
+    clk = clocks.stop()
+    total_ms, value = job_throughput(sum(times), wl.tokens, args.steps, world)
+    ms = total_ms / args.steps
+    if int(wl.status.item()) != 0:
+        raise RuntimeError(f"device status {int(wl.status.item())}")
+    tflops = wl.flops / (ms / 1e3) / 1e12
+    fp32 = args.workload == "fp32"
+    line = {"metric": f"{args.workload} chunked-prefill tokens/s (real rows)", "value": value, "unit": "tokens/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32" if fp32 else "f16",
+            "data": "synthetic", "config": wl.config(), "flops_per_step": wl.flops, "tflops_whole_step": tflops,
+            "tensor_frac_whole_step": None if fp32 else tflops / float(pk["bf16_tflops"]),
+            "gpu_launches": wl.launches * args.steps, "clocks": clk, "peaks": pk_src}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
 
 
 def run_paged(args, rank, world, dev, pk, pk_src):
