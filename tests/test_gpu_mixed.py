@@ -265,3 +265,57 @@ def test_sequence_without_rows_is_reported():
     P.step([0, 1, 2], [0, 2, 1], [39, 299, 89], q.cuda(), kn.cuda(), vn.cuda(), 301)
     torch.cuda.synchronize()
     assert int(P.status.item()) & cp.CP_DEV_BOUNDS
+
+
+@pytest.mark.parametrize("page", [32, 64, 128])
+def test_mixed_step_page_sizes(page):
+    """One mixed step (decode rows at page and split edges plus a prompt
+    chunk) with 32-, 64- and 128-token pages: every row matches the oracle and
+    the pools match it bit for bit."""
+    ctx = [page, page + 1, 513, 1100]
+    prompt = 300
+    n_dec = len(ctx)
+    need = [-(-(n + 64) // page) for n in ctx + [prompt]]
+    max_blocks, num_pages = max(need), sum(need)
+    perm = torch.randperm(num_pages, generator=torch.Generator().manual_seed(page))
+    table = torch.full((len(need), max_blocks), -1, dtype=torch.int32)
+    off = 0
+    for s, nb in enumerate(need):
+        table[s, :nb] = perm[off:off + nb].to(torch.int32)
+        off += nb
+    desc = cp.layer_desc(torch.bfloat16, 0, HQ, HKV, D, cp.CP_CACHE_PAGED, page_size=page,
+                         num_pages=num_pages, max_blocks=max_blocks)
+    kp = torch.full((num_pages, HKV, page, D), float("nan"), dtype=torch.bfloat16, device="cuda")
+    vp = torch.full_like(kp, float("nan"))
+    ok = np.full(tuple(kp.shape), np.nan)
+    ov = np.full(tuple(kp.shape), np.nan)
+    for s, c in enumerate(ctx):  # history: positions [0, c - 1)
+        hk, hv = SI.normal((c - 1, HKV, D), 1200 + s), SI.normal((c - 1, HKV, D), 1300 + s)
+        a = torch.arange(c - 1)
+        pg = table[s, a // page].long()
+        kp[pg, :, a % page] = hk.to("cuda", torch.bfloat16)
+        vp[pg, :, a % page] = hv.to("cuda", torch.bfloat16)
+        ok[pg.numpy(), :, (a % page).numpy()] = f64(hk.to(torch.bfloat16))
+        ov[pg.numpy(), :, (a % page).numpy()] = f64(hv.to(torch.bfloat16))
+    dq, dk, dv = SI.gqa_prompt(n_dec, seed=70 + page)
+    pq, pk, pv = SI.gqa_prompt(prompt, seed=71 + page)
+    q = torch.cat([dq, pq]); kn = torch.cat([dk, pk]); vn = torch.cat([dv, pv])
+    rows = [1] * n_dec + [prompt]
+    past = [c - 1 for c in ctx] + [0]
+    S, T = len(rows), sum(rows)
+    max_ctx = max(p + r for p, r in zip(past, rows))
+    cu = torch.tensor(np.concatenate([[0], np.cumsum(rows)]), dtype=torch.int32, device="cuda")
+    pl = torch.tensor(past, dtype=torch.int32, device="cuda")
+    out = torch.empty(T, HQ, D, dtype=torch.bfloat16, device="cuda")
+    ws = torch.empty(cp.cp_workspace_size(desc, T, max_ctx, S), dtype=torch.uint8, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    cp.cp_mixed_step(desc, q.cuda(), kn.cuda(), vn.cuda(), kp, vp, table.cuda(), cu, pl, S, T, max_ctx, out, ws,
+                     dev_status=status)
+    torch.cuda.synchronize()
+    ref, ok, ov, newp = oracle.mixed_step(f64(q), f64(kn), f64(vn), ok, ov, table.numpy(), rows, past)
+    assert int(status.item()) == 0
+    assert np.abs(f64(out) - ref).max() < BF16_TOL
+    assert pl.tolist() == newp
+    got_k, got_v = f64(kp), f64(vp)
+    mask = ~np.isnan(ok)
+    assert np.array_equal(got_k[mask], ok[mask]) and np.array_equal(got_v[mask], ov[mask])

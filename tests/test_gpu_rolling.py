@@ -75,3 +75,44 @@ def test_rolling_no_overflow_768_equals_plain_prefill():
 def test_rolling_small_ragged():
     """A cache that is not a multiple of the 128-key tile, bf16, head_dim 64."""
     _run_rolling(300, 48, 176, 4, 64, torch.bfloat16, seed=11)
+
+
+def test_rolling_gqa():
+    """Rolling window with grouped-query heads (8 query / 2 KV heads, bf16):
+    compared with the oracle's rolling prefill on the K/V heads repeated per
+    query head (grouped-query attention equals that multi-head attention)."""
+    n_real, c, C, hq, hkv, d = 500, 128, 384, 8, 2, 128
+    G = hq // hkv
+    L = cp.cp_aligned_length(n_real, c)
+    lp = L - n_real
+    q, _, _ = SI.rolling_prompt(L, seed=21, heads=hq, dim=d, dtype=torch.bfloat16)
+    _, k, v = SI.rolling_prompt(L, seed=22, heads=hkv, dim=d, dtype=torch.bfloat16)
+    desc = cp.layer_desc(torch.bfloat16, 1, hq, hkv, d, cp.CP_CACHE_ROLLING, capacity=C)
+    kc = torch.full((1, hkv, C, d), float("nan"), dtype=torch.bfloat16, device="cuda")
+    vc = torch.full_like(kc, float("nan"))
+    lens = torch.zeros(1, dtype=torch.int32, device="cuda")
+    left = torch.tensor([lp], dtype=torch.int32, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = torch.empty(L, hq, d, dtype=torch.bfloat16, device="cuda")
+    qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
+    for ci in range(L // c):
+        sl = slice(ci * c, (ci + 1) * c)
+        cp.cp_kv_append(desc, kd[None, sl], vd[None, sl], c, kc, vc, lens, ci * c, dev_status=status)
+        cp.cp_prefill_chunk_attn(desc, qd[None, sl], kc, vc, lens, c, c, ci * c, out[None, sl], None,
+                                 commit=True, left_pad=left, dev_status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0 and int(lens.item()) == L
+    k_rep = np.repeat(f64(k), G, axis=1)
+    v_rep = np.repeat(f64(v), G, axis=1)
+    ref, snaps = oracle.rolling_prefill(f64(q), k_rep, v_rep, c, C, lp)
+    got = f64(out)
+    assert np.abs(got[lp:] - ref[lp:]).max() < BF16_TOL
+    assert np.isfinite(got).all()
+    # final window: logical slot j holds position a = L - C + j, stored at a mod C
+    ok_k, ok_v = snaps[-1]
+    j = np.arange(C)
+    a = L - C + j
+    keep = a >= 0
+    phys = torch.from_numpy(a[keep] % C)
+    assert torch.equal(kc[0, :, phys].cpu().double(), torch.from_numpy(ok_k[::G][:, keep]))
+    assert torch.equal(vc[0, :, phys].cpu().double(), torch.from_numpy(ok_v[::G][:, keep]))
