@@ -169,6 +169,7 @@ template <typename T, int D>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
+                   const __grid_constant__ CUtensorMap tm_kn, const __grid_constant__ CUtensorMap tm_vn,
                    const AttnArgs a) {
   using L = TcSmem<D>;
   constexpr int DB = L::DB;
@@ -210,6 +211,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_prefetch_desc(&tm_k);
     tma_prefetch_desc(&tm_v);
     tma_prefetch_desc(&tm_o);
+    if (a.kv_direct) {
+      tma_prefetch_desc(&tm_kn);
+      tma_prefetch_desc(&tm_vn);
+    }
   }
   if (warp == 1) {
     tmem_alloc(&bar->tmem_base, kTmemCols);
@@ -278,8 +283,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int st = i & 1;
       const uint32_t ph = (i >> 1) & 1;
       const int j0 = (rank + 2 * i) * kTcBlockN;
+      // A paged tile made only of this call's rows is read from k_new / v_new:
+      // two 16 KB boxes per tensor instead of one small box per page.
+      const bool direct = paged && a.kv_direct && j0 >= past;
       int my_page = -1;  // paged: lane l looks up the page of keys [j0 + l*ps, ...)
-      if (paged && lane < npg) {
+      if (paged && !direct && lane < npg) {
         const int key = j0 + lane * ps;
         if (key < n_valid) {
           const int blk = key / ps;
@@ -303,6 +311,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int db = 0; db < DB; ++db) {
             tma_load_3d(dk + db * kBlockBytes, &tm_k, full, db * 64, j0, s * a.hkv + g);
             tma_load_3d(dv + db * kBlockBytes, &tm_v, full, db * 64, j0, s * a.hkv + g);
+          }
+        }
+      } else if (direct) {
+        // Keys [j0, j0 + 128) are rows row0 + (j0 - past) ... of k_new / v_new
+        // (rows past this sequence's are masked, and zeroed in the last V tile).
+        if (lane == 0) {
+          mbar_arrive_expect_tx(full, 2 * DB * kBlockBytes);
+          for (int db = 0; db < DB; ++db) {
+            tma_load_3d(dk + db * kBlockBytes, &tm_kn, full, db * 64, g, row0 + (j0 - past));
+            tma_load_3d(dv + db * kBlockBytes, &tm_vn, full, db * 64, g, row0 + (j0 - past));
           }
         }
       } else {
@@ -610,7 +628,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 template <typename T, int D>
 cudaError_t launch_t(const AttnArgs& a, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                     const CUtensorMap& to, int pairs_bound, cudaStream_t st) {
+                     const CUtensorMap& to, const CUtensorMap& tkn, const CUtensorMap& tvn, int pairs_bound,
+                     cudaStream_t st) {
   // D = 64 would fit two CTAs per SM, but each CTA takes all 512 TMEM
   // columns; ask for enough shared memory to keep it at one CTA per SM.
   const uint32_t smem = TcSmem<D>::alloc < 120u * 1024u ? 120u * 1024u : TcSmem<D>::alloc;
@@ -642,7 +661,7 @@ cudaError_t launch_t(const AttnArgs& a, const CUtensorMap& tq, const CUtensorMap
   cfg.stream = st;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  e = cudaLaunchKernelEx(&cfg, attn_tc_kernel<T, D>, tq, tk, tv, to, a);
+  e = cudaLaunchKernelEx(&cfg, attn_tc_kernel<T, D>, tq, tk, tv, to, tkn, tvn, a);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
@@ -656,14 +675,16 @@ bool attn_tc_supported(int d, int group, int dtype) {
 
 // pairs_bound: number of 2*128-row Q-tile pairs to cover (one 2-CTA cluster each).
 // to: the output [rows, Hq, D] with the same box as tq (finished tiles are TMA-stored).
+// tkn, tvn: this call's new K/V rows [rows, Hkv, D], box {64, 1, 128} (used when a.kv_direct).
 cudaError_t launch_attn_tc(const AttnArgs& a, int dtype, const CUtensorMap& tq, const CUtensorMap& tk,
-                           const CUtensorMap& tv, const CUtensorMap& to, int pairs_bound, cudaStream_t st) {
+                           const CUtensorMap& tv, const CUtensorMap& to, const CUtensorMap& tkn,
+                           const CUtensorMap& tvn, int pairs_bound, cudaStream_t st) {
   if (pairs_bound <= 0) return cudaSuccess;
   if (dtype == CP_BF16)
-    return a.d == 64 ? launch_t<__nv_bfloat16, 64>(a, tq, tk, tv, to, pairs_bound, st)
-                     : launch_t<__nv_bfloat16, 128>(a, tq, tk, tv, to, pairs_bound, st);
-  return a.d == 64 ? launch_t<__half, 64>(a, tq, tk, tv, to, pairs_bound, st)
-                   : launch_t<__half, 128>(a, tq, tk, tv, to, pairs_bound, st);
+    return a.d == 64 ? launch_t<__nv_bfloat16, 64>(a, tq, tk, tv, to, tkn, tvn, pairs_bound, st)
+                     : launch_t<__nv_bfloat16, 128>(a, tq, tk, tv, to, tkn, tvn, pairs_bound, st);
+  return a.d == 64 ? launch_t<__half, 64>(a, tq, tk, tv, to, tkn, tvn, pairs_bound, st)
+                   : launch_t<__half, 128>(a, tq, tk, tv, to, tkn, tvn, pairs_bound, st);
 }
 
 }  // namespace cp

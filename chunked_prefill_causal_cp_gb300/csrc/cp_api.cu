@@ -136,9 +136,11 @@ bool make_tc_maps(const cp_layer_desc* d, const void* q, const void* out, int64_
 int launch_result(cudaError_t e) { return e == cudaSuccess ? CP_OK : CP_ERR_CUDA; }
 
 // Attention over every sequence of `rows`, routed by dtype and row count.
+// k_new / v_new (may be NULL): this call's new K/V rows [rows_total, Hkv, D]; when given with a
+// paged cache, the tensor-core kernel reads the tiles made only of new rows from them.
 int run_attention(const cp_layer_desc* d, const AttnArgs& base, int64_t rows_total, int rows_max_per_seq,
                   const void* k, const void* v, int batch_for_maps, void* workspace, size_t ws_bytes,
-                  cudaStream_t st) {
+                  cudaStream_t st, const void* k_new = nullptr, const void* v_new = nullptr) {
   const int G = d->num_q_heads / d->num_kv_heads;
   AttnArgs a = base;
   if (d->dtype == CP_F32) {
@@ -162,8 +164,18 @@ int run_attention(const cp_layer_desc* d, const AttnArgs& base, int64_t rows_tot
   }
   if (any_multi || !decode_ok) {
     a.min_rows = decode_ok ? 2 : 1;
-    CUtensorMap tq, to, tk, tv;
+    CUtensorMap tq, to, tk, tv, tkn, tvn;
     if (!make_tc_maps(d, a.q, a.out, rows_total, k, v, batch_for_maps, &tq, &to, &tk, &tv)) return CP_ERR_CUDA;
+    std::memset(&tkn, 0, sizeof(tkn));
+    std::memset(&tvn, 0, sizeof(tvn));
+    a.kv_direct = 0;
+    if (d->kind == CP_CACHE_PAGED && k_new && v_new) {
+      const uint64_t D = d->head_dim;
+      if (!encode_3d(&tkn, d->dtype, k_new, D, d->num_kv_heads, (uint64_t)rows_total, 64, 1, kTcBlockN) ||
+          !encode_3d(&tvn, d->dtype, v_new, D, d->num_kv_heads, (uint64_t)rows_total, 64, 1, kTcBlockN))
+        return CP_ERR_CUDA;
+      a.kv_direct = 1;
+    }
     const int ppt = 2 * (kTcBlockM / G);  // tokens per pair of 128-row Q tiles
     int64_t pairs;
     if (a.rows.rows_uniform > 0)
@@ -171,7 +183,7 @@ int run_attention(const cp_layer_desc* d, const AttnArgs& base, int64_t rows_tot
     else
       pairs = (rows_total + ppt - 1) / ppt + a.rows.num_seqs;
     if (2 * pairs > INT32_MAX) return CP_ERR_UNSUPPORTED;
-    return launch_result(launch_attn_tc(a, d->dtype, tq, tk, tv, to, (int)pairs, st));
+    return launch_result(launch_attn_tc(a, d->dtype, tq, tk, tv, to, tkn, tvn, (int)pairs, st));
   }
   return CP_OK;
 }
@@ -337,7 +349,7 @@ int cp_mixed_step(const cp_layer_desc* desc, const void* q, const void* k_new, c
   // work and is not launched.
   const int64_t max_rows_per_seq = total_rows >= num_seqs ? (int64_t)total_rows - num_seqs + 1 : total_rows;
   r = run_attention(desc, a, total_rows, (int)max_rows_per_seq, k_pages, v_pages, 0, workspace, workspace_bytes,
-                    st);
+                    st, k_new, v_new);
   if (r != CP_OK) return r;
   return launch_result(launch_commit(past_len, rows, -1, dev_status, st));
 }

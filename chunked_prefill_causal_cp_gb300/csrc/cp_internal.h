@@ -60,6 +60,8 @@ struct AttnArgs {
   float* part_ml;          // [num_seqs, hq, max_splits, 2] (max, sum) in log2 domain
   int max_splits;
   int* status;             // optional CP_DEV_* bits
+  int kv_direct;           // tensor-core kernel: this call's new K/V rows may be read from
+                           // k_new / v_new ([rows_total, hkv, d]) instead of the paged pool
 };
 
 struct AppendArgs {
@@ -114,7 +116,8 @@ cudaError_t launch_commit(int* lens, const SeqRows& rows, int add_uniform, int* 
 cudaError_t launch_pad_rows(void* base, int batch, int rows_padded, int real_rows, int row_bytes, cudaStream_t st);
 cudaError_t launch_attn_f32(const AttnArgs& a, int rows_bound, cudaStream_t st);
 cudaError_t launch_attn_tc(const AttnArgs& a, int dtype, const CUtensorMap& tq, const CUtensorMap& tk,
-                           const CUtensorMap& tv, const CUtensorMap& to, int pairs_bound, cudaStream_t st);
+                           const CUtensorMap& tv, const CUtensorMap& to, const CUtensorMap& tkn,
+                           const CUtensorMap& tvn, int pairs_bound, cudaStream_t st);
 // Split-KV decode; `counter` is one int of device scratch (the persistent
 // grid's work counter, cleared by the launch).
 cudaError_t launch_decode(const AttnArgs& a, int dtype, int* counter, cudaStream_t st);
