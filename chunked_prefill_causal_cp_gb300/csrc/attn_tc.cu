@@ -20,14 +20,18 @@
 // padded and an unpadded run of the same rows do identical arithmetic; tiles
 // past the pair's last query position are never loaded (causal tile skip).
 //
-// Warp roles (320 threads per CTA):
+// Warp roles (384 threads per CTA, three warpgroups):
 //   warp 0      TMA producer: both Q tiles once, then this CTA's K and V tiles
-//               in a 2-stage ring, one stage = one K tile + one V tile (paged
-//               caches: one box per page).
+//               in a 2-stage ring, one stage = one K tile + one V tile, each
+//               with its own barrier (paged caches: one box per page).  The
+//               first stage is issued as Q0, K, Q1, V, so the first MMA waits
+//               for a quarter of the start-up bytes.
 //   warp 1      TMEM allocator and MMA issuer (one elected lane).  Per KV tile:
 //               S0 = Q0 K^T, S1 = Q1 K^T (A, B K-major in shared memory);
 //               O0 += P0 V, O1 += P1 V (A = P in TMEM, B = V MN-major).
-//   warps 2-5   softmax group 0 (Q tile 0);  warps 6-9  softmax group 1 (Q tile 1).
+//   warps 2-3   idle after set-up (they fill the control warpgroup, whose
+//               registers go to the softmax warpgroups).
+//   warps 4-7   softmax group 0 (Q tile 0);  warps 8-11 softmax group 1 (Q tile 1).
 // TMEM (512 columns): group w uses [256w, 256w+128) for S/P, [256w+128, +D) for O.
 // Thread m of a group owns row m (TMEM lane m): it reads its S row, masks by
 // absolute position, exponentiates in the log2 domain against a running max,
@@ -43,11 +47,13 @@
 // a fixed order (even-tile half first): rank r finishes the rows of Q tile r.
 // Once a CTA's own MMAs are complete it tells its peer (a remote mbarrier
 // arrive) that its K/V stages may receive; the peer's group for the other Q
-// tile stages its partial O rows in its own K stages (16-byte chunks XOR-
-// swizzled by row, so the row-per-thread stores are conflict-free) and sends
-// them with one bulk shared-to-shared copy, completed on the receiver's
-// mbarrier.  The receiver combines, writes the finished 16-bit rows into its
-// Q buffer in the TMA layout and stores the tile with a TMA tensor store.
+// tile stages its partial O rows in its own K stages, 32 columns at a time
+// (16-byte pieces XOR-swizzled by row, so the row-per-thread stores are
+// conflict-free), and sends each 16 KB chunk with a bulk shared-to-shared
+// copy as soon as it is staged, completed on one of the receiver's mbarriers.
+// The receiver combines each chunk as it lands, writes the finished 16-bit
+// rows into its Q buffer in the TMA layout and stores the tile with a TMA
+// tensor store.
 //
 // Keys beyond the written length inside the last tile may hold stale or
 // poisoned bytes; their scores are masked and the MMA warp zeroes those V rows
@@ -66,18 +72,25 @@
 namespace cp {
 namespace {
 
-constexpr int kThreads = 320;
+constexpr int kThreads = 384;
+// Register split: the kernel is compiled at kRegsLaunch per thread (the most
+// 384 threads may have); the control warpgroup (warps 0-3) then drops to
+// kRegsControl and hands the rest to the two softmax warpgroups.
+constexpr int kRegsLaunch = 168;
+constexpr int kRegsControl = 104;
+constexpr int kRegsSoftmax = 200;
+static_assert(128 * kRegsControl + 256 * kRegsSoftmax == kThreads * kRegsLaunch, "the split must add up");
 constexpr int kStages = 2;
 constexpr uint32_t kBlockBytes = 128 * 128;  // [128 rows][64 x 16-bit] = 16 KB
 constexpr uint32_t kTmemCols = 512;
 constexpr float kRescaleLog2 = 8.0f;         // O is rescaled when the max grows by > 2^8
 
 struct __align__(16) TcBarriers {
-  uint64_t q_full;
-  uint64_t kv_full[kStages], kv_empty[kStages];  // a stage holds one K tile and one V tile
+  uint64_t q_full[2];                                          // Q tile 0 / Q tile 1 landed
+  uint64_t k_full[kStages], v_full[kStages], kv_empty[kStages];  // a stage holds one K tile and one V tile
   uint64_t s_full[2], p_ready[2];
   uint64_t o_final;
-  uint64_t merge_full;  // the peer's partial for this CTA's rows has landed
+  uint64_t merge_full[4];  // column chunk c of the peer's partial for this CTA's rows has landed
   uint64_t peer_free;   // the peer's K/V stages may receive this CTA's partial
   uint32_t tmem_base;
   int abort;
@@ -95,17 +108,21 @@ struct TcSmem {
   static constexpr uint32_t bytes = bar_off + sizeof(TcBarriers);
   static constexpr uint32_t alloc = bytes + 1024;  // slack for 1024-byte alignment
   // After the main loop the K stages hold this CTA's outgoing partial O rows
-  // and the V stages the peer's incoming ones: [128][D] fp32 each.
+  // and the V stages the peer's incoming ones: 128 rows x D fp32 each, as
+  // D/32 column chunks of 16 KB that travel (and are combined) one by one.
   static constexpr uint32_t kMergeBytes = 128u * D * 4u;
+  static constexpr int kMergeChunks = D / 32;
+  static constexpr uint32_t kChunkBytes = 128u * 32u * 4u;
   static_assert(kStages * DB * kBlockBytes == kMergeBytes, "a merge buffer is exactly the K (or V) stages");
+  static_assert(kMergeChunks <= 4, "merge_full has one barrier per column chunk");
 };
 
-// Byte offset of 16-byte chunk q of row m in a [128][D] fp32 merge buffer:
-// chunks are XOR-swizzled by (m mod 8), so the 8 rows a quarter-warp touches
-// at once fall on distinct banks.
-template <int D>
-__device__ __forceinline__ uint32_t merge_off(int m, int q) {
-  return (uint32_t)m * (D * 4) + (uint32_t)((q ^ (m & 7)) * 16);
+// Byte offset of 16-byte piece e (columns 32c + 4e .. +3) of row m in a merge
+// buffer: chunk c is a contiguous [128 rows][128 B] block, and the pieces of
+// a row are XOR-swizzled by (m mod 8), so the 8 rows a quarter-warp touches at
+// once fall on distinct banks.
+__device__ __forceinline__ uint32_t merge_off(int m, int c, int e) {
+  return (uint32_t)c * (128u * 128u) + (uint32_t)m * 128u + (uint32_t)((e ^ (m & 7)) * 16);
 }
 
 template <typename T>
@@ -193,17 +210,18 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   // ---- set-up that reads no global memory: it may overlap the previous kernel
   if (threadIdx.x == 0) {
-    mbar_init(&bar->q_full, 1);
     for (int i = 0; i < kStages; ++i) {
-      mbar_init(&bar->kv_full[i], 1);
+      mbar_init(&bar->k_full[i], 1);
+      mbar_init(&bar->v_full[i], 1);
       mbar_init(&bar->kv_empty[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
+      mbar_init(&bar->q_full[i], 1);
       mbar_init(&bar->s_full[i], 1);
       mbar_init(&bar->p_ready[i], 128);
     }
     mbar_init(&bar->o_final, 1);
-    mbar_init(&bar->merge_full, 1);
+    for (int c = 0; c < L::kMergeChunks; ++c) mbar_init(&bar->merge_full[c], 1);
     mbar_init(&bar->peer_free, 1);
     bar->abort = 0;
     fence_barrier_init();
@@ -265,16 +283,25 @@ __global__ void __launch_bounds__(kThreads, 1)
   const bool own_tile = rank == 0 || q1;   // Q tile `rank` (finished here) has rows
   const bool peer_tile = rank == 1 || q1;  // Q tile `1 - rank` (finished by the peer) has rows
   const uint32_t peer = (uint32_t)(1 - rank);
-  if (threadIdx.x == 0 && own_tile) mbar_arrive_expect_tx(&bar->merge_full, L::kMergeBytes + 256u * 4u);
+  if (threadIdx.x == 0 && own_tile)
+    for (int c = 0; c < L::kMergeChunks; ++c)  // chunk 0 also brings the peer's (max, sum)
+      mbar_arrive_expect_tx(&bar->merge_full[c], L::kChunkBytes + (c == 0 ? 256u * 4u : 0u));
 
+  if (warp < 4) {
+  // The control warpgroup gives up registers for the softmax warpgroups.  Each
+  // role keeps to its own branch up to the final cluster barrier, so the
+  // compiler holds each branch to its own register budget.
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsControl));
   if (warp == 0) {
     // ================================================================ producer
-    if (lane == 0 && nmine > 0) {
-      mbar_arrive_expect_tx(&bar->q_full, (q1 ? 2 : 1) * DB * kBlockBytes);
-      for (int w = 0; w < (q1 ? 2 : 1); ++w)
-        for (int db = 0; db < DB; ++db)
-          tma_load_3d(sQ + (w * DB + db) * kBlockBytes, &tm_q, &bar->q_full, db * 64, g * G, row0 + t0 + w * rpt);
-    }
+    // Issue order Q0, K0, Q1, V0, K1, V1, ...: the first MMA (S0 = Q0 K0^T)
+    // waits for 64 KB instead of both Q tiles and the whole first stage.
+    auto load_q = [&](int w) {
+      mbar_arrive_expect_tx(&bar->q_full[w], DB * kBlockBytes);
+      for (int db = 0; db < DB; ++db)
+        tma_load_3d(sQ + (w * DB + db) * kBlockBytes, &tm_q, &bar->q_full[w], db * 64, g * G, row0 + t0 + w * rpt);
+    };
+    if (lane == 0 && nmine > 0) load_q(0);
     const int ps = a.cache.page_size;
     const int npg = paged ? kTcBlockN / ps : 0;
     // One stage = the K tile and the V tile of one KV tile, signalled together.
@@ -302,37 +329,44 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       if (lane == 0) ok = mbar_wait(&bar->kv_empty[st], ph ^ 1, abort_flag, a.status);
       if (!__shfl_sync(0xffffffffu, ok, 0)) break;
-      uint64_t* full = &bar->kv_full[st];
+      uint64_t* kf = &bar->k_full[st];
+      uint64_t* vf = &bar->v_full[st];
       uint8_t* dk = sK + st * DB * kBlockBytes;
       uint8_t* dv = sV + st * DB * kBlockBytes;
-      if (!paged) {
+      if (!paged || direct) {
+        // Contiguous: keys [j0, j0 + 128) of KV head g.  Direct: they are rows
+        // row0 + (j0 - past) ... of k_new / v_new (rows past this sequence's
+        // are masked, and zeroed in the last V tile).
         if (lane == 0) {
-          mbar_arrive_expect_tx(full, 2 * DB * kBlockBytes);
-          for (int db = 0; db < DB; ++db) {
-            tma_load_3d(dk + db * kBlockBytes, &tm_k, full, db * 64, j0, s * a.hkv + g);
-            tma_load_3d(dv + db * kBlockBytes, &tm_v, full, db * 64, j0, s * a.hkv + g);
-          }
-        }
-      } else if (direct) {
-        // Keys [j0, j0 + 128) are rows row0 + (j0 - past) ... of k_new / v_new
-        // (rows past this sequence's are masked, and zeroed in the last V tile).
-        if (lane == 0) {
-          mbar_arrive_expect_tx(full, 2 * DB * kBlockBytes);
-          for (int db = 0; db < DB; ++db) {
-            tma_load_3d(dk + db * kBlockBytes, &tm_kn, full, db * 64, g, row0 + (j0 - past));
-            tma_load_3d(dv + db * kBlockBytes, &tm_vn, full, db * 64, g, row0 + (j0 - past));
-          }
+          const CUtensorMap* mk = direct ? &tm_kn : &tm_k;
+          const CUtensorMap* mv = direct ? &tm_vn : &tm_v;
+          const int c1 = direct ? g : j0;
+          const int c2 = direct ? row0 + (j0 - past) : s * a.hkv + g;
+          mbar_arrive_expect_tx(kf, DB * kBlockBytes);
+          for (int db = 0; db < DB; ++db) tma_load_3d(dk + db * kBlockBytes, mk, kf, db * 64, c1, c2);
+          if (i == 0 && q1) load_q(1);
+          mbar_arrive_expect_tx(vf, DB * kBlockBytes);
+          for (int db = 0; db < DB; ++db) tma_load_3d(dv + db * kBlockBytes, mv, vf, db * 64, c1, c2);
         }
       } else {
-        if (lane == 0) mbar_arrive_expect_tx(full, 2u * (uint32_t)__popc(page_mask) * DB * ps * 128u);
+        const uint32_t bytes = (uint32_t)__popc(page_mask) * DB * ps * 128u;
+        if (lane == 0) {
+          mbar_arrive_expect_tx(kf, bytes);
+          mbar_arrive_expect_tx(vf, bytes);
+        }
         __syncwarp();
         for (int pi = 0; pi < npg; ++pi) {
           const int page = __shfl_sync(0xffffffffu, my_page, pi);
           if (lane == 0 && page >= 0)
-            for (int db = 0; db < DB; ++db) {
-              tma_load_3d(dk + db * kBlockBytes + pi * ps * 128, &tm_k, full, db * 64, 0, page * a.hkv + g);
-              tma_load_3d(dv + db * kBlockBytes + pi * ps * 128, &tm_v, full, db * 64, 0, page * a.hkv + g);
-            }
+            for (int db = 0; db < DB; ++db)
+              tma_load_3d(dk + db * kBlockBytes + pi * ps * 128, &tm_k, kf, db * 64, 0, page * a.hkv + g);
+        }
+        if (lane == 0 && i == 0 && q1) load_q(1);
+        for (int pi = 0; pi < npg; ++pi) {
+          const int page = __shfl_sync(0xffffffffu, my_page, pi);
+          if (lane == 0 && page >= 0)
+            for (int db = 0; db < DB; ++db)
+              tma_load_3d(dv + db * kBlockBytes + pi * ps * 128, &tm_v, vf, db * 64, 0, page * a.hkv + g);
         }
       }
       issued = i;
@@ -340,14 +374,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0 && *abort_flag) {
       // Let copies already in flight land before the CTA's shared memory is released.
       volatile int zero = 0;
+      if (nmine > 0) mbar_wait(&bar->q_full[0], 0, &zero, nullptr);
+      if (q1 && issued >= 0) mbar_wait(&bar->q_full[1], 0, &zero, nullptr);
       for (int t = issued - 1; t <= issued; ++t)
-        if (t >= 0) mbar_wait(&bar->kv_full[t & 1], (t >> 1) & 1, &zero, nullptr);
+        if (t >= 0) {
+          mbar_wait(&bar->k_full[t & 1], (t >> 1) & 1, &zero, nullptr);
+          mbar_wait(&bar->v_full[t & 1], (t >> 1) & 1, &zero, nullptr);
+        }
     }
   } else if (warp == 1) {
     // ================================================================ MMA issuer
     // Lane 0 alone polls and issues; a tcgen05.mma holds its thread for most
     // of its own execution time, so the loop keeps work between MMAs minimal:
-    // per KV tile three waits (P0, K/V of the next tile, P1) and three commits.
+    // per KV tile four waits (P0, V, K of the next tile, P1) and three commits.
     if (lane == 0) {
       auto wait = [&](uint64_t* b, uint32_t parity) { return mbar_wait(b, parity, abort_flag, a.status); };
       constexpr uint64_t kTileStep = (DB * kBlockBytes) >> 4;
@@ -371,15 +410,22 @@ __global__ void __launch_bounds__(kThreads, 1)
           mma_ts(tmem + 256u * w + 128u, tmem + 256u * w + kk * 8, v_desc + ((kk * 2048) >> 4), kIdescPV,
                  (i > 0 || kk > 0) ? 1u : 0u);
       };
-      bool ok = nmine > 0 && wait(&bar->q_full, 0) && wait(&bar->kv_full[0], 0);
+      bool ok = nmine > 0 && wait(&bar->q_full[0], 0) && wait(&bar->k_full[0], 0);
       if (ok) {
         tc_fence_after();
         issue_qk(0, 0);
-        if (q1) issue_qk(1, 0);
+      }
+      if (ok && q1) {
+        ok = wait(&bar->q_full[1], 0);
+        if (ok) {
+          tc_fence_after();
+          issue_qk(1, 0);
+        }
       }
       for (int i = 0; ok && i < nmine; ++i) {
         const bool more = i + 1 < nmine;
         if (!wait(&bar->p_ready[0], i & 1)) break;
+        if (!wait(&bar->v_full[i & 1], (i >> 1) & 1)) break;
         if (rank + 2 * i == ntiles - 1) {  // last KV tile: zero V rows past the written keys
           const int tail = n_valid - (ntiles - 1) * kTcBlockN;
           if (tail < kTcBlockN) {
@@ -395,7 +441,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         issue_pv(0, i);
         if (more) {
-          if (!wait(&bar->kv_full[(i + 1) & 1], ((i + 1) >> 1) & 1)) break;
+          if (!wait(&bar->k_full[(i + 1) & 1], ((i + 1) >> 1) & 1)) break;
           issue_qk(0, i + 1);
         }
         if (q1) {
@@ -413,10 +459,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     __syncwarp();
   }
-
+  cluster_wait();  // the peer's barriers are initialised
+  if (warp == 1 && lane == 0 && own_tile) {
+    // This CTA's MMAs are complete (the issuer waited o_final): its K/V stages are free.
+    mbar_arrive_remote(mapa_shared(smem_u32(&bar->peer_free), peer));
+  }
+  } else {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsSoftmax));
   // ================================================================ softmax groups
-  const bool is_softmax = warp >= 2;
-  const int grp = (warp - 2) >> 2;          // Q tile of this group
+  const int grp = (warp - 4) >> 2;          // Q tile of this group
   const int quarter = warp & 3;             // TMEM lanes [32*quarter, +32)
   const int mrow = quarter * 32 + lane;     // this thread's row of its Q tile
   const int tok = t0 + grp * rpt + mrow / G;
@@ -428,7 +479,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   float m_run = -INFINITY;  // max used for exponentiation (log2 domain)
   float l_run = 0.f;
   bool alive = true;
-  if (is_softmax && (grp == 0 || q1)) {
+  if (grp == 0 || q1) {
     const int p_row = row_ok ? past + tok : -1;  // absolute query position
     const int lo = rolling ? max(a.left_pad ? a.left_pad[s] : 0, 0) : 0;
     // Rolling: slot -> absolute position (see cp_kv.cuh), split at slot r_slot.
@@ -512,19 +563,20 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   // ================================================================ merge across the pair
   volatile int zero = 0;
-  const bool done = (!is_softmax || warp_wait(&bar->o_final, 0, &zero, a.status)) && alive;
+  const bool done = warp_wait(&bar->o_final, 0, &zero, a.status) && alive;
   tc_fence_after();
   __syncwarp();
   cluster_wait();  // the peer's barriers are initialised
   const bool have_o = nmine > 0;  // this CTA wrote O (else its TMEM O is unset: send zeros)
-  if (warp == 1 && lane == 0 && own_tile) {
-    // This CTA's MMAs are complete (the issuer waited o_final): its K/V stages are free.
-    mbar_arrive_remote(mapa_shared(smem_u32(&bar->peer_free), peer));
-  }
-  if (is_softmax && grp != rank && peer_tile) {
-    // Rows of Q tile (1 - rank) are finished by the peer: stage and send this CTA's partial.
+  if (grp != rank && peer_tile) {
+    // Rows of Q tile (1 - rank) are finished by the peer: stage this CTA's
+    // partial one 32-column chunk at a time and send each chunk as soon as it
+    // is staged, so one chunk's transfer overlaps the staging of the next.
+    bar->out_ml[mrow] = have_o ? m_run : -INFINITY;
+    bar->out_ml[128 + mrow] = have_o ? l_run : 0.f;
+    bool send = true;  // (meaningful in the thread of row 0, which sends)
 #pragma unroll
-    for (int c = 0; c < D / 32; ++c) {
+    for (int c = 0; c < L::kMergeChunks; ++c) {
       uint32_t ov[32];
       if (have_o) {
         tmem_ld32(o_col + 32 * c, ov);
@@ -535,22 +587,25 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
 #pragma unroll
       for (int e = 0; e < 8; ++e)
-        *reinterpret_cast<uint4*>(sK + merge_off<D>(mrow, c * 8 + e)) =
+        *reinterpret_cast<uint4*>(sK + merge_off(mrow, c, e)) =
             make_uint4(ov[4 * e], ov[4 * e + 1], ov[4 * e + 2], ov[4 * e + 3]);
-    }
-    bar->out_ml[mrow] = have_o ? m_run : -INFINITY;
-    bar->out_ml[128 + mrow] = have_o ? l_run : 0.f;
-    fence_proxy_async_smem();  // the bulk copy reads these through the async proxy
-    asm volatile("bar.sync 1, 128;" ::: "memory");
-    if (mrow == 0 && mbar_wait_cluster(&bar->peer_free, 0, a.status)) {
-      const uint32_t rbar = mapa_shared(smem_u32(&bar->merge_full), peer);
-      bulk_copy_to_peer(mapa_shared(smem_u32(sV), peer), sK, L::kMergeBytes, rbar);
-      bulk_copy_to_peer(mapa_shared(smem_u32(bar->peer_ml), peer), bar->out_ml, 256u * 4u, rbar);
+      fence_proxy_async_smem();  // the bulk copy reads these through the async proxy
+      asm volatile("bar.sync 1, 128;" ::: "memory");
+      if (mrow == 0) {
+        if (c == 0) send = mbar_wait_cluster(&bar->peer_free, 0, a.status);
+        if (send) {
+          const uint32_t rbar = mapa_shared(smem_u32(&bar->merge_full[c]), peer);
+          bulk_copy_to_peer(mapa_shared(smem_u32(sV + c * L::kChunkBytes), peer), sK + c * L::kChunkBytes,
+                            L::kChunkBytes, rbar);
+          if (c == 0) bulk_copy_to_peer(mapa_shared(smem_u32(bar->peer_ml), peer), bar->out_ml, 256u * 4u, rbar);
+        }
+      }
     }
   }
-  if (is_softmax && grp == rank && own_tile) {
-    // Fixed order: the even-tile half (rank 0's partial) first.
-    const bool got = mbar_wait_cluster(&bar->merge_full, 0, a.status);
+  if (grp == rank && own_tile) {
+    // Fixed order: the even-tile half (rank 0's partial) first.  Chunk 0
+    // brings the peer's (max, sum); each chunk is combined as it lands.
+    bool got = mbar_wait_cluster(&bar->merge_full[0], 0, a.status);
     const float m_own = have_o ? m_run : -INFINITY, l_own = have_o ? l_run : 0.f;
     const float m_peer = bar->peer_ml[mrow], l_peer = bar->peer_ml[128 + mrow];
     const float mA = rank == 0 ? m_own : m_peer, lA = rank == 0 ? l_own : l_peer;
@@ -567,7 +622,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t* sOut = sQ + rank * DB * kBlockBytes;
     T* out = static_cast<T*>(a.out) + ((long long)(row0 + tok) * a.hq + head) * D;
 #pragma unroll
-    for (int c = 0; c < D / 32; ++c) {
+    for (int c = 0; c < L::kMergeChunks; ++c) {
+      if (c > 0 && got) got = mbar_wait_cluster(&bar->merge_full[c], 0, a.status);
       uint32_t ov[32];
       if (have_o) {
         tmem_ld32(o_col + 32 * c, ov);
@@ -579,7 +635,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t pk[16];
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
-        const float4 pr = *reinterpret_cast<const float4*>(sV + merge_off<D>(mrow, c * 8 + e));
+        const float4 pr = *reinterpret_cast<const float4*>(sV + merge_off(mrow, c, e));
         const float own[4] = {__uint_as_float(ov[4 * e]), __uint_as_float(ov[4 * e + 1]),
                               __uint_as_float(ov[4 * e + 2]), __uint_as_float(ov[4 * e + 3])};
         const float prv[4] = {pr.x, pr.y, pr.z, pr.w};
@@ -611,10 +667,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int db = 0; db < DB; ++db)
           tma_store_3d(&tm_o, sOut + db * kBlockBytes, db * 64, g * G, row0 + tile_tok0);
         bulk_commit_group();
-        bulk_wait_all();
+        bulk_wait_read_all();  // the Q buffer is read out; the writes finish with the grid
       }
     }
   }
+  }  // softmax warpgroups
 
   // Both CTAs leave together: the copies each sent into the other have landed
   // and been read before either CTA's shared memory is released.
@@ -642,6 +699,12 @@ cudaError_t launch_t(const AttnArgs& a, const CUtensorMap& tq, const CUtensorMap
   if (e != cudaSuccess) return e;
   const uint64_t bit = 1ull << (dev & 63);
   if (!(ready_mask.load(std::memory_order_acquire) & bit)) {
+    // The register split is only sound at the per-thread count it was sized
+    // for: refuse to launch a build that came out at another count.
+    cudaFuncAttributes fa;
+    e = cudaFuncGetAttributes(&fa, attn_tc_kernel<T, D>);
+    if (e != cudaSuccess) return e;
+    if (fa.numRegs != kRegsLaunch) return cudaErrorInvalidDeviceFunction;
     e = cudaFuncSetAttribute(attn_tc_kernel<T, D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     ready_mask.fetch_or(bit, std::memory_order_release);

@@ -165,9 +165,11 @@ __device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, const void*
 
 __device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 
-// Wait until every committed bulk group of this thread has completed (its
-// shared-memory source read and its global writes performed).
-__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+// Wait until every committed bulk group of this thread has read its
+// shared-memory source (the source may then be reused or released).
+__device__ __forceinline__ void bulk_wait_read_all() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
 
 // ---------------------------------------------------------------- clusters
 
