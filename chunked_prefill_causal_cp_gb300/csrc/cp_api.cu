@@ -68,13 +68,10 @@ float scale_log2(const cp_layer_desc* d) {
 
 int64_t max_splits_for(int32_t max_ctx) { return ((int64_t)max_ctx + kDecodeSplit - 1) / kDecodeSplit; }
 
-// Decode workspace: the persistent grid's work counter (its own 256 bytes),
-// then the split partials (output rows, then max and sum).
-constexpr int64_t kDecodeCounterBytes = 256;
-
+// Decode workspace: the split partials (output rows, then max and sum).
 int64_t decode_ws_bytes(const cp_layer_desc* d, int32_t max_ctx, int32_t num_seqs) {
   const int64_t ms = max_splits_for(max_ctx);
-  return kDecodeCounterBytes + (int64_t)num_seqs * d->num_q_heads * ms * (d->head_dim + 2) * (int64_t)sizeof(float);
+  return (int64_t)num_seqs * d->num_q_heads * ms * (d->head_dim + 2) * (int64_t)sizeof(float);
 }
 
 // ---- tensor maps (driver entry point fetched through the runtime)
@@ -155,11 +152,10 @@ int run_attention(const cp_layer_desc* d, const AttnArgs& base, int64_t rows_tot
     const int64_t need = decode_ws_bytes(d, a.max_ctx, a.rows.num_seqs);
     if (workspace == nullptr || (int64_t)ws_bytes < need) return CP_ERR_WORKSPACE;
     AttnArgs dec = a;
-    int* counter = static_cast<int*>(workspace);
-    dec.part_o = reinterpret_cast<float*>(static_cast<char*>(workspace) + kDecodeCounterBytes);
+    dec.part_o = static_cast<float*>(workspace);
     dec.max_splits = (int)max_splits_for(a.max_ctx);
     dec.part_ml = dec.part_o + (int64_t)a.rows.num_seqs * d->num_q_heads * dec.max_splits * d->head_dim;
-    const int r = launch_result(launch_decode(dec, d->dtype, counter, st));
+    const int r = launch_result(launch_decode(dec, d->dtype, st));
     if (r != CP_OK) return r;
   }
   if (any_multi || !decode_ok) {

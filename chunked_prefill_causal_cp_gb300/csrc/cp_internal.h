@@ -118,9 +118,8 @@ cudaError_t launch_attn_f32(const AttnArgs& a, int rows_bound, cudaStream_t st);
 cudaError_t launch_attn_tc(const AttnArgs& a, int dtype, const CUtensorMap& tq, const CUtensorMap& tk,
                            const CUtensorMap& tv, const CUtensorMap& to, const CUtensorMap& tkn,
                            const CUtensorMap& tvn, int pairs_bound, cudaStream_t st);
-// Split-KV decode; `counter` is one int of device scratch (the persistent
-// grid's work counter, cleared by the launch).
-cudaError_t launch_decode(const AttnArgs& a, int dtype, int* counter, cudaStream_t st);
+// Split-KV decode: partials into a.part_o / a.part_ml, then their combine.
+cudaError_t launch_decode(const AttnArgs& a, int dtype, cudaStream_t st);
 
 // Tensor-core path tiling (shared with the host so it can size grids and
 // tensor-map boxes).

@@ -2,24 +2,37 @@
 //
 // A decode row reads its sequence's whole K/V once and does ~1 FLOP per byte
 // (Ultralytics glossary "Chunked Prefill", "Prefill, decode and generation
-// stalls": decode is memory-bandwidth bound), so this path is built around
-// coalesced 16-byte loads, not the tensor cores.
+// stalls": decode is memory-bandwidth bound), so this path is built to keep
+// HBM streaming: K and V rows go straight from global memory into registers
+// with coalesced 16-byte loads, and the few FLOPs per byte run on the warp-
+// level tensor-core MMA (m16n8k16, fp32 accumulate), which spends one
+// instruction where fp32 FMAs and lane reductions would spend dozens.
 //
-// decode_split_kernel: one CTA per (split of 512 keys, KV head, sequence).
-//   The GQA group's query heads share every K/V row the CTA loads.  A group
-//   of D/16 lanes holds one key row (16 elements = two 16-byte loads per
-//   lane); each lane keeps the group's q values for its 16 dimensions, the
-//   products accumulate with packed fp32x2 FMAs, the partial dot products
-//   are reduced with xor shuffles, scores go to shared memory, the CTA takes
-//   the split's max and sum (log2 domain), then streams V once (again with
-//   packed FMAs) and writes the unnormalised partial output.  Instruction
-//   count per loaded byte, not bandwidth, is what limits this path, hence
-//   the wide lanes and packed arithmetic.
+// decode_split_kernel: one CTA per (split of 512 keys, KV head, sequence), four
+//   warps of 128 keys each.  The GQA group's G <= 8 query heads ride in the
+//   MMA's 8-wide N dimension (heads past G are zero).
+//   Scores: S^T[16 keys x 8 heads] = K[16 keys x D] Q^T, as D/16 MMAs per
+//   16-key tile.  Lane (g, q) (g = lane / 4, q = lane % 4) loads keys g and
+//   g + 8 of the tile, 16-byte chunks q, q + 4, ...; under the head-dimension
+//   order that maps MMA column pair (2q, 2q + 1) of slice (j, u) to elements
+//   4u, 4u + 1 of chunk q + 4j (and columns 2q + 8, 2q + 9 to 4u + 2, 4u + 3),
+//   those loaded registers ARE the A fragments, and the query is loaded into
+//   B fragments in the same order.  The dot product does not depend on the
+//   order in which the head dimension is summed.
+//   Softmax: each warp takes its own max per head over its 128 keys (log2
+//   domain), writes P (16-bit) to shared memory and sums it.
+//   Output: O^T[16 dims x 8 heads] += V^T[16 dims x 16 keys] P^T.  Lane (g, q)
+//   loads keys 2q, 2q + 1, 2q + 8, 2q + 9 of the tile, chunks g, g + 8, ...;
+//   byte permutes pair up the same element of two keys, which is the A
+//   fragment of the 16-row block of dims {8c + 2i, 8c + 2i + 1 : c = g + 8m}.
+//   The four warps' partials are merged in warp order with their maxima, and
+//   the split's unnormalised output and (max, sum) are written for the
+//   combine kernel.
 // decode_combine_kernel: merges a row's split partials in split order
 //   (log-sum-exp), so the result depends only on the row's own context.
-#include <atomic>
 #include <cmath>
 #include <cstdint>
+#include <type_traits>
 
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -31,11 +44,12 @@
 namespace cp {
 namespace {
 
-constexpr int kDecConsumers = 4;     // consumer warps per CTA (plus an issuer and a resolver warp)
-constexpr int kDecCtasPerSm = 3;     // resident CTAs per SM of the persistent grid
-constexpr int kDecStageBytes = 8192; // one ring stage: 32 rows at D = 128, 64 at D = 64
-constexpr int kDecStages = 5;        // ring depth
-constexpr int kDecSlots = 3;         // resolved items held ahead of the consumers
+constexpr int kDecWarps = 4;                          // warps per CTA
+constexpr int kDecWarpKeys = kDecodeSplit / kDecWarps;  // 128 keys per warp
+constexpr int kDecTiles = kDecWarpKeys / 16;          // 16-key MMA tiles per warp
+constexpr int kDecHeads = 8;                          // MMA N: query heads of a group, zero-padded
+constexpr int kPStride = kDecWarpKeys + 8;            // 16-bit P row stride: conflict-free fragment reads
+static_assert(kDecWarps * kDecWarpKeys == kDecodeSplit, "the warps cover a split");
 
 template <typename T>
 __device__ __forceinline__ T from_float(float x);
@@ -44,498 +58,251 @@ __device__ __forceinline__ __nv_bfloat16 from_float<__nv_bfloat16>(float x) { re
 template <>
 __device__ __forceinline__ __half from_float<__half>(float x) { return __float2half_rn(x); }
 
-// Two 16-bit values packed in a 32-bit word -> (low, high) as floats.
 template <typename T>
-__device__ __forceinline__ float2 unpack2(uint32_t w);
-template <>
-__device__ __forceinline__ float2 unpack2<__nv_bfloat16>(uint32_t w) {
-  return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
-}
-template <>
-__device__ __forceinline__ float2 unpack2<__half>(uint32_t w) {
-  return __half22float2(*reinterpret_cast<const __half2*>(&w));
+__device__ __forceinline__ uint16_t bits16(float x) {
+  const T h = from_float<T>(x);
+  return *reinterpret_cast<const uint16_t*>(&h);
 }
 
-// (a.x, a.y) += (b.x, b.y) * (c.x, c.y) as one packed instruction.
-__device__ __forceinline__ void ffma2v(float2& a, float2 b, float2 c) {
-  asm("{\n\t.reg .b64 ra, rb, rc;\n\t"
-      "mov.b64 ra, {%0, %1};\n\tmov.b64 rb, {%2, %3};\n\tmov.b64 rc, {%4, %5};\n\t"
-      "fma.rn.f32x2 ra, rb, rc, ra;\n\tmov.b64 {%0, %1}, ra;\n\t}"
-      : "+f"(a.x), "+f"(a.y)
-      : "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+// 16 bytes from global memory that is read once: no L1 allocation.
+__device__ __forceinline__ uint4 ldg_stream(const void* p) {
+  uint4 r;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "l"(p));
+  return r;
 }
 
-// Shared-memory plan of decode_split_kernel<T, D, H>.
-template <int D, int H>
-struct DecSmem {
-  static constexpr int kRow = D * 2;                        // bytes of one K or V row
-  static constexpr int kStageRows = kDecStageBytes / kRow;  // 32 (D = 128) or 64 (D = 64)
-  static constexpr int ring = 0;                                      // [kDecStages][kDecStageBytes]
-  static constexpr int q = ring + kDecStages * kDecStageBytes;        // 16-bit [kDecSlots][H][D]
-  static constexpr int rows = q + kDecSlots * H * D * 2;              // uint32 [kDecSlots][kDecodeSplit]
-  static constexpr int pages = rows + kDecSlots * 4 * kDecodeSplit;   // int [kDecodeSplit + 1] (resolver)
-  static constexpr int sc = pages + 4 * (kDecodeSplit + 4);           // float [H][kDecodeSplit]
-  static constexpr int red = sc + 4 * H * kDecodeSplit;               // float [kDecConsumers][H][D]
-  static constexpr int bars = red + 4 * kDecConsumers * H * D;        // uint64 full, empty, ready, freed
-  static constexpr int items = bars + 8 * (2 * kDecStages + 2 * kDecSlots);  // int [kDecSlots][2]
-  static constexpr int misc = items + 8 * kDecSlots;                  // int bad[kDecSlots], abort
-  static constexpr int ml = misc + 4 * (kDecSlots + 1);               // float max[kDecConsumers][H], sum[..][H]
-  static constexpr int bytes = ml + 8 * kDecConsumers * H;
-  static_assert(kDecCtasPerSm * (bytes + 1024) <= 228 * 1024, "two CTAs per SM");
-};
-
-// Row index (in rows of D elements) of an invalid key: never copied.
-constexpr uint32_t kNoRow = 0xffffffffu;
-
-__device__ __forceinline__ void consumers_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kDecConsumers * 32) : "memory"); }
-
-// Named barrier over the consumer warps that also ORs a predicate across them.
-__device__ __forceinline__ bool consumers_sync_or(bool p) {
-  uint32_t r;
-  asm volatile(
-      "{\n\t.reg .pred pi, po;\n\t"
-      "setp.ne.u32 pi, %1, 0;\n\t"
-      "bar.red.or.pred po, 1, %2, pi;\n\t"
-      "selp.u32 %0, 1, 0, po;\n\t}"
-      : "=r"(r)
-      : "r"((uint32_t)p), "n"(kDecConsumers * 32)
-      : "memory");
-  return r != 0;
+__device__ __forceinline__ uint32_t word(const uint4& v, int i) {
+  return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w;
 }
 
-// Row of a staged tile, as the two 16-byte chunks c0 = sub and c1 = sub + LPK.
-__device__ __forceinline__ void lds_row(const unsigned char* row, int sub, int lpk, uint32_t (&w)[8]) {
-  const uint4 a = *reinterpret_cast<const uint4*>(row + sub * 16);
-  const uint4 b = *reinterpret_cast<const uint4*>(row + (sub + lpk) * 16);
-  w[0] = a.x; w[1] = a.y; w[2] = a.z; w[3] = a.w;
-  w[4] = b.x; w[5] = b.y; w[6] = b.z; w[7] = b.w;
-}
-
-// A work item: one split of kDecodeSplit keys, for H query heads of one KV
-// group of one decode sequence.  Ids run sequence-major, then split, then
-// head block, so the H-head blocks of one split are neighbours (a group of 8
-// heads takes two blocks that read the same rows close together in time, the
-// second mostly from L2), and a sequence's empty splits (those past its
-// length) are the tail of its id range, which a claim skips in one step.
-struct DecItem {
-  int s, split, hb, nk;
-};
-
-__device__ __forceinline__ void dec_ids(const AttnArgs& a, int id, int nhb, DecItem& it) {
-  it.hb = id % nhb;
-  it.split = (id / nhb) % a.max_splits;
-  it.s = (id / nhb) / a.max_splits;
-}
-
-__device__ __forceinline__ bool dec_item(const AttnArgs& a, int id, int nhb, DecItem& it) {
-  dec_ids(a, id, nhb, it);
-  if (seq_rows(a.rows, it.s) != 1) return false;
-  const int past = a.past[it.s];
-  const int n = past + 1;
-  if (past < 0 || n > a.max_ctx) {
-    if (a.status && it.split == 0 && it.hb == 0) atomicOr(a.status, CP_DEV_BOUNDS);
-    return false;
+// D (16x8, fp32) += A (16x16, row) * B (16x8, col), 16-bit inputs.
+template <typename T>
+__device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                         uint32_t b0, uint32_t b1) {
+  if constexpr (std::is_same<T, __nv_bfloat16>::value) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+        "{%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+  } else {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+        "{%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
   }
-  const int k0 = it.split * kDecodeSplit;
-  if (k0 >= n) return false;
-  it.nk = min(n - k0, kDecodeSplit);
-  return true;
 }
 
-// Persistent split-KV decode: kDecCtasPerSm CTAs per SM, each with
-// kDecConsumers consumer warps, an issuer warp and a resolver warp.
-//
-// The resolver claims work items from a device counter (lane 0, one atomic
-// per claim, the next claim issued ahead; a claim that lands on a sequence's
-// empty tail moves the counter to the next sequence), reads the sequence's
-// length and page table, and writes the item's row indices into one of
-// kDecSlots item slots, up to kDecSlots items ahead of the consumers, so the
-// latency of those reads is off the copy path.  The issuer streams each
-// resolved item's q heads, then its K rows, then its V rows through a ring of
-// kDecStages stages with bulk copies: one copy per run of contiguous rows (a
-// whole stage for a contiguous cache, one page per copy for a paged one).  It
-// runs across item boundaries without a gap, so the ring stays full and the
-// bytes in flight are bounded by shared memory, not registers.  After the last
-// item both pass a sentinel that ends the consumers.
-//
-// In the K phase the consumers take a row per group of LPK = D/16 lanes, 16
-// elements per lane (chunks sub and sub + LPK, so a quarter-warp reads 128
-// contiguous bytes), with packed fp32x2 FMAs; scores go to shared memory, the
-// split's max and sum are taken in the log2 domain, the V stages are
-// accumulated with D/8 lanes per row (half the accumulator registers),
-// warps' partial sums are added in a fixed order and the unnormalised partial
-// output is written for the combine kernel.
-template <typename T, int D, int H>
-__global__ void __launch_bounds__((kDecConsumers + 2) * 32, kDecCtasPerSm)
-    decode_split_kernel(const AttnArgs a, int* counter) {
-  using L = DecSmem<D, H>;
-  constexpr int LPK = D / 16;               // lanes per row (K phase)
-  constexpr int KPW = 32 / LPK;             // rows per warp per stage
-  constexpr int SR = L::kStageRows;
-  constexpr int NST = kDecStages;
-  constexpr int NSL = kDecSlots;
-  constexpr int KPP = kDecConsumers * KPW;  // rows per K pass of all consumers
-  constexpr int KPASS = SR / KPP;
-  static_assert(KPASS * KPP == SR, "K passes cover a stage");
-  static_assert(SR % 32 == 0, "the issuer covers a stage in rounds of 32 rows");
-  constexpr int LPV = D / 8;                // lanes per row in the V phase
-  constexpr int RPW = 32 / LPV;             // rows per warp per V pass
-  constexpr int VPASS = SR / (kDecConsumers * RPW);
-  static_assert(VPASS * kDecConsumers * RPW == SR, "V passes cover a stage");
-  extern __shared__ __align__(128) unsigned char smem[];
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::bars);
-  uint64_t* empty = full + NST;
-  uint64_t* ready = empty + NST;
-  uint64_t* freed = ready + NSL;
-  int* s_items = reinterpret_cast<int*>(smem + L::items);
-  int* s_bad = reinterpret_cast<int*>(smem + L::misc);
-  volatile int* s_abort = s_bad + NSL;
-  float (*s_wmax)[H] = reinterpret_cast<float (*)[H]>(smem + L::ml);            // per warp, per head
-  float (*s_psum)[H] = reinterpret_cast<float (*)[H]>(smem + L::ml + 4 * kDecConsumers * H);
+template <typename T, int D>
+__global__ void __launch_bounds__(kDecWarps * 32, 3) decode_split_kernel(const AttnArgs a) {
+  constexpr int NJ = D / 32;  // score phase: chunks per lane per key
+  constexpr int NM = D / 64;  // output phase: chunks per lane per key
+  constexpr int kRowBytes = D * 2;
+  __shared__ __align__(16) uint16_t sP[kDecWarps][kDecHeads][kPStride];
+  __shared__ __align__(16) float sO[kDecWarps][kDecHeads][D];
+  __shared__ float sM[kDecWarps][kDecHeads], sL[kDecWarps][kDecHeads];
 
   pdl_launch_dependents();
-  const int nhb = a.hq / H;
-  const int total = a.max_splits * a.rows.num_seqs * nhb;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  if (threadIdx.x == 0) {
-    for (int i = 0; i < NST; ++i) {
-      mbar_init(&full[i], 1);
-      mbar_init(&empty[i], kDecConsumers);
-    }
-    for (int i = 0; i < NSL; ++i) {
-      mbar_init(&ready[i], 1);
-      mbar_init(&freed[i], kDecConsumers);
-    }
-    *s_abort = 0;
-    fence_barrier_init();
-  }
-  __syncthreads();
+  const int split = blockIdx.x % a.max_splits, s = blockIdx.x / a.max_splits, gk = blockIdx.y;
   pdl_wait();  // everything below reads what earlier kernels wrote
-
-  if (warp == kDecConsumers + 1) {
-    // ------------------------------------------------ resolver warp
-    int* s_pg = reinterpret_cast<int*>(smem + L::pages);
-    int next = lane == 0 ? atomicAdd(counter, 1) : 0;
-    for (int j = 0;; ++j) {
-      const int sl = j % NSL;
-      DecItem it;
-      int id;
-      for (;;) {
-        id = __shfl_sync(0xffffffffu, next, 0);
-        if (id >= total) break;
-        if (lane == 0) next = atomicAdd(counter, 1);
-        if (dec_item(a, id, nhb, it)) break;
-        // Every later id of this sequence is empty too: move the counter past them.
-        if (lane == 0) atomicMax(counter, (it.s + 1) * a.max_splits * nhb);
-      }
-      if (j >= NSL && !warp_wait(&freed[sl], ((j - NSL) / NSL) & 1, s_abort, a.status)) return;
-      if (id >= total) {  // sentinel
-        if (lane == 0) {
-          s_items[sl * 2] = -1;
-          mbar_arrive(&ready[sl]);
-        }
-        return;
-      }
-      const int g = (it.hb * H) / a.group, k0 = it.split * kDecodeSplit;
-      uint32_t* rows = reinterpret_cast<uint32_t*>(smem + L::rows) + sl * kDecodeSplit;
-      bool bad = false;
-      if (a.cache.kind == CP_CACHE_PAGED) {
-        // The item's page ids first (one load per page, all in flight together),
-        // then each row from its page.
-        const int ps = a.cache.page_size;
-        const int b0 = k0 / ps, nb = (k0 + it.nk - 1) / ps - b0 + 1;
-        for (int b = lane; b < nb; b += 32) {
-          const int blk = b0 + b;
-          int pg = -1;
-          if (blk < a.cache.max_blocks) pg = a.cache.block_table[(long long)it.s * a.cache.max_blocks + blk];
-          s_pg[b] = (pg >= 0 && pg < a.cache.num_pages) ? pg : -1;
-        }
-        __syncwarp();
-        for (int kk = lane; kk < it.nk; kk += 32) {
-          const int jj = k0 + kk;
-          const int pg = s_pg[jj / ps - b0];
-          rows[kk] = pg < 0 ? kNoRow : (uint32_t)(((long long)pg * a.hkv + g) * ps + jj % ps);
-          bad |= pg < 0;
-        }
-        __syncwarp();
-      } else {
-        const uint32_t base = (uint32_t)(((long long)it.s * a.hkv + g) * a.cache.capacity + k0);
-        for (int kk = lane; kk < it.nk; kk += 32) rows[kk] = base + kk;
-      }
-      bad = __any_sync(0xffffffffu, bad);
-      if (lane == 0) {
-        s_bad[sl] = bad ? 1 : 0;
-        if (bad && a.status) atomicOr(a.status, CP_DEV_BOUNDS);
-        s_items[sl * 2] = id;
-        s_items[sl * 2 + 1] = it.nk;
-      }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&ready[sl]);
-    }
-  }
-
-  if (warp == kDecConsumers) {
-    // ------------------------------------------------ issuer warp
-    const unsigned char* kbase = static_cast<const unsigned char*>(a.k);
-    const unsigned char* vbase = static_cast<const unsigned char*>(a.v);
-    int t = 0;  // stages issued
-    for (int j = 0;; ++j) {
-      const int sl = j % NSL;
-      if (!warp_wait(&ready[sl], (j / NSL) & 1, s_abort, a.status)) break;
-      const int id = s_items[sl * 2];
-      if (id < 0) {  // sentinel stage: ends the consumers
-        const int st = t % NST, use = t / NST;
-        if (use > 0 && !warp_wait(&empty[st], (use - 1) & 1, s_abort, a.status)) break;
-        if (lane == 0) mbar_arrive(&full[st]);
-        ++t;
-        break;
-      }
-      DecItem it;
-      dec_ids(a, id, nhb, it);
-      it.nk = s_items[sl * 2 + 1];
-      const uint32_t* rows = reinterpret_cast<const uint32_t*>(smem + L::rows) + sl * kDecodeSplit;
-      const int ntl = (it.nk + SR - 1) / SR;
-      bool alive = true;
-      for (int tt = 0; tt < 2 * ntl; ++tt, ++t) {
-        const int st = t % NST, use = t / NST;
-        if (use > 0 && !warp_wait(&empty[st], (use - 1) & 1, s_abort, a.status)) {
-          alive = false;
-          break;
-        }
-        const int tl = tt < ntl ? tt : tt - ntl;
-        const unsigned char* base = tt < ntl ? kbase : vbase;
-        unsigned char* stage = smem + L::ring + st * kDecStageBytes;
-#pragma unroll
-        for (int rd = 0; rd < SR / 32; ++rd) {
-          const int r = rd * 32 + lane;
-          const int kk = tl * SR + r;
-          const uint32_t row = kk < it.nk ? rows[kk] : kNoRow;
-          const bool valid = row != kNoRow;
-          const uint32_t prev = __shfl_up_sync(0xffffffffu, row, 1);
-          const bool start = valid && (lane == 0 || prev == kNoRow || row != prev + 1);
-          const uint32_t brk = __ballot_sync(0xffffffffu, start || !valid);
-          const uint32_t nvalid = __popc(__ballot_sync(0xffffffffu, valid));
-          if (lane == 0 && nvalid) mbar_expect_tx(&full[st], nvalid * L::kRow);
-          __syncwarp();
-          if (start) {
-            const uint32_t later = lane == 31 ? 0u : (brk >> (lane + 1));
-            const int len = later ? __ffs(later) : 32 - lane;
-            bulk_load(stage + r * L::kRow, base + (long long)row * L::kRow, len * L::kRow, &full[st]);
-          }
-        }
-        if (tt == 0 && lane == 0) {  // the item's q heads ride on its first stage
-          const T* q = static_cast<const T*>(a.q) + ((long long)seq_row0(a.rows, it.s) * a.hq + it.hb * H) * D;
-          mbar_expect_tx(&full[st], H * D * 2);
-          bulk_load(smem + L::q + sl * H * D * 2, q, H * D * 2, &full[st]);
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&full[st]);
-      }
-      if (!alive) break;
-    }
-    // Let every issued copy land before the CTA can exit.
-    if (lane == 0) {
-      for (int u = t - NST < 0 ? 0 : t - NST; u < t; ++u)
-        if (!mbar_wait_drain(&full[u % NST], (u / NST) & 1) && a.status) atomicOr(a.status, CP_DEV_TIMEOUT);
-    }
+  if (seq_rows(a.rows, s) != 1) return;
+  const int past = a.past[s];
+  const int n = past + 1;
+  if (past < 0 || n > a.max_ctx) {
+    if (a.status && split == 0 && gk == 0 && threadIdx.x == 0) atomicOr(a.status, CP_DEV_BOUNDS);
     return;
   }
-  if (warp > kDecConsumers) return;
+  const int k0 = split * kDecodeSplit;
+  if (k0 >= n) return;
+  const int nk = min(n - k0, kDecodeSplit);
 
-  // -------------------------------------------------- consumer warps
-  const int sub = lane % LPK;
-  const int r = warp * KPW + lane / LPK;  // this lane's row within a stage (K phase)
-  // The LPK lanes of a row reduce their H partial dot products by halving:
-  // at each xor level a lane keeps half of the heads it holds and adds its
-  // partner's half, so after log2(LPK) levels lane `sub` holds the full dot
-  // product of head hb (lanes sub and sub ^ 1 ... hold the same head).
-  int hb = 0;
-#pragma unroll
-  for (int lvl = 0; (LPK >> (lvl + 1)) >= 1; ++lvl)
-    if ((H >> lvl) > 1 && (lane & (LPK >> (lvl + 1)))) hb += (H >> lvl) / 2;
-  constexpr int kHeadLanes = LPK / H;     // lanes of a row holding the same head
-  const int subv = lane % LPV;
-  const int rv = warp * RPW + lane / LPV;  // this lane's row within a V pass
-  float (*sc)[kDecodeSplit] = reinterpret_cast<float (*)[kDecodeSplit]>(smem + L::sc);
-  float (*red)[H][D] = reinterpret_cast<float (*)[H][D]>(smem + L::red);
-  bool ok = true;
-  int t = 0;
-  for (int j = 0;; ++j) {
-    const int sl = j % NSL;
-    ok = ok && warp_wait(&full[t % NST], (t / NST) & 1, s_abort, a.status);
-    const int id = ok ? s_items[sl * 2] : -1;
-    if (consumers_sync_or(!ok || id < 0)) break;
-    DecItem it;
-    dec_ids(a, id, nhb, it);
-    it.nk = s_items[sl * 2 + 1];
-    const int ntl = (it.nk + SR - 1) / SR;
-    const uint32_t* rows = reinterpret_cast<const uint32_t*>(smem + L::rows) + sl * kDecodeSplit;
-    const bool bad = s_bad[sl] != 0;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g8 = lane >> 2, q4 = lane & 3;
+  const int G = a.group;
+  const int kw = warp * kDecWarpKeys;                   // the warp's first key in the split
+  const int nkw = max(0, min(nk - kw, kDecWarpKeys));   // its valid keys
+  const int ntile = (nkw + 15) / 16;
+  const bool paged = a.cache.kind == CP_CACHE_PAGED;
+  const int ps = a.cache.page_size;
 
-    // q slices (chunks sub, sub + LPK) of the H heads, scaled into the log2 domain.
-    float2 qv[H][8];
-    {
-      const unsigned char* qs = smem + L::q + sl * H * D * 2;
+  // Page of each of the warp's tiles (a page holds whole 16-key tiles).
+  int pgv = -1;
+  if (paged && lane < ntile) {
+    const int blk = (k0 + kw + 16 * lane) / ps;
+    int pg = blk < a.cache.max_blocks ? a.cache.block_table[(long long)s * a.cache.max_blocks + blk] : -1;
+    if (pg < 0 || pg >= a.cache.num_pages) {
+      if (a.status) atomicOr(a.status, CP_DEV_BOUNDS);
+      pg = -1;
+    }
+    pgv = pg;
+  }
+  // Byte offset of row 0 of tile t in the K (or V) cache, or -1 (tile's page invalid).
+  auto tile_off = [&](int t) -> long long {
+    if (paged) {
+      const int pg = __shfl_sync(0xffffffffu, pgv, t);
+      if (pg < 0) return -1;
+      return (((long long)pg * a.hkv + gk) * ps + (k0 + kw + 16 * t) % ps) * kRowBytes;
+    }
+    return (((long long)s * a.hkv + gk) * a.cache.capacity + k0 + kw + 16 * t) * kRowBytes;
+  };
+  const unsigned char* kbase = static_cast<const unsigned char*>(a.k);
+  const unsigned char* vbase = static_cast<const unsigned char*>(a.v);
+
+  // Query B fragments: head g8 (zero past the group), chunks q4 + 4j.
+  uint4 qf[NJ];
+  {
+    const bool hv = g8 < G;
+    const unsigned char* qrow =
+        static_cast<const unsigned char*>(a.q) + (((long long)seq_row0(a.rows, s) * a.hq + gk * G + g8) * D) * 2;
 #pragma unroll
-      for (int h = 0; h < H; ++h) {
-        uint32_t w[8];
-        lds_row(qs + h * D * 2, sub, LPK, w);
+    for (int j = 0; j < NJ; ++j) qf[j] = hv ? *reinterpret_cast<const uint4*>(qrow + (q4 + 4 * j) * 16) : make_uint4(0, 0, 0, 0);
+  }
+
+  // ---- scores: keys g8 and g8 + 8 of each tile, heads 2q4 and 2q4 + 1
+  float sc[kDecTiles][4];
+  auto load_k = [&](int t, uint4 (&kr)[2][NJ]) {
+    const long long off = t < ntile ? tile_off(t) : -1;
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const float2 f = unpack2<T>(w[e]);
-          qv[h][e] = make_float2(f.x * a.scale_log2, f.y * a.scale_log2);
+    for (int r = 0; r < 2; ++r) {
+      const int key = 16 * t + g8 + 8 * r;
+      const bool ok = off >= 0 && key < nkw;
+#pragma unroll
+      for (int j = 0; j < NJ; ++j)
+        kr[r][j] = ok ? ldg_stream(kbase + off + (g8 + 8 * r) * kRowBytes + (q4 + 4 * j) * 16) : make_uint4(0, 0, 0, 0);
+    }
+  };
+  uint4 kb[2][2][NJ];
+  load_k(0, kb[0]);
+  float mx0 = -INFINITY, mx1 = -INFINITY;
+  const bool h0v = 2 * q4 < G, h1v = 2 * q4 + 1 < G;
+#pragma unroll
+  for (int t = 0; t < kDecTiles; ++t) {
+    if (t + 1 < kDecTiles) load_k(t + 1, kb[(t + 1) & 1]);
+    float c[4] = {0.f, 0.f, 0.f, 0.f};
+    const uint4 (&kr)[2][NJ] = kb[t & 1];
+#pragma unroll
+    for (int j = 0; j < NJ; ++j)
+#pragma unroll
+      for (int u = 0; u < 2; ++u)
+        mma16816<T>(c, word(kr[0][j], 2 * u), word(kr[1][j], 2 * u), word(kr[0][j], 2 * u + 1),
+                    word(kr[1][j], 2 * u + 1), word(qf[j], 2 * u), word(qf[j], 2 * u + 1));
+    const long long off = t < ntile ? tile_off(t) : -1;
+    const bool k0v = off >= 0 && 16 * t + g8 < nkw, k1v = off >= 0 && 16 * t + g8 + 8 < nkw;
+    sc[t][0] = (k0v && h0v) ? c[0] * a.scale_log2 : -INFINITY;
+    sc[t][1] = (k0v && h1v) ? c[1] * a.scale_log2 : -INFINITY;
+    sc[t][2] = (k1v && h0v) ? c[2] * a.scale_log2 : -INFINITY;
+    sc[t][3] = (k1v && h1v) ? c[3] * a.scale_log2 : -INFINITY;
+    mx0 = fmaxf(mx0, fmaxf(sc[t][0], sc[t][2]));
+    mx1 = fmaxf(mx1, fmaxf(sc[t][1], sc[t][3]));
+  }
+  // The warp's max per head: over the eight lanes g8 that share q4.
+#pragma unroll
+  for (int o = 4; o < 32; o <<= 1) {
+    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
+    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
+  }
+  // P (16-bit) for the output MMAs, and its sum in fp32.
+  float l0 = 0.f, l1 = 0.f;
+  uint16_t(*pw)[kPStride] = sP[warp];
+#pragma unroll
+  for (int t = 0; t < kDecTiles; ++t) {
+    const float p0 = mx0 == -INFINITY ? 0.f : ex2_approx(sc[t][0] - mx0);
+    const float p1 = mx1 == -INFINITY ? 0.f : ex2_approx(sc[t][1] - mx1);
+    const float p2 = mx0 == -INFINITY ? 0.f : ex2_approx(sc[t][2] - mx0);
+    const float p3 = mx1 == -INFINITY ? 0.f : ex2_approx(sc[t][3] - mx1);
+    l0 += p0 + p2;
+    l1 += p1 + p3;
+    pw[2 * q4][16 * t + g8] = bits16<T>(p0);
+    pw[2 * q4 + 1][16 * t + g8] = bits16<T>(p1);
+    pw[2 * q4][16 * t + g8 + 8] = bits16<T>(p2);
+    pw[2 * q4 + 1][16 * t + g8 + 8] = bits16<T>(p3);
+  }
+#pragma unroll
+  for (int o = 4; o < 32; o <<= 1) {
+    l0 += __shfl_xor_sync(0xffffffffu, l0, o);
+    l1 += __shfl_xor_sync(0xffffffffu, l1, o);
+  }
+  __syncwarp();
+
+  // ---- output: dims 8(g8 + 8m) + 2i2 (+1) for heads 2q4, 2q4 + 1
+  float o[NM * 4][4];
+#pragma unroll
+  for (int b = 0; b < NM * 4; ++b) o[b][0] = o[b][1] = o[b][2] = o[b][3] = 0.f;
+  auto load_v = [&](int t, uint4 (&vr)[4][NM]) {
+    const long long off = t < ntile ? tile_off(t) : -1;
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      const int kt = 2 * q4 + (r & 1) + 8 * (r >> 1);  // key within the tile: 2q, 2q+1, 2q+8, 2q+9
+      const bool ok = off >= 0 && 16 * t + kt < nkw;
+#pragma unroll
+      for (int m = 0; m < NM; ++m)
+        vr[r][m] = ok ? ldg_stream(vbase + off + kt * kRowBytes + (g8 + 8 * m) * 16) : make_uint4(0, 0, 0, 0);
+    }
+  };
+  uint4 vb[2][4][NM];
+  if (ntile > 0) load_v(0, vb[0]);
+#pragma unroll
+  for (int t = 0; t < kDecTiles; ++t) {
+    if (t < ntile) {
+      if (t + 1 < ntile) load_v(t + 1, vb[(t + 1) & 1]);
+      const uint4 (&vr)[4][NM] = vb[t & 1];
+      const uint32_t b0 = *reinterpret_cast<const uint32_t*>(&pw[g8][16 * t + 2 * q4]);
+      const uint32_t b1 = *reinterpret_cast<const uint32_t*>(&pw[g8][16 * t + 2 * q4 + 8]);
+#pragma unroll
+      for (int m = 0; m < NM; ++m)
+#pragma unroll
+        for (int i2 = 0; i2 < 4; ++i2) {
+          const uint32_t x0 = word(vr[0][m], i2), x1 = word(vr[1][m], i2);
+          const uint32_t x2 = word(vr[2][m], i2), x3 = word(vr[3][m], i2);
+          mma16816<T>(o[m * 4 + i2], __byte_perm(x0, x1, 0x5410), __byte_perm(x0, x1, 0x7632),
+                      __byte_perm(x2, x3, 0x5410), __byte_perm(x2, x3, 0x7632), b0, b1);
         }
-      }
     }
+  }
+  // The warp's partial: heads 2q4, 2q4 + 1 (those of the group), rows of dims.
+#pragma unroll
+  for (int m = 0; m < NM; ++m)
+#pragma unroll
+    for (int i2 = 0; i2 < 4; ++i2) {
+      const int d0 = 8 * (g8 + 8 * m) + 2 * i2;
+      if (h0v) *reinterpret_cast<float2*>(&sO[warp][2 * q4][d0]) = make_float2(o[m * 4 + i2][0], o[m * 4 + i2][2]);
+      if (h1v) *reinterpret_cast<float2*>(&sO[warp][2 * q4 + 1][d0]) = make_float2(o[m * 4 + i2][1], o[m * 4 + i2][3]);
+    }
+  if (g8 == 0) {
+    sM[warp][2 * q4] = mx0;
+    sL[warp][2 * q4] = l0;
+    sM[warp][2 * q4 + 1] = mx1;
+    sL[warp][2 * q4 + 1] = l1;
+  }
+  __syncthreads();
 
-    // ---- scores over the K stages
-    float mx = -INFINITY;  // running max of this lane's head over its rows
-    for (int tl = 0; tl < ntl; ++tl, ++t) {
-      const int st = t % NST;
-      if (tl > 0) ok = ok && warp_wait(&full[st], (t / NST) & 1, s_abort, a.status);
-      if (!ok) continue;
+  // ---- the split's partial: the warps' partials merged in warp order
+  const long long part_base = ((long long)s * a.hq + gk * G) * a.max_splits;
+  for (int i = threadIdx.x; i < G * D; i += kDecWarps * 32) {
+    const int h = i / D, dd = i % D;
+    float m = -INFINITY;
 #pragma unroll
-      for (int kp = 0; kp < KPASS; ++kp) {
-      const int kk = tl * SR + kp * KPP + r;
-      uint32_t w[8];
-      lds_row(smem + L::ring + st * kDecStageBytes + (kp * KPP + r) * L::kRow, sub, LPK, w);
-      float2 acc[H];
+    for (int w = 0; w < kDecWarps; ++w) m = fmaxf(m, sM[w][h]);
+    float v = 0.f;
 #pragma unroll
-      for (int h = 0; h < H; ++h) acc[h] = make_float2(0.f, 0.f);
+    for (int w = 0; w < kDecWarps; ++w)
+      if (sM[w][h] != -INFINITY) v += ex2_approx(sM[w][h] - m) * sO[w][h][dd];
+    a.part_o[((part_base + (long long)h * a.max_splits) + split) * D + dd] = v;
+  }
+  if (threadIdx.x < G) {
+    const int h = threadIdx.x;
+    float m = -INFINITY, l = 0.f;
 #pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        const float2 kf = unpack2<T>(w[e]);
+    for (int w = 0; w < kDecWarps; ++w) m = fmaxf(m, sM[w][h]);
 #pragma unroll
-        for (int h = 0; h < H; ++h) ffma2v(acc[h], qv[h][e], kf);
-      }
-      float v[H];
-#pragma unroll
-      for (int h = 0; h < H; ++h) v[h] = acc[h].x + acc[h].y;
-#pragma unroll
-      for (int lvl = 0; (LPK >> (lvl + 1)) >= 1; ++lvl) {
-        const int o = LPK >> (lvl + 1);
-        constexpr int kMaxH = H;
-        const int nh = kMaxH >> lvl;
-        if (nh > 1) {
-          const bool up = (lane & o) != 0;
-#pragma unroll
-          for (int i = 0; i < nh / 2; ++i) {
-            const float send = up ? v[i] : v[i + nh / 2];
-            const float keep = up ? v[i + nh / 2] : v[i];
-            v[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
-          }
-        } else {
-          v[0] += __shfl_xor_sync(0xffffffffu, v[0], o);
-        }
-      }
-      if (kk < it.nk) {
-        const float sv = (bad && rows[kk] == kNoRow) ? -INFINITY : v[0];
-        if (sub % kHeadLanes == 0) sc[hb][kk] = sv;
-        mx = fmaxf(mx, sv);
-      }
-      }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&empty[st]);
-    }
-    // The warp's max per head: lanes holding the same head across the row groups.
-#pragma unroll
-    for (int o = LPK; o < 32; o <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-    if (lane < LPK && sub % kHeadLanes == 0) s_wmax[warp][hb] = mx;
-    consumers_sync();
-
-    // ---- split max / sum per query head (log2 domain): kDecConsumers / H
-    // warps per head, each over an interleaved share of the split's keys.
-    constexpr int WPH = kDecConsumers / H;
-    if (ok) {
-      const int h = warp % H, part = warp / H;
-      float m = -INFINITY;
-#pragma unroll
-      for (int w = 0; w < kDecConsumers; ++w) m = fmaxf(m, s_wmax[w][h]);
-      float l = 0.f;
-      for (int kk = part * 32 + lane; kk < it.nk; kk += 32 * WPH) {
-        const float pr = (m == -INFINITY) ? 0.f : ex2_approx(sc[h][kk] - m);
-        sc[h][kk] = pr;
-        l += pr;
-      }
-#pragma unroll
-      for (int o = 16; o; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
-      if (lane == 0) s_psum[part][h] = l;
-    }
-    consumers_sync();
-
-    // ---- p . V over the V stages: a group of LPV = D/8 lanes per row, one
-    // 16-byte chunk per lane, so a quarter-warp again reads 128 contiguous bytes.
-    float2 acc[H][4];
-#pragma unroll
-    for (int h = 0; h < H; ++h)
-#pragma unroll
-      for (int e = 0; e < 4; ++e) acc[h][e] = make_float2(0.f, 0.f);
-    for (int tl = 0; tl < ntl; ++tl, ++t) {
-      const int st = t % NST;
-      ok = ok && warp_wait(&full[st], (t / NST) & 1, s_abort, a.status);
-      if (!ok) continue;
-      const unsigned char* stage = smem + L::ring + st * kDecStageBytes;
-#pragma unroll
-      for (int p = 0; p < VPASS; ++p) {
-        const int row = p * kDecConsumers * RPW + rv;
-        const int kk = tl * SR + row;
-        if (kk < it.nk && !(bad && rows[kk] == kNoRow)) {
-          const uint4 c = *reinterpret_cast<const uint4*>(stage + row * L::kRow + subv * 16);
-          const uint32_t w[4] = {c.x, c.y, c.z, c.w};
-          float2 pp[H];
-#pragma unroll
-          for (int h = 0; h < H; ++h) pp[h] = make_float2(sc[h][kk], sc[h][kk]);
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const float2 vf = unpack2<T>(w[e]);
-#pragma unroll
-            for (int h = 0; h < H; ++h) ffma2v(acc[h][e], pp[h], vf);
-          }
-        }
-      }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&empty[st]);
-    }
-    // Sum the RPW row slots of the warp (lanes with the same `subv`).
-#pragma unroll
-    for (int h = 0; h < H; ++h)
-#pragma unroll
-      for (int e = 0; e < 4; ++e)
-#pragma unroll
-        for (int o = LPV; o < 32; o <<= 1) {
-          acc[h][e].x += __shfl_xor_sync(0xffffffffu, acc[h][e].x, o);
-          acc[h][e].y += __shfl_xor_sync(0xffffffffu, acc[h][e].y, o);
-        }
-    if (lane < LPV) {
-#pragma unroll
-      for (int h = 0; h < H; ++h)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) *reinterpret_cast<float2*>(&red[warp][h][subv * 8 + 2 * e]) = acc[h][e];
-    }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&freed[sl]);  // done with this item's slot: q and row indices
-    consumers_sync();
-    if (!ok) continue;
-    const int h0 = it.hb * H;
-    const long long part_base = ((long long)it.s * a.hq + h0) * a.max_splits;
-    for (int i = threadIdx.x; i < H * D; i += kDecConsumers * 32) {
-      const int h = i / D, dd = i % D;
-      float v = 0.f;
-#pragma unroll
-      for (int w = 0; w < kDecConsumers; ++w) v += red[w][h][dd];
-      a.part_o[((part_base + (long long)h * a.max_splits) + it.split) * D + dd] = v;
-    }
-    if (threadIdx.x < H) {
-      const int h = threadIdx.x;
-      float m = -INFINITY, l = 0.f;
-#pragma unroll
-      for (int w = 0; w < kDecConsumers; ++w) m = fmaxf(m, s_wmax[w][h]);
-#pragma unroll
-      for (int p = 0; p < WPH; ++p) l += s_psum[p][h];
-      const long long idx = (part_base + (long long)h * a.max_splits) + it.split;
-      a.part_ml[idx * 2 + 0] = m;
-      a.part_ml[idx * 2 + 1] = l;
-    }
+    for (int w = 0; w < kDecWarps; ++w)
+      if (sM[w][h] != -INFINITY) l += ex2_approx(sM[w][h] - m) * sL[w][h];
+    const long long idx = (part_base + (long long)h * a.max_splits) + split;
+    a.part_ml[idx * 2 + 0] = m;
+    a.part_ml[idx * 2 + 1] = l;
   }
 }
 
@@ -564,51 +331,13 @@ __global__ void __launch_bounds__(D) decode_combine_kernel(const AttnArgs a) {
   out[((long long)seq_row0(a.rows, s) * a.hq + h) * D + dd] = from_float<T>(o);
 }
 
-template <typename T, int D, int H>
-cudaError_t launch_decode_t(const AttnArgs& a, int* counter, cudaStream_t st) {
-  constexpr int smem = DecSmem<D, H>::bytes;
-  // The dynamic shared-memory limit is a per-device function attribute: raise
-  // it once per device, so later calls (including ones being captured into a
-  // CUDA graph) only launch.
-  static std::atomic<uint64_t> ready_mask{0};
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  const uint64_t bit = 1ull << (dev & 63);
-  if (!(ready_mask.load(std::memory_order_acquire) & bit)) {
-    e = cudaFuncSetAttribute(decode_split_kernel<T, D, H>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-    ready_mask.fetch_or(bit, std::memory_order_release);
-  }
-  int sms = 0;
-  e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  if (e != cudaSuccess) return e;
-  const long long items = (long long)a.max_splits * a.rows.num_seqs * (a.hq / H);
-  if (items >= (1ll << 31) - (1ll << 20)) return cudaErrorInvalidValue;
-  // Row indices are 32-bit: the cache must hold fewer than 2^32 - 1 rows.
-  const long long cache_rows = a.cache.kind == CP_CACHE_PAGED
-                                   ? (long long)a.cache.num_pages * a.hkv * a.cache.page_size
-                                   : (long long)a.rows.num_seqs * a.hkv * a.cache.capacity;
-  if (cache_rows >= (long long)kNoRow) return cudaErrorInvalidValue;
-  const int grid = (int)(items < (long long)sms * kDecCtasPerSm ? items : (long long)sms * kDecCtasPerSm);
-  e = cudaMemsetAsync(counter, 0, sizeof(int), st);
-  if (e != cudaSuccess) return e;
-  e = launch_pdl(decode_split_kernel<T, D, H>, dim3(grid), dim3((kDecConsumers + 2) * 32), smem, st, a, counter);
+template <typename T, int D>
+cudaError_t launch_decode_t(const AttnArgs& a, cudaStream_t st) {
+  if ((long long)a.rows.num_seqs * a.max_splits >= (1ll << 31) || a.hkv > 65535) return cudaErrorInvalidValue;
+  cudaError_t e = launch_pdl(decode_split_kernel<T, D>, dim3(a.rows.num_seqs * a.max_splits, a.hkv),
+                             dim3(kDecWarps * 32), 0, st, a);
   if (e != cudaSuccess) return e;
   return launch_pdl(decode_combine_kernel<T, D>, dim3(a.rows.num_seqs, a.hq), dim3(D), 0, st, a);
-}
-
-// Query heads per CTA: the whole GQA group up to 4 (a group of 8 takes two
-// CTAs, which read the same K/V rows, the second mostly from L2).
-template <typename T, int D>
-cudaError_t launch_decode_d(const AttnArgs& a, int* counter, cudaStream_t st) {
-  switch (a.group) {
-    case 1: return launch_decode_t<T, D, 1>(a, counter, st);
-    case 2: return launch_decode_t<T, D, 2>(a, counter, st);
-    case 4:
-    case 8: return launch_decode_t<T, D, 4>(a, counter, st);
-    default: return cudaErrorInvalidValue;
-  }
 }
 
 }  // namespace
@@ -618,11 +347,11 @@ bool decode_supported(int d, int group, int dtype) {
          (dtype == CP_BF16 || dtype == CP_F16);
 }
 
-cudaError_t launch_decode(const AttnArgs& a, int dtype, int* counter, cudaStream_t st) {
+cudaError_t launch_decode(const AttnArgs& a, int dtype, cudaStream_t st) {
   if (a.rows.num_seqs == 0 || a.max_splits == 0) return cudaSuccess;
-  if (dtype == CP_BF16) return a.d == 64 ? launch_decode_d<__nv_bfloat16, 64>(a, counter, st)
-                                         : launch_decode_d<__nv_bfloat16, 128>(a, counter, st);
-  return a.d == 64 ? launch_decode_d<__half, 64>(a, counter, st) : launch_decode_d<__half, 128>(a, counter, st);
+  if (dtype == CP_BF16) return a.d == 64 ? launch_decode_t<__nv_bfloat16, 64>(a, st)
+                                         : launch_decode_t<__nv_bfloat16, 128>(a, st);
+  return a.d == 64 ? launch_decode_t<__half, 64>(a, st) : launch_decode_t<__half, 128>(a, st);
 }
 
 }  // namespace cp

@@ -66,8 +66,7 @@ int cp_mixed_step_noalloc(const cp_layer_desc* desc, const void* q, const void* 
   void* scratch = nullptr;
   const int r = scratch_for_current_device(&scratch);
   if (r != CP_OK) return r;
-  // The decode launch clears the work counter at the start of the scratch on
-  // the call's stream; the split partials are written before they are read.
+  // The split partials are written before they are read.
   return cp_mixed_step(desc, q, k_new, v_new, k_pages, v_pages, block_table, cu_rows, past_len, num_seqs,
                        total_rows, max_ctx, out, scratch, kNoAllocScratchBytes, dev_status, stream);
 }

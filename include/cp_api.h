@@ -208,8 +208,7 @@ int cp_mixed_step(const cp_layer_desc* desc, const void* q, const void* k_new,
  *   device, with that device current); make that first call before any stream
  *   capture on that device.
  *   Every call uses the same array, which keeps the last call's contents:
- *   each call clears the work counter at its start (an asynchronous memset on
- *   the call's stream) and writes every other entry before reading it.
+ *   each call writes every entry it uses before reading it.
  *   Calls whose work overlaps on the GPU -- on different streams or from
  *   different host threads -- race on the array; the caller must serialise
  *   them. */

@@ -134,6 +134,6 @@ def test_append_and_mixed_reject_bad_arguments():
 
 def test_workspace_size_formula():
     d = _desc()
-    # a 256-byte work counter, then num_seqs * Hq * ceil(ctx / 512) * (D + 2) floats
-    assert cp.cp_workspace_size(d, 64, 8192, 64) == 256 + 64 * 32 * 16 * 130 * 4
-    assert cp.cp_workspace_size(d, 1, 1, 1) == 256 + 32 * 1 * 130 * 4
+    # num_seqs * Hq * ceil(ctx / 512) * (D + 2) floats of split partials
+    assert cp.cp_workspace_size(d, 64, 8192, 64) == 64 * 32 * 16 * 130 * 4
+    assert cp.cp_workspace_size(d, 1, 1, 1) == 32 * 1 * 130 * 4
