@@ -97,7 +97,7 @@ __device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1
 }
 
 template <typename T, int D>
-__global__ void __launch_bounds__(kDecWarps * 32, 3) decode_split_kernel(const AttnArgs a) {
+__global__ void __launch_bounds__(kDecWarps * 32, 4) decode_split_kernel(const AttnArgs a) {
   constexpr int NJ = D / 32;  // score phase: chunks per lane per key
   constexpr int NM = D / 64;  // output phase: chunks per lane per key
   constexpr int kRowBytes = D * 2;
@@ -198,6 +198,20 @@ __global__ void __launch_bounds__(kDecWarps * 32, 3) decode_split_kernel(const A
     mx0 = fmaxf(mx0, fmaxf(sc[t][0], sc[t][2]));
     mx1 = fmaxf(mx1, fmaxf(sc[t][1], sc[t][3]));
   }
+  // The first V tile is in flight while the softmax runs.
+  auto load_v = [&](int t, uint4 (&vr)[4][NM]) {
+    const long long off = t < ntile ? tile_off(t) : -1;
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      const int kt = 2 * q4 + (r & 1) + 8 * (r >> 1);  // key within the tile: 2q, 2q+1, 2q+8, 2q+9
+      const bool ok = off >= 0 && 16 * t + kt < nkw;
+#pragma unroll
+      for (int m = 0; m < NM; ++m)
+        vr[r][m] = ok ? ldg_stream(vbase + off + kt * kRowBytes + (g8 + 8 * m) * 16) : make_uint4(0, 0, 0, 0);
+    }
+  };
+  uint4 vb[2][4][NM];
+  if (ntile > 0) load_v(0, vb[0]);
   // The warp's max per head: over the eight lanes g8 that share q4.
 #pragma unroll
   for (int o = 4; o < 32; o <<= 1) {
@@ -231,19 +245,6 @@ __global__ void __launch_bounds__(kDecWarps * 32, 3) decode_split_kernel(const A
   float o[NM * 4][4];
 #pragma unroll
   for (int b = 0; b < NM * 4; ++b) o[b][0] = o[b][1] = o[b][2] = o[b][3] = 0.f;
-  auto load_v = [&](int t, uint4 (&vr)[4][NM]) {
-    const long long off = t < ntile ? tile_off(t) : -1;
-#pragma unroll
-    for (int r = 0; r < 4; ++r) {
-      const int kt = 2 * q4 + (r & 1) + 8 * (r >> 1);  // key within the tile: 2q, 2q+1, 2q+8, 2q+9
-      const bool ok = off >= 0 && 16 * t + kt < nkw;
-#pragma unroll
-      for (int m = 0; m < NM; ++m)
-        vr[r][m] = ok ? ldg_stream(vbase + off + kt * kRowBytes + (g8 + 8 * m) * 16) : make_uint4(0, 0, 0, 0);
-    }
-  };
-  uint4 vb[2][4][NM];
-  if (ntile > 0) load_v(0, vb[0]);
 #pragma unroll
   for (int t = 0; t < kDecTiles; ++t) {
     if (t < ntile) {
