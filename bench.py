@@ -10,8 +10,10 @@ chunks of 512 (7 x 512 + 416) into a KV cache of physical capacity 8192.  One
 step is the whole path for one prompt: chunk plan, query-width ladder (the
 416-row tail is widened to 512 by repeating its last row), and per chunk the
 KV append, the chunk attention and the commit of seqlens_k to past + real
-rows.  Each step is one replay of a CUDA graph captured from the library's
-public calls; L2 is flushed (512 MiB write) between timed steps.
+rows, made as one cp_prefill_chunk call (two kernels: the append, then the
+attention, which also advances seqlens_k).  Each step is one replay of a CUDA
+graph captured from the library's public calls; L2 is flushed (512 MiB write)
+between timed steps.
 
 Prints one JSON line (rank 0).  ``--impl reference`` times the CPU oracle
 (test infrastructure, float64 numpy) on a bounded sample of the same
@@ -225,8 +227,9 @@ class GqaPrefill:
             past += r
         self.flops = sum(self.flops_chunk)
         self.tokens = self.N
-        # launches of this library per step: pad (if any) + per chunk append, attention, commit
-        self.launches = sum(1 for r, w in zip(self.sizes, self.widths) if w > r) * 3 + 3 * len(self.sizes)
+        # launches of this library per step: pad (if any; q, k, v) + per chunk the append and the
+        # attention (which advances seqlens_k itself)
+        self.launches = sum(1 for r, w in zip(self.sizes, self.widths) if w > r) * 3 + 2 * len(self.sizes)
 
     def _chunk(self, i, attn=True, append=True, commit=True):
         cp = self.cp
@@ -234,9 +237,13 @@ class GqaPrefill:
         past = sum(self.sizes[:i])
         sl = slice(past, past + w)
         q, k, v = self.q[None, sl], self.k[None, sl], self.v[None, sl]
+        if append and w > r:
+            cp.cp_pad_chunk(self.desc, q, k, v, r, w)
+        if append and attn and commit:  # the whole chunk in one call
+            cp.cp_prefill_chunk(self.desc, q, k, v, self.kc, self.vc, self.lens, w, r, past, self.out[None, sl],
+                                self.ws, dev_status=self.status)
+            return
         if append:
-            if w > r:
-                cp.cp_pad_chunk(self.desc, q, k, v, r, w)
             cp.cp_kv_append(self.desc, k, v, w, self.kc, self.vc, self.lens, past, dev_status=self.status)
         if attn:
             cp.cp_prefill_chunk_attn(self.desc, q, self.kc, self.vc, self.lens, w, r, past, self.out[None, sl],
@@ -604,9 +611,13 @@ class ChunkLoop:
             r["left"] = torch.tensor([r["lp"]], dtype=torch.int32, device=dev)
             r["out"] = torch.empty(r["L"], r["H"], r["d"], dtype=r["dtype"], device=dev)
             r["sizes"] = cp.cp_chunk_plan(r["L"], r["W"])
+            r["ws"] = torch.empty(cp.cp_workspace_size(r["desc"], r["W"], r["cap"], 1), dtype=torch.uint8,
+                                  device=dev)
         self.tokens = sum(r["L"] - r["lp"] for r in self.runs)
         self.flops = sum(4 * r["d"] * r["H"] * r["pairs"] for r in self.runs)
-        self.launches = sum(3 * len(r["sizes"]) for r in self.runs)
+        # one cp_prefill_chunk call per chunk: the append and the attention (the tensor-core kernel
+        # advances seqlens_k itself; the fp32 path takes a separate advance)
+        self.launches = sum((2 if r["dtype"] != torch.float32 else 3) * len(r["sizes"]) for r in self.runs)
 
     def step(self):
         cp = self.cp
@@ -616,11 +627,9 @@ class ChunkLoop:
             past = 0
             for w in r["sizes"]:
                 sl = slice(past, past + w)
-                cp.cp_kv_append(r["desc"], r["kd"][None, sl], r["vd"][None, sl], w, r["kc"], r["vc"], r["lens"],
-                                past, dev_status=self.status)
-                cp.cp_prefill_chunk_attn(r["desc"], r["qd"][None, sl], r["kc"], r["vc"], r["lens"], w, w, past,
-                                         r["out"][None, sl], None, commit=True,
-                                         left_pad=r["left"] if rolling else None, dev_status=self.status)
+                cp.cp_prefill_chunk(r["desc"], r["qd"][None, sl], r["kd"][None, sl], r["vd"][None, sl], r["kc"],
+                                    r["vc"], r["lens"], w, w, past, r["out"][None, sl], r["ws"],
+                                    left_pad=r["left"] if rolling else None, dev_status=self.status)
                 past += w
 
     def config(self):

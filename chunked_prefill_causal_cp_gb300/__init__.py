@@ -71,6 +71,8 @@ def lib():
         L.cp_pad_chunk.argtypes = [POINTER(LayerDesc), P, P, P, c_int32, c_int32, P]
         L.cp_prefill_chunk_attn.argtypes = [POINTER(LayerDesc), P, P, P, P, P, P, c_int32, c_int32,
                                             c_int32, P, P, c_size_t, c_int32, P, P]
+        L.cp_prefill_chunk.argtypes = [POINTER(LayerDesc), P, P, P, P, P, P, P, P, c_int32, c_int32,
+                                       c_int32, P, P, c_size_t, P, P]
         L.cp_mixed_step.argtypes = [POINTER(LayerDesc), P, P, P, P, P, P, P, P, c_int32, c_int32,
                                     c_int32, P, P, c_size_t, P, P]
         L.cp_mixed_step_noalloc.argtypes = [POINTER(LayerDesc), P, P, P, P, P, P, P, P, c_int32, c_int32,
@@ -88,7 +90,8 @@ def lib():
         L.cp_schedule.argtypes = [c_int32, c_int32, POINTER(c_int32), c_int32, POINTER(SchedEntry), c_int32]
         L.cp_status_string.argtypes = [c_int32]
         L.cp_status_string.restype = ctypes.c_char_p
-        for name in ("cp_kv_append", "cp_pad_chunk", "cp_prefill_chunk_attn", "cp_mixed_step", "cp_chunk_plan",
+        for name in ("cp_kv_append", "cp_pad_chunk", "cp_prefill_chunk_attn", "cp_prefill_chunk",
+                     "cp_mixed_step", "cp_chunk_plan",
                      "cp_query_ladder", "cp_query_width", "cp_aligned_length", "cp_rolling_mask",
                      "cp_schedule", "cp_abi_version"):
             getattr(L, name).restype = c_int32
@@ -148,6 +151,17 @@ def cp_prefill_chunk_attn(desc, q, k_cache, v_cache, seqlens_k, rows_padded, rea
                                     real_rows, max_past, _ptr(out), _ptr(workspace), ws_bytes,
                                     1 if commit else 0, _ptr(dev_status), _stream(stream, q))
     _check(s, "cp_prefill_chunk_attn")
+
+
+def cp_prefill_chunk(desc, q, k_new, v_new, k_cache, v_cache, seqlens_k, rows_padded, real_rows, max_past,
+                     out, workspace, block_table=None, left_pad=None, dev_status=None, stream=None):
+    """Append, attention and commit of one chunk in one call (see include/cp_api.h)."""
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    s = lib().cp_prefill_chunk(ctypes.byref(desc), _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_cache),
+                               _ptr(v_cache), _ptr(seqlens_k), _ptr(block_table), _ptr(left_pad), rows_padded,
+                               real_rows, max_past, _ptr(out), _ptr(workspace), ws_bytes, _ptr(dev_status),
+                               _stream(stream, q))
+    _check(s, "cp_prefill_chunk")
 
 
 def cp_mixed_step(desc, q, k_new, v_new, k_pages, v_pages, block_table, cu_rows, past_len,

@@ -245,6 +245,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = bar->tmem_base;
   volatile int* abort_flag = &bar->abort;
   pdl_wait();  // everything below reads what earlier kernels wrote
+  if (a.commit_lens && blockIdx.x == 0 && blockIdx.y == 0)
+    for (int q = threadIdx.x; q < a.rows.num_seqs; q += kThreads) a.commit_lens[q] += a.commit_add;
 
   // ---- this cluster's pair (the same for both CTAs, so both leave together)
   int s = 0, t0 = 0, rows = 0, past = 0;

@@ -68,6 +68,11 @@ float scale_log2(const cp_layer_desc* d) {
 
 int64_t max_splits_for(int32_t max_ctx) { return ((int64_t)max_ctx + kDecodeSplit - 1) / kDecodeSplit; }
 
+// Workspace of cp_prefill_chunk: a snapshot of seqlens_k (its own 256-byte
+// aligned block), then the split partials.  The other calls use the partials
+// only, from the start of the workspace.
+int64_t snapshot_bytes(int32_t num_seqs) { return ((int64_t)num_seqs * 4 + 255) / 256 * 256; }
+
 // Decode workspace: the split partials (output rows, then max and sum).
 int64_t decode_ws_bytes(const cp_layer_desc* d, int32_t max_ctx, int32_t num_seqs) {
   const int64_t ms = max_splits_for(max_ctx);
@@ -191,7 +196,7 @@ extern "C" {
 size_t cp_workspace_size(const cp_layer_desc* desc, int32_t max_rows, int32_t max_ctx, int32_t num_seqs) {
   if (check_desc(desc, false) != CP_OK || max_rows < 0 || max_ctx < 0 || num_seqs < 0) return 0;
   (void)max_rows;
-  return (size_t)decode_ws_bytes(desc, max_ctx, num_seqs);
+  return (size_t)(snapshot_bytes(num_seqs) + decode_ws_bytes(desc, max_ctx, num_seqs));
 }
 
 int cp_kv_append(const cp_layer_desc* desc, const void* k_new, const void* v_new, int32_t rows, void* k_cache,
@@ -286,6 +291,86 @@ int cp_prefill_chunk_attn(const cp_layer_desc* desc, const void* q, const void* 
   r = run_attention(desc, a, rows_total, rows_padded, k_cache, v_cache, desc->batch, workspace, workspace_bytes, st);
   if (r != CP_OK) return r;
   if (commit) return launch_result(launch_commit(seqlens_k, a.rows, real_rows, nullptr, st));
+  return CP_OK;
+}
+
+int cp_prefill_chunk(const cp_layer_desc* desc, const void* q, void* k_new, void* v_new, void* k_cache,
+                     void* v_cache, int32_t* seqlens_k, const int32_t* block_table, const int32_t* left_pad,
+                     int32_t rows_padded, int32_t real_rows, int32_t max_past, void* out, void* workspace,
+                     size_t workspace_bytes, int32_t* dev_status, void* stream) {
+  int r = check_desc(desc, true);
+  if (r != CP_OK) return r;
+  if (rows_padded <= 0 || real_rows <= 0 || real_rows > rows_padded || max_past < 0) return CP_ERR_INVALID_ARG;
+  if (!q || !k_new || !v_new || !k_cache || !v_cache || !seqlens_k || !out) return CP_ERR_INVALID_ARG;
+  if (desc->kind == CP_CACHE_PAGED && !block_table) return CP_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k_new) || !aligned16(v_new) || !aligned16(k_cache) || !aligned16(v_cache) ||
+      !aligned16(out))
+    return CP_ERR_INVALID_ARG;
+  if (desc->kind == CP_CACHE_ROLLING) {
+    if (real_rows != rows_padded) return CP_ERR_INVALID_ARG;
+    if (rows_padded > desc->capacity) return CP_ERR_CAPACITY;
+  } else if ((int64_t)max_past + rows_padded > layout_limit(desc)) {
+    return CP_ERR_CAPACITY;
+  }
+  const int64_t rows_total = (int64_t)desc->batch * rows_padded;
+  if (rows_total > INT32_MAX || (int64_t)max_past + rows_padded > INT32_MAX) return CP_ERR_UNSUPPORTED;
+  // The copy of the lengths always; the split-KV partials only when one-row
+  // chunks take the decode path (checked here, before anything is enqueued).
+  const int G0 = desc->num_q_heads / desc->num_kv_heads;
+  const bool decode_rows = rows_padded == 1 && desc->dtype != CP_F32 && desc->kind != CP_CACHE_ROLLING &&
+                           decode_supported(desc->head_dim, G0, desc->dtype);
+  const int64_t snap = snapshot_bytes(desc->batch);
+  const int64_t need = snap + (decode_rows ? decode_ws_bytes(desc, max_past + rows_padded, desc->batch) : 0);
+  if (workspace == nullptr || (int64_t)workspace_bytes < need || !aligned16(workspace)) return CP_ERR_WORKSPACE;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  int* past = static_cast<int*>(workspace);
+
+  AppendArgs ap;
+  ap.hkv = desc->num_kv_heads;
+  ap.d = desc->head_dim;
+  ap.esize = esize_of(desc->dtype);
+  ap.rows = SeqRows{desc->batch, rows_padded, nullptr};
+  ap.cache = make_cache(desc, block_table);
+  ap.past = seqlens_k;
+  ap.max_ctx = max_past + rows_padded;
+  ap.k_new = k_new;
+  ap.v_new = v_new;
+  ap.k_cache = k_cache;
+  ap.v_cache = v_cache;
+  ap.status = dev_status;
+  ap.past_snapshot = past;
+  r = launch_result(launch_kv_append(ap, (int)rows_total, st));
+  if (r != CP_OK) return r;
+
+  AttnArgs a;
+  std::memset(&a, 0, sizeof(a));
+  a.hq = desc->num_q_heads;
+  a.hkv = desc->num_kv_heads;
+  a.d = desc->head_dim;
+  a.group = a.hq / a.hkv;
+  a.scale_log2 = scale_log2(desc);
+  a.rows = SeqRows{desc->batch, rows_padded, nullptr};
+  a.cache = make_cache(desc, block_table);
+  a.past = past;  // the snapshot: seqlens_k itself may then be advanced by the attention kernel
+  a.left_pad = desc->kind == CP_CACHE_ROLLING ? left_pad : nullptr;
+  a.max_ctx = max_past + rows_padded;
+  a.q = q;
+  a.k = k_cache;
+  a.v = v_cache;
+  a.out = out;
+  a.status = dev_status;
+  // One launch for the attention and the commit when the tensor-core kernel takes every row.
+  const int G = desc->num_q_heads / desc->num_kv_heads;
+  const bool tc_only = desc->dtype != CP_F32 && rows_padded > 1 && attn_tc_supported(desc->head_dim, G, desc->dtype);
+  if (tc_only) {
+    a.commit_lens = seqlens_k;
+    a.commit_add = real_rows;
+  }
+  r = run_attention(desc, a, rows_total, rows_padded, k_cache, v_cache, desc->batch,
+                    static_cast<char*>(workspace) + snap, (size_t)(workspace_bytes - snap), st,
+                    desc->kind == CP_CACHE_PAGED ? k_new : nullptr, desc->kind == CP_CACHE_PAGED ? v_new : nullptr);
+  if (r != CP_OK) return r;
+  if (!tc_only) return launch_result(launch_commit(seqlens_k, a.rows, real_rows, nullptr, st));
   return CP_OK;
 }
 

@@ -62,6 +62,8 @@ struct AttnArgs {
   int* status;             // optional CP_DEV_* bits
   int kv_direct;           // tensor-core kernel: this call's new K/V rows may be read from
                            // k_new / v_new ([rows_total, hkv, d]) instead of the paged pool
+  int* commit_lens = nullptr;  // tensor-core kernel: if set, CTA (0, 0) adds commit_add to each
+  int commit_add = 0;          // commit_lens[s] after the dependency wait (`past` must not alias it)
 };
 
 struct AppendArgs {
@@ -75,6 +77,7 @@ struct AppendArgs {
   void* k_cache;
   void* v_cache;
   int* status;
+  int* past_snapshot = nullptr;  // optional [num_seqs]: CTA 0 copies past[] here
 };
 
 // Launches `kernel` with programmatic dependent launch allowed: the grid may

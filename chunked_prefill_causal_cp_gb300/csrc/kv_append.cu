@@ -46,6 +46,8 @@ __device__ __forceinline__ long long slot_offset(const CacheView& c, int hkv, in
 __global__ void kv_append_kernel(const AppendArgs a, int rows_total) {
   pdl_launch_dependents();
   pdl_wait();
+  if (a.past_snapshot && blockIdx.x == 0)
+    for (int s = threadIdx.x; s < a.rows.num_seqs; s += blockDim.x) a.past_snapshot[s] = a.past[s];
   const int vec_per_row = a.d * a.esize / 16;           // 16-byte vectors per row
   const long long gid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   const long long row = gid / vec_per_row;              // (token, head) row

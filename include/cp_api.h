@@ -160,6 +160,28 @@ int cp_prefill_chunk_attn(const cp_layer_desc* desc, const void* q, const void* 
                           int32_t max_past, void* out, void* workspace, size_t workspace_bytes,
                           int32_t commit, int32_t* dev_status, void* stream);
 
+/* cp_prefill_chunk -- one chunk of a prompt in one call: cp_kv_append of the
+ * chunk's K/V rows, cp_prefill_chunk_attn of its query rows, and the advance of
+ * seqlens_k by real_rows, with the same arguments and results as those two
+ * calls made back to back with commit = 1 ([Glossary] "How chunked prefill
+ * works": each chunk's K/V join the cache and its rows attend to the cache).
+ * The append copies seqlens_k into the workspace and the attention reads the
+ * copy, so the attention kernel itself advances seqlens_k (no separate commit
+ * launch when the tensor-core path takes every row).
+ *   q, out        device [B, rows_padded, Hq, D]
+ *   k_new, v_new  device [B, rows_padded, Hkv, D] (rows [real_rows,
+ *                 rows_padded) are appended too: cp_pad_chunk fills them)
+ *   workspace     device scratch, 16-byte aligned, of at least
+ *                 cp_workspace_size(desc, B * R, max_past + R, B) bytes (that
+ *                 size always suffices; the call needs the split-KV part only
+ *                 for one-row chunks)
+ * Other arguments as in cp_prefill_chunk_attn. */
+int cp_prefill_chunk(const cp_layer_desc* desc, const void* q, void* k_new, void* v_new, void* k_cache,
+                     void* v_cache, int32_t* seqlens_k, const int32_t* block_table,
+                     const int32_t* left_pad, int32_t rows_padded, int32_t real_rows, int32_t max_past,
+                     void* out, void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                     void* stream);
+
 /* cp_mixed_step -- one token-budget step over a paged cache.
  *
  * [Glossary] "How chunked prefill works": a step holds one row for every
@@ -222,9 +244,10 @@ int cp_mixed_step_noalloc(const cp_layer_desc* desc, const void* q, const void* 
  * cp_mixed_step_noalloc (no GPU work). */
 size_t cp_noalloc_scratch_bytes(void);
 
-/* cp_workspace_size -- bytes of device scratch the two attention calls need
- * for up to `max_rows` query rows, contexts of up to `max_ctx` keys and
- * `num_seqs` sequences (split-KV partial results and the work list). */
+/* cp_workspace_size -- bytes of device scratch the attention calls need for up
+ * to `max_rows` query rows, contexts of up to `max_ctx` keys and `num_seqs`
+ * sequences: a copy of the sequences' lengths (cp_prefill_chunk; 256-byte
+ * blocks) and the split-KV partial results. */
 size_t cp_workspace_size(const cp_layer_desc* desc, int32_t max_rows, int32_t max_ctx,
                          int32_t num_seqs);
 

@@ -18,7 +18,7 @@ def f64(t: torch.Tensor) -> np.ndarray:
 class Contig:
     """A contiguous cache at fixed physical capacity plus its valid length."""
 
-    def __init__(self, dtype, hq, hkv, d, cap, batch=1, poison=True, dev="cuda"):
+    def __init__(self, dtype, hq, hkv, d, cap, batch=1, poison=True, dev="cuda", fused=False):
         self.desc = cp.layer_desc(dtype, batch, hq, hkv, d, cp.CP_CACHE_CONTIG, capacity=cap)
         fill = float("nan") if poison else 0.0
         self.k = torch.full((batch, hkv, cap, d), fill, dtype=dtype, device=dev)
@@ -26,6 +26,7 @@ class Contig:
         self.lens = torch.zeros(batch, dtype=torch.int32, device=dev)
         self.status = torch.zeros(1, dtype=torch.int32, device=dev)
         self.cap = cap
+        self.fused = fused  # one cp_prefill_chunk call per chunk instead of append + attention
         self.ws = torch.empty(max(cp.cp_workspace_size(self.desc, 1, cap, batch), 16), dtype=torch.uint8,
                               device=dev)
 
@@ -34,6 +35,10 @@ class Contig:
         R = q.shape[1]
         if out is None:
             out = torch.empty_like(q)
+        if self.fused:
+            cp.cp_prefill_chunk(self.desc, q, k_new, v_new, self.k, self.v, self.lens, R, real_rows, past, out,
+                                self.ws, dev_status=self.status)
+            return out
         cp.cp_kv_append(self.desc, k_new, v_new, R, self.k, self.v, self.lens, past,
                         dev_status=self.status)
         cp.cp_prefill_chunk_attn(self.desc, q, self.k, self.v, self.lens, R, real_rows, past, out,

@@ -35,6 +35,7 @@ def _declared_functions():
 def test_exports_every_declared_symbol():
     names = _declared_functions()
     assert "cp_kv_append" in names and "cp_prefill_chunk_attn" in names and "cp_mixed_step" in names
+    assert "cp_prefill_chunk" in names
     L = ctypes.CDLL(cp.LIB_PATH)
     missing = [n for n in names if not hasattr(L, n)]
     assert not missing, missing
@@ -118,6 +119,26 @@ def test_prefill_rejects_bad_arguments_before_launch():
     assert _prefill(_desc(), rows=1, real=1, max_past=100, ws=None) == cp.CP_ERR_WORKSPACE
 
 
+def _chunk(desc, rows=512, real=512, max_past=0, k_new=FAKE, ws=FAKE, ws_bytes=1 << 30):
+    L = cp.lib()
+    return L.cp_prefill_chunk(ctypes.byref(desc), FAKE, k_new, FAKE, FAKE, FAKE, FAKE, None, None, rows, real,
+                              max_past, FAKE, ws, ws_bytes, None, None)
+
+
+def test_fused_chunk_rejects_bad_arguments_before_launch():
+    assert _chunk(_desc(head_dim=96)) == cp.CP_ERR_UNSUPPORTED
+    assert _chunk(_desc(), rows=100, real=101) == cp.CP_ERR_INVALID_ARG
+    assert _chunk(_desc(), max_past=8192 - 511) == cp.CP_ERR_CAPACITY
+    assert _chunk(_desc(), k_new=None) == cp.CP_ERR_INVALID_ARG
+    assert _chunk(_desc(), k_new=FAKE + 8) == cp.CP_ERR_INVALID_ARG
+    # the copy of the lengths always needs the workspace; one-row chunks (decode) need the partials too
+    assert _chunk(_desc(), ws=None) == cp.CP_ERR_WORKSPACE
+    assert _chunk(_desc(), ws_bytes=255) == cp.CP_ERR_WORKSPACE
+    need = cp.cp_workspace_size(_desc(), 1, 101, 1)
+    assert _chunk(_desc(), rows=1, real=1, max_past=100, ws_bytes=need - 1) == cp.CP_ERR_WORKSPACE
+    assert _chunk(_desc(), ws=FAKE + 4) == cp.CP_ERR_WORKSPACE
+
+
 def test_append_and_mixed_reject_bad_arguments():
     L = cp.lib()
     d = _desc()
@@ -134,6 +155,8 @@ def test_append_and_mixed_reject_bad_arguments():
 
 def test_workspace_size_formula():
     d = _desc()
-    # num_seqs * Hq * ceil(ctx / 512) * (D + 2) floats of split partials
-    assert cp.cp_workspace_size(d, 64, 8192, 64) == 64 * 32 * 16 * 130 * 4
-    assert cp.cp_workspace_size(d, 1, 1, 1) == 32 * 1 * 130 * 4
+    # a copy of the lengths in 256-byte blocks, then num_seqs * Hq * ceil(ctx / 512) * (D + 2)
+    # floats of split partials
+    assert cp.cp_workspace_size(d, 64, 8192, 64) == 256 + 64 * 32 * 16 * 130 * 4
+    assert cp.cp_workspace_size(d, 1, 1, 1) == 256 + 32 * 1 * 130 * 4
+    assert cp.cp_workspace_size(d, 1, 1, 65) == 512 + 65 * 32 * 1 * 130 * 4

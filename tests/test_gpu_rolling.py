@@ -21,7 +21,7 @@ def _gpu():
     _build.build()
 
 
-def _run_rolling(n_real, c, C, H, d, dtype, seed):
+def _run_rolling(n_real, c, C, H, d, dtype, seed, fused=False):
     L = cp.cp_aligned_length(n_real, c)
     lp = L - n_real
     q, k, v = SI.rolling_prompt(L, seed=seed, heads=H, dim=d, dtype=dtype)
@@ -33,12 +33,17 @@ def _run_rolling(n_real, c, C, H, d, dtype, seed):
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
     out = torch.empty(L, H, d, dtype=dtype, device="cuda")
     qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
+    ws = torch.empty(cp.cp_workspace_size(desc, c, C, 1), dtype=torch.uint8, device="cuda")
     ref_out, snaps = oracle.rolling_prefill(f64(q), f64(k), f64(v), c, C, lp)
     for ci in range(L // c):
         sl = slice(ci * c, (ci + 1) * c)
-        cp.cp_kv_append(desc, kd[None, sl], vd[None, sl], c, kc, vc, lens, ci * c, dev_status=status)
-        cp.cp_prefill_chunk_attn(desc, qd[None, sl], kc, vc, lens, c, c, ci * c, out[None, sl], None,
-                                 commit=True, left_pad=left, dev_status=status)
+        if fused:
+            cp.cp_prefill_chunk(desc, qd[None, sl], kd[None, sl], vd[None, sl], kc, vc, lens, c, c, ci * c,
+                                out[None, sl], ws, left_pad=left, dev_status=status)
+        else:
+            cp.cp_kv_append(desc, kd[None, sl], vd[None, sl], c, kc, vc, lens, ci * c, dev_status=status)
+            cp.cp_prefill_chunk_attn(desc, qd[None, sl], kc, vc, lens, c, c, ci * c, out[None, sl], None,
+                                     commit=True, left_pad=left, dev_status=status)
         torch.cuda.synchronize()
         # De-rotate: logical slot j holds position a = n - C + j, stored at a mod C.
         n = (ci + 1) * c
@@ -70,6 +75,14 @@ def test_rolling_no_overflow_768_equals_plain_prefill():
     got, _, lp, q, k, v = _run_rolling(700, 256, 1024, 16, 128, torch.float16, seed=3)
     plain = oracle.causal_attention(f64(q[lp:]), f64(k[lp:]), f64(v[lp:]))
     assert np.abs(got[lp:] - plain).max() < BF16_TOL
+
+
+def test_rolling_sliding_window_fused_call():
+    """The same window through the one-call chunk entry point: identical to
+    the append + attention calls, bit for bit."""
+    got, _, lp, _, _, _ = _run_rolling(2000, 256, 1024, 16, 128, torch.float16, seed=3, fused=True)
+    ref, _, _, _, _, _ = _run_rolling(2000, 256, 1024, 16, 128, torch.float16, seed=3)
+    assert np.array_equal(got, ref)
 
 
 def test_rolling_small_ragged():
