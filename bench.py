@@ -715,6 +715,14 @@ def run_paged(args, rank, world, dev, pk, pk_src):
                 "decode_ctx_mean": sum(wl.mb.decode_ctx) / len(wl.mb.decode_ctx), "page_size": wl.mb.page_size,
                 "l2": "flushed between timed steps (512 MiB write)", "cuda_graph": True},
             "decode_bytes_per_step": wl.decode_bytes, "flops_per_step": wl.flops,
+            "roofline": ({"bound": "hbm", "achieved": wl.decode_bytes / (ms / 1e3) / 1e9, "peak": hbm,
+                          "unit": "GB/s", "frac": wl.decode_bytes / (ms / 1e3) / 1e9 / hbm,
+                          "traffic": kernel_traffic("decode.cu", "decode_split_paged.md"),
+                          "kernel": "decode_split_kernel",
+                          "scope": "K/V bytes of the decode rows over the whole step (append, split-KV "
+                                   "kernel, combine, commit): a lower bound on the kernel's own rate",
+                          "peak_source": "measured hbm_gbs (copy)"}
+                         if args.workload == "decode" else None),
             "decode_gbs_whole_step": wl.decode_bytes / (ms / 1e3) / 1e9,
             "hbm_frac_whole_step": wl.decode_bytes / (ms / 1e3) / 1e9 / hbm,
             "tflops_whole_step": wl.flops / (ms / 1e3) / 1e12,
