@@ -227,9 +227,9 @@ class GqaPrefill:
             past += r
         self.flops = sum(self.flops_chunk)
         self.tokens = self.N
-        # launches of this library per step: pad (if any; q, k, v) + per chunk the append and the
-        # attention (which advances seqlens_k itself)
-        self.launches = sum(1 for r, w in zip(self.sizes, self.widths) if w > r) * 3 + 2 * len(self.sizes)
+        # launches of this library per step: one pad launch (q, k and v) per widened chunk + per chunk
+        # the append and the attention (which advances seqlens_k itself)
+        self.launches = sum(1 for r, w in zip(self.sizes, self.widths) if w > r) + 2 * len(self.sizes)
 
     def _chunk(self, i, attn=True, append=True, commit=True):
         cp = self.cp

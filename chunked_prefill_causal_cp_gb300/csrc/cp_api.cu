@@ -244,12 +244,9 @@ int cp_pad_chunk(const cp_layer_desc* desc, void* q, void* k_new, void* v_new, i
   const int es = esize_of(desc->dtype);
   const int qb = desc->num_q_heads * desc->head_dim * es;
   const int kb = desc->num_kv_heads * desc->head_dim * es;
-  if (q && (r = launch_result(launch_pad_rows(q, desc->batch, rows_padded, real_rows, qb, st))) != CP_OK) return r;
-  if (k_new && (r = launch_result(launch_pad_rows(k_new, desc->batch, rows_padded, real_rows, kb, st))) != CP_OK)
-    return r;
-  if (v_new && (r = launch_result(launch_pad_rows(v_new, desc->batch, rows_padded, real_rows, kb, st))) != CP_OK)
-    return r;
-  return CP_OK;
+  void* const base[3] = {q, k_new, v_new};
+  const int row_bytes[3] = {qb, kb, kb};
+  return launch_result(launch_pad_rows(base, row_bytes, desc->batch, rows_padded, real_rows, st));
 }
 
 int cp_prefill_chunk_attn(const cp_layer_desc* desc, const void* q, const void* k_cache, const void* v_cache,

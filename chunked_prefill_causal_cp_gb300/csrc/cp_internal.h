@@ -116,7 +116,9 @@ __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;"
 cudaError_t launch_kv_append(const AppendArgs& a, int rows_total, cudaStream_t st);
 // status (optional): CP_DEV_BOUNDS is set for a sequence with no rows.
 cudaError_t launch_commit(int* lens, const SeqRows& rows, int add_uniform, int* status, cudaStream_t st);
-cudaError_t launch_pad_rows(void* base, int batch, int rows_padded, int real_rows, int row_bytes, cudaStream_t st);
+// Widens up to three tensors (null entries skipped) in one launch.
+cudaError_t launch_pad_rows(void* const base[3], const int row_bytes[3], int batch, int rows_padded, int real_rows,
+                            cudaStream_t st);
 cudaError_t launch_attn_f32(const AttnArgs& a, int rows_bound, cudaStream_t st);
 cudaError_t launch_attn_tc(const AttnArgs& a, int dtype, const CUtensorMap& tq, const CUtensorMap& tk,
                            const CUtensorMap& tv, const CUtensorMap& to, const CUtensorMap& tkn,

@@ -71,10 +71,19 @@ __global__ void kv_append_kernel(const AppendArgs a, int rows_total) {
 }
 
 // Rows [real_rows, rows_padded) of each sequence become copies of row
-// real_rows - 1 ([Wiki] 四: pad rows repeat the last real token).
-__global__ void pad_rows_kernel(char* base, int batch, int rows_padded, int real_rows, int row_bytes) {
+// real_rows - 1 ([Wiki] 四: pad rows repeat the last real token).  One launch
+// widens up to three tensors: blockIdx.y picks the tensor (a null one is skipped).
+struct PadTensors {
+  char* base[3];
+  int row_bytes[3];
+};
+
+__global__ void pad_rows_kernel(const PadTensors p, int batch, int rows_padded, int real_rows) {
   pdl_launch_dependents();
   pdl_wait();
+  char* base = p.base[blockIdx.y];
+  const int row_bytes = p.row_bytes[blockIdx.y];
+  if (base == nullptr) return;
   const int vecs = row_bytes / 16;
   const int pad = rows_padded - real_rows;
   const long long gid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
@@ -112,12 +121,20 @@ cudaError_t launch_kv_append(const AppendArgs& a, int rows_total, cudaStream_t s
   return launch_pdl(kv_append_kernel, dim3((unsigned)grid), dim3(block), 0, st, a, rows_total);
 }
 
-cudaError_t launch_pad_rows(void* base, int batch, int rows_padded, int real_rows, int row_bytes, cudaStream_t st) {
-  const long long threads = (long long)batch * (rows_padded - real_rows) * (row_bytes / 16);
+cudaError_t launch_pad_rows(void* const base[3], const int row_bytes[3], int batch, int rows_padded, int real_rows,
+                            cudaStream_t st) {
+  PadTensors p;
+  long long threads = 0;
+  for (int i = 0; i < 3; ++i) {
+    p.base[i] = static_cast<char*>(base[i]);
+    p.row_bytes[i] = row_bytes[i];
+    const long long t = base[i] ? (long long)batch * (rows_padded - real_rows) * (row_bytes[i] / 16) : 0;
+    if (t > threads) threads = t;
+  }
   if (threads <= 0) return cudaSuccess;
   const int block = 256;
-  return launch_pdl(pad_rows_kernel, dim3((unsigned)((threads + block - 1) / block)), dim3(block), 0, st,
-                    static_cast<char*>(base), batch, rows_padded, real_rows, row_bytes);
+  return launch_pdl(pad_rows_kernel, dim3((unsigned)((threads + block - 1) / block), 3), dim3(block), 0, st, p,
+                    batch, rows_padded, real_rows);
 }
 
 // add_uniform >= 0 adds that count to every sequence; -1 adds each
