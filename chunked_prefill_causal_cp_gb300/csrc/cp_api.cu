@@ -314,6 +314,7 @@ int cp_prefill_chunk(const cp_layer_desc* desc, const void* q, void* k_new, void
   // The copy of the lengths always; the split-KV partials only when one-row
   // chunks take the decode path (checked here, before anything is enqueued).
   const int G0 = desc->num_q_heads / desc->num_kv_heads;
+  if (desc->dtype != CP_F32 && !attn_tc_supported(desc->head_dim, G0, desc->dtype)) return CP_ERR_UNSUPPORTED;
   const bool decode_rows = rows_padded == 1 && desc->dtype != CP_F32 && desc->kind != CP_CACHE_ROLLING &&
                            decode_supported(desc->head_dim, G0, desc->dtype);
   const int64_t snap = snapshot_bytes(desc->batch);
@@ -386,6 +387,14 @@ int cp_mixed_step(const cp_layer_desc* desc, const void* q, const void* k_new, c
       !aligned16(out))
     return CP_ERR_INVALID_ARG;
   if ((int64_t)max_ctx > layout_limit(desc)) return CP_ERR_CAPACITY;
+  // Checks the attention launches would make, taken before the append is enqueued.
+  const int G0 = desc->num_q_heads / desc->num_kv_heads;
+  if (desc->dtype != CP_F32) {
+    if (!attn_tc_supported(desc->head_dim, G0, desc->dtype)) return CP_ERR_UNSUPPORTED;
+    if (decode_supported(desc->head_dim, G0, desc->dtype) &&
+        (workspace == nullptr || (int64_t)workspace_bytes < decode_ws_bytes(desc, max_ctx, num_seqs)))
+      return CP_ERR_WORKSPACE;
+  }
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const SeqRows rows{num_seqs, 0, cu_rows};
   const CacheView cache = make_cache(desc, block_table);

@@ -127,6 +127,9 @@ def _chunk(desc, rows=512, real=512, max_past=0, k_new=FAKE, ws=FAKE, ws_bytes=1
 
 def test_fused_chunk_rejects_bad_arguments_before_launch():
     assert _chunk(_desc(head_dim=96)) == cp.CP_ERR_UNSUPPORTED
+    # a GQA group the tensor-core kernel does not take is refused before the append is enqueued
+    assert _chunk(_desc(num_q_heads=32, num_kv_heads=1)) == cp.CP_ERR_UNSUPPORTED
+    assert _chunk(_desc(num_q_heads=24, num_kv_heads=8)) == cp.CP_ERR_UNSUPPORTED
     assert _chunk(_desc(), rows=100, real=101) == cp.CP_ERR_INVALID_ARG
     assert _chunk(_desc(), max_past=8192 - 511) == cp.CP_ERR_CAPACITY
     assert _chunk(_desc(), k_new=None) == cp.CP_ERR_INVALID_ARG
@@ -151,6 +154,16 @@ def test_append_and_mixed_reject_bad_arguments():
                            FAKE, FAKE, 1 << 20, None, None) == cp.CP_ERR_UNSUPPORTED
     assert L.cp_mixed_step(ctypes.byref(pd), FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 2, 10, 8 * 16 + 1,
                            FAKE, FAKE, 1 << 20, None, None) == cp.CP_ERR_CAPACITY
+    # refused before the append is enqueued: a group the tensor-core kernel does not take, and a
+    # workspace too small for the split-KV partials (a launch here, without a GPU, would give CP_ERR_CUDA)
+    pg = _desc(kind=cp.CP_CACHE_PAGED, page_size=16, num_pages=64, max_blocks=8, num_q_heads=32, num_kv_heads=1)
+    assert L.cp_mixed_step(ctypes.byref(pg), FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 2, 10, 100,
+                           FAKE, FAKE, 1 << 20, None, None) == cp.CP_ERR_UNSUPPORTED
+    need = cp.cp_workspace_size(pd, 10, 100, 2)
+    assert L.cp_mixed_step(ctypes.byref(pd), FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 2, 10, 100,
+                           FAKE, None, 0, None, None) == cp.CP_ERR_WORKSPACE
+    assert L.cp_mixed_step(ctypes.byref(pd), FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 2, 10, 100,
+                           FAKE, FAKE, need // 4, None, None) == cp.CP_ERR_WORKSPACE
 
 
 def test_workspace_size_formula():
