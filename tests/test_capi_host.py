@@ -140,6 +140,10 @@ def test_fused_chunk_rejects_bad_arguments_before_launch():
     need = cp.cp_workspace_size(_desc(), 1, 101, 1)
     assert _chunk(_desc(), rows=1, real=1, max_past=100, ws_bytes=need - 1) == cp.CP_ERR_WORKSPACE
     assert _chunk(_desc(), ws=FAKE + 4) == cp.CP_ERR_WORKSPACE
+    # the same layout rules as the separate calls
+    assert _chunk(_desc(kind=cp.CP_CACHE_ROLLING, capacity=1024), rows=256, real=200) == cp.CP_ERR_INVALID_ARG
+    assert _chunk(_desc(kind=cp.CP_CACHE_ROLLING, capacity=128), rows=256, real=256) == cp.CP_ERR_CAPACITY
+    assert _chunk(_desc(kind=cp.CP_CACHE_PAGED, page_size=16, num_pages=64, max_blocks=8)) == cp.CP_ERR_INVALID_ARG
 
 
 def test_append_and_mixed_reject_bad_arguments():
