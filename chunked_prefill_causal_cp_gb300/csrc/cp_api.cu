@@ -191,6 +191,39 @@ int run_attention(const cp_layer_desc* d, const AttnArgs& base, int64_t rows_tot
 
 }  // namespace
 
+namespace cp {
+
+// Every check cp_mixed_step makes before it enqueues anything; *ws_need is the
+// workspace it then needs (the decode rows' split-KV partials; 0 when the
+// layer takes no decode path).  Returns CP_OK or the status cp_mixed_step
+// returns.
+int mixed_step_check(const cp_layer_desc* desc, const void* q, const void* k_new, const void* v_new,
+                     const void* k_pages, const void* v_pages, const int32_t* block_table, const int32_t* cu_rows,
+                     const int32_t* past_len, int32_t num_seqs, int32_t total_rows, int32_t max_ctx, const void* out,
+                     size_t* ws_need) {
+  *ws_need = 0;
+  int r = check_desc(desc, false);
+  if (r != CP_OK) return r;
+  if (desc->kind != CP_CACHE_PAGED) return CP_ERR_UNSUPPORTED;
+  if (num_seqs <= 0 || total_rows < 0 || max_ctx <= 0) return CP_ERR_INVALID_ARG;
+  if (total_rows == 0) return CP_OK;
+  if (!q || !k_new || !v_new || !k_pages || !v_pages || !block_table || !cu_rows || !past_len || !out)
+    return CP_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k_new) || !aligned16(v_new) || !aligned16(k_pages) || !aligned16(v_pages) ||
+      !aligned16(out))
+    return CP_ERR_INVALID_ARG;
+  if ((int64_t)max_ctx > layout_limit(desc)) return CP_ERR_CAPACITY;
+  // Checks the attention launches would make, taken before the append is enqueued.
+  const int G0 = desc->num_q_heads / desc->num_kv_heads;
+  if (desc->dtype != CP_F32) {
+    if (!attn_tc_supported(desc->head_dim, G0, desc->dtype)) return CP_ERR_UNSUPPORTED;
+    if (decode_supported(desc->head_dim, G0, desc->dtype)) *ws_need = (size_t)decode_ws_bytes(desc, max_ctx, num_seqs);
+  }
+  return CP_OK;
+}
+
+}  // namespace cp
+
 extern "C" {
 
 size_t cp_workspace_size(const cp_layer_desc* desc, int32_t max_rows, int32_t max_ctx, int32_t num_seqs) {
@@ -376,25 +409,12 @@ int cp_mixed_step(const cp_layer_desc* desc, const void* q, const void* k_new, c
                   void* v_pages, const int32_t* block_table, const int32_t* cu_rows, int32_t* past_len,
                   int32_t num_seqs, int32_t total_rows, int32_t max_ctx, void* out, void* workspace,
                   size_t workspace_bytes, int32_t* dev_status, void* stream) {
-  int r = check_desc(desc, false);
+  size_t need = 0;
+  int r = cp::mixed_step_check(desc, q, k_new, v_new, k_pages, v_pages, block_table, cu_rows, past_len, num_seqs,
+                               total_rows, max_ctx, out, &need);
   if (r != CP_OK) return r;
-  if (desc->kind != CP_CACHE_PAGED) return CP_ERR_UNSUPPORTED;
-  if (num_seqs <= 0 || total_rows < 0 || max_ctx <= 0) return CP_ERR_INVALID_ARG;
   if (total_rows == 0) return CP_OK;
-  if (!q || !k_new || !v_new || !k_pages || !v_pages || !block_table || !cu_rows || !past_len || !out)
-    return CP_ERR_INVALID_ARG;
-  if (!aligned16(q) || !aligned16(k_new) || !aligned16(v_new) || !aligned16(k_pages) || !aligned16(v_pages) ||
-      !aligned16(out))
-    return CP_ERR_INVALID_ARG;
-  if ((int64_t)max_ctx > layout_limit(desc)) return CP_ERR_CAPACITY;
-  // Checks the attention launches would make, taken before the append is enqueued.
-  const int G0 = desc->num_q_heads / desc->num_kv_heads;
-  if (desc->dtype != CP_F32) {
-    if (!attn_tc_supported(desc->head_dim, G0, desc->dtype)) return CP_ERR_UNSUPPORTED;
-    if (decode_supported(desc->head_dim, G0, desc->dtype) &&
-        (workspace == nullptr || (int64_t)workspace_bytes < decode_ws_bytes(desc, max_ctx, num_seqs)))
-      return CP_ERR_WORKSPACE;
-  }
+  if (need > 0 && (workspace == nullptr || workspace_bytes < need || !aligned16(workspace))) return CP_ERR_WORKSPACE;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const SeqRows rows{num_seqs, 0, cu_rows};
   const CacheView cache = make_cache(desc, block_table);

@@ -126,6 +126,13 @@ cudaError_t launch_attn_tc(const AttnArgs& a, int dtype, const CUtensorMap& tq, 
 // Split-KV decode: partials into a.part_o / a.part_ml, then their combine.
 cudaError_t launch_decode(const AttnArgs& a, int dtype, cudaStream_t st);
 
+// Every check cp_mixed_step makes before enqueueing anything (returns its
+// status); *ws_need is the workspace the step then needs (decode partials).
+int mixed_step_check(const cp_layer_desc* desc, const void* q, const void* k_new, const void* v_new,
+                     const void* k_pages, const void* v_pages, const int32_t* block_table, const int32_t* cu_rows,
+                     const int32_t* past_len, int32_t num_seqs, int32_t total_rows, int32_t max_ctx, const void* out,
+                     size_t* ws_need);
+
 // Tensor-core path tiling (shared with the host so it can size grids and
 // tensor-map boxes).
 constexpr int kTcBlockM = 128;   // packed (token, head) rows per CTA

@@ -10,6 +10,11 @@
 // runtime does not allow cudaMalloc at all (for example from a stream
 // callback).  This entry point gives them the same step with its scratch in a
 // fixed array that is part of the library image itself.
+//
+// This translation unit is its own CUDA module.  Under the runtime's lazy
+// module loading (the default) the module, and with it the array's 8 MiB of
+// device memory, is loaded on a device by the first call that needs it: the
+// address lookup in this entry point's first call on that device.
 #include <cstddef>
 #include <cstdint>
 #include <mutex>
@@ -21,14 +26,16 @@
 namespace {
 
 // Split-KV scratch of the no-allocation entry point: 8 MiB on every GPU that
-// loads the library, held until the process exits.  Enough for, e.g., 16
+// loads this module, held until the process exits.  Enough for, e.g., 16
 // sequences x 32 query heads x contexts up to 8192 keys at head_dim 128.
 constexpr size_t kNoAllocScratchBytes = size_t(8) << 20;
 __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
-// Device address of g_noalloc_scratch, looked up once per device.  In host
-// code the symbol itself is only a host-side stand-in and must never be
-// passed to a kernel.
+// Device address of g_noalloc_scratch, looked up once per device with that
+// device current.  In host code the symbol itself is only a host-side
+// stand-in and must never be passed to a kernel.  The cached address belongs
+// to the device's primary context: after cudaDeviceReset it is stale, so calls
+// after a reset are not supported.
 constexpr int kMaxDevices = 64;
 std::mutex g_setup_mutex;
 void* g_scratch_addr[kMaxDevices] = {};
@@ -57,11 +64,14 @@ int cp_mixed_step_noalloc(const cp_layer_desc* desc, const void* q, const void* 
                           void* k_pages, void* v_pages, const int32_t* block_table, const int32_t* cu_rows,
                           int32_t* past_len, int32_t num_seqs, int32_t total_rows, int32_t max_ctx, void* out,
                           int32_t* dev_status, void* stream) {
-  // Size check first, before any CUDA call: a request that does not fit the
-  // fixed scratch is refused with CP_ERR_WORKSPACE.
-  if (desc == nullptr || num_seqs <= 0 || total_rows < 0 || max_ctx <= 0) return CP_ERR_INVALID_ARG;
-  const size_t need = cp_workspace_size(desc, total_rows, max_ctx, num_seqs);
-  if (need == 0) return CP_ERR_INVALID_ARG;
+  // The same checks as cp_mixed_step, in the same order and with the same
+  // status codes, then the size check against the fixed scratch -- all before
+  // any CUDA call.
+  size_t need = 0;
+  const int r0 = cp::mixed_step_check(desc, q, k_new, v_new, k_pages, v_pages, block_table, cu_rows, past_len,
+                                      num_seqs, total_rows, max_ctx, out, &need);
+  if (r0 != CP_OK) return r0;
+  if (total_rows == 0) return CP_OK;
   if (need > kNoAllocScratchBytes) return CP_ERR_WORKSPACE;
   void* scratch = nullptr;
   const int r = scratch_for_current_device(&scratch);

@@ -202,7 +202,9 @@ int cp_prefill_chunk(const cp_layer_desc* desc, const void* q, void* k_new, void
  *                 sequence with no rows sets CP_DEV_BOUNDS in *dev_status
  *   past_len      device int32 [num_seqs]: positions already cached
  *   max_ctx       host bound on past_len[s] + rows of s (<= max_blocks*page_size)
- *   workspace     >= cp_workspace_size(desc, T, max_ctx, num_seqs) bytes */
+ *   workspace     device scratch, 16-byte aligned, of at least
+ *                 cp_workspace_size(desc, T, max_ctx, num_seqs) bytes (that size
+ *                 always suffices; fp32 layers need none and may pass NULL) */
 int cp_mixed_step(const cp_layer_desc* desc, const void* q, const void* k_new,
                   const void* v_new, void* k_pages, void* v_pages, const int32_t* block_table,
                   const int32_t* cu_rows, int32_t* past_len, int32_t num_seqs,
@@ -219,16 +221,19 @@ int cp_mixed_step(const cp_layer_desc* desc, const void* q, const void* k_new,
  * and code running where cudaMalloc is not allowed (for example inside a
  * stream callback).  This is cp_mixed_step with its split-KV scratch taken from
  * a fixed array of cp_noalloc_scratch_bytes() bytes (8 MiB) compiled into the
- * library; every GPU that loads the library holds that array until the
- * process exits.  It allocates nothing: no cudaMalloc, cudaFree or allocating
- * library routine.
- *   Arguments and results are those of cp_mixed_step, without the workspace.
- *   A step whose cp_workspace_size(desc, total_rows, max_ctx, num_seqs)
- *   exceeds the array is refused with CP_ERR_WORKSPACE before anything is
- *   enqueued.
- *   The first call on a device looks up the array's device address (once per
- *   device, with that device current); make that first call before any stream
- *   capture on that device.
+ * library.  It calls no cudaMalloc, cudaFree or allocating library routine.
+ *   Arguments, checks, status codes and results are those of cp_mixed_step,
+ *   without the workspace.  A step whose split-KV partials (the workspace
+ *   cp_mixed_step would use for it) exceed the array is refused with
+ *   CP_ERR_WORKSPACE before anything is enqueued.
+ *   Set-up: the array lives in its own CUDA module.  With the CUDA runtime's
+ *   lazy module loading (the default) that module -- and so the array's 8 MiB
+ *   of device memory -- is loaded on a device by this entry point's first call
+ *   there, which also looks up the array's device address (once per device,
+ *   with that device current).  Make that first call on each device during
+ *   set-up (a small warm-up step), before reserving the rest of the device's
+ *   memory and before any stream capture.  Calls after cudaDeviceReset are not
+ *   supported (the looked-up address belongs to the reset context).
  *   Every call uses the same array, which keeps the last call's contents:
  *   each call writes every entry it uses before reading it.
  *   Calls whose work overlaps on the GPU -- on different streams or from

@@ -177,3 +177,60 @@ def test_workspace_size_formula():
     assert cp.cp_workspace_size(d, 64, 8192, 64) == 256 + 64 * 32 * 16 * 130 * 4
     assert cp.cp_workspace_size(d, 1, 1, 1) == 256 + 32 * 1 * 130 * 4
     assert cp.cp_workspace_size(d, 1, 1, 65) == 512 + 65 * 32 * 1 * 130 * 4
+
+
+def test_mixed_step_rejects_misaligned_workspace():
+    """The decode rows' float partials need a 16-byte aligned workspace; a
+    misaligned one is refused before the append is enqueued."""
+    L = cp.lib()
+    pd = _desc(kind=cp.CP_CACHE_PAGED, page_size=16, num_pages=64, max_blocks=8)
+    assert L.cp_mixed_step(ctypes.byref(pd), FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 2, 10, 100,
+                           FAKE, FAKE + 4, 1 << 20, None, None) == cp.CP_ERR_WORKSPACE
+
+
+def _mixed_pair(desc, num_seqs=2, total_rows=10, max_ctx=100, q=FAKE, out=FAKE):
+    """Status of cp_mixed_step (with an ample aligned workspace) and of
+    cp_mixed_step_noalloc on the same arguments."""
+    L = cp.lib()
+    a = L.cp_mixed_step(ctypes.byref(desc) if desc is not None else None, q, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE,
+                        FAKE, num_seqs, total_rows, max_ctx, out, FAKE, 1 << 30, None, None)
+    b = L.cp_mixed_step_noalloc(ctypes.byref(desc) if desc is not None else None, q, FAKE, FAKE, FAKE, FAKE, FAKE,
+                                FAKE, FAKE, num_seqs, total_rows, max_ctx, out, None, None)
+    return a, b
+
+
+def test_noalloc_status_codes_match_mixed_step():
+    """cp_mixed_step_noalloc makes the same argument checks as cp_mixed_step, in
+    the same order, and returns the same status for each bad argument."""
+    pd = dict(kind=cp.CP_CACHE_PAGED, page_size=16, num_pages=64, max_blocks=8)
+    cases = [
+        (_desc(head_dim=96, **pd), {}, cp.CP_ERR_UNSUPPORTED),
+        (_desc(kind=cp.CP_CACHE_PAGED, page_size=24, num_pages=64, max_blocks=8), {}, cp.CP_ERR_UNSUPPORTED),
+        (_desc(), {}, cp.CP_ERR_UNSUPPORTED),                                  # contiguous layout
+        (_desc(num_q_heads=30, **pd), {}, cp.CP_ERR_INVALID_ARG),              # Hq % Hkv != 0
+        (_desc(num_q_heads=32, num_kv_heads=1, **pd), {}, cp.CP_ERR_UNSUPPORTED),  # group 32
+        (_desc(dtype=7, **pd), {}, cp.CP_ERR_INVALID_ARG),
+        (_desc(**pd), dict(num_seqs=0), cp.CP_ERR_INVALID_ARG),
+        (_desc(**pd), dict(total_rows=-1), cp.CP_ERR_INVALID_ARG),
+        (_desc(**pd), dict(q=None), cp.CP_ERR_INVALID_ARG),
+        (_desc(**pd), dict(out=FAKE + 8), cp.CP_ERR_INVALID_ARG),
+        (_desc(**pd), dict(max_ctx=8 * 16 + 1), cp.CP_ERR_CAPACITY),
+        (_desc(**pd), dict(total_rows=0), cp.CP_OK),                           # nothing to do
+        (None, {}, cp.CP_ERR_INVALID_ARG),
+    ]
+    for desc, kw, want in cases:
+        a, b = _mixed_pair(desc, **kw)
+        assert a == want and b == want, (kw, a, b, want)
+
+
+def test_noalloc_refuses_a_step_whose_partials_exceed_the_scratch():
+    """The fixed scratch is compared with the split-KV partials cp_mixed_step
+    would use for the step: one sequence more than fits is refused with
+    CP_ERR_WORKSPACE before anything is enqueued."""
+    L = cp.lib()
+    d = _desc(kind=cp.CP_CACHE_PAGED, page_size=16, num_pages=1 << 20, max_blocks=1 << 12)
+    per_seq = 32 * ((8192 + 511) // 512) * (128 + 2) * 4     # partials of one sequence at max_ctx 8192
+    fits = cp.cp_noalloc_scratch_bytes() // per_seq           # sequences whose partials fit the array
+    st = L.cp_mixed_step_noalloc(ctypes.byref(d), FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, fits + 1,
+                                 fits + 1, 8192, FAKE, None, None)
+    assert st == cp.CP_ERR_WORKSPACE
