@@ -218,7 +218,7 @@ class GqaPrefill:
         self.pasts = torch.tensor([0] + list(torch.tensor(self.sizes).cumsum(0)[:-1].tolist()),
                                   dtype=torch.int32, device=dev)
         self.status = torch.zeros(1, dtype=torch.int32, device=dev)
-        self.ws = torch.empty(max(16, cp.cp_workspace_size(self.desc, self.W, self.CAP, 1)),
+        self.ws = torch.zeros(max(16, cp.cp_workspace_size(self.desc, self.W, self.CAP, 1)),
                               dtype=torch.uint8, device=dev)
         self.flops_chunk = []
         past = 0
@@ -545,7 +545,7 @@ class PagedStep:
         self.past0 = torch.tensor(past, dtype=torch.int32, device=dev)
         self.past = self.past0.clone()
         self.status = torch.zeros(1, dtype=torch.int32, device=dev)
-        self.ws = torch.empty(cp.cp_workspace_size(self.desc, self.T, self.max_ctx, self.S), dtype=torch.uint8,
+        self.ws = torch.zeros(cp.cp_workspace_size(self.desc, self.T, self.max_ctx, self.S), dtype=torch.uint8,
                               device=dev)
         # algorithmic work
         kv_row = self.HKV * self.D * 2
@@ -611,7 +611,7 @@ class ChunkLoop:
             r["left"] = torch.tensor([r["lp"]], dtype=torch.int32, device=dev)
             r["out"] = torch.empty(r["L"], r["H"], r["d"], dtype=r["dtype"], device=dev)
             r["sizes"] = cp.cp_chunk_plan(r["L"], r["W"])
-            r["ws"] = torch.empty(cp.cp_workspace_size(r["desc"], r["W"], r["cap"], 1), dtype=torch.uint8,
+            r["ws"] = torch.zeros(cp.cp_workspace_size(r["desc"], r["W"], r["cap"], 1), dtype=torch.uint8,
                                   device=dev)
         self.tokens = sum(r["L"] - r["lp"] for r in self.runs)
         self.flops = sum(4 * r["d"] * r["H"] * r["pairs"] for r in self.runs)

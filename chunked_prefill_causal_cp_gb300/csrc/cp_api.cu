@@ -68,9 +68,11 @@ float scale_log2(const cp_layer_desc* d) {
 
 int64_t max_splits_for(int32_t max_ctx) { return ((int64_t)max_ctx + kDecodeSplit - 1) / kDecodeSplit; }
 
-// Workspace of cp_prefill_chunk: a snapshot of seqlens_k (its own 256-byte
-// aligned block), then the split partials.  The other calls use the partials
-// only, from the start of the workspace.
+// Workspace of cp_prefill_chunk: a 256-byte control block (the paired-SM
+// kernel's ticket counter, zero between calls), then a copy of seqlens_k in
+// whole 256-byte blocks, then the split partials.  The other calls use the
+// partials only, from the start of the workspace.
+constexpr int64_t kControlBytes = 256;
 int64_t snapshot_bytes(int32_t num_seqs) { return ((int64_t)num_seqs * 4 + 255) / 256 * 256; }
 
 // Decode workspace: the split partials (output rows, then max and sum).
@@ -112,6 +114,22 @@ bool encode_3d(CUtensorMap* m, int dtype, const void* base, uint64_t d0, uint64_
   const CUtensorMapDataType ty =
       dtype == CP_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
   return fn(m, ty, 3, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// 4-D tensor of 16-bit elements {d0 (contiguous), d1, d2, d3}, 128-byte swizzled boxes.
+bool encode_4d(CUtensorMap* m, int dtype, const void* base, uint64_t d0, uint64_t d1, uint64_t d2, uint64_t d3,
+               uint32_t b0, uint32_t b1, uint32_t b2, uint32_t b3) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[4] = {d0, d1, d2, d3};
+  const cuuint64_t strides[3] = {d0 * 2, d0 * d1 * 2, d0 * d1 * d2 * 2};
+  const cuuint32_t box[4] = {b0, b1, b2, b3};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  const CUtensorMapDataType ty =
+      dtype == CP_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  return fn(m, ty, 4, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -189,6 +207,61 @@ int run_attention(const cp_layer_desc* d, const AttnArgs& base, int64_t rows_tot
   return CP_OK;
 }
 
+// The paired-SM kernel takes contiguous-cache chunks of head_dim 128 with more
+// than one row per sequence.
+bool use_pair(const cp_layer_desc* d, int32_t rows_padded) {
+  const int G = d->num_q_heads / d->num_kv_heads;
+  return d->kind == CP_CACHE_CONTIG && rows_padded > 1 && attn_pair_supported(d->head_dim, G, d->dtype);
+}
+
+// Attention of B uniform chunks on the paired-SM kernel.  k_new/v_new non-null:
+// fused append (the chunk's tiles come from them and the kernel writes them into
+// the cache); ticket/commit_lens non-null: the kernel advances the lengths.
+int run_pair(const cp_layer_desc* d, const void* q, const void* k_cache, const void* v_cache, int32_t* seqlens_k,
+             int32_t rows_padded, int32_t max_past, void* out, const void* k_new, const void* v_new,
+             unsigned* ticket, int32_t* commit_lens, int32_t commit_add, int32_t* dev_status, cudaStream_t st) {
+  const int G = d->num_q_heads / d->num_kv_heads;
+  const uint64_t D = d->head_dim;
+  const int64_t rows_total = (int64_t)d->batch * rows_padded;
+  const uint64_t planes = (uint64_t)d->batch * d->num_kv_heads;
+  CUtensorMap tq, to, tkh, tvh, tknh, tvnh;
+  if (!encode_3d(&tq, d->dtype, q, D, d->num_q_heads, (uint64_t)rows_total, 64, G, kTcBlockM / G) ||
+      !encode_3d(&to, d->dtype, out, D, d->num_q_heads, (uint64_t)rows_total, 64, G, kTcBlockM / G) ||
+      !encode_3d(&tkh, d->dtype, k_cache, D, d->capacity, planes, 64, 64, 1) ||
+      !encode_3d(&tvh, d->dtype, v_cache, D, d->capacity, planes, 64, 128, 1))
+    return CP_ERR_CUDA;
+  std::memset(&tknh, 0, sizeof(tknh));
+  std::memset(&tvnh, 0, sizeof(tvnh));
+  const bool fused = k_new != nullptr;
+  if (fused && (!encode_4d(&tknh, d->dtype, k_new, D, d->num_kv_heads, rows_padded, d->batch, 64, 1, 64, 1) ||
+                !encode_4d(&tvnh, d->dtype, v_new, D, d->num_kv_heads, rows_padded, d->batch, 64, 1, 128, 1)))
+    return CP_ERR_CUDA;
+  PairArgs a;
+  std::memset(&a, 0, sizeof(a));
+  a.hq = d->num_q_heads;
+  a.hkv = d->num_kv_heads;
+  a.group = G;
+  a.scale_log2 = scale_log2(d);
+  a.rows = SeqRows{d->batch, rows_padded, nullptr};
+  a.capacity = d->capacity;
+  a.past = seqlens_k;
+  a.max_ctx = max_past + rows_padded;
+  a.out = out;
+  a.status = dev_status;
+  a.fused = fused ? 1 : 0;
+  a.k_new = k_new;
+  a.v_new = v_new;
+  a.k_cache = const_cast<void*>(k_cache);
+  a.v_cache = const_cast<void*>(v_cache);
+  a.ticket = ticket;
+  a.commit_lens = commit_lens;
+  a.commit_add = commit_add;
+  const int ppt = 2 * (kTcBlockM / G);
+  const int64_t pairs = (int64_t)d->batch * ((rows_padded + ppt - 1) / ppt);
+  if (2 * pairs > INT32_MAX || pairs * d->num_kv_heads > INT32_MAX) return CP_ERR_UNSUPPORTED;
+  return launch_result(launch_attn_pair(a, d->dtype, tq, to, tkh, tvh, tknh, tvnh, (int)pairs, st));
+}
+
 }  // namespace
 
 namespace cp {
@@ -229,7 +302,7 @@ extern "C" {
 size_t cp_workspace_size(const cp_layer_desc* desc, int32_t max_rows, int32_t max_ctx, int32_t num_seqs) {
   if (check_desc(desc, false) != CP_OK || max_rows < 0 || max_ctx < 0 || num_seqs < 0) return 0;
   (void)max_rows;
-  return (size_t)(snapshot_bytes(num_seqs) + decode_ws_bytes(desc, max_ctx, num_seqs));
+  return (size_t)(kControlBytes + snapshot_bytes(num_seqs) + decode_ws_bytes(desc, max_ctx, num_seqs));
 }
 
 int cp_kv_append(const cp_layer_desc* desc, const void* k_new, const void* v_new, int32_t rows, void* k_cache,
@@ -318,7 +391,12 @@ int cp_prefill_chunk_attn(const cp_layer_desc* desc, const void* q, const void* 
   a.v = v_cache;
   a.out = out;
   a.status = dev_status;
-  r = run_attention(desc, a, rows_total, rows_padded, k_cache, v_cache, desc->batch, workspace, workspace_bytes, st);
+  if (use_pair(desc, rows_padded))
+    r = run_pair(desc, q, k_cache, v_cache, seqlens_k, rows_padded, max_past, out, nullptr, nullptr, nullptr,
+                 nullptr, 0, dev_status, st);
+  else
+    r = run_attention(desc, a, rows_total, rows_padded, k_cache, v_cache, desc->batch, workspace, workspace_bytes,
+                      st);
   if (r != CP_OK) return r;
   if (commit) return launch_result(launch_commit(seqlens_k, a.rows, real_rows, nullptr, st));
   return CP_OK;
@@ -351,10 +429,14 @@ int cp_prefill_chunk(const cp_layer_desc* desc, const void* q, void* k_new, void
   const bool decode_rows = rows_padded == 1 && desc->dtype != CP_F32 && desc->kind != CP_CACHE_ROLLING &&
                            decode_supported(desc->head_dim, G0, desc->dtype);
   const int64_t snap = snapshot_bytes(desc->batch);
-  const int64_t need = snap + (decode_rows ? decode_ws_bytes(desc, max_past + rows_padded, desc->batch) : 0);
+  const int64_t need =
+      kControlBytes + snap + (decode_rows ? decode_ws_bytes(desc, max_past + rows_padded, desc->batch) : 0);
   if (workspace == nullptr || (int64_t)workspace_bytes < need || !aligned16(workspace)) return CP_ERR_WORKSPACE;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  int* past = static_cast<int*>(workspace);
+  if (use_pair(desc, rows_padded))  // one launch: append, attention and the advance of the lengths
+    return run_pair(desc, q, k_cache, v_cache, seqlens_k, rows_padded, max_past, out, k_new, v_new,
+                    static_cast<unsigned*>(workspace), seqlens_k, real_rows, dev_status, st);
+  int* past = reinterpret_cast<int*>(static_cast<char*>(workspace) + kControlBytes);
 
   AppendArgs ap;
   ap.hkv = desc->num_kv_heads;
@@ -398,7 +480,8 @@ int cp_prefill_chunk(const cp_layer_desc* desc, const void* q, void* k_new, void
     a.commit_add = real_rows;
   }
   r = run_attention(desc, a, rows_total, rows_padded, k_cache, v_cache, desc->batch,
-                    static_cast<char*>(workspace) + snap, (size_t)(workspace_bytes - snap), st,
+                    static_cast<char*>(workspace) + kControlBytes + snap,
+                    (size_t)(workspace_bytes - kControlBytes - snap), st,
                     desc->kind == CP_CACHE_PAGED ? k_new : nullptr, desc->kind == CP_CACHE_PAGED ? v_new : nullptr);
   if (r != CP_OK) return r;
   if (!tc_only) return launch_result(launch_commit(seqlens_k, a.rows, real_rows, nullptr, st));

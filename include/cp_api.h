@@ -165,16 +165,21 @@ int cp_prefill_chunk_attn(const cp_layer_desc* desc, const void* q, const void* 
  * seqlens_k by real_rows, with the same arguments and results as those two
  * calls made back to back with commit = 1 ([Glossary] "How chunked prefill
  * works": each chunk's K/V join the cache and its rows attend to the cache).
- * The append copies seqlens_k into the workspace and the attention reads the
- * copy, so the attention kernel itself advances seqlens_k (no separate commit
- * launch when the tensor-core path takes every row).
+ * For a contiguous cache with head_dim 128 and more than one row this is one
+ * kernel launch: the kernel reads the tiles that hold the chunk's own keys
+ * straight from k_new / v_new, copies those rows into the cache, and the last
+ * of its CTAs to have read seqlens_k advances it.  Other layouts take an append
+ * launch followed by the attention.
  *   q, out        device [B, rows_padded, Hq, D]
  *   k_new, v_new  device [B, rows_padded, Hkv, D] (rows [real_rows,
- *                 rows_padded) are appended too: cp_pad_chunk fills them)
+ *                 rows_padded) are appended too: cp_pad_chunk fills them); they
+ *                 must not alias the cache or out
  *   workspace     device scratch, 16-byte aligned, of at least
  *                 cp_workspace_size(desc, B * R, max_past + R, B) bytes (that
- *                 size always suffices; the call needs the split-KV part only
- *                 for one-row chunks)
+ *                 size always suffices).  Its first 256 bytes are a control
+ *                 block that must be zero before the first call that uses this
+ *                 workspace (allocate it zeroed); every call leaves it zero.
+ *                 Calls whose work overlaps on the GPU need separate workspaces.
  * Other arguments as in cp_prefill_chunk_attn. */
 int cp_prefill_chunk(const cp_layer_desc* desc, const void* q, void* k_new, void* v_new, void* k_cache,
                      void* v_cache, int32_t* seqlens_k, const int32_t* block_table,
@@ -251,8 +256,9 @@ size_t cp_noalloc_scratch_bytes(void);
 
 /* cp_workspace_size -- bytes of device scratch the attention calls need for up
  * to `max_rows` query rows, contexts of up to `max_ctx` keys and `num_seqs`
- * sequences: a copy of the sequences' lengths (cp_prefill_chunk; 256-byte
- * blocks) and the split-KV partial results. */
+ * sequences: a 256-byte control block and a copy of the sequences' lengths
+ * (cp_prefill_chunk; the control block must be zero before first use, see
+ * there) and the split-KV partial results. */
 size_t cp_workspace_size(const cp_layer_desc* desc, int32_t max_rows, int32_t max_ctx,
                          int32_t num_seqs);
 

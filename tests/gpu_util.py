@@ -27,7 +27,7 @@ class Contig:
         self.status = torch.zeros(1, dtype=torch.int32, device=dev)
         self.cap = cap
         self.fused = fused  # one cp_prefill_chunk call per chunk instead of append + attention
-        self.ws = torch.empty(max(cp.cp_workspace_size(self.desc, 1, cap, batch), 16), dtype=torch.uint8,
+        self.ws = torch.zeros(max(cp.cp_workspace_size(self.desc, 1, cap, batch), 16), dtype=torch.uint8,
                               device=dev)
 
     def chunk(self, q, k_new, v_new, real_rows, past, out=None):

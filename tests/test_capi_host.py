@@ -136,7 +136,7 @@ def test_fused_chunk_rejects_bad_arguments_before_launch():
     assert _chunk(_desc(), k_new=FAKE + 8) == cp.CP_ERR_INVALID_ARG
     # the copy of the lengths always needs the workspace; one-row chunks (decode) need the partials too
     assert _chunk(_desc(), ws=None) == cp.CP_ERR_WORKSPACE
-    assert _chunk(_desc(), ws_bytes=255) == cp.CP_ERR_WORKSPACE
+    assert _chunk(_desc(), ws_bytes=511) == cp.CP_ERR_WORKSPACE
     need = cp.cp_workspace_size(_desc(), 1, 101, 1)
     assert _chunk(_desc(), rows=1, real=1, max_past=100, ws_bytes=need - 1) == cp.CP_ERR_WORKSPACE
     assert _chunk(_desc(), ws=FAKE + 4) == cp.CP_ERR_WORKSPACE
@@ -172,11 +172,12 @@ def test_append_and_mixed_reject_bad_arguments():
 
 def test_workspace_size_formula():
     d = _desc()
-    # a copy of the lengths in 256-byte blocks, then num_seqs * Hq * ceil(ctx / 512) * (D + 2)
+    # a 256-byte control block, a copy of the lengths in 256-byte blocks, then
+    # num_seqs * Hq * ceil(ctx / 512) * (D + 2)
     # floats of split partials
-    assert cp.cp_workspace_size(d, 64, 8192, 64) == 256 + 64 * 32 * 16 * 130 * 4
-    assert cp.cp_workspace_size(d, 1, 1, 1) == 256 + 32 * 1 * 130 * 4
-    assert cp.cp_workspace_size(d, 1, 1, 65) == 512 + 65 * 32 * 1 * 130 * 4
+    assert cp.cp_workspace_size(d, 64, 8192, 64) == 256 + 256 + 64 * 32 * 16 * 130 * 4
+    assert cp.cp_workspace_size(d, 1, 1, 1) == 256 + 256 + 32 * 1 * 130 * 4
+    assert cp.cp_workspace_size(d, 1, 1, 65) == 256 + 512 + 65 * 32 * 1 * 130 * 4
 
 
 def test_mixed_step_rejects_misaligned_workspace():

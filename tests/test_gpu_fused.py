@@ -132,7 +132,7 @@ def test_fused_paged_prompt():
     table = perm[None].cuda()
     lens = torch.zeros(1, dtype=torch.int32, device="cuda")
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
-    ws = torch.empty(cp.cp_workspace_size(desc, W, nb * ps, 1), dtype=torch.uint8, device="cuda")
+    ws = torch.zeros(cp.cp_workspace_size(desc, W, nb * ps, 1), dtype=torch.uint8, device="cuda")
     out = torch.empty(n, hq, d, dtype=torch.bfloat16, device="cuda")
     qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
     past = 0

@@ -56,7 +56,7 @@ class Paged:
         bt = self.table[torch.tensor(seqs, device="cuda")].contiguous()
         T = int(sum(rows))
         out = torch.empty(T, HQ, D, dtype=self.dtype, device="cuda")
-        ws = torch.empty(cp.cp_workspace_size(self.desc, T, max_ctx, S), dtype=torch.uint8, device="cuda")
+        ws = torch.zeros(cp.cp_workspace_size(self.desc, T, max_ctx, S), dtype=torch.uint8, device="cuda")
         cp.cp_mixed_step(self.desc, q, kn, vn, self.k, self.v, bt, cu, pl, S, T, max_ctx, out, ws,
                          dev_status=self.status)
         return out, pl
@@ -307,7 +307,7 @@ def test_mixed_step_page_sizes(page):
     cu = torch.tensor(np.concatenate([[0], np.cumsum(rows)]), dtype=torch.int32, device="cuda")
     pl = torch.tensor(past, dtype=torch.int32, device="cuda")
     out = torch.empty(T, HQ, D, dtype=torch.bfloat16, device="cuda")
-    ws = torch.empty(cp.cp_workspace_size(desc, T, max_ctx, S), dtype=torch.uint8, device="cuda")
+    ws = torch.zeros(cp.cp_workspace_size(desc, T, max_ctx, S), dtype=torch.uint8, device="cuda")
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
     cp.cp_mixed_step(desc, q.cuda(), kn.cuda(), vn.cuda(), kp, vp, table.cuda(), cu, pl, S, T, max_ctx, out, ws,
                      dev_status=status)

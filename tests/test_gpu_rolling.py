@@ -33,7 +33,7 @@ def _run_rolling(n_real, c, C, H, d, dtype, seed, fused=False):
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
     out = torch.empty(L, H, d, dtype=dtype, device="cuda")
     qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
-    ws = torch.empty(cp.cp_workspace_size(desc, c, C, 1), dtype=torch.uint8, device="cuda")
+    ws = torch.zeros(cp.cp_workspace_size(desc, c, C, 1), dtype=torch.uint8, device="cuda")
     ref_out, snaps = oracle.rolling_prefill(f64(q), f64(k), f64(v), c, C, lp)
     for ci in range(L // c):
         sl = slice(ci * c, (ci + 1) * c)

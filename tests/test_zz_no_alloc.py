@@ -15,7 +15,6 @@ import chunked_prefill_causal_cp_gb300 as cp
 import synth_inputs as SI
 
 HQ, HKV, D, PAGE = 32, 8, 128, 16
-TOL = 2e-2  # the max-abs bound the other bf16 parity tests use
 
 
 def test_oversized_step_is_refused_before_any_gpu_work():
@@ -60,6 +59,12 @@ def _pool_state(seed):
 
 @pytest.mark.gpu
 def test_noalloc_matches_workspace_path_on_consecutive_calls():
+    """Two calls in a row through both entry points: the outputs, pools and
+    past lengths are bit-identical (both run the same kernels on the same
+    inputs, with a fixed merge order).  The second call lists fewer and shorter
+    sequences than the first, so it uses fewer split-KV partials laid out
+    differently in the shared scratch: leftovers of the first call must not
+    reach its results."""
     if not torch.cuda.is_available():
         pytest.skip("needs a GPU")
     from chunked_prefill_causal_cp_gb300 import _build
@@ -73,27 +78,34 @@ def test_noalloc_matches_workspace_path_on_consecutive_calls():
     S = len(past)
     prompt_q, prompt_k, prompt_v = SI.gqa_prompt(350, seed=32)
     start = 0
-    for step, chunk in enumerate([200, 150]):  # two calls in a row, reusing the scratch
-        dq, dk, dv = SI.gqa_prompt(S - 1, seed=40 + step)
+    # call 1: the five decodes (contexts up to 1000: two 512-key splits) and 200 prompt rows;
+    # call 2: decodes 0 and 1 only (contexts 41 and 301: one split) and the next 150 prompt rows
+    for step, (seqs, chunk) in enumerate([(list(range(S)), 200), ([0, 1, S - 1], 150)]):
+        nd = len(seqs) - 1
+        dq, dk, dv = SI.gqa_prompt(nd, seed=40 + step)
         q = torch.cat([dq, prompt_q[start:start + chunk]]).cuda()
         kn = torch.cat([dk, prompt_k[start:start + chunk]]).cuda()
         vn = torch.cat([dv, prompt_v[start:start + chunk]]).cuda()
-        rows = [1] * (S - 1) + [chunk]
+        rows = [1] * nd + [chunk]
         cu = torch.tensor(np.concatenate([[0], np.cumsum(rows)]), dtype=torch.int32, device="cuda")
         T = int(sum(rows))
-        max_ctx = int(max(p + r for p, r in zip(past_a.tolist(), rows)))
+        idx = torch.tensor(seqs, device="cuda")
+        pa, pb = past_a[idx].contiguous(), past_b[idx].contiguous()
+        tb = table[idx].contiguous()
+        max_ctx = int(max(p + r for p, r in zip(pa.tolist(), rows)))
         out_a = torch.empty(T, HQ, D, dtype=torch.bfloat16, device="cuda")
         out_b = torch.full_like(out_a, float("nan"))
-        ws = torch.empty(cp.cp_workspace_size(desc, T, max_ctx, S), dtype=torch.uint8, device="cuda")
-        cp.cp_mixed_step(desc, q, kn, vn, kp, vp, table, cu, past_a, S, T, max_ctx, out_a, ws,
+        ws = torch.empty(cp.cp_workspace_size(desc, T, max_ctx, len(seqs)), dtype=torch.uint8, device="cuda")
+        cp.cp_mixed_step(desc, q, kn, vn, kp, vp, tb, cu, pa, len(seqs), T, max_ctx, out_a, ws,
                          dev_status=status_a)
-        cp.cp_mixed_step_noalloc(desc, q, kn, vn, kp_b, vp_b, table, cu, past_b, S, T, max_ctx, out_b,
+        cp.cp_mixed_step_noalloc(desc, q, kn, vn, kp_b, vp_b, tb, cu, pb, len(seqs), T, max_ctx, out_b,
                                  dev_status=status_b)
         torch.cuda.synchronize()
-        err = (out_a.float() - out_b.float()).abs().max().item()
-        assert err <= TOL, (step, err)
-        assert torch.isfinite(out_b.float()).all()
-        assert torch.equal(past_a, past_b)
+        assert torch.equal(out_a, out_b), step
+        assert torch.equal(pa, pb)
+        past_a[idx] = pa
+        past_b[idx] = pb
         start += chunk
     assert torch.equal(kp, kp_b) and torch.equal(vp, vp_b)
+    assert torch.equal(past_a, past_b)
     assert int(status_a.item()) == 0 and int(status_b.item()) == 0
