@@ -31,13 +31,16 @@
 // Warp roles (384 threads, three warpgroups):
 //   warp 0      TMA producer: this CTA's Q tile, then per KV tile its K half and
 //               V half into a 5-stage ring.
-//   warp 1      TMEM allocation (both CTAs); in CTA 0 the MMA issuer (one lane).
+//   warp 1      TMEM allocation (both CTAs); in CTA 0 the issuer of S = Q K^T
+//               (the whole warp, one elected lane issuing), in CTA 1 the
+//               forwarder of "S read out" to CTA 0.
 //   warp 2      forwarder: when a stage lands in this CTA it zeroes V rows that
 //               hold no key of the tile's source (so 0 * stale data never reaches
 //               O) and tells CTA 0's issuer (local or remote mbarrier arrive).
 //   warp 3      fused append: copies this Q tile's tokens' K/V rows of the
-//               KV head into the cache with 16-byte loads and stores; then, in
-//               CTA 1, forwards each tile's P-ready to CTA 0's issuer.
+//               KV head into the cache with 16-byte loads and stores; then the
+//               issuer of O += P V in CTA 0, the forwarder of "P written" to
+//               CTA 0 in CTA 1.
 //   warps 4-11  softmax: warps 4-7 take the even tiles, warps 8-11 the odd ones;
 //               thread (warp, lane) owns row 32*(warp%4) + lane and all 128 keys
 //               of its tiles.  The running max of a row is handed from one
@@ -45,10 +48,10 @@
 //               row max, so one warpgroup exponentiates while the other loads
 //               and reduces the next tile; each keeps its own share of the row
 //               sum and the two are added at the end.
-// TMEM (512 columns): S/P triple buffer [0,128), [128,256), [256,384), O
-// [384,512).  The issuer keeps S two tiles ahead of P V: S of tile i+3 goes into
-// the buffer P V of tile i has just read, so the softmax warps run from one tile
-// to the next without waiting for the tensor core.
+// TMEM (512 columns): S double buffer [0,128) and [128,256), P double buffer
+// [256,320) and [320,384) (16-bit pairs), O [384,512).  P has its own columns,
+// so S of tile i+2 is computed as soon as the softmax has read S of tile i
+// (into registers), while P of tile i still waits for its P V.
 #include <atomic>
 #include <cmath>
 #include <cstdint>
@@ -77,7 +80,9 @@ constexpr uint32_t kKHalfBlock = 64u * 128u;  // [64 keys][64 x 16-bit]: one 64-
 constexpr uint32_t kVOff = 2u * kKHalfBlock;  // V half after the two K-half blocks of a stage
 constexpr uint32_t kStageBytes = kVOff + kQBlock;  // K half 16 KB + V half [128 keys][64 dims] 16 KB
 constexpr uint32_t kTmemCols = 512;
-constexpr int kSBufs = 3;
+constexpr int kSBufs = 2;
+constexpr int kORing = 8;  // slots of the "P V of tile t done" barrier ring
+constexpr uint32_t kColP = 256;  // P of buffer b at kColP + 64 b
 constexpr uint32_t kColO = 384;
 constexpr float kRescaleLog2 = 8.0f;  // O is rescaled when a row's max grows by more than 2^8
 
@@ -88,9 +93,12 @@ struct __align__(16) PairBarriers {
   uint64_t q_ready;              // CTA 0: both Q tiles landed (2 forwarders)
   uint64_t kv_ready[kPStages];   // CTA 0: both CTAs' halves of the stage are ready (2 forwarders)
   uint64_t s_full[kSBufs];       // S buffer b holds its tile's scores (multicast)
-  uint64_t p_ready[kSBufs];      // CTA 0: P of buffer b written in both CTAs (4 local warps + CTA 1's forward)
-  uint64_t p_local[kSBufs];      // CTA 1: P of buffer b written by the 4 warps of its warpgroup
-  uint64_t o_done[2];            // P V of an even / odd tile completed (multicast)
+  uint64_t s_free[kSBufs];       // CTA 0: S buffer b read out in both CTAs (4 local warps + CTA 1's forward)
+  uint64_t s_local[kSBufs];      // CTA 1: S buffer b read out by the 4 warps of the tile's warpgroup
+  uint64_t p_ready[kSBufs];      // CTA 0: P buffer b written in both CTAs (4 local warps + CTA 1's forward)
+  uint64_t p_local[kSBufs];      // CTA 1: P buffer b written by the 4 warps of the tile's warpgroup
+  uint64_t o_done[kORing];       // P V of tile t completed, in slot t % kORing (multicast)
+  uint64_t qk_final;             // CTA 0: every S MMA issued has completed
   uint64_t o_final;              // every MMA issued has completed (multicast, once)
   uint32_t tmem_base;
   int abort;
@@ -199,11 +207,13 @@ __global__ void __launch_bounds__(kPThreads, 1)
     }
     for (int b = 0; b < kSBufs; ++b) {
       mbar_init(&bar->s_full[b], 1);
+      mbar_init(&bar->s_free[b], 5);
+      mbar_init(&bar->s_local[b], 4);
       mbar_init(&bar->p_ready[b], 5);
       mbar_init(&bar->p_local[b], 4);
     }
-    mbar_init(&bar->o_done[0], 1);
-    mbar_init(&bar->o_done[1], 1);
+    for (int t = 0; t < kORing; ++t) mbar_init(&bar->o_done[t], 1);
+    mbar_init(&bar->qk_final, 1);
     mbar_init(&bar->o_final, 1);
     bar->abort = 0;
     fence_barrier_init();
@@ -327,61 +337,49 @@ __global__ void __launch_bounds__(kPThreads, 1)
     }
     __syncwarp();
   } else if (warp == 1) {
-    // ================================================================ MMA issuer (CTA 0)
-    // The whole warp runs the loop, converged; one elected lane issues each
-    // tcgen05 instruction.
+    // ================================================================ S issuer (CTA 0)
+    // Two threads issue the pair's MMAs: this warp the S = Q K^T of each tile,
+    // warp 3 the O += P V.  Each waits only for its own inputs; tcgen05 work of
+    // one thread completes in issue order, which is all the commits below rely on.
+    // The whole warp runs the loop, converged; one elected lane issues.
     if (rank == 0) {
-      auto wait = [&](uint64_t* b, uint32_t parity) { return warp_wait_cl(b, parity, abort_flag, a.status); };
       const uint64_t q_desc = make_sdesc_sw128(smem_u32(sQ), 16, 1024);
       const uint64_t k_desc0 = make_sdesc_sw128(smem_u32(sStage), 16, 1024);
-      const uint64_t v_desc0 = make_sdesc_sw128(smem_u32(sStage + kVOff), kQBlock, 1024);
       constexpr uint64_t kStageStep = kStageBytes >> 4;
-      auto issue_qk = [&](int j) {  // S[j % 3] = Q K_j^T
+      bool ok = warp_wait_cl(&bar->q_ready, 0, abort_flag, a.status);
+      for (int j = 0; ok && j < nvt; ++j) {
+        // S buffer j % 2 is free once both CTAs read out S of tile j-2.
+        if (j >= kSBufs && !warp_wait_cl(&bar->s_free[j % kSBufs], ((j - kSBufs) / kSBufs) & 1, abort_flag, a.status))
+          break;
+        if (!warp_wait_cl(&bar->kv_ready[j % kPStages], (j / kPStages) & 1, abort_flag, a.status)) break;
+        tc_fence_after();
         const uint64_t kd = k_desc0 + (uint64_t)(j % kPStages) * kStageStep;
         const uint32_t d = tmem + 128u * (uint32_t)(j % kSBufs);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint64_t oq = ((kk >> 2) * kQBlock + (kk & 3) * 32) >> 4;
-          const uint64_t ok = ((kk >> 2) * kKHalfBlock + (kk & 3) * 32) >> 4;
-          mma_ss_pair_elect(d, q_desc + oq, kd + ok, kIdescQK, kk > 0);
+          const uint64_t ok2 = ((kk >> 2) * kKHalfBlock + (kk & 3) * 32) >> 4;
+          mma_ss_pair_elect(d, q_desc + oq, kd + ok2, kIdescQK, kk > 0);
         }
         mma_commit_pair_elect(&bar->s_full[j % kSBufs], 0x3);
-      };
-      auto issue_pv = [&](int j) {  // O += P[j % 3] V_j
-        const uint64_t vd = v_desc0 + (uint64_t)(j % kPStages) * kStageStep;
-        const uint32_t p = tmem + 128u * (uint32_t)(j % kSBufs);
-#pragma unroll
-        for (int kk = 0; kk < 128 / 16; ++kk)
-          mma_ts_pair_elect(tmem + kColO, p + kk * 8, vd + ((kk * 2048) >> 4), kIdescPV,
-                            (j > 0 || kk > 0) ? 1u : 0u);
-        mma_commit_pair_elect(&bar->kv_empty[j % kPStages], 0x3);
-        mma_commit_pair_elect(&bar->o_done[j & 1], 0x3);
-      };
-      bool ok = wait(&bar->q_ready, 0);
-      for (int j = 0; ok && j < kSBufs && j < nvt; ++j) {
-        ok = wait(&bar->kv_ready[j % kPStages], (j / kPStages) & 1);
-        if (ok) {
-          tc_fence_after();
-          issue_qk(j);
-        }
       }
-      for (int i = 0; ok && i < nvt; ++i) {
-        if (!wait(&bar->p_ready[i % kSBufs], (i / kSBufs) & 1)) break;
-        tc_fence_after();
-        issue_pv(i);
-        const int j = i + kSBufs;
-        if (j < nvt) {
-          if (!wait(&bar->kv_ready[j % kPStages], (j / kPStages) & 1)) break;
-          tc_fence_after();
-          issue_qk(j);
-        }
-      }
-      // Every MMA issued (they write both CTAs' TMEM and read both CTAs' shared
-      // memory) completes before either CTA releases them; wait even after an abort.
-      mma_commit_pair_elect(&bar->o_final, 0x3);
+      // Every S MMA issued completes before shared memory or TMEM is released
+      // (wait even after an abort).
+      mma_commit_pair_elect(&bar->qk_final, 0x1);
       volatile int zero = 0;
-      mbar_wait(&bar->o_final, 0, &zero, a.status);
+      mbar_wait(&bar->qk_final, 0, &zero, a.status);
       __syncwarp();
+    } else if (lane == 0) {
+      // CTA 1: once the 4 softmax warps of the tile's warpgroup have read S out,
+      // tell CTA 0's S issuer with one remote arrive.  (S of tile i+2 goes into
+      // the buffer only after that arrive, so no phase is skipped.)
+      for (int i = 0; i + kSBufs < nvt; ++i) {
+        const int b = i % kSBufs;
+        if (!mbar_wait(&bar->s_local[b], (i / kSBufs) & 1, abort_flag, a.status)) break;
+        tc_fence_after();
+        tc_fence_before();
+        mbar_arrive_remote_light(mapa_shared(smem_u32(&bar->s_free[b]), 0));
+      }
     }
   } else if (warp == 2) {
     // ================================================================ forwarder
@@ -429,9 +427,36 @@ __global__ void __launch_bounds__(kPThreads, 1)
         reinterpret_cast<uint4*>(a.v_cache)[dof] = vv;
       }
     }
-    // CTA 1: once its 4 softmax warps of the tile's warpgroup have written P, tell CTA 0's
-    // issuer with one remote arrive.  (P of tile i+3 reuses the buffer only after
-    // P V of tile i, which waits for this arrive, so no phase is skipped.)
+    if (rank == 0) {
+      // ================================================================ P V issuer (CTA 0)
+      const uint64_t v_desc0 = make_sdesc_sw128(smem_u32(sStage + kVOff), kQBlock, 1024);
+      constexpr uint64_t kStageStep = kStageBytes >> 4;
+      for (int i = 0; i < nvt; ++i) {
+        if (!warp_wait_cl(&bar->p_ready[i % kSBufs], (i / kSBufs) & 1, abort_flag, a.status)) break;
+        // The tile's V halves landed before its S was computed (same stage).
+        tc_fence_after();
+        const uint64_t vd = v_desc0 + (uint64_t)(i % kPStages) * kStageStep;
+        const uint32_t p = tmem + kColP + 64u * (uint32_t)(i % kSBufs);
+#pragma unroll
+        for (int kk = 0; kk < 128 / 16; ++kk)
+          mma_ts_pair_elect(tmem + kColO, p + kk * 8, vd + ((kk * 2048) >> 4), kIdescPV,
+                            (i > 0 || kk > 0) ? 1u : 0u);
+        // The stage's K (read by S of this tile, complete before its P existed)
+        // and V are free; P V of this tile is done.
+        mma_commit_pair_elect(&bar->kv_empty[i % kPStages], 0x3);
+        mma_commit_pair_elect(&bar->o_done[i % kORing], 0x3);
+      }
+      // Every P V issued (they write both CTAs' TMEM and read both CTAs' shared
+      // memory) completes before either CTA releases them; wait even after an abort.
+      mma_commit_pair_elect(&bar->o_final, 0x3);
+      volatile int zero = 0;
+      mbar_wait(&bar->o_final, 0, &zero, a.status);
+      __syncwarp();
+    }
+    // CTA 1: once the 4 softmax warps of the tile's warpgroup have written P,
+    // tell CTA 0's P V issuer with one remote arrive.  (P of tile i+2 reuses the
+    // buffer only after P V of tile i, which waits for this arrive, so no phase
+    // is skipped.)
     if (rank == 1 && lane == 0) {
       for (int i = 0; i < nvt; ++i) {
         const int b = i % kSBufs;
@@ -461,9 +486,11 @@ __global__ void __launch_bounds__(kPThreads, 1)
     // 1 -> 0 ids 5-8.  Each is a producer arrive / consumer sync pair made in
     // every iteration whatever happens, so no warp can be left waiting.
     const int id_send = 1 + quarter + 4 * wg, id_recv = 1 + quarter + 4 * (wg ^ 1);
-    // P-ready: CTA 0's softmax warps arrive on the issuer's p_ready directly,
-    // CTA 1's on p_local, which warp 3 forwards to CTA 0 with one remote arrive.
+    // P-ready and S-free: CTA 0's softmax warps arrive on the issuers' barriers
+    // directly, CTA 1's on local ones that warps 3 and 1 forward to CTA 0 with one
+    // remote arrive each.
     uint64_t* p_bar = rank == 0 ? bar->p_ready : bar->p_local;
+    uint64_t* s_bar = rank == 0 ? bar->s_free : bar->s_local;  // the same for "S read out"
     float m_used = -INFINITY;  // max (log2 domain) this warpgroup last exponentiated against
     float l_part = 0.f;        // this warpgroup's share of the row sum, relative to m_used
     bool good = true;
@@ -480,6 +507,10 @@ __global__ void __launch_bounds__(kPThreads, 1)
         tmem_ld32(s_col + 64, &sv[64]);
         tmem_ld32(s_col + 96, &sv[96]);
         tmem_wait_ld();
+        // S buffer b may take the scores of tile i+2.
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&s_bar[b]);
       }
       int tile, lo, hi;
       bool is_new;
@@ -536,15 +567,14 @@ __global__ void __launch_bounds__(kPThreads, 1)
       m_used = m_i;
       if (i > 0 && __any_sync(0xffffffffu, grow && m_prev != -INFINITY)) {
         // Rows whose max grew rescale O (P V of tiles < i, relative to m_prev)
-        // once P V of tile i-1 has completed (the tensor core runs them in issue
-        // order).  o_done[(i-1) % 2] counts the P V of tiles of that parity: P V
-        // of tile i-3 completed before S of tile i (issued after it) and P V of
-        // tile i+1 cannot start before P V of tile i, which waits for this P, so
-        // the barrier has completed (i-1)/2 or (i-1)/2 + 1 phases here and the
-        // parity of phase (i-1)/2 tells which.  sv[64..95] (S values already
-        // used) stage O.
+        // once P V of tile i-1 has completed (P V runs in issue order).  Slot
+        // (i-1) % 8 of the o_done ring last held P V of tile i-9, completed
+        // before P V of tile i-4, which this warpgroup saw complete at its
+        // previous tile; P V of tile i+7 is far from issued.  So the parity of
+        // phase (i-1) / 8 tells whether P V of tile i-1 is done.  sv[64..95] (S
+        // values already used) stage O.
         const float alpha = (grow && m_prev != -INFINITY) ? ex2_approx(m_prev - m_i) : 1.f;
-        if (!warp_wait(&bar->o_done[(i - 1) & 1], ((i - 1) >> 1) & 1, abort_flag, a.status)) good = false;
+        if (!warp_wait(&bar->o_done[(i - 1) % kORing], ((i - 1) / kORing) & 1, abort_flag, a.status)) good = false;
         tc_fence_after();
         if (good) {
 #pragma unroll
@@ -559,9 +589,18 @@ __global__ void __launch_bounds__(kPThreads, 1)
           }
         }
       }
+      if (good && i >= kSBufs) {
+        // P buffer b is free once P V of tile i-2 has completed.  Slot
+        // (i-2) % 8 of the o_done ring last held P V of tile i-10, completed
+        // before P V of tile i-4, which this warpgroup saw complete at its
+        // previous tile (every warpgroup waits here at each of its tiles).
+        if (!warp_wait(&bar->o_done[(i - 2) % kORing], ((i - 2) / kORing) & 1, abort_flag, a.status)) good = false;
+        tc_fence_after();
+      }
       if (good) {
-        tmem_st32(s_col, &sv[0]);
-        tmem_st32(s_col + 32, &sv[32]);
+        const uint32_t p_col = tmem + lane_off + kColP + 64u * (uint32_t)b;
+        tmem_st32(p_col, &sv[0]);
+        tmem_st32(p_col + 32, &sv[32]);
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
