@@ -29,18 +29,17 @@
 // extra tiles only hold keys that real rows do not see).
 //
 // Warp roles (384 threads, three warpgroups):
-//   warp 0      TMA producer: this CTA's Q tile, then per KV tile its K half and
-//               V half into a 5-stage ring.
+//   warp 0      TMA producer: this CTA's Q tile (issued right after the
+//               dependency wait), then per KV tile its K half and V half into a
+//               5-stage ring.
 //   warp 1      TMEM allocation (both CTAs); in CTA 0 the issuer of S = Q K^T
-//               (the whole warp, one elected lane issuing), in CTA 1 the
-//               forwarder of "S read out" to CTA 0.
+//               (the whole warp, one elected lane issuing).
 //   warp 2      forwarder: when a stage lands in this CTA it zeroes V rows that
 //               hold no key of the tile's source (so 0 * stale data never reaches
 //               O) and tells CTA 0's issuer (local or remote mbarrier arrive).
 //   warp 3      fused append: copies this Q tile's tokens' K/V rows of the
-//               KV head into the cache with 16-byte loads and stores; then the
-//               issuer of O += P V in CTA 0, the forwarder of "P written" to
-//               CTA 0 in CTA 1.
+//               KV head into the cache with 16-byte loads and stores; then, in
+//               CTA 0, the issuer of O += P V.
 //   warps 4-11  softmax: warps 4-7 take the even tiles, warps 8-11 the odd ones;
 //               thread (warp, lane) owns row 32*(warp%4) + lane and all 128 keys
 //               of its tiles.  The running max of a row is handed from one
@@ -93,16 +92,15 @@ struct __align__(16) PairBarriers {
   uint64_t q_ready;              // CTA 0: both Q tiles landed (2 forwarders)
   uint64_t kv_ready[kPStages];   // CTA 0: both CTAs' halves of the stage are ready (2 forwarders)
   uint64_t s_full[kSBufs];       // S buffer b holds its tile's scores (multicast)
-  uint64_t s_free[kSBufs];       // CTA 0: S buffer b read out in both CTAs (4 local warps + CTA 1's forward)
-  uint64_t s_local[kSBufs];      // CTA 1: S buffer b read out by the 4 warps of the tile's warpgroup
-  uint64_t p_ready[kSBufs];      // CTA 0: P buffer b written in both CTAs (4 local warps + CTA 1's forward)
-  uint64_t p_local[kSBufs];      // CTA 1: P buffer b written by the 4 warps of the tile's warpgroup
+  uint64_t s_free[kSBufs];       // CTA 0: S buffer b read out in both CTAs (the tile's 4 warps in each)
+  uint64_t p_ready[kSBufs];      // CTA 0: P buffer b written in both CTAs (the tile's 4 warps in each)
   uint64_t o_done[kORing];       // P V of tile t completed, in slot t % kORing (multicast)
   uint64_t qk_final;             // CTA 0: every S MMA issued has completed
   uint64_t o_final;              // every MMA issued has completed (multicast, once)
   uint32_t tmem_base;
   int abort;
   int s, t0, rows, past, have;   // this cluster's pair, read once after the dependency wait
+  int q_issued;                  // the Q tile's load was issued
   float xmax[2][2][128];         // [warpgroup][0: running max handed on, 1: last max used][row]
   float xsum[2][128];            // [warpgroup][row] share of the row sum, exchanged at the end
 };
@@ -165,11 +163,39 @@ struct TilePlan {
   }
 };
 
+// The same with the light remote arrive (the data the waiter needs travels
+// through the tensor core, ordered by tcgen05 fences around the arrive).
+__device__ __forceinline__ void arrive_leader_light(uint64_t* bar, int rank) {
+  if (rank == 0)
+    mbar_arrive(bar);
+  else
+    mbar_arrive_remote_light(mapa_shared(smem_u32(bar), 0));
+}
+
 __device__ __forceinline__ void arrive_leader(uint64_t* bar, int rank) {
   if (rank == 0)
     mbar_arrive(bar);
   else
     mbar_arrive_remote(mapa_shared(smem_u32(bar), 0));
+}
+
+// The last CTA of the grid to take a ticket -- every CTA takes one after it
+// has read its sequence's length -- adds commit_add to every length and resets
+// the counter for the next launch.  A counter found above the grid size was not
+// zero before the launch: reported as CP_DEV_BOUNDS, nothing is advanced.
+__device__ __forceinline__ void take_ticket(const PairArgs& a) {
+  if (!a.commit_lens) return;
+  __threadfence();
+  const unsigned total = gridDim.x * gridDim.y;
+  const unsigned t = atomicAdd(a.ticket, 1u);
+  if (t == total - 1) {
+    __threadfence();
+    for (int q = 0; q < a.rows.num_seqs; ++q) a.commit_lens[q] += a.commit_add;
+    __threadfence();
+    atomicExch(a.ticket, 0u);
+  } else if (t >= total && a.status) {
+    atomicOr(a.status, CP_DEV_BOUNDS);
+  }
 }
 
 template <typename T>
@@ -207,10 +233,8 @@ __global__ void __launch_bounds__(kPThreads, 1)
     }
     for (int b = 0; b < kSBufs; ++b) {
       mbar_init(&bar->s_full[b], 1);
-      mbar_init(&bar->s_free[b], 5);
-      mbar_init(&bar->s_local[b], 4);
-      mbar_init(&bar->p_ready[b], 5);
-      mbar_init(&bar->p_local[b], 4);
+      mbar_init(&bar->s_free[b], 8);
+      mbar_init(&bar->p_ready[b], 8);
     }
     for (int t = 0; t < kORing; ++t) mbar_init(&bar->o_done[t], 1);
     mbar_init(&bar->qk_final, 1);
@@ -248,6 +272,12 @@ __global__ void __launch_bounds__(kPThreads, 1)
     const int pair = np - 1 - w / a.rows.num_seqs;
     const int s = w % a.rows.num_seqs;
     int have = pair >= 0 ? 1 : 0, past = 0;
+    if (have && lane == 0) {
+      // This CTA's Q tile does not depend on the lengths: start loading it now.
+      mbar_arrive_expect_tx(&bar->q_full, 2 * kQBlock);
+      for (int db = 0; db < 2; ++db)
+        tma_load_3d(sQ + db * kQBlock, &tm_q, &bar->q_full, db * 64, g * G, s * R + pair * ppt + rank * rpt);
+    }
     if (have) {
       past = a.past[s];
       if (past < 0 || past + R > a.max_ctx) {
@@ -261,26 +291,18 @@ __global__ void __launch_bounds__(kPThreads, 1)
       bar->rows = R;
       bar->past = past;
       bar->have = have;
+      bar->q_issued = pair >= 0 ? 1 : 0;
     }
   }
   __syncthreads();
-  // Every CTA has read its length; the last one to get here advances them all.
-  if (threadIdx.x == 0 && a.commit_lens) {
-    __threadfence();
-    const unsigned total = gridDim.x * gridDim.y;
-    const unsigned t = atomicAdd(a.ticket, 1u);
-    if (t == total - 1) {
-      __threadfence();
-      for (int q = 0; q < a.rows.num_seqs; ++q) a.commit_lens[q] += a.commit_add;
-      __threadfence();
-      atomicExch(a.ticket, 0u);
-    } else if (t >= total && a.status) {
-      atomicOr(a.status, CP_DEV_BOUNDS);  // the counter was not zero before the launch
-    }
-  }
   cluster_wait();  // the peer's barriers are initialised
   const int s = bar->s, t0 = bar->t0, rows = bar->rows, past = bar->past;
   if (!bar->have) {
+    if (threadIdx.x == 0) {
+      take_ticket(a);
+      volatile int zero = 0;  // a Q load in flight lands before shared memory is released
+      if (bar->q_issued) mbar_wait(&bar->q_full, 0, &zero, nullptr);
+    }
     tc_fence_before();
     cluster_sync_all();
     if (warp == 1) {
@@ -302,10 +324,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
   if (warp == 0) {
     // ================================================================ producer
     if (lane == 0) {
-      mbar_arrive_expect_tx(&bar->q_full, 2 * kQBlock);
-      for (int db = 0; db < 2; ++db)
-        tma_load_3d(sQ + db * kQBlock, &tm_q, &bar->q_full, db * 64, g * G, row0 + t0 + rank * rpt);
-      const int plane = s * a.hkv + g;
+      const int plane = s * a.hkv + g;  // (the Q tile was issued right after the dependency wait)
       int issued = -1;
       for (int j = 0; j < nvt; ++j) {
         const int st = j % kPStages;
@@ -369,20 +388,13 @@ __global__ void __launch_bounds__(kPThreads, 1)
       volatile int zero = 0;
       mbar_wait(&bar->qk_final, 0, &zero, a.status);
       __syncwarp();
-    } else if (lane == 0) {
-      // CTA 1: once the 4 softmax warps of the tile's warpgroup have read S out,
-      // tell CTA 0's S issuer with one remote arrive.  (S of tile i+2 goes into
-      // the buffer only after that arrive, so no phase is skipped.)
-      for (int i = 0; i + kSBufs < nvt; ++i) {
-        const int b = i % kSBufs;
-        if (!mbar_wait(&bar->s_local[b], (i / kSBufs) & 1, abort_flag, a.status)) break;
-        tc_fence_after();
-        tc_fence_before();
-        mbar_arrive_remote_light(mapa_shared(smem_u32(&bar->s_free[b]), 0));
-      }
     }
   } else if (warp == 2) {
     // ================================================================ forwarder
+    // Every CTA has read its length (before the __syncthreads above); the last
+    // one to take a ticket advances them all.  The atomic's latency overlaps the
+    // wait for the Q tile.
+    if (lane == 0) take_ticket(a);
     bool ok = warp_wait(&bar->q_full, 0, abort_flag, a.status);
     if (ok && lane == 0) arrive_leader(&bar->q_ready, rank);
     uint8_t* vbase = sStage + kVOff;
@@ -453,19 +465,6 @@ __global__ void __launch_bounds__(kPThreads, 1)
       mbar_wait(&bar->o_final, 0, &zero, a.status);
       __syncwarp();
     }
-    // CTA 1: once the 4 softmax warps of the tile's warpgroup have written P,
-    // tell CTA 0's P V issuer with one remote arrive.  (P of tile i+2 reuses the
-    // buffer only after P V of tile i, which waits for this arrive, so no phase
-    // is skipped.)
-    if (rank == 1 && lane == 0) {
-      for (int i = 0; i < nvt; ++i) {
-        const int b = i % kSBufs;
-        if (!mbar_wait(&bar->p_local[b], (i / kSBufs) & 1, abort_flag, a.status)) break;
-        tc_fence_after();
-        tc_fence_before();
-        mbar_arrive_remote_light(mapa_shared(smem_u32(&bar->p_ready[b]), 0));
-      }
-    }
   }
   } else {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kPRegsSoftmax));
@@ -486,11 +485,8 @@ __global__ void __launch_bounds__(kPThreads, 1)
     // 1 -> 0 ids 5-8.  Each is a producer arrive / consumer sync pair made in
     // every iteration whatever happens, so no warp can be left waiting.
     const int id_send = 1 + quarter + 4 * wg, id_recv = 1 + quarter + 4 * (wg ^ 1);
-    // P-ready and S-free: CTA 0's softmax warps arrive on the issuers' barriers
-    // directly, CTA 1's on local ones that warps 3 and 1 forward to CTA 0 with one
-    // remote arrive each.
-    uint64_t* p_bar = rank == 0 ? bar->p_ready : bar->p_local;
-    uint64_t* s_bar = rank == 0 ? bar->s_free : bar->s_local;  // the same for "S read out"
+    // P-ready and S-free: every softmax warp arrives on CTA 0's barriers itself
+    // (CTA 1's warps with a remote arrive).
     float m_used = -INFINITY;  // max (log2 domain) this warpgroup last exponentiated against
     float l_part = 0.f;        // this warpgroup's share of the row sum, relative to m_used
     bool good = true;
@@ -510,7 +506,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
         // S buffer b may take the scores of tile i+2.
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&s_bar[b]);
+        if (lane == 0) arrive_leader_light(&bar->s_free[b], rank);
       }
       int tile, lo, hi;
       bool is_new;
@@ -604,7 +600,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&p_bar[b]);
+        if (lane == 0) arrive_leader_light(&bar->p_ready[b], rank);
       }
     }
 

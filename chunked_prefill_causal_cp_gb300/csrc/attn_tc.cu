@@ -386,11 +386,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 1) {
     // ================================================================ MMA issuer
-    // Lane 0 alone polls and issues; a tcgen05.mma holds its thread for most
-    // of its own execution time, so the loop keeps work between MMAs minimal:
-    // per KV tile four waits (P0, V, K of the next tile, P1) and three commits.
-    if (lane == 0) {
-      auto wait = [&](uint64_t* b, uint32_t parity) { return mbar_wait(b, parity, abort_flag, a.status); };
+    // The whole warp runs the loop, converged; one elected lane issues each
+    // tcgen05 instruction (operands stay warp-uniform, so MMAs issue back to
+    // back).  Per KV tile four waits (P0, V, K of the next tile, P1) and three
+    // commits.
+    {
+      auto wait = [&](uint64_t* b, uint32_t parity) { return warp_wait(b, parity, abort_flag, a.status); };
       constexpr uint64_t kTileStep = (DB * kBlockBytes) >> 4;
       const uint64_t q_desc0 = make_sdesc_sw128(smem_u32(sQ), 16, 1024);
       const uint64_t k_desc0 = make_sdesc_sw128(smem_u32(sK), 16, 1024);
@@ -401,16 +402,16 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint64_t off = ((kk >> 2) * kBlockBytes + (kk & 3) * 32) >> 4;
-          mma_ss(tmem + 256u * w, q_desc + off, k_desc + off, kIdescQK, kk > 0);
+          mma_ss_elect(tmem + 256u * w, q_desc + off, k_desc + off, kIdescQK, kk > 0);
         }
-        mma_commit(&bar->s_full[w]);
+        mma_commit_elect(&bar->s_full[w]);
       };
       auto issue_pv = [&](int w, int i) {  // O_w += P_w V_i
         const uint64_t v_desc = v_desc0 + (i & 1) * kTileStep;
 #pragma unroll
         for (int kk = 0; kk < kTcBlockN / 16; ++kk)
-          mma_ts(tmem + 256u * w + 128u, tmem + 256u * w + kk * 8, v_desc + ((kk * 2048) >> 4), kIdescPV,
-                 (i > 0 || kk > 0) ? 1u : 0u);
+          mma_ts_elect(tmem + 256u * w + 128u, tmem + 256u * w + kk * 8, v_desc + ((kk * 2048) >> 4), kIdescPV,
+                       (i > 0 || kk > 0) ? 1u : 0u);
       };
       bool ok = nmine > 0 && wait(&bar->q_full[0], 0) && wait(&bar->k_full[0], 0);
       if (ok) {
@@ -432,12 +433,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int tail = n_valid - (ntiles - 1) * kTcBlockN;
           if (tail < kTcBlockN) {
             uint8_t* v_stage = sV + (i & 1) * DB * kBlockBytes;
+            const int nvec = (kTcBlockN - tail) * 128 / 16;
             for (int db = 0; db < DB; ++db) {
               uint4* p = reinterpret_cast<uint4*>(v_stage + db * kBlockBytes + tail * 128);
-              const int nvec = (kTcBlockN - tail) * 128 / 16;
-              for (int e = 0; e < nvec; ++e) p[e] = make_uint4(0, 0, 0, 0);
+              for (int e = lane; e < nvec; e += 32) p[e] = make_uint4(0, 0, 0, 0);
             }
             fence_proxy_async_smem();
+            __syncwarp();
           }
         }
         tc_fence_after();
@@ -451,11 +453,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_fence_after();
           issue_pv(1, i);
         }
-        mma_commit(&bar->kv_empty[i & 1]);
+        mma_commit_elect(&bar->kv_empty[i & 1]);
         if (more && q1) issue_qk(1, i + 1);
       }
       // o_final: every MMA issued has completed (epilogue and TMEM release wait on it).
-      mma_commit(&bar->o_final);
+      mma_commit_elect(&bar->o_final);
       volatile int zero = 0;  // wait even after an abort: MMAs may still be in flight
       mbar_wait(&bar->o_final, 0, &zero, a.status);
     }
