@@ -19,6 +19,15 @@
 // boundaries and the parity split depend only on absolute positions, so a
 // padded and an unpadded run of the same rows do identical arithmetic; tiles
 // past the pair's last query position are never loaded (causal tile skip).
+// On a contiguous cache the tile that straddles `past` is walked twice, once
+// for its cached keys and once for the chunk's own (see Walk), so that the
+// fused append below and a separate append do the same arithmetic.
+//
+// Fused append (contiguous caches): the walks over the chunk's own keys read
+// them straight from k_new / v_new, warp 2 copies the K/V rows of its Q tile's
+// tokens into their cache slots ([Wiki] 一.1), and the last CTA to take a
+// ticket advances seqlens_k by the real rows ([Wiki] 四) -- append, attention
+// and commit in one launch.
 //
 // Warp roles (384 threads per CTA, three warpgroups):
 //   warp 0      TMA producer: both Q tiles once, then this CTA's K and V tiles
@@ -29,8 +38,9 @@
 //   warp 1      TMEM allocator and MMA issuer (one elected lane).  Per KV tile:
 //               S0 = Q0 K^T, S1 = Q1 K^T (A, B K-major in shared memory);
 //               O0 += P0 V, O1 += P1 V (A = P in TMEM, B = V MN-major).
-//   warps 2-3   idle after set-up (they fill the control warpgroup, whose
-//               registers go to the softmax warpgroups).
+//   warp 2      fused append: copies this CTA's Q tile's K/V rows into the cache.
+//   warp 3      takes the CTA's ticket (fused append); both fill the control
+//               warpgroup, whose registers go to the softmax warpgroups.
 //   warps 4-7   softmax group 0 (Q tile 0);  warps 8-11 softmax group 1 (Q tile 1).
 // TMEM (512 columns): group w uses [256w, 256w+128) for S/P, [256w+128, +D) for O.
 // Thread m of a group owns row m (TMEM lane m): it reads its S row, masks by
@@ -182,6 +192,67 @@ __device__ __forceinline__ bool find_pair(const AttnArgs& a, int ppt, int w, int
   return false;
 }
 
+// The KV tiles a pair walks.  Tile t holds key indices [128t, 128t + 128).  On
+// a contiguous cache the tiles below `past` hold cached keys and those at or
+// above it the call's own rows; a tile that straddles `past` is walked twice
+// (its cached keys, then its new ones), whether or not the append is fused, so
+// the fused and the separate-call paths do the same arithmetic.  Other layouts
+// walk each tile once.  Virtual tile j goes to CTA rank j % 2.
+struct Walk {
+  bool split;
+  int past, n_valid, tp, count;
+  bool straddle;
+  __device__ __forceinline__ Walk(bool contig, int past_, int n_valid_, int ntiles) {
+    split = contig;
+    past = past_;
+    n_valid = n_valid_;
+    tp = past_ / kTcBlockN;
+    straddle = contig && (past_ % kTcBlockN) != 0;
+    count = ntiles + (straddle ? 1 : 0);
+  }
+  __device__ __forceinline__ void at(int j, int& tile, bool& is_new) const {
+    if (!split || j < tp) {
+      tile = j;
+      is_new = false;
+    } else if (straddle) {
+      tile = j == tp ? tp : j - 1;
+      is_new = j != tp;
+    } else {
+      tile = j;
+      is_new = true;
+    }
+  }
+  // Key indices [lo, hi) of the tile that belong to this walk.
+  __device__ __forceinline__ void range(int tile, bool is_new, int& lo, int& hi) const {
+    const int j0 = tile * kTcBlockN;
+    if (!split) {
+      lo = j0;
+      hi = min(j0 + kTcBlockN, n_valid);
+    } else {
+      lo = is_new ? max(j0, past) : j0;
+      hi = is_new ? min(j0 + kTcBlockN, n_valid) : min(j0 + kTcBlockN, past);
+    }
+  }
+};
+
+// The last CTA of the grid to take a ticket -- every CTA takes one after all its
+// threads have read their sequence's length -- adds commit_add to every length
+// and resets the counter for the next launch.  A counter found above the grid
+// size was not zero before the launch: reported as CP_DEV_BOUNDS.
+__device__ __forceinline__ void take_ticket(const AttnArgs& a) {
+  __threadfence();
+  const unsigned total = gridDim.x * gridDim.y;
+  const unsigned t = atomicAdd(a.ticket, 1u);
+  if (t == total - 1) {
+    __threadfence();
+    for (int q = 0; q < a.rows.num_seqs; ++q) a.commit_lens[q] += a.commit_add;
+    __threadfence();
+    atomicExch(a.ticket, 0u);
+  } else if (t >= total && a.status) {
+    atomicOr(a.status, CP_DEV_BOUNDS);
+  }
+}
+
 template <typename T, int D>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -229,7 +300,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_prefetch_desc(&tm_k);
     tma_prefetch_desc(&tm_v);
     tma_prefetch_desc(&tm_o);
-    if (a.kv_direct) {
+    if (a.kv_direct || a.fused) {
       tma_prefetch_desc(&tm_kn);
       tma_prefetch_desc(&tm_vn);
     }
@@ -245,7 +316,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = bar->tmem_base;
   volatile int* abort_flag = &bar->abort;
   pdl_wait();  // everything below reads what earlier kernels wrote
-  if (a.commit_lens && blockIdx.x == 0 && blockIdx.y == 0)
+  if (a.commit_lens && !a.ticket && blockIdx.x == 0 && blockIdx.y == 0)
     for (int q = threadIdx.x; q < a.rows.num_seqs; q += kThreads) a.commit_lens[q] += a.commit_add;
 
   // ---- this cluster's pair (the same for both CTAs, so both leave together)
@@ -259,7 +330,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       have_pair = false;
     }
   }
+  if (a.ticket) __syncthreads();  // every thread has read its length before this CTA takes a ticket
   if (!have_pair) {
+    if (a.ticket && threadIdx.x == 0) take_ticket(a);
     cluster_wait();
     tc_fence_before();
     __syncthreads();
@@ -280,7 +353,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int nkeys = rolling ? min(n, cap) : past + t_end;
   const int n_valid = rolling ? nkeys : n;  // key indices holding written data
   const int ntiles = (nkeys + kTcBlockN - 1) / kTcBlockN;
-  const int nmine = ntiles > rank ? (ntiles - rank + 1) / 2 : 0;  // this CTA's KV tiles: rank + 2i
+  const Walk walk(!rolling && !paged, past, n_valid, ntiles);
+  const int nmine = walk.count > rank ? (walk.count - rank + 1) / 2 : 0;  // this CTA's walks: rank + 2i
   const bool q1 = t0 + rpt < rows;  // Q tile 1 holds at least one row (else it is skipped)
   const bool own_tile = rank == 0 || q1;   // Q tile `rank` (finished here) has rows
   const bool peer_tile = rank == 1 || q1;  // Q tile `1 - rank` (finished by the peer) has rows
@@ -311,7 +385,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = 0; i < nmine; ++i) {
       const int st = i & 1;
       const uint32_t ph = (i >> 1) & 1;
-      const int j0 = (rank + 2 * i) * kTcBlockN;
+      int tile;
+      bool is_new;
+      walk.at(rank + 2 * i, tile, is_new);
+      const int j0 = tile * kTcBlockN;
+      const bool from_new = a.fused && is_new;  // the call's own rows, read from k_new / v_new
       // A paged tile made only of this call's rows is read from k_new / v_new:
       // two 16 KB boxes per tensor instead of one small box per page.
       const bool direct = paged && a.kv_direct && j0 >= past;
@@ -335,7 +413,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint64_t* vf = &bar->v_full[st];
       uint8_t* dk = sK + st * DB * kBlockBytes;
       uint8_t* dv = sV + st * DB * kBlockBytes;
-      if (!paged || direct) {
+      if (from_new) {
+        // Fused append: keys [j0, j0 + 128) are rows j0 - past ... of this
+        // sequence's k_new / v_new (4-D maps: rows outside [0, rows) read as zero).
+        if (lane == 0) {
+          mbar_arrive_expect_tx(kf, DB * kBlockBytes);
+          for (int db = 0; db < DB; ++db) tma_load_4d(dk + db * kBlockBytes, &tm_kn, kf, db * 64, g, j0 - past, s);
+          if (i == 0 && q1) load_q(1);
+          mbar_arrive_expect_tx(vf, DB * kBlockBytes);
+          for (int db = 0; db < DB; ++db) tma_load_4d(dv + db * kBlockBytes, &tm_vn, vf, db * 64, g, j0 - past, s);
+        }
+      } else if (!paged || direct) {
         // Contiguous: keys [j0, j0 + 128) of KV head g.  Direct: they are rows
         // row0 + (j0 - past) ... of k_new / v_new (rows past this sequence's
         // are masked, and zeroed in the last V tile).
@@ -429,8 +517,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool more = i + 1 < nmine;
         if (!wait(&bar->p_ready[0], i & 1)) break;
         if (!wait(&bar->v_full[i & 1], (i >> 1) & 1)) break;
-        if (rank + 2 * i == ntiles - 1) {  // last KV tile: zero V rows past the written keys
-          const int tail = n_valid - (ntiles - 1) * kTcBlockN;
+        int ztile;
+        bool znew;
+        walk.at(rank + 2 * i, ztile, znew);
+        if (!(a.fused && znew)) {  // read from the cache: zero V rows that hold no key of this walk
+          int zlo, zhi;
+          walk.range(ztile, znew, zlo, zhi);
+          const int tail = max(zhi - ztile * kTcBlockN, 0);
           if (tail < kTcBlockN) {
             uint8_t* v_stage = sV + (i & 1) * DB * kBlockBytes;
             const int nvec = (kTcBlockN - tail) * 128 / 16;
@@ -462,6 +555,32 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_wait(&bar->o_final, 0, &zero, a.status);
     }
     __syncwarp();
+  } else if (warp == 2) {
+    // ================================================================ fused append
+    // The K/V rows of Q tile `rank`'s tokens for KV head g go to their slots
+    // past + t of the cache ([Wiki] 一.1); every (token, KV head) row of the
+    // chunk belongs to exactly one Q tile.  No tile of this launch reads them
+    // from the cache: the walks that hold them read k_new / v_new.
+    if (a.fused) {
+      const int tk0 = t0 + rank * rpt, tk1 = min(tk0 + rpt, rows);
+      const int nrow = max(tk1 - tk0, 0);
+      constexpr int kVec = D * 2 / 16;  // 16-byte vectors per row
+      const long long src_row = (long long)row0 + tk0;
+      const long long dst_row = ((long long)(s * a.hkv + g)) * cap + past + tk0;
+      for (int e = lane; e < nrow * kVec; e += 32) {
+        const int r = e / kVec, c = e % kVec;
+        const long long so = ((src_row + r) * a.hkv + g) * kVec + c;
+        const long long dof = (dst_row + r) * kVec + c;
+        const uint4 kv = reinterpret_cast<const uint4*>(a.k_new)[so];
+        const uint4 vv = reinterpret_cast<const uint4*>(a.v_new)[so];
+        reinterpret_cast<uint4*>(a.k_cache)[dof] = kv;
+        reinterpret_cast<uint4*>(a.v_cache)[dof] = vv;
+      }
+    }
+  } else if (warp == 3) {
+    // Every thread of this CTA has read its length (the __syncthreads after the
+    // lookup); the last CTA to take a ticket advances them all.
+    if (a.ticket && lane == 0) take_ticket(a);
   }
   cluster_wait();  // the peer's barriers are initialised
   if (warp == 1 && lane == 0 && own_tile) {
@@ -499,19 +618,27 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_ld32(s_col + 64, &sv[64]);
       tmem_ld32(s_col + 96, &sv[96]);
       tmem_wait_ld();
-      const int j0 = (rank + 2 * i) * kTcBlockN;
+      int tile;
+      bool is_new;
+      walk.at(rank + 2 * i, tile, is_new);
+      const int j0 = tile * kTcBlockN;
       float mx = -INFINITY;
-      if (!(!rolling && j0 + kTcBlockN - 1 <= p_row)) {  // not fully visible: mask first
+      if (!rolling) {
+        // Visible columns [c_lo, c_hi): keys of this walk at or before the row.
+        int klo, khi;
+        walk.range(tile, is_new, klo, khi);
+        const int c_lo = klo - j0, c_hi = min(khi, p_row + 1) - j0;
+        if (c_lo > 0 || c_hi < kTcBlockN) {
+#pragma unroll
+          for (int c = 0; c < 128; ++c)
+            if (c < c_lo || c >= c_hi) sv[c] = __float_as_uint(-INFINITY);
+        }
+      } else {
 #pragma unroll
         for (int c = 0; c < 128; ++c) {
           const int key = j0 + c;
-          bool vis;
-          if (!rolling) {
-            vis = key <= p_row;
-          } else {
-            const int pos = key + base_hi - (key > r_slot ? cap : 0);
-            vis = key < nkeys && pos >= lo && pos <= p_row;
-          }
+          const int pos = key + base_hi - (key > r_slot ? cap : 0);
+          const bool vis = key < nkeys && pos >= lo && pos <= p_row;
           if (!vis) sv[c] = __float_as_uint(-INFINITY);
         }
       }
@@ -742,7 +869,8 @@ bool attn_tc_supported(int d, int group, int dtype) {
 
 // pairs_bound: number of 2*128-row Q-tile pairs to cover (one 2-CTA cluster each).
 // to: the output [rows, Hq, D] with the same box as tq (finished tiles are TMA-stored).
-// tkn, tvn: this call's new K/V rows [rows, Hkv, D], box {64, 1, 128} (used when a.kv_direct).
+// tkn, tvn: this call's new K/V rows: [rows, Hkv, D] with box {64, 1, 128} when a.kv_direct
+// (paged), [num_seqs, rows_uniform, Hkv, D] with box {64, 1, 128, 1} when a.fused (contiguous).
 cudaError_t launch_attn_tc(const AttnArgs& a, int dtype, const CUtensorMap& tq, const CUtensorMap& tk,
                            const CUtensorMap& tv, const CUtensorMap& to, const CUtensorMap& tkn,
                            const CUtensorMap& tvn, int pairs_bound, cudaStream_t st) {

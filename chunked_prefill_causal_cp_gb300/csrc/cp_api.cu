@@ -68,7 +68,7 @@ float scale_log2(const cp_layer_desc* d) {
 
 int64_t max_splits_for(int32_t max_ctx) { return ((int64_t)max_ctx + kDecodeSplit - 1) / kDecodeSplit; }
 
-// Workspace of cp_prefill_chunk: a 256-byte control block (the paired-SM
+// Workspace of cp_prefill_chunk: a 256-byte control block (the fused
 // kernel's ticket counter, zero between calls), then a copy of seqlens_k in
 // whole 256-byte blocks, then the split partials.  The other calls use the
 // partials only, from the start of the workspace.
@@ -207,59 +207,39 @@ int run_attention(const cp_layer_desc* d, const AttnArgs& base, int64_t rows_tot
   return CP_OK;
 }
 
-// The paired-SM kernel takes contiguous-cache chunks of head_dim 128 with more
-// than one row per sequence.
-bool use_pair(const cp_layer_desc* d, int32_t rows_padded) {
+// A contiguous-cache chunk of uniform rows (more than one) in half precision
+// goes to the tensor-core kernel with the append fused in.
+bool use_fused(const cp_layer_desc* d, int32_t rows_padded) {
   const int G = d->num_q_heads / d->num_kv_heads;
-  return d->kind == CP_CACHE_CONTIG && rows_padded > 1 && attn_pair_supported(d->head_dim, G, d->dtype);
+  return d->kind == CP_CACHE_CONTIG && rows_padded > 1 && d->dtype != CP_F32 &&
+         attn_tc_supported(d->head_dim, G, d->dtype);
 }
 
-// Attention of B uniform chunks on the paired-SM kernel.  k_new/v_new non-null:
-// fused append (the chunk's tiles come from them and the kernel writes them into
-// the cache); ticket/commit_lens non-null: the kernel advances the lengths.
-int run_pair(const cp_layer_desc* d, const void* q, const void* k_cache, const void* v_cache, int32_t* seqlens_k,
-             int32_t rows_padded, int32_t max_past, void* out, const void* k_new, const void* v_new,
-             unsigned* ticket, int32_t* commit_lens, int32_t commit_add, int32_t* dev_status, cudaStream_t st) {
+// One launch for append, attention and the advance of the lengths: the tiles
+// that hold the chunk's keys are read from k_new / v_new (4-D maps over
+// [batch, rows_padded, Hkv, D]), the kernel copies those rows into the cache,
+// and the last CTA to take a ticket adds a.commit_add to a.commit_lens.
+int run_fused(const cp_layer_desc* d, AttnArgs a, int64_t rows_total, const void* k_new, const void* v_new,
+              cudaStream_t st) {
   const int G = d->num_q_heads / d->num_kv_heads;
   const uint64_t D = d->head_dim;
-  const int64_t rows_total = (int64_t)d->batch * rows_padded;
-  const uint64_t planes = (uint64_t)d->batch * d->num_kv_heads;
-  CUtensorMap tq, to, tkh, tvh, tknh, tvnh;
-  if (!encode_3d(&tq, d->dtype, q, D, d->num_q_heads, (uint64_t)rows_total, 64, G, kTcBlockM / G) ||
-      !encode_3d(&to, d->dtype, out, D, d->num_q_heads, (uint64_t)rows_total, 64, G, kTcBlockM / G) ||
-      !encode_3d(&tkh, d->dtype, k_cache, D, d->capacity, planes, 64, 64, 1) ||
-      !encode_3d(&tvh, d->dtype, v_cache, D, d->capacity, planes, 64, 128, 1))
+  const int rows_padded = a.rows.rows_uniform;
+  CUtensorMap tq, to, tk, tv, tkn, tvn;
+  if (!make_tc_maps(d, a.q, a.out, rows_total, a.k, a.v, d->batch, &tq, &to, &tk, &tv) ||
+      !encode_4d(&tkn, d->dtype, k_new, D, d->num_kv_heads, rows_padded, d->batch, 64, 1, kTcBlockN, 1) ||
+      !encode_4d(&tvn, d->dtype, v_new, D, d->num_kv_heads, rows_padded, d->batch, 64, 1, kTcBlockN, 1))
     return CP_ERR_CUDA;
-  std::memset(&tknh, 0, sizeof(tknh));
-  std::memset(&tvnh, 0, sizeof(tvnh));
-  const bool fused = k_new != nullptr;
-  if (fused && (!encode_4d(&tknh, d->dtype, k_new, D, d->num_kv_heads, rows_padded, d->batch, 64, 1, 64, 1) ||
-                !encode_4d(&tvnh, d->dtype, v_new, D, d->num_kv_heads, rows_padded, d->batch, 64, 1, 128, 1)))
-    return CP_ERR_CUDA;
-  PairArgs a;
-  std::memset(&a, 0, sizeof(a));
-  a.hq = d->num_q_heads;
-  a.hkv = d->num_kv_heads;
-  a.group = G;
-  a.scale_log2 = scale_log2(d);
-  a.rows = SeqRows{d->batch, rows_padded, nullptr};
-  a.capacity = d->capacity;
-  a.past = seqlens_k;
-  a.max_ctx = max_past + rows_padded;
-  a.out = out;
-  a.status = dev_status;
-  a.fused = fused ? 1 : 0;
+  a.min_rows = 1;
+  a.kv_direct = 0;
+  a.fused = 1;
   a.k_new = k_new;
   a.v_new = v_new;
-  a.k_cache = const_cast<void*>(k_cache);
-  a.v_cache = const_cast<void*>(v_cache);
-  a.ticket = ticket;
-  a.commit_lens = commit_lens;
-  a.commit_add = commit_add;
+  a.k_cache = const_cast<void*>(a.k);
+  a.v_cache = const_cast<void*>(a.v);
   const int ppt = 2 * (kTcBlockM / G);
   const int64_t pairs = (int64_t)d->batch * ((rows_padded + ppt - 1) / ppt);
-  if (2 * pairs > INT32_MAX || pairs * d->num_kv_heads > INT32_MAX) return CP_ERR_UNSUPPORTED;
-  return launch_result(launch_attn_pair(a, d->dtype, tq, to, tkh, tvh, tknh, tvnh, (int)pairs, st));
+  if (2 * pairs > INT32_MAX) return CP_ERR_UNSUPPORTED;
+  return launch_result(launch_attn_tc(a, d->dtype, tq, tk, tv, to, tkn, tvn, (int)pairs, st));
 }
 
 }  // namespace
@@ -391,12 +371,7 @@ int cp_prefill_chunk_attn(const cp_layer_desc* desc, const void* q, const void* 
   a.v = v_cache;
   a.out = out;
   a.status = dev_status;
-  if (use_pair(desc, rows_padded))
-    r = run_pair(desc, q, k_cache, v_cache, seqlens_k, rows_padded, max_past, out, nullptr, nullptr, nullptr,
-                 nullptr, 0, dev_status, st);
-  else
-    r = run_attention(desc, a, rows_total, rows_padded, k_cache, v_cache, desc->batch, workspace, workspace_bytes,
-                      st);
+  r = run_attention(desc, a, rows_total, rows_padded, k_cache, v_cache, desc->batch, workspace, workspace_bytes, st);
   if (r != CP_OK) return r;
   if (commit) return launch_result(launch_commit(seqlens_k, a.rows, real_rows, nullptr, st));
   return CP_OK;
@@ -433,9 +408,29 @@ int cp_prefill_chunk(const cp_layer_desc* desc, const void* q, void* k_new, void
       kControlBytes + snap + (decode_rows ? decode_ws_bytes(desc, max_past + rows_padded, desc->batch) : 0);
   if (workspace == nullptr || (int64_t)workspace_bytes < need || !aligned16(workspace)) return CP_ERR_WORKSPACE;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (use_pair(desc, rows_padded))  // one launch: append, attention and the advance of the lengths
-    return run_pair(desc, q, k_cache, v_cache, seqlens_k, rows_padded, max_past, out, k_new, v_new,
-                    static_cast<unsigned*>(workspace), seqlens_k, real_rows, dev_status, st);
+  AttnArgs a;
+  std::memset(&a, 0, sizeof(a));
+  a.hq = desc->num_q_heads;
+  a.hkv = desc->num_kv_heads;
+  a.d = desc->head_dim;
+  a.group = a.hq / a.hkv;
+  a.scale_log2 = scale_log2(desc);
+  a.rows = SeqRows{desc->batch, rows_padded, nullptr};
+  a.cache = make_cache(desc, block_table);
+  a.left_pad = desc->kind == CP_CACHE_ROLLING ? left_pad : nullptr;
+  a.max_ctx = max_past + rows_padded;
+  a.q = q;
+  a.k = k_cache;
+  a.v = v_cache;
+  a.out = out;
+  a.status = dev_status;
+  if (use_fused(desc, rows_padded)) {
+    a.past = seqlens_k;  // read before any CTA takes its ticket
+    a.ticket = static_cast<unsigned*>(workspace);
+    a.commit_lens = seqlens_k;
+    a.commit_add = real_rows;
+    return run_fused(desc, a, rows_total, k_new, v_new, st);
+  }
   int* past = reinterpret_cast<int*>(static_cast<char*>(workspace) + kControlBytes);
 
   AppendArgs ap;
@@ -455,23 +450,7 @@ int cp_prefill_chunk(const cp_layer_desc* desc, const void* q, void* k_new, void
   r = launch_result(launch_kv_append(ap, (int)rows_total, st));
   if (r != CP_OK) return r;
 
-  AttnArgs a;
-  std::memset(&a, 0, sizeof(a));
-  a.hq = desc->num_q_heads;
-  a.hkv = desc->num_kv_heads;
-  a.d = desc->head_dim;
-  a.group = a.hq / a.hkv;
-  a.scale_log2 = scale_log2(desc);
-  a.rows = SeqRows{desc->batch, rows_padded, nullptr};
-  a.cache = make_cache(desc, block_table);
   a.past = past;  // the snapshot: seqlens_k itself may then be advanced by the attention kernel
-  a.left_pad = desc->kind == CP_CACHE_ROLLING ? left_pad : nullptr;
-  a.max_ctx = max_past + rows_padded;
-  a.q = q;
-  a.k = k_cache;
-  a.v = v_cache;
-  a.out = out;
-  a.status = dev_status;
   // One launch for the attention and the commit when the tensor-core kernel takes every row.
   const int G = desc->num_q_heads / desc->num_kv_heads;
   const bool tc_only = desc->dtype != CP_F32 && rows_padded > 1 && attn_tc_supported(desc->head_dim, G, desc->dtype);

@@ -62,8 +62,18 @@ struct AttnArgs {
   int* status;             // optional CP_DEV_* bits
   int kv_direct;           // tensor-core kernel: this call's new K/V rows may be read from
                            // k_new / v_new ([rows_total, hkv, d]) instead of the paged pool
-  int* commit_lens = nullptr;  // tensor-core kernel: if set, CTA (0, 0) adds commit_add to each
-  int commit_add = 0;          // commit_lens[s] after the dependency wait (`past` must not alias it)
+  int* commit_lens = nullptr;  // tensor-core kernel: if set, lengths advanced by commit_add after the
+  int commit_add = 0;          // attention reads them: by CTA (0, 0) right after the dependency wait
+                               // when `past` is a copy (it must not alias commit_lens), else through
+  unsigned* ticket = nullptr;  // the ticket counter (zero before the launch, left zero)
+  // Tensor-core kernel, contiguous cache, fused append: the tiles that hold this
+  // call's keys are read from k_new / v_new [num_seqs, rows_uniform, hkv, d] and
+  // the kernel copies those rows into the cache [num_seqs, hkv, capacity, d].
+  int fused = 0;
+  const void* k_new = nullptr;
+  const void* v_new = nullptr;
+  void* k_cache = nullptr;
+  void* v_cache = nullptr;
 };
 
 // Arguments of the paired-SM tensor-core kernel (contiguous cache, head_dim
