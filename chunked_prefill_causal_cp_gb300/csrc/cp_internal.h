@@ -76,34 +76,6 @@ struct AttnArgs {
   void* v_cache = nullptr;
 };
 
-// Arguments of the paired-SM tensor-core kernel (contiguous cache, head_dim
-// 128, the same row count for every sequence).
-struct PairArgs {
-  int hq, hkv, group;      // group = hq / hkv
-  float scale_log2;        // softmax scale * log2(e)
-  SeqRows rows;            // rows_uniform > 0
-  int capacity;            // slots per (sequence, KV head)
-  const int* past;         // seqlens_k [num_seqs], read after the dependency wait
-  int max_ctx;             // host bound: past + rows <= max_ctx (checked in kernel)
-  void* out;               // [num_seqs * rows, hq, 128]
-  int* status;             // optional CP_DEV_* bits
-  // Fused append: the tiles that hold this call's keys are read from k_new /
-  // v_new [num_seqs, rows, hkv, 128] and the kernel copies those rows into the
-  // cache [num_seqs, hkv, capacity, 128].  Otherwise every key is read from the
-  // cache, which already holds the chunk's rows.
-  int fused;
-  const void* k_new;
-  const void* v_new;
-  void* k_cache;
-  void* v_cache;
-  // Advance of the lengths inside the kernel: the last CTA to have read
-  // `past` adds commit_add to commit_lens[s] (ticket: a zeroed counter the
-  // kernel leaves zero).  commit_lens == nullptr: no advance.
-  unsigned* ticket;
-  int* commit_lens;
-  int commit_add;
-};
-
 struct AppendArgs {
   int hkv, d, esize;       // esize: bytes per element
   SeqRows rows;
@@ -161,13 +133,6 @@ cudaError_t launch_attn_f32(const AttnArgs& a, int rows_bound, cudaStream_t st);
 cudaError_t launch_attn_tc(const AttnArgs& a, int dtype, const CUtensorMap& tq, const CUtensorMap& tk,
                            const CUtensorMap& tv, const CUtensorMap& to, const CUtensorMap& tkn,
                            const CUtensorMap& tvn, int pairs_bound, cudaStream_t st);
-// Paired-SM chunk attention (head_dim 128).  tq/to: q/out [rows_total, hq, 128], box {64, G, 128/G};
-// tkh/tvh: cache K/V planes, boxes {64, 64, 1} and {64, 128, 1}; tknh/tvnh (fused only): k_new/v_new as
-// [num_seqs, rows, hkv, 128] 4-D maps, boxes {64, 1, 64, 1} and {64, 1, 128, 1}.
-cudaError_t launch_attn_pair(const PairArgs& a, int dtype, const CUtensorMap& tq, const CUtensorMap& to,
-                             const CUtensorMap& tkh, const CUtensorMap& tvh, const CUtensorMap& tknh,
-                             const CUtensorMap& tvnh, int pairs_bound, cudaStream_t st);
-bool attn_pair_supported(int d, int group, int dtype);
 // Split-KV decode: partials into a.part_o / a.part_ml, then their combine.
 cudaError_t launch_decode(const AttnArgs& a, int dtype, cudaStream_t st);
 
