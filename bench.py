@@ -2,31 +2,38 @@
 """Benchmark of the chunked-prefill causal attention hot path on one GB300.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
-                    [--workload gqa_prefill|decode|mixed|rolling|fp32] [--no-pad]
+                    [--workload gqa_prefill|fp32|ladder|rolling|decode|mixed]
+                    [--chunk W] [--prompt N] [--budget B] [--no-pad] [--no-extras]
 
 Default workload (the one the headline metric is quoted on): one GQA layer,
 32 query / 8 KV heads, head_dim 128, bf16, a 4000-token prompt prefilled in
 chunks of 512 (7 x 512 + 416) into a KV cache of physical capacity 8192.  One
 step is the whole path for one prompt: chunk plan, query-width ladder (the
-416-row tail is widened to 512 by repeating its last row), and per chunk the
-KV append, the chunk attention and the commit of seqlens_k to past + real
-rows, made as one cp_prefill_chunk call (two kernels: the append, then the
-attention, which also advances seqlens_k).  Each step is one replay of a CUDA
+416-row tail is widened to 512 by repeating its last row, one cp_pad_chunk
+launch), and per chunk one cp_prefill_chunk call, which is one kernel launch
+on a contiguous cache: the chunk's K/V append, the chunk attention and the
+advance of seqlens_k to past + real rows.  Each step is one replay of a CUDA
 graph captured from the library's public calls; L2 is flushed (512 MiB write)
 between timed steps.
 
-Prints one JSON line (rank 0).  ``--impl reference`` times the CPU oracle
-(test infrastructure, float64 numpy) on a bounded sample of the same
-workload instead.  Other workloads (decode rows, mixed step) print the same
-kind of line with their own metric.
+Before anything is timed, each workload checks one replay of its own graph
+(cache bytes, lengths, and sampled output rows against a float32 PyTorch
+evaluation of the attention definition); a failed check ends the run without
+a line.
+
+The default line also carries, under "configs", one measurement of each of
+the other workloads of the problem statement (fp32 example, padding ladder,
+rolling cache, decode rows, and the whole mixed token-budget schedule at
+budgets 8192 and 2048), each with its own check.  ``--workload X`` prints X's
+line alone; ``--chunk`` / ``--budget`` sweep the chunk width and the token
+budget.  ``--impl reference`` times the CPU oracle (test infrastructure,
+float64) on a bounded sample of the default workload instead.
 """
 from __future__ import annotations
 
 import argparse
-import hashlib
 import json
 import os
-import re
 import statistics
 import subprocess
 import sys
@@ -38,19 +45,27 @@ sys.path.insert(0, ROOT)
 
 METRIC = "chunked-prefill attn tokens/s & effective TFLOP/s; % of GB300 BF16/HBM roofline"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+BF16_TOL = 2e-2   # max-abs error bound for 16-bit inputs with fp32 accumulation
+FP32_TOL = 1e-4   # max-abs error bound for the fp32 path
+L2_NOTE = "flushed between timed steps (512 MiB write)"
 
 
-def parse_args():
+def parse_args(argv=None):
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
     p.add_argument("--steps", type=int, default=3000)
     p.add_argument("--warmup", type=int, default=20)
     p.add_argument("--impl", default="native", choices=["native", "reference"])
-    p.add_argument("--workload", default="gqa_prefill", choices=["gqa_prefill", "decode", "mixed", "rolling", "fp32"])
+    p.add_argument("--workload", default="gqa_prefill",
+                   choices=["gqa_prefill", "fp32", "ladder", "rolling", "decode", "mixed"])
+    p.add_argument("--chunk", type=int, default=512, help="chunk width W of the gqa_prefill workload")
+    p.add_argument("--prompt", type=int, default=4000, help="prompt tokens of the gqa_prefill workload")
+    p.add_argument("--budget", type=int, default=8192, help="token budget of the mixed workload")
     p.add_argument("--no-pad", action="store_true", help="do not widen chunks to the query-width ladder")
+    p.add_argument("--no-extras", action="store_true", help="default line without the other workloads")
     p.add_argument("--cpu-seconds", type=float, default=12.0, help="CPU-baseline sample budget")
     p.add_argument("--skip-cpu", action="store_true")
-    return p.parse_args()
+    return p.parse_args(argv)
 
 
 def peaks():
@@ -106,7 +121,7 @@ def job_throughput(local_ms, units_per_step, steps, world):
 # --------------------------------------------------------------------------- clocks
 
 class ClockSampler:
-    """nvidia-smi sampling of SM clock and throttle reasons during the timed region."""
+    """nvidia-smi sampling of SM clock and throttle reasons while the GPU is loaded."""
 
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -126,7 +141,6 @@ class ClockSampler:
             self.proc = subprocess.Popen(cmd, stdout=self.f, stderr=subprocess.DEVNULL)
         except OSError:
             self.proc = None
-        time.sleep(0.3)
 
     def stop(self):
         if self.proc is None:
@@ -160,20 +174,23 @@ class ClockSampler:
 
 # --------------------------------------------------------------------------- helpers
 
-def kernel_traffic(kernel_file, profile_name):
-    """DRAM bytes per launch recorded in profiles/<profile_name> for the kernel
-    source it was measured on; None when the source has changed since."""
+def kernel_traffic(profile_name):
+    """DRAM bytes per launch recorded in profiles/<profile_name> (a JSON record
+    written from an ncu capture), or None when the kernel source it names has
+    changed since the capture."""
+    import hashlib
     prof = os.path.join(ROOT, "profiles", profile_name)
     if not os.path.exists(prof):
         return None
-    text = open(prof).read()
-    m_sha = re.search(r"source_sha256:\s*([0-9a-f]{64})", text)
-    m_b = re.search(r"dram_bytes_per_launch:\s*([0-9.e+]+)", text)
-    if not (m_sha and m_b):
+    with open(prof) as f:
+        rec = json.load(f)
+    src = os.path.join(ROOT, "chunked_prefill_causal_cp_gb300", "csrc", rec.get("kernel_source", ""))
+    if not os.path.isfile(src):
         return None
-    src = os.path.join(ROOT, "chunked_prefill_causal_cp_gb300", "csrc", kernel_file)
     sha = hashlib.sha256(open(src, "rb").read()).hexdigest()
-    return float(m_b.group(1)) if sha == m_sha.group(1) else None
+    if sha != rec.get("source_sha256"):
+        return None
+    return float(rec["dram_bytes_per_launch"])
 
 
 def cpu_cores():
@@ -185,22 +202,102 @@ def visible_pairs(past, rows):
     return rows * past + rows * (rows + 1) // 2
 
 
+def rolling_visible_pairs(L, c, C, left_pad):
+    """Visible (query, key) pairs of the rolling workload, real query rows only:
+    chunk k row i is position p = k*c + i; logical slot j holds position
+    a = (k+1)*c - C + j, visible iff a >= 0, a >= left_pad and a <= p."""
+    total = 0
+    for k in range(L // c):
+        lo = max(0, (k + 1) * c - C, left_pad)
+        for i in range(c):
+            p = k * c + i
+            if p >= left_pad:
+                total += max(0, p - lo + 1)
+    return total
+
+
+def ref_rows(q_tok, keys, vals, scale):
+    """float32 PyTorch evaluation of the attention definition for one token:
+    q_tok [Hq, D] over visible keys / values [n, Hkv, D]; query head h reads
+    KV head h // (Hq / Hkv).  Returns [Hq, D] (float32)."""
+    import torch
+    hq, d = q_tok.shape
+    hkv = keys.shape[1]
+    qf = q_tok.float().view(hkv, hq // hkv, d)
+    s = torch.einsum("gjd,ngd->gjn", qf, keys.float()) * scale
+    p = torch.softmax(s, dim=-1)
+    return torch.einsum("gjn,ngd->gjd", p, vals.float()).reshape(hq, d)
+
+
+def bits_equal(a, b):
+    """Byte equality of two tensors of the same shape and dtype."""
+    import torch
+    if a.shape != b.shape or a.dtype != b.dtype:
+        return False
+    if a.element_size() == 2:
+        return torch.equal(a.contiguous().view(torch.int16), b.contiguous().view(torch.int16))
+    return torch.equal(a.contiguous().view(torch.int32), b.contiguous().view(torch.int32))
+
+
+def time_steps(run_step, flush, steps, torch):
+    """Per-step CUDA-event times (ms) on the current stream, L2 flushed between."""
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    for i in range(steps):
+        flush.zero_()
+        starts[i].record()
+        run_step()
+        ends[i].record()
+    torch.cuda.synchronize()
+    return [s.elapsed_time(e) for s, e in zip(starts, ends)]
+
+
+def capture(step, dev):
+    """Two eager runs on a side stream, then one CUDA graph of `step`."""
+    import torch
+    s = torch.cuda.Stream(dev)
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        for _ in range(2):
+            step()
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        step()
+    return g
+
+
+class CheckFailed(RuntimeError):
+    pass
+
+
+def require(check, what):
+    """Ends the run (no line is printed) when a pre-timing check failed."""
+    if not check.get("ok"):
+        raise CheckFailed(f"{what}: check before timing failed: {json.dumps(check)}")
+    return check
+
+
 # --------------------------------------------------------------------------- workloads
 
 class GqaPrefill:
-    """The 4000-token GQA prompt, chunk 512, capacity 8192 (see module doc)."""
+    """The GQA prompt (default 4000 tokens, chunk 512, capacity 8192; see module doc)."""
 
-    N, W, HQ, HKV, D, CAP = 4000, 512, 32, 8, 128, 8192
+    HQ, HKV, D, CAP = 32, 8, 128, 8192
 
-    def __init__(self, dev, pad=True):
+    def __init__(self, dev, pad=True, N=4000, W=512):
         import torch
         import chunked_prefill_causal_cp_gb300 as cp
         import synth_inputs as SI
 
         self.cp, self.torch, self.dev, self.pad = cp, torch, dev, pad
+        self.N, self.W = N, W
         self.sizes = cp.cp_chunk_plan(self.N, self.W)
         self.widths = [cp.cp_query_width(r, self.W) if pad else r for r in self.sizes]
         self.rows_alloc = sum(self.sizes[:-1]) + self.widths[-1]
+        if self.rows_alloc > self.CAP:
+            raise ValueError(f"prompt {N} with chunk {W} needs {self.rows_alloc} slots > capacity {self.CAP}")
         q, k, v = SI.gqa_prompt(self.N, seed=1)
         self.host_q, self.host_k, self.host_v = q, k, v
         bf = torch.bfloat16
@@ -215,8 +312,6 @@ class GqaPrefill:
         self.kc = torch.zeros(1, self.HKV, self.CAP, self.D, dtype=bf, device=dev)
         self.vc = torch.zeros_like(self.kc)
         self.lens = torch.zeros(1, dtype=torch.int32, device=dev)
-        self.pasts = torch.tensor([0] + list(torch.tensor(self.sizes).cumsum(0)[:-1].tolist()),
-                                  dtype=torch.int32, device=dev)
         self.status = torch.zeros(1, dtype=torch.int32, device=dev)
         self.ws = torch.zeros(max(16, cp.cp_workspace_size(self.desc, self.W, self.CAP, 1)),
                               dtype=torch.uint8, device=dev)
@@ -227,17 +322,17 @@ class GqaPrefill:
             past += r
         self.flops = sum(self.flops_chunk)
         self.tokens = self.N
-        # launches of this library per step: one pad launch (q, k and v) per widened chunk + per chunk
-        # the append and the attention (which advances seqlens_k itself)
-        self.launches = sum(1 for r, w in zip(self.sizes, self.widths) if w > r) + 2 * len(self.sizes)
+        # launches of this library per step: one pad launch (q, k and v together) per widened
+        # chunk, then one launch per chunk (append, attention and the advance of seqlens_k)
+        self.launches = sum(1 for r, w in zip(self.sizes, self.widths) if w > r) + len(self.sizes)
 
-    def _chunk(self, i, attn=True, append=True, commit=True):
+    def _chunk(self, i, attn=True, append=True, commit=True, pad=True):
         cp = self.cp
         r, w = self.sizes[i], self.widths[i]
         past = sum(self.sizes[:i])
         sl = slice(past, past + w)
         q, k, v = self.q[None, sl], self.k[None, sl], self.v[None, sl]
-        if append and w > r:
+        if append and pad and w > r:
             cp.cp_pad_chunk(self.desc, q, k, v, r, w)
         if append and attn and commit:  # the whole chunk in one call
             cp.cp_prefill_chunk(self.desc, q, k, v, self.kc, self.vc, self.lens, w, r, past, self.out[None, sl],
@@ -255,35 +350,81 @@ class GqaPrefill:
             self._chunk(i)
 
     def capture(self):
+        self.graph = capture(self.step, self.dev)
+        return self.graph
+
+    def capture_prefixes(self):
+        """Graphs of the first k chunk calls (k = 0 .. n) without the pad launch
+        (the widened rows are already in place after one step): graph k runs
+        chunks 0 .. k-1 in the same launch chain as the step, so the attention
+        launches' in-situ time is T(n) - T(0) and chunk k's is T(k+1) - T(k)."""
         torch = self.torch
-        s = torch.cuda.Stream(self.dev)
-        s.wait_stream(torch.cuda.current_stream())
-        with torch.cuda.stream(s):
-            for _ in range(2):
-                self.step()
-        torch.cuda.current_stream().wait_stream(s)
+        self.prefix_graphs = []
+        for k in range(len(self.sizes) + 1):
+            def body(k=k):
+                self.lens.zero_()
+                for i in range(k):
+                    self._chunk(i, pad=False)
+            self.prefix_graphs.append(capture(body, self.dev))
         torch.cuda.synchronize()
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g):
-            self.step()
-        # per-chunk graphs for the kernel-level timing: state set-up, then attention alone
-        self.setup_graphs, self.attn_graphs = [], []
-        for i in range(len(self.sizes)):
-            gs, ga = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
-            with torch.cuda.graph(gs):
-                self.lens.copy_(self.pasts[i:i + 1])
-                self._chunk(i, attn=False)
-            with torch.cuda.graph(ga):
-                self._chunk(i, append=False, commit=False)
-            self.setup_graphs.append(gs)
-            self.attn_graphs.append(ga)
-        self.graph = g
-        return g
+
+    def self_check(self, n_sample=26, seed=7):
+        """One replayed step against what it must hold: the cache holds the
+        prompt's K/V rows bit for bit and, in the slots of the widened tail,
+        copies of the last real row; seqlens_k = N; the device status is clear;
+        each chunk's first and last rows and random rows agree with ref_rows."""
+        torch = self.torch
+        torch.cuda.synchronize()
+        N = self.N
+        kc = self.kc[0].transpose(0, 1)
+        vc = self.vc[0].transpose(0, 1)
+        cache_ok = bits_equal(kc[:N], self.k[:N]) and bits_equal(vc[:N], self.v[:N])
+        pad = self.widths[-1] - self.sizes[-1]
+        if pad:
+            cache_ok = cache_ok and bits_equal(kc[N:N + pad], self.k[N - 1:N].expand(pad, -1, -1)) \
+                and bits_equal(vc[N:N + pad], self.v[N - 1:N].expand(pad, -1, -1))
+        toks = set()
+        past = 0
+        for r in self.sizes:
+            toks.update((past, past + r - 1))
+            past += r
+        g = torch.Generator().manual_seed(seed)
+        while len(toks) < n_sample:
+            toks.add(int(torch.randint(0, N, (1,), generator=g)))
+        scale = self.D ** -0.5
+        err = 0.0
+        for t in sorted(toks):
+            ref = ref_rows(self.q[t], self.k[:t + 1], self.v[:t + 1], scale)
+            err = max(err, float((self.out[t].float() - ref).abs().max()))
+        lens = int(self.lens.item())
+        status = int(self.status.item())
+        ok = cache_ok and lens == N and status == 0 and err < BF16_TOL
+        return {"ok": ok, "rows_checked": len(toks), "max_abs_err": err, "tol": BF16_TOL,
+                "cache_bit_exact": cache_ok, "seqlens_k": lens, "status": status,
+                "reference": "float32 PyTorch evaluation of the definition on the GPU"}
+
+    def config(self):
+        return {"workload": f"gqa32x8_d128_bf16_prompt{self.N}_chunk{self.W}_cap{self.CAP}",
+                "model": "single GQA attention layer (synthetic N(0,1) q/k/v)",
+                "prompt_tokens": self.N, "chunk": self.W, "chunks": self.sizes,
+                "query_widths": self.widths, "kv_capacity": self.CAP, "heads_q": self.HQ,
+                "heads_kv": self.HKV, "head_dim": self.D, "global_batch": 1, "seq_len": self.N,
+                "padding": "ladder" if self.pad else "none", "parallelism": "replica per GPU",
+                "l2": L2_NOTE, "cuda_graph": True}
+
+    # ---- end to end: host buffers in, result out, through the captured public calls
+    def pin(self):
+        self.hq = self.host_q.pin_memory()
+        self.hk = self.host_k.pin_memory()
+        self.hv = self.host_v.pin_memory()
+        self.ho = self.torch.empty(self.N, self.HQ, self.D, dtype=self.torch.bfloat16).pin_memory()
+        self.h2d = (self.hq.numel() + self.hk.numel() + self.hv.numel()) * 2
+        self.d2h = self.ho.numel() * 2
 
     def capture_e2e(self):
         """One CUDA graph of a whole step with its host traffic, pipelined the way
         a serving loop runs chunked prefill: chunk i's q/k/v rows go host ->
-        device on one copy stream while chunk i-1 is computed, and chunk i's
+        device on one copy stream ahead of chunk i's compute, and chunk i's
         output rows go device -> host on another as soon as chunk i is done.
         Every input byte and every output byte of the step crosses the bus inside
         the graph; the step ends when the last output row is on the host."""
@@ -298,21 +439,22 @@ class GqaPrefill:
             self.lens.zero_()
             up.wait_stream(main)
             down.wait_stream(main)
-            past = 0
-            for i, r in enumerate(self.sizes):
-                sl = slice(past, past + r)
-                with torch.cuda.stream(up):
+            starts = [sum(self.sizes[:i]) for i in range(n)]
+            with torch.cuda.stream(up):  # all uploads queue at once, in chunk order
+                for i, r in enumerate(self.sizes):
+                    sl = slice(starts[i], starts[i] + r)
                     self.q[sl].copy_(self.hq[sl], non_blocking=True)
                     self.k[sl].copy_(self.hk[sl], non_blocking=True)
                     self.v[sl].copy_(self.hv[sl], non_blocking=True)
                     ev_in[i].record(up)
+            for i, r in enumerate(self.sizes):
                 main.wait_event(ev_in[i])
                 self._chunk(i)
                 ev_done[i].record(main)
                 with torch.cuda.stream(down):
                     down.wait_event(ev_done[i])
+                    sl = slice(starts[i], starts[i] + r)
                     self.ho[sl].copy_(self.out[sl], non_blocking=True)
-                past += r
             main.wait_stream(up)
             main.wait_stream(down)
 
@@ -328,250 +470,34 @@ class GqaPrefill:
         self.e2e_graph = g
         return g
 
-    def pin(self):
-        self.hq = self.host_q.pin_memory()
-        self.hk = self.host_k.pin_memory()
-        self.hv = self.host_v.pin_memory()
-        self.ho = self.torch.empty(self.N, self.HQ, self.D, dtype=self.torch.bfloat16).pin_memory()
-        self.h2d = (self.hq.numel() + self.hk.numel() + self.hv.numel()) * 2
-        self.d2h = self.ho.numel() * 2
-
-    def config(self):
-        return {"workload": "gqa32x8_d128_bf16_prompt4000_chunk512_cap8192",
-                "model": "single GQA attention layer (synthetic N(0,1) q/k/v)",
-                "prompt_tokens": self.N, "chunk": self.W, "chunks": self.sizes,
-                "query_widths": self.widths, "kv_capacity": self.CAP, "heads_q": self.HQ,
-                "heads_kv": self.HKV, "head_dim": self.D, "global_batch": 1, "seq_len": self.N,
-                "padding": "ladder" if self.pad else "none", "parallelism": "replica per GPU",
-                "l2": "flushed between timed steps (512 MiB write)", "cuda_graph": True}
-
     def cpu_sample(self, budget_s):
         """Oracle (as it stands) on whole KV-head groups of the same prompt until
-        the time budget is spent; returns (tokens/s scaled to all heads, sample)."""
+        the time budget is spent; returns (tokens/s scaled to all heads, sample,
+        seconds, max-abs difference between the oracle's rows and this
+        workload's last GPU output for the groups it ran)."""
         import numpy as np
         import oracle
         q = self.host_q.double().numpy()
         k = self.host_k.double().numpy()
         v = self.host_v.double().numpy()
+        gpu = self.out[:self.N].float().cpu().double().numpy()
         G = self.HQ // self.HKV
         t0 = time.perf_counter()
         groups = 0
+        diff = 0.0
         while groups < self.HKV:
             g = groups
-            oracle.chunked_prefill(q[:, g * G:(g + 1) * G], k[:, g:g + 1], v[:, g:g + 1], self.W)
+            o, _, _ = oracle.chunked_prefill(q[:, g * G:(g + 1) * G], k[:, g:g + 1], v[:, g:g + 1], self.W)
+            diff = max(diff, float(np.abs(o - gpu[:, g * G:(g + 1) * G]).max()))
             groups += 1
             if time.perf_counter() - t0 > budget_s:
                 break
         t = time.perf_counter() - t0
         full = t * self.HKV / groups
-        sample = (f"oracle.chunked_prefill of the 4000-token prompt (chunks {self.sizes[0]}x"
+        sample = (f"oracle.chunked_prefill of the {self.N}-token prompt (chunks {self.sizes[0]}x"
                   f"{len(self.sizes) - 1}+{self.sizes[-1]}, unpadded) for {groups} of {self.HKV} KV-head "
                   f"groups ({groups * G} of {self.HQ} query heads), {t:.1f} s, scaled to all heads")
-        return self.N / full, sample, t
-
-
-def time_steps(run_step, flush, steps, torch):
-    """Per-step CUDA-event times (ms) on the current stream, L2 flushed between."""
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
-    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
-    for i in range(steps):
-        flush.zero_()
-        starts[i].record()
-        run_step()
-        ends[i].record()
-    torch.cuda.synchronize()
-    return [s.elapsed_time(e) for s, e in zip(starts, ends)]
-
-
-def run_native(args):
-    import torch
-    rank, world, local = dist_init(args.gpus)
-    dev = torch.device("cuda", local)
-    torch.cuda.set_device(dev)
-    from chunked_prefill_causal_cp_gb300 import _build
-    if rank == 0 or world == 1:
-        _build.build()
-    barrier(world)
-    import chunked_prefill_causal_cp_gb300 as cp
-    cp.lib()
-    pk, pk_src = peaks()
-    if args.workload in ("rolling", "fp32"):
-        return run_chunk_loop(args, rank, world, dev, pk, pk_src)
-    if args.workload != "gqa_prefill":
-        return run_paged(args, rank, world, dev, pk, pk_src)
-
-    wl = GqaPrefill(dev, pad=not args.no_pad)
-    wl.capture()
-    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
-    for _ in range(max(args.warmup, 3)):
-        wl.graph.replay()
-    torch.cuda.synchronize()
-    if int(wl.status.item()) != 0:
-        raise RuntimeError(f"device status {int(wl.status.item())}")
-
-    bus = None
-    try:
-        bus = torch.cuda.get_device_properties(dev).pci_bus_id
-    except AttributeError:
-        pass
-    clocks = ClockSampler(bus)
-    barrier(world)
-    torch.cuda.synchronize()
-    clocks.start()
-    times = time_steps(wl.graph.replay, flush, args.steps, torch)
-    clk = clocks.stop()
-    torch.cuda.synchronize()
-    barrier(world)
-    total_ms, value = job_throughput(sum(times), wl.tokens, args.steps, world)
-    ms_per_step = total_ms / args.steps
-
-    # ---- kernel-level timing of the attention kernel (per chunk, same state as in the step).
-    # A short spin kernel (no memory traffic) keeps the GPU busy while the start
-    # event, the one-kernel graph and the end event are enqueued, so the events
-    # bracket the kernel's execution and not the host's launch latency.
-    reps = 20
-    spin_cycles = int(30e-6 * float(pk.get("sm_max_mhz", 2070.0)) * 1e6)
-    attn_ms = [0.0] * len(wl.sizes)
-    for _ in range(reps):
-        for i in range(len(wl.sizes)):
-            wl.setup_graphs[i].replay()
-            torch.cuda._sleep(spin_cycles)
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            e0.record()
-            wl.attn_graphs[i].replay()
-            e1.record()
-            e1.synchronize()
-            attn_ms[i] += e0.elapsed_time(e1) / reps
-    attn_tflops = wl.flops / (sum(attn_ms) / 1e3) / 1e12
-    peak = float(pk["bf16_tflops"])
-    traffic = kernel_traffic("attn_tc.cu", "attn_tc_gqa_prefill.md")
-
-    # ---- end to end: host buffers in, result out, through the captured public calls
-    wl.pin()
-    e2e_steps = max(20, min(args.steps // 10, 300))
-
-    wl.capture_e2e()
-
-    def e2e_step():
-        wl.e2e_graph.replay()
-
-    for _ in range(3):
-        e2e_step()
-    torch.cuda.synchronize()
-    e2e_times = time_steps(e2e_step, flush, e2e_steps, torch)
-    _, e2e_value = job_throughput(sum(e2e_times), wl.tokens, e2e_steps, world)
-    if int(wl.status.item()) != 0:
-        raise RuntimeError(f"device status {int(wl.status.item())}")
-
-    line = {
-        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded N(0,1) q/k/v)",
-        "config": wl.config(),
-        "effective_tflops": wl.flops * args.steps * world / (total_ms / 1e3) / 1e12,
-        "flops_per_step": wl.flops,
-        "roofline": {"bound": "tensor", "achieved": attn_tflops, "peak": peak, "unit": "TFLOP/s",
-                     "frac": attn_tflops / peak, "traffic": traffic, "kernel": "attn_tc_kernel",
-                     "peak_source": f"{pk_src} bf16_tflops (burst; kernel timed alone)",
-                     "frac_of_sustained": attn_tflops / float(pk.get("bf16_tflops_sustained", peak)),
-                     "per_chunk_us": [round(t * 1e3, 2) for t in attn_ms],
-                     "kernel_timing": ("CUDA events around a one-kernel graph of each chunk's attention, "
-                                       "enqueued behind a 30 us spin kernel so launch latency is excluded; "
-                                       "same cache state as in the step, mean of 20"),
-                     "per_chunk_tflops": [round(f / (t / 1e3) / 1e12, 1) for f, t in zip(wl.flops_chunk, attn_ms)]},
-        "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": wl.h2d,
-                "d2h_bytes_per_step": wl.d2h,
-                "path": ("one captured graph per step of the public calls with its host traffic: chunk i's "
-                         "q/k/v rows pinned host -> device on a copy stream while chunk i-1 computes, chunk i's "
-                         "output rows device -> pinned host on a second copy stream once chunk i is done")},
-        "gpu_launches": wl.launches * args.steps,
-        "clocks": clk,
-    }
-    if rank == 0 and world == 1 and not args.skip_cpu:
-        v_cpu, sample, _ = wl.cpu_sample(args.cpu_seconds)
-        line["cpu_baseline"] = {"value": v_cpu, "unit": "tokens/s", "cores": cpu_cores(), "kind": "oracle",
-                                "sample": sample}
-    if rank == 0:
-        print(json.dumps(line), flush=True)
-    if world > 1:
-        import torch.distributed as dist
-        dist.destroy_process_group()
-
-
-class PagedStep:
-    """The mixed-step workload: 64 running decodes with contexts U{512..8192} in
-    16-token pages (seeded page permutation), GQA 32/8 x 128 bf16.  ``decode``:
-    the 64 decode rows alone.  ``mixed``: the first step of the 8192-token
-    budget (64 decode rows + the first 8128 rows of a 20000-token prompt)."""
-
-    HQ, HKV, D = 32, 8, 128
-
-    def __init__(self, dev, mode):
-        import torch
-        import chunked_prefill_causal_cp_gb300 as cp
-        import synth_inputs as SI
-
-        self.cp, self.torch, self.mode = cp, torch, mode
-        mb = SI.mixed_batch()
-        self.mb = mb
-        bf = torch.bfloat16
-        self.desc = cp.layer_desc(bf, 0, self.HQ, self.HKV, self.D, cp.CP_CACHE_PAGED, page_size=mb.page_size,
-                                  num_pages=mb.num_pages, max_blocks=mb.max_blocks)
-        g = torch.Generator(device=dev).manual_seed(mb.seed)
-        self.kp = torch.randn(mb.num_pages, self.HKV, mb.page_size, self.D, generator=g, device=dev).to(bf)
-        self.vp = torch.randn(mb.num_pages, self.HKV, mb.page_size, self.D, generator=g, device=dev).to(bf)
-        nd = len(mb.decode_ctx)
-        rows = [1] * nd
-        if mode == "mixed":
-            entries = [e for e in cp.cp_schedule(8192, nd, mb.prompt_lens) if e[0] == 0]
-            rows = [e[3] for e in entries]
-            seqs = [e[1] for e in entries]
-        else:
-            seqs = list(range(nd))
-        past = [c - 1 for c in mb.decode_ctx] + [0] * (len(seqs) - nd)
-        self.rows, self.seqs, self.past_host = rows, seqs, past
-        self.T = sum(rows)
-        self.S = len(seqs)
-        self.max_ctx = max(p + r for p, r in zip(past, rows))
-        self.q = torch.randn(self.T, self.HQ, self.D, generator=g, device=dev).to(bf)
-        self.kn = torch.randn(self.T, self.HKV, self.D, generator=g, device=dev).to(bf)
-        self.vn = torch.randn(self.T, self.HKV, self.D, generator=g, device=dev).to(bf)
-        self.out = torch.empty(self.T, self.HQ, self.D, dtype=bf, device=dev)
-        self.bt = mb.block_table[seqs].contiguous().to(dev)
-        cu = [0]
-        for r in rows:
-            cu.append(cu[-1] + r)
-        self.cu = torch.tensor(cu, dtype=torch.int32, device=dev)
-        self.past0 = torch.tensor(past, dtype=torch.int32, device=dev)
-        self.past = self.past0.clone()
-        self.status = torch.zeros(1, dtype=torch.int32, device=dev)
-        self.ws = torch.zeros(cp.cp_workspace_size(self.desc, self.T, self.max_ctx, self.S), dtype=torch.uint8,
-                              device=dev)
-        # algorithmic work
-        kv_row = self.HKV * self.D * 2
-        self.decode_bytes = sum((p + 1) * kv_row * 2 for p, r in zip(past, rows) if r == 1) \
-            + sum(self.HQ * self.D * 2 * 2 + kv_row * 2 for r in rows if r == 1)
-        self.flops = sum(4 * self.D * self.HQ * visible_pairs(p, r) for p, r in zip(past, rows))
-        self.launches = 5 if mode == "mixed" else 4  # append, decode split, combine, [prefill], commit
-
-    def step(self):
-        self.past.copy_(self.past0)
-        self.cp.cp_mixed_step(self.desc, self.q, self.kn, self.vn, self.kp, self.vp, self.bt, self.cu, self.past,
-                              self.S, self.T, self.max_ctx, self.out, self.ws, dev_status=self.status)
-
-
-def rolling_visible_pairs(L, c, C, left_pad):
-    """Visible (query, key) pairs of the rolling workload, real query rows only:
-    chunk k row i is position p = k*c + i; logical slot j holds position
-    a = (k+1)*c - C + j, visible iff a >= 0, a >= left_pad and a <= p."""
-    total = 0
-    for k in range(L // c):
-        lo = max(0, (k + 1) * c - C, left_pad)
-        for i in range(c):
-            p = k * c + i
-            if p >= left_pad:
-                total += max(0, p - lo + 1)
-    return total
+        return self.N / full, sample, t, diff, groups * G
 
 
 class ChunkLoop:
@@ -585,7 +511,7 @@ class ChunkLoop:
         import chunked_prefill_causal_cp_gb300 as cp
         import synth_inputs as SI
 
-        self.cp, self.torch, self.mode = cp, torch, mode
+        self.cp, self.torch, self.mode, self.dev = cp, torch, mode, dev
         self.runs = []
         if mode == "rolling":
             H, d, c, C = 16, 128, 256, 1024
@@ -632,70 +558,503 @@ class ChunkLoop:
                                     left_pad=r["left"] if rolling else None, dev_status=self.status)
                 past += w
 
+    def self_check(self, n_sample=24, seed=11):
+        """fp32: every row against a float64 evaluation of causal attention on
+        the GPU (1e-4).  Rolling: the ring holds position p in slot p mod C bit
+        for bit for the last C positions; sampled real rows agree with ref_rows
+        over the window the chunk sees, positions [max(0, (k+1)c - C, left_pad), p]."""
+        torch = self.torch
+        torch.cuda.synchronize()
+        status = int(self.status.item())
+        if self.mode == "fp32":
+            r = self.runs[0]
+            q, k, v = (t.double() for t in (r["qd"], r["kd"], r["vd"]))
+            s = torch.einsum("thd,shd->hts", q, k) * r["d"] ** -0.5
+            n = q.shape[0]
+            s.masked_fill_(torch.ones(n, n, dtype=torch.bool, device=s.device).triu(1), float("-inf"))
+            ref = torch.einsum("hts,shd->thd", torch.softmax(s, dim=-1), v)
+            err = float((r["out"].double() - ref).abs().max())
+            lens = int(r["lens"].item())
+            ok = err < FP32_TOL and lens == n and status == 0
+            return {"ok": ok, "rows_checked": n, "max_abs_err": err, "tol": FP32_TOL, "seqlens_k": lens,
+                    "status": status, "reference": "float64 PyTorch causal attention on the GPU, every row"}
+        err, rows, ring_ok, lens_ok = 0.0, 0, True, True
+        g = torch.Generator().manual_seed(seed)
+        for r in self.runs:
+            L, lp, c, C = r["L"], r["lp"], r["W"], r["cap"]
+            lens_ok = lens_ok and int(r["lens"].item()) == L
+            for p in range(max(0, L - C), L):
+                ring_ok = ring_ok and bits_equal(r["kc"][0, :, p % C], r["kd"][p]) \
+                    and bits_equal(r["vc"][0, :, p % C], r["vd"][p])
+                if not ring_ok:
+                    break
+            picks = {lp, L - 1}
+            while len(picks) < n_sample // len(self.runs):
+                picks.add(int(torch.randint(lp, L, (1,), generator=g)))
+            for p in sorted(picks):
+                k_ = p // c
+                lo = max(0, (k_ + 1) * c - C, lp)
+                ref = ref_rows(r["qd"][p], r["kd"][lo:p + 1], r["vd"][lo:p + 1], r["d"] ** -0.5)
+                err = max(err, float((r["out"][p].float() - ref).abs().max()))
+                rows += 1
+        ok = ring_ok and lens_ok and status == 0 and err < BF16_TOL
+        return {"ok": ok, "rows_checked": rows, "max_abs_err": err, "tol": BF16_TOL, "ring_bit_exact": ring_ok,
+                "seqlens_k_ok": lens_ok, "status": status,
+                "reference": "float32 PyTorch evaluation of the windowed definition on the GPU"}
+
     def config(self):
         if self.mode == "rolling":
             return {"workload": "rolling_fp16_mha16_d128_window1024_chunk256_len2048+768",
                     "aligned_lengths": [r["L"] for r in self.runs], "left_pad": [r["lp"] for r in self.runs],
-                    "visible_pairs": [r["pairs"] for r in self.runs],
-                    "l2": "flushed between timed steps (512 MiB write)", "cuda_graph": True}
+                    "visible_pairs": [r["pairs"] for r in self.runs], "l2": L2_NOTE, "cuda_graph": True}
         return {"workload": "fp32_mha8_d64_prompt1000_chunk256", "visible_pairs": self.runs[0]["pairs"],
-                "l2": "flushed between timed steps (512 MiB write)", "cuda_graph": True}
+                "l2": L2_NOTE, "cuda_graph": True}
 
 
-def run_chunk_loop(args, rank, world, dev, pk, pk_src):
-    import torch
-    wl = ChunkLoop(dev, args.workload)
-    s = torch.cuda.Stream(dev)
-    s.wait_stream(torch.cuda.current_stream())
-    with torch.cuda.stream(s):
+class LadderRuns:
+    """The query-padding workload: the GQA layer with chunk 512 and prompts
+    {1041, 1468, 3118, 3788, 1137, 1200} (seeds 10 + idx), each prefilled
+    twice; the last chunk of each is widened to its ladder tier {171, 342, 512}
+    by repeating its last real row.  Contiguous cache of capacity 4096."""
+
+    HQ, HKV, D, W, CAP = 32, 8, 128, 512, 4096
+
+    def __init__(self, dev, pad=True):
+        import torch
+        import chunked_prefill_causal_cp_gb300 as cp
+        import synth_inputs as SI
+
+        self.cp, self.torch, self.dev, self.pad = cp, torch, dev, pad
+        bf = torch.bfloat16
+        self.desc = cp.layer_desc(bf, 1, self.HQ, self.HKV, self.D, cp.CP_CACHE_CONTIG, capacity=self.CAP)
+        self.status = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.ws = torch.zeros(cp.cp_workspace_size(self.desc, self.W, self.CAP, 1), dtype=torch.uint8, device=dev)
+        self.runs = []
+        for idx, n in enumerate(SI.LADDER_PROMPT_LENGTHS):
+            q, k, v = SI.ladder_prompt(idx)
+            sizes = cp.cp_chunk_plan(n, self.W)
+            widths = [cp.cp_query_width(r, self.W) if pad else r for r in sizes]
+            alloc = sum(sizes[:-1]) + widths[-1]
+            r = dict(n=n, sizes=sizes, widths=widths)
+            for name, t, h in (("q", q, self.HQ), ("k", k, self.HKV), ("v", v, self.HKV)):
+                buf = torch.zeros(alloc, h, self.D, dtype=bf, device=dev)
+                buf[:n].copy_(t)
+                r[name] = buf
+            r["out"] = torch.zeros(alloc, self.HQ, self.D, dtype=bf, device=dev)
+            r["kc"] = torch.zeros(1, self.HKV, self.CAP, self.D, dtype=bf, device=dev)
+            r["vc"] = torch.zeros_like(r["kc"])
+            r["lens"] = torch.zeros(1, dtype=torch.int32, device=dev)
+            self.runs.append(r)
+        self.tokens = 2 * sum(r["n"] for r in self.runs)
+        self.flops = 2 * sum(4 * self.D * self.HQ * visible_pairs(0, r["n"]) for r in self.runs)
+        self.padded_rows = 2 * sum(r["widths"][-1] - r["sizes"][-1] for r in self.runs)
+        self.launches = 2 * sum(len(r["sizes"]) + (r["widths"][-1] > r["sizes"][-1]) for r in self.runs)
+
+    def run_once(self, r):
+        cp = self.cp
+        r["lens"].zero_()
+        past = 0
+        for rr, w in zip(r["sizes"], r["widths"]):
+            sl = slice(past, past + w)
+            q, k, v = r["q"][None, sl], r["k"][None, sl], r["v"][None, sl]
+            if w > rr:
+                cp.cp_pad_chunk(self.desc, q, k, v, rr, w)
+            cp.cp_prefill_chunk(self.desc, q, k, v, r["kc"], r["vc"], r["lens"], w, rr, past, r["out"][None, sl],
+                                self.ws, dev_status=self.status)
+            past += rr
+
+    def step(self):
         for _ in range(2):
-            wl.step()
-    torch.cuda.current_stream().wait_stream(s)
+            for r in self.runs:
+                self.run_once(r)
+
+    def self_check(self, unpadded=None, n_sample=4, seed=13):
+        """Real rows bit-identical to an unpadded run of the same prompts; the
+        cache holds the prompt rows bit for bit and, after them, the pad rows
+        (copies of the last real row); seqlens_k = the real length; sampled rows
+        agree with ref_rows."""
+        torch = self.torch
+        torch.cuda.synchronize()
+        same, cache_ok, lens_ok, err, rows = True, True, True, 0.0, 0
+        g = torch.Generator().manual_seed(seed)
+        for i, r in enumerate(self.runs):
+            n = r["n"]
+            if unpadded is not None:
+                same = same and bits_equal(r["out"][:n], unpadded.runs[i]["out"][:n])
+            kc = r["kc"][0].transpose(0, 1)
+            cache_ok = cache_ok and bits_equal(kc[:n], r["k"][:n])
+            pad = r["widths"][-1] - r["sizes"][-1]
+            if pad:
+                cache_ok = cache_ok and bits_equal(kc[n:n + pad], r["k"][n - 1:n].expand(pad, -1, -1))
+            lens_ok = lens_ok and int(r["lens"].item()) == n
+            picks = {n - 1}
+            while len(picks) < n_sample:
+                picks.add(int(torch.randint(0, n, (1,), generator=g)))
+            for t in sorted(picks):
+                ref = ref_rows(r["q"][t], r["k"][:t + 1], r["v"][:t + 1], self.D ** -0.5)
+                err = max(err, float((r["out"][t].float() - ref).abs().max()))
+                rows += 1
+        status = int(self.status.item())
+        ok = same and cache_ok and lens_ok and status == 0 and err < BF16_TOL
+        return {"ok": ok, "real_rows_bit_identical_to_unpadded": same, "cache_bit_exact": cache_ok,
+                "seqlens_k_ok": lens_ok, "rows_checked": rows, "max_abs_err": err, "tol": BF16_TOL,
+                "status": status}
+
+    def config(self):
+        return {"workload": "ladder_gqa32x8_d128_bf16_chunk512_prompts1041-3788_x2",
+                "prompts": [r["n"] for r in self.runs], "last_widths": [r["widths"][-1] for r in self.runs],
+                "padded_rows_per_step": self.padded_rows, "l2": L2_NOTE, "cuda_graph": True}
+
+
+class MixedSchedule:
+    """The token-budget workload over a paged cache: 64 running decodes with
+    contexts U{512..8192} and 4 waiting prompts of 20000 tokens, 16-token pages
+    (seeded page permutation), GQA 32/8 x 128 bf16.  One step of this workload
+    is the whole schedule cp_schedule gives for `budget` (10 mixed steps at
+    8192, 41 at 2048), each one cp_mixed_step call; ``decode_only`` is instead
+    the 64 decode rows alone, one call."""
+
+    HQ, HKV, D = 32, 8, 128
+
+    def __init__(self, dev, budget=8192, decode_only=False):
+        import torch
+        import chunked_prefill_causal_cp_gb300 as cp
+        import synth_inputs as SI
+
+        self.cp, self.torch, self.dev = cp, torch, dev
+        self.budget, self.decode_only = budget, decode_only
+        mb = SI.mixed_batch()
+        self.mb = mb
+        bf = torch.bfloat16
+        self.desc = cp.layer_desc(bf, 0, self.HQ, self.HKV, self.D, cp.CP_CACHE_PAGED, page_size=mb.page_size,
+                                  num_pages=mb.num_pages, max_blocks=mb.max_blocks)
+        g = torch.Generator(device=dev).manual_seed(mb.seed)
+        self.kp = torch.randn(mb.num_pages, self.HKV, mb.page_size, self.D, generator=g, device=dev).to(bf)
+        self.vp = torch.randn(mb.num_pages, self.HKV, mb.page_size, self.D, generator=g, device=dev).to(bf)
+        nd = len(mb.decode_ctx)
+        pos = [c - 1 for c in mb.decode_ctx] + [0] * len(mb.prompt_lens)
+        if decode_only:
+            plan = [[(s, -1, 1) for s in range(nd)]]
+        else:
+            steps = {}
+            for st, seq, start, r in cp.cp_schedule(budget, nd, mb.prompt_lens):
+                steps.setdefault(st, []).append((seq, start, r))
+            plan = [steps[i] for i in sorted(steps)]
+        self.steps = []
+        row_seq, row_pos = [], []
+        off = 0
+        kv_row = self.HKV * self.D * 2
+        self.flops, self.decode_bytes, self.decode_rows, self.prefill_rows = 0, 0, 0, 0
+        for entries in plan:
+            seqs = [e[0] for e in entries]
+            rows = [e[2] for e in entries]
+            past = [pos[s] for s in seqs]
+            T = sum(rows)
+            st = dict(seqs=seqs, rows=rows, past=past, off=off, T=T, S=len(seqs),
+                      max_ctx=max(p + r for p, r in zip(past, rows)))
+            cu = [0]
+            for r in rows:
+                cu.append(cu[-1] + r)
+            st["cu"] = torch.tensor(cu, dtype=torch.int32, device=dev)
+            st["past0"] = torch.tensor(past, dtype=torch.int32, device=dev)
+            st["past_dev"] = st["past0"].clone()
+            st["bt"] = mb.block_table[seqs].contiguous().to(dev)
+            st["flops"] = sum(4 * self.D * self.HQ * visible_pairs(p, r) for p, r in zip(past, rows))
+            st["bytes"] = sum((p + 1) * kv_row * 2 + self.HQ * self.D * 2 * 2 + kv_row * 2
+                              for p, r in zip(past, rows) if r == 1)
+            self.flops += st["flops"]
+            self.decode_bytes += st["bytes"]
+            self.decode_rows += sum(1 for r in rows if r == 1)
+            self.prefill_rows += sum(r for r in rows if r > 1)
+            for s, p, r in zip(seqs, past, rows):
+                row_seq += [s] * r
+                row_pos += list(range(p, p + r))
+                pos[s] = p + r
+            off += T
+            self.steps.append(st)
+        self.R = off
+        self.row_seq = torch.tensor(row_seq, dtype=torch.long)
+        self.row_pos = torch.tensor(row_pos, dtype=torch.long)
+        self.q = torch.randn(self.R, self.HQ, self.D, generator=g, device=dev).to(bf)
+        self.kn = torch.randn(self.R, self.HKV, self.D, generator=g, device=dev).to(bf)
+        self.vn = torch.randn(self.R, self.HKV, self.D, generator=g, device=dev).to(bf)
+        self.out = torch.zeros(self.R, self.HQ, self.D, dtype=bf, device=dev)
+        self.status = torch.zeros(1, dtype=torch.int32, device=dev)
+        ws = max(cp.cp_workspace_size(self.desc, st["T"], st["max_ctx"], st["S"]) for st in self.steps)
+        self.ws = torch.zeros(max(ws, 16), dtype=torch.uint8, device=dev)
+        # launches per cp_mixed_step: append, decode split + combine (when decode rows), tensor-core
+        # prefill (when chunks), commit
+        self.launches = sum(2 + 2 * any(r == 1 for r in st["rows"]) + any(r > 1 for r in st["rows"])
+                            for st in self.steps)
+        self.tokens = self.R
+
+    def step(self):
+        cp = self.cp
+        for st in self.steps:
+            st["past_dev"].copy_(st["past0"])
+        for st in self.steps:
+            sl = slice(st["off"], st["off"] + st["T"])
+            cp.cp_mixed_step(self.desc, self.q[sl], self.kn[sl], self.vn[sl], self.kp, self.vp, st["bt"],
+                             st["cu"], st["past_dev"], st["S"], st["T"], st["max_ctx"], self.out[sl], self.ws,
+                             dev_status=self.status)
+
+    def self_check(self, n_sample=24, seed=17):
+        """Every row's K/V lands in its page slot bit for bit (page =
+        block_table[seq][pos / 16], offset pos mod 16); past lengths advance by
+        the rows; sampled decode and prefill rows agree with ref_rows over the
+        sequence's positions [0, pos] gathered from the pools."""
+        torch = self.torch
+        torch.cuda.synchronize()
+        P = self.mb.page_size
+        table = self.mb.block_table.to(self.dev).long()
+        seq = self.row_seq.to(self.dev)
+        pos = self.row_pos.to(self.dev)
+        page = table[seq, pos // P]
+        slot = pos % P
+        kv_ok = bits_equal(self.kp[page, :, slot], self.kn) and bits_equal(self.vp[page, :, slot], self.vn)
+        past_ok = all(st["past_dev"].tolist() == [p + r for p, r in zip(st["past"], st["rows"])]
+                      for st in self.steps)
+        g = torch.Generator().manual_seed(seed)
+        picks = {0, self.R - 1}
+        while len(picks) < n_sample:
+            picks.add(int(torch.randint(0, self.R, (1,), generator=g)))
+        err = 0.0
+        for i in sorted(picks):
+            s, p = int(self.row_seq[i]), int(self.row_pos[i])
+            a = torch.arange(p + 1, device=self.dev)
+            pg = table[s, a // P]
+            keys = self.kp[pg, :, a % P]
+            vals = self.vp[pg, :, a % P]
+            ref = ref_rows(self.q[i], keys, vals, self.D ** -0.5)
+            err = max(err, float((self.out[i].float() - ref).abs().max()))
+        status = int(self.status.item())
+        ok = kv_ok and past_ok and status == 0 and err < BF16_TOL
+        return {"ok": ok, "pages_bit_exact": kv_ok, "past_len_ok": past_ok, "rows_checked": len(picks),
+                "max_abs_err": err, "tol": BF16_TOL, "status": status}
+
+    def config(self):
+        name = "decode64" if self.decode_only else f"mixed_budget{self.budget}"
+        return {"workload": f"paged_{name}_gqa32x8_d128_bf16_page16",
+                "schedule_steps": len(self.steps), "rows_per_schedule": self.R,
+                "decode_rows": self.decode_rows, "prefill_rows": self.prefill_rows,
+                "decode_ctx_mean": sum(self.mb.decode_ctx) / len(self.mb.decode_ctx),
+                "prompts": self.mb.prompt_lens, "page_size": self.mb.page_size, "l2": L2_NOTE,
+                "cuda_graph": True}
+
+
+# --------------------------------------------------------------------------- measurement
+
+def measure(wl, graph, flush, reps, warmup, torch, check_kw=None):
+    """Warm-up replays, the workload's own check (a failure ends the run), then
+    `reps` timed replays with L2 flushed between.  Returns (mean ms, check)."""
+    for _ in range(max(warmup, 3)):
+        graph.replay()
     torch.cuda.synchronize()
-    g = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g):
-        wl.step()
+    check = require(wl.self_check(**(check_kw or {})), type(wl).__name__)
+    times = time_steps(graph.replay, flush, reps, torch)
+    return sum(times) / len(times), check
+
+
+def other_configs(dev, flush, pk, reps, warmup):
+    """One measurement of each other workload, each checked before it is timed."""
+    import torch
+    tc, hbm = float(pk["bf16_tflops"]), float(pk["hbm_gbs"])
+    res = {}
+
+    wl = ChunkLoop(dev, "fp32")
+    ms, chk = measure(wl, capture(wl.step, dev), flush, reps, warmup, torch)
+    res["fp32_example"] = {**wl.config(), "tokens_per_s": wl.tokens / (ms / 1e3), "ms_per_step": ms,
+                           "tflops": wl.flops / (ms / 1e3) / 1e12, "dtype": "f32", "check": chk,
+                           "gpu_launches_per_step": wl.launches}
+    del wl
+
+    unp = LadderRuns(dev, pad=False)
+    g_unp = capture(unp.step, dev)
+    g_unp.replay()
+    wl = LadderRuns(dev, pad=True)
+    ms, chk = measure(wl, capture(wl.step, dev), flush, reps, warmup, torch, {"unpadded": unp})
+    res["padding_ladder"] = {**wl.config(), "tokens_per_s": wl.tokens / (ms / 1e3), "ms_per_step": ms,
+                             "tflops_real_rows": wl.flops / (ms / 1e3) / 1e12,
+                             "tensor_frac_whole_step": wl.flops / (ms / 1e3) / 1e12 / tc, "dtype": "bf16",
+                             "check": chk, "gpu_launches_per_step": wl.launches}
+    del wl, unp, g_unp
+
+    wl = ChunkLoop(dev, "rolling")
+    ms, chk = measure(wl, capture(wl.step, dev), flush, reps, warmup, torch)
+    res["rolling"] = {**wl.config(), "tokens_per_s": wl.tokens / (ms / 1e3), "ms_per_step": ms,
+                      "tflops": wl.flops / (ms / 1e3) / 1e12,
+                      "tensor_frac_whole_step": wl.flops / (ms / 1e3) / 1e12 / tc, "dtype": "f16",
+                      "check": chk, "gpu_launches_per_step": wl.launches}
+    del wl
+
+    wl = MixedSchedule(dev, decode_only=True)
+    ms, chk = measure(wl, capture(wl.step, dev), flush, reps, warmup, torch)
+    gbs = wl.decode_bytes / (ms / 1e3) / 1e9
+    res["decode"] = {**wl.config(), "rows_per_s": wl.tokens / (ms / 1e3), "ms_per_step": ms,
+                     "decode_bytes_per_step": wl.decode_bytes, "gbs_whole_step": gbs, "hbm_frac_whole_step": gbs / hbm,
+                     "traffic": kernel_traffic("decode_split_paged.json"),
+                     "scope": ("K/V, q and out bytes of the 64 decode rows over the whole cp_mixed_step call "
+                               "(append, split-KV kernel, combine, commit): a lower bound on the kernel's rate"),
+                     "dtype": "bf16", "check": chk, "gpu_launches_per_step": wl.launches}
+    del wl
+
+    for budget in (8192, 2048):
+        wl = MixedSchedule(dev, budget=budget)
+        ms, chk = measure(wl, capture(wl.step, dev), flush, max(3, reps // 4), warmup, torch)
+        t_star = sum(max(st["flops"] / (tc * 1e12), st["bytes"] / (hbm * 1e9)) for st in wl.steps) * 1e3
+        res[f"mixed_budget{budget}"] = {
+            **wl.config(), "rows_per_s": wl.tokens / (ms / 1e3), "ms_per_schedule": ms,
+            "flops_per_schedule": wl.flops, "decode_bytes_per_schedule": wl.decode_bytes,
+            "roofline_time_ms": t_star, "roofline_frac": t_star / ms, "dtype": "bf16", "check": chk,
+            "gpu_launches_per_step": wl.launches}
+        del wl
+    torch.cuda.synchronize()
+    return res
+
+
+def run_native(args):
+    import torch
+    rank, world, local = dist_init(args.gpus)
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    from chunked_prefill_causal_cp_gb300 import _build
+    if rank == 0 or world == 1:
+        _build.build()
+    barrier(world)
+    import chunked_prefill_causal_cp_gb300 as cp
+    cp.lib()
+    pk, pk_src = peaks()
+    if args.workload != "gqa_prefill":
+        return run_single(args, rank, world, dev, pk, pk_src)
+
+    wl = GqaPrefill(dev, pad=not args.no_pad, N=args.prompt, W=args.chunk)
+    wl.capture()
     flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
     for _ in range(max(args.warmup, 3)):
-        g.replay()
+        wl.graph.replay()
     torch.cuda.synchronize()
-    clocks = ClockSampler()
+    check = require(wl.self_check(), "gqa_prefill")
+
+    bus = None
+    try:
+        bus = torch.cuda.get_device_properties(dev).pci_bus_id
+    except AttributeError:
+        pass
+    clocks = ClockSampler(bus)
+    barrier(world)
+    torch.cuda.synchronize()
     clocks.start()
-    times = time_steps(g.replay, flush, args.steps, torch)
+    # the clock record starts under the same load: replays of the step for about half a second
+    t_end = time.perf_counter() + 0.5
+    while time.perf_counter() < t_end:
+        for _ in range(50):
+            flush.zero_()
+            wl.graph.replay()
+        torch.cuda.synchronize()
+    times = time_steps(wl.graph.replay, flush, args.steps, torch)
     clk = clocks.stop()
+    torch.cuda.synchronize()
+    barrier(world)
     total_ms, value = job_throughput(sum(times), wl.tokens, args.steps, world)
-    ms = total_ms / args.steps
+    ms_per_step = total_ms / args.steps
     if int(wl.status.item()) != 0:
-        raise RuntimeError(f"device status {int(wl.status.item())}")
-    tflops = wl.flops / (ms / 1e3) / 1e12
-    fp32 = args.workload == "fp32"
-    line = {"metric": f"{args.workload} chunked-prefill tokens/s (real rows)", "value": value, "unit": "tokens/s",
-            "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32" if fp32 else "f16",
-            "data": "synthetic", "config": wl.config(), "flops_per_step": wl.flops, "tflops_whole_step": tflops,
-            "tensor_frac_whole_step": None if fp32 else tflops / float(pk["bf16_tflops"]),
-            "gpu_launches": wl.launches * args.steps, "clocks": clk, "peaks": pk_src}
+        raise CheckFailed(f"device status {int(wl.status.item())} after the timed steps")
+
+    # ---- in-situ time of the attention launches: prefix graphs of the same launch chain
+    wl.capture_prefixes()
+    reps = max(20, min(args.steps, 200))
+    n = len(wl.sizes)
+    acc = [0.0] * (n + 1)
+    for _ in range(reps):
+        for k in range(n + 1):
+            t = time_steps(wl.prefix_graphs[k].replay, flush, 1, torch)[0]
+            acc[k] += t / reps
+    attn_ms = acc[n] - acc[0]
+    per_chunk_us = [round((acc[k + 1] - acc[k]) * 1e3, 2) for k in range(n)]
+    attn_tflops = wl.flops / (attn_ms / 1e3) / 1e12
+    peak = float(pk["bf16_tflops"])
+    traffic = kernel_traffic("attn_tc_gqa_prefill.json")
+
+    # ---- end to end: host buffers in, result out, through the captured public calls
+    wl.pin()
+    e2e_steps = max(20, min(args.steps // 10, 300))
+    wl.capture_e2e()
+    for _ in range(3):
+        wl.e2e_graph.replay()
+    torch.cuda.synchronize()
+    e2e_times = time_steps(wl.e2e_graph.replay, flush, e2e_steps, torch)
+    _, e2e_value = job_throughput(sum(e2e_times), wl.tokens, e2e_steps, world)
+    e2e_ok = bits_equal(wl.ho, wl.out[:wl.N].cpu())
+    if int(wl.status.item()) != 0 or not e2e_ok:
+        raise CheckFailed("end-to-end graph: device status set or host output differs from the device rows")
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded N(0,1) q/k/v)",
+        "config": wl.config(),
+        "effective_tflops": wl.flops * args.steps * world / (total_ms / 1e3) / 1e12,
+        "flops_per_step": wl.flops,
+        "check": check,
+        "roofline": {"bound": "tensor", "achieved": attn_tflops, "peak": peak, "unit": "TFLOP/s",
+                     "frac": attn_tflops / peak, "traffic": traffic, "kernel": "attn_tc_kernel",
+                     "peak_source": f"{pk_src} bf16_tflops (burst)",
+                     "frac_of_sustained": attn_tflops / float(pk.get("bf16_tflops_sustained", peak)),
+                     "attention_ms_per_step": attn_ms, "launches_per_step": n,
+                     "per_chunk_us": per_chunk_us,
+                     "per_chunk_tflops": [round(f / (t / 1e6) / 1e12, 1) if t > 0 else None
+                                          for f, t in zip(wl.flops_chunk, per_chunk_us)],
+                     "kernel_timing": ("in situ: CUDA events around graphs of the first k chunk calls of the "
+                                       "step (k = 0..n, the same launch chain without the pad launch), L2 "
+                                       f"flushed before each, mean of {reps}; attention = T(n) - T(0), "
+                                       "chunk k = T(k+1) - T(k)"),
+                     "traffic_note": "mean DRAM bytes per launch over the step's chunk launches (ncu)"},
+        "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": wl.h2d,
+                "d2h_bytes_per_step": wl.d2h,
+                "path": ("one captured graph per step of the public calls with its host traffic: all chunks' "
+                         "q/k/v rows pinned host -> device queued in chunk order on a copy stream, each chunk's "
+                         "call waiting for its own rows, and its output rows device -> pinned host on a second "
+                         "copy stream once it is done")},
+        "gpu_launches": wl.launches * args.steps,
+        "clocks": clk,
+    }
+    if rank == 0 and world == 1 and not args.no_extras:
+        line["configs"] = other_configs(dev, flush, pk, max(10, min(args.steps, 50)), args.warmup)
+    if rank == 0 and world == 1 and not args.skip_cpu:
+        v_cpu, sample, _, diff, heads = wl.cpu_sample(args.cpu_seconds)
+        if not diff < BF16_TOL:
+            raise CheckFailed(f"GPU output differs from the oracle by {diff} on the sampled heads")
+        line["cpu_baseline"] = {"value": v_cpu, "unit": "tokens/s", "cores": cpu_cores(), "kind": "oracle",
+                                "sample": sample,
+                                "parity": {"max_abs_err_vs_gpu": diff, "tol": BF16_TOL, "query_heads": heads,
+                                           "rows": wl.N}}
     if rank == 0:
         print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
 
 
-def run_paged(args, rank, world, dev, pk, pk_src):
+def run_single(args, rank, world, dev, pk, pk_src):
+    """One line for one of the other workloads."""
     import torch
-    wl = PagedStep(dev, args.workload)
-    s = torch.cuda.Stream(dev)
-    s.wait_stream(torch.cuda.current_stream())
-    with torch.cuda.stream(s):
-        for _ in range(2):
-            wl.step()
-    torch.cuda.current_stream().wait_stream(s)
-    torch.cuda.synchronize()
-    g = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g):
-        wl.step()
+    tc, hbm = float(pk["bf16_tflops"]), float(pk["hbm_gbs"])
     flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    kw = None
+    if args.workload in ("fp32", "rolling"):
+        wl = ChunkLoop(dev, args.workload)
+    elif args.workload == "ladder":
+        unp = LadderRuns(dev, pad=False)
+        capture(unp.step, dev).replay()
+        kw = {"unpadded": unp}
+        wl = LadderRuns(dev, pad=not args.no_pad)
+    else:
+        wl = MixedSchedule(dev, budget=args.budget, decode_only=args.workload == "decode")
+    g = capture(wl.step, dev)
     for _ in range(max(args.warmup, 3)):
         g.replay()
     torch.cuda.synchronize()
+    check = require(wl.self_check(**(kw or {})), args.workload)
     clocks = ClockSampler()
     clocks.start()
     times = time_steps(g.replay, flush, args.steps, torch)
@@ -703,31 +1062,29 @@ def run_paged(args, rank, world, dev, pk, pk_src):
     total_ms = max_over_ranks(sum(times), world)
     ms = total_ms / args.steps
     if int(wl.status.item()) != 0:
-        raise RuntimeError(f"device status {int(wl.status.item())}")
-    hbm = float(pk["hbm_gbs"])
-    tc = float(pk["bf16_tflops"])
-    line = {"metric": f"{args.workload} step rows/s (paged KV, 16-token pages)",
-            "value": world * wl.T * args.steps / (total_ms / 1e3), "unit": "rows/s", "n_gpus": world,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": {"workload": f"paged_{args.workload}_gqa32x8_d128_bf16", "decode_rows": sum(
-                1 for r in wl.rows if r == 1), "prefill_rows": sum(r for r in wl.rows if r > 1),
-                "decode_ctx_mean": sum(wl.mb.decode_ctx) / len(wl.mb.decode_ctx), "page_size": wl.mb.page_size,
-                "l2": "flushed between timed steps (512 MiB write)", "cuda_graph": True},
-            "decode_bytes_per_step": wl.decode_bytes, "flops_per_step": wl.flops,
-            "roofline": ({"bound": "hbm", "achieved": wl.decode_bytes / (ms / 1e3) / 1e9, "peak": hbm,
-                          "unit": "GB/s", "frac": wl.decode_bytes / (ms / 1e3) / 1e9 / hbm,
-                          "traffic": kernel_traffic("decode.cu", "decode_split_paged.md"),
-                          "kernel": "decode_split_kernel",
-                          "scope": "K/V bytes of the decode rows over the whole step (append, split-KV "
-                                   "kernel, combine, commit): a lower bound on the kernel's own rate",
-                          "peak_source": "measured hbm_gbs (copy)"}
-                         if args.workload == "decode" else None),
-            "decode_gbs_whole_step": wl.decode_bytes / (ms / 1e3) / 1e9,
-            "hbm_frac_whole_step": wl.decode_bytes / (ms / 1e3) / 1e9 / hbm,
-            "tflops_whole_step": wl.flops / (ms / 1e3) / 1e12,
-            "roofline_time_us": max(wl.flops / (tc * 1e12), wl.decode_bytes / (hbm * 1e9)) * 1e6,
-            "gpu_launches": wl.launches * args.steps, "clocks": clk, "peaks": pk_src}
+        raise CheckFailed(f"device status {int(wl.status.item())} after the timed steps")
+    units = wl.tokens
+    line = {"metric": f"{args.workload} tokens/s", "value": world * units * args.steps / (total_ms / 1e3),
+            "unit": "tokens/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "data": "synthetic",
+            "config": wl.config(), "flops_per_step": wl.flops, "tflops_whole_step": wl.flops / (ms / 1e3) / 1e12,
+            "check": check, "gpu_launches": wl.launches * args.steps, "clocks": clk, "peaks": pk_src}
+    if args.workload == "fp32":
+        line["dtype"] = "f32"
+    else:
+        line["dtype"] = "f16" if args.workload == "rolling" else "bf16"
+        line["tensor_frac_whole_step"] = wl.flops / (ms / 1e3) / 1e12 / tc
+    if args.workload == "decode":
+        gbs = wl.decode_bytes / (ms / 1e3) / 1e9
+        line["roofline"] = {"bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s", "frac": gbs / hbm,
+                            "traffic": kernel_traffic("decode_split_paged.json"), "kernel": "decode_split_kernel",
+                            "scope": "decode rows' bytes over the whole call: a lower bound on the kernel's rate"}
+    if args.workload == "mixed":
+        t_star = sum(max(st["flops"] / (tc * 1e12), st["bytes"] / (hbm * 1e9)) for st in wl.steps) * 1e3
+        line["roofline_time_ms"] = t_star
+        line["roofline_frac"] = t_star / ms
+    if args.workload == "ladder":
+        line["padded_rows_per_step"] = wl.padded_rows
     if rank == 0:
         print(json.dumps(line), flush=True)
 
@@ -737,33 +1094,32 @@ def run_reference(args):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return
-    import numpy as np
     import oracle
     import synth_inputs as SI
-    wl = GqaPrefill.__new__(GqaPrefill)
-    q, k, v = SI.gqa_prompt(GqaPrefill.N, seed=1)
+    N, W, HQ, HKV = 4000, 512, GqaPrefill.HQ, GqaPrefill.HKV
+    q, k, v = SI.gqa_prompt(N, seed=1)
     qn, kn, vn = (t.double().numpy() for t in (q, k, v))
-    G = GqaPrefill.HQ // GqaPrefill.HKV
-    sizes = oracle.chunk_plan(GqaPrefill.N, GqaPrefill.W)
+    G = HQ // HKV
+    sizes = oracle.chunk_plan(N, W)
 
     def one_group(g):
-        oracle.chunked_prefill(qn[:, g * G:(g + 1) * G], kn[:, g:g + 1], vn[:, g:g + 1], GqaPrefill.W)
+        oracle.chunked_prefill(qn[:, g * G:(g + 1) * G], kn[:, g:g + 1], vn[:, g:g + 1], W)
 
     for i in range(args.warmup):
-        one_group(i % GqaPrefill.HKV)
+        one_group(i % HKV)
     times = []
     t_budget = 150.0
     t_start = time.perf_counter()
     for i in range(args.steps):
         t0 = time.perf_counter()
-        one_group(i % GqaPrefill.HKV)
+        one_group(i % HKV)
         times.append(time.perf_counter() - t0)
         if time.perf_counter() - t_start > t_budget:
             break
     per_group = sum(times) / len(times)
-    value = GqaPrefill.N / (per_group * GqaPrefill.HKV)
+    value = N / (per_group * HKV)
     sample = (f"each step: oracle.chunked_prefill of the 4000-token prompt (chunks {sizes}) for one KV-head "
-              f"group ({G} of {GqaPrefill.HQ} query heads); tokens/s scaled to all {GqaPrefill.HKV} groups; "
+              f"group ({G} of {HQ} query heads); tokens/s scaled to all {HKV} groups; "
               f"{len(times)} of {args.steps} requested steps timed within a {t_budget:.0f} s budget")
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
             "steps": len(times), "steps_requested": args.steps, "warmup": args.warmup,

@@ -1,8 +1,9 @@
 """bench.py's host-side bookkeeping, on the CPU: the DRAM-traffic figure is
-taken from a committed profile summary only while the kernel source it was
+taken from a committed JSON record only while the kernel source it was
 measured on is unchanged, and the visible-pair counts behind the FLOP totals
 match brute force."""
 import hashlib
+import json
 import os
 
 import numpy as np
@@ -18,22 +19,25 @@ def test_traffic_follows_the_profiled_source(tmp_path, monkeypatch):
     src = csrc / "kern.cu"
     src.write_text("// kernel v1\n")
     sha = hashlib.sha256(src.read_bytes()).hexdigest()
-    (prof / "kern.md").write_text(f"# kern\n\nsource_sha256: {sha} (kern.cu)\ndram_bytes_per_launch: 12345\n")
+    (prof / "kern.json").write_text(json.dumps({"kernel_source": "kern.cu", "source_sha256": sha,
+                                                "dram_bytes_per_launch": 12345}))
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
-    assert bench.kernel_traffic("kern.cu", "kern.md") == 12345.0
+    assert bench.kernel_traffic("kern.json") == 12345.0
     src.write_text("// kernel v2\n")  # the kernel changed since the capture
-    assert bench.kernel_traffic("kern.cu", "kern.md") is None
-    assert bench.kernel_traffic("kern.cu", "missing.md") is None
+    assert bench.kernel_traffic("kern.json") is None
+    assert bench.kernel_traffic("missing.json") is None
 
 
 def test_committed_profiles_name_current_sources():
-    """Every committed summary that carries a traffic figure names a source
-    file that exists, and the figure is read back for it."""
+    """Every committed traffic record names a kernel source that exists and
+    carries a positive byte count."""
     root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-    for name, src in (("attn_tc_gqa_prefill.md", "attn_tc.cu"), ("decode_split_paged.md", "decode.cu")):
-        text = open(os.path.join(root, "profiles", name)).read()
-        assert "source_sha256:" in text and "dram_bytes_per_launch:" in text
-        assert os.path.exists(os.path.join(root, "chunked_prefill_causal_cp_gb300", "csrc", src))
+    names = [n for n in os.listdir(os.path.join(root, "profiles")) if n.endswith(".json")]
+    assert "decode_split_paged.json" in names
+    for name in names:
+        rec = json.load(open(os.path.join(root, "profiles", name)))
+        assert len(rec["source_sha256"]) == 64 and rec["dram_bytes_per_launch"] > 0
+        assert os.path.exists(os.path.join(root, "chunked_prefill_causal_cp_gb300", "csrc", rec["kernel_source"]))
 
 
 def test_visible_pairs_brute_force():

@@ -69,31 +69,40 @@ def _schedule_steps(budget, n_dec, prompts):
     return [steps[i] for i in sorted(steps)]
 
 
-def test_mixed_steps_reduced_full_check():
-    """8 decodes with contexts at page and split edges plus 2 prompts, budget
-    256: every step's every row matches the oracle's mixed step, the pools
-    match the oracle's bit for bit, and past lengths advance by the rows."""
-    ctx = [1, 2, 16, 17, 511, 512, 513, 700]
-    prompts = [600, 450]
-    mb = SI.mixed_batch(n_decode=len(ctx), ctx_lo=1, ctx_hi=2, n_prompt=2, prompt_len=600, decode_tail=64, seed=21)
-    mb.decode_ctx = ctx
-    need = [-(-(n + 64) // PAGE) for n in ctx + prompts]
+def _layout(ctx, prompts, seed):
+    """A MixedBatch for the given decode contexts and prompt lengths, pages from a seeded permutation."""
+    mb = SI.mixed_batch(n_decode=len(ctx), ctx_lo=1, ctx_hi=2, n_prompt=len(prompts), prompt_len=prompts[0],
+                        decode_tail=64, seed=seed)
+    mb.decode_ctx = list(ctx)
+    mb.prompt_lens = list(prompts)
+    need = [-(-(n + 64) // PAGE) for n in list(ctx) + list(prompts)]
     mb.max_blocks = max(need)
     mb.num_pages = sum(need)
-    g = torch.Generator().manual_seed(21)
-    perm = torch.randperm(mb.num_pages, generator=g)
+    perm = torch.randperm(mb.num_pages, generator=torch.Generator().manual_seed(seed))
     mb.block_table = torch.full((len(need), mb.max_blocks), -1, dtype=torch.int32)
     off = 0
     for s, nb in enumerate(need):
         mb.block_table[s, :nb] = perm[off:off + nb].to(torch.int32)
         off += nb
+    return mb
+
+
+def _run_schedule(budget, ctx, prompts, seed):
+    """Every step cp_schedule gives for `budget`, on the GPU and in the oracle:
+    each step's every row within tolerance, past lengths advanced by the rows,
+    and at the end the pools equal the oracle's bit for bit (slots never
+    written stay NaN).  Returns the number of steps."""
+    mb = _layout(ctx, prompts, seed)
     P = Paged(mb)
-    pos = [c - 1 for c in ctx] + [0, 0]
+    pos = [c - 1 for c in ctx] + [0] * len(prompts)
     for s, c in enumerate(ctx):
-        P.prefill_history(s, SI.normal((c - 1, HKV, D), 100 + s), SI.normal((c - 1, HKV, D), 200 + s))
+        if c > 1:
+            P.prefill_history(s, SI.normal((c - 1, HKV, D), 100 + s), SI.normal((c - 1, HKV, D), 200 + s))
     pq = [SI.gqa_prompt(n, seed=30 + i) for i, n in enumerate(prompts)]
     nd = len(ctx)
-    for si, entries in enumerate(_schedule_steps(256, nd, prompts)):
+    plan = _schedule_steps(budget, nd, prompts)
+    for si, entries in enumerate(plan):
+        assert sum(r for _, _, r in entries) <= budget
         seqs, rows, qs, ks, vs = [], [], [], [], []
         for seq, start, r in entries:
             seqs.append(seq)
@@ -117,10 +126,27 @@ def test_mixed_steps_reduced_full_check():
         for s, p in zip(seqs, newp):
             pos[s] = p
     assert int(P.status.item()) == 0
-    got_k = f64(P.k)
-    mask = ~np.isnan(P.ok)
-    assert np.array_equal(got_k[mask], P.ok[mask])
-    assert np.isnan(got_k[~mask]).all()
+    for got, want in ((f64(P.k), P.ok), (f64(P.v), P.ov)):
+        mask = ~np.isnan(want)
+        assert np.array_equal(got[mask], want[mask])
+        assert np.isnan(got[~mask]).all()
+    assert all(pos[nd + i] >= n for i, n in enumerate(prompts))  # every prompt was scheduled in full
+    return len(plan)
+
+
+def test_mixed_steps_reduced_full_check():
+    """8 decodes with contexts at page and split edges plus 2 prompts, budget 256."""
+    n = _run_schedule(256, [1, 2, 16, 17, 511, 512, 513, 700], [600, 450], seed=21)
+    assert n >= 5
+
+
+def test_mixed_schedule_budget_2048():
+    """The budget-2048 schedule of the mixed workload at reduced sizes: 64
+    running decodes (contexts U{1..600}) and 4 prompts of 1500 tokens; every
+    step of the whole schedule is checked row by row, then the pools."""
+    ctx = torch.randint(1, 601, (64,), generator=torch.Generator().manual_seed(23)).tolist()
+    n = _run_schedule(2048, ctx, [1500] * 4, seed=23)
+    assert n == 4  # 6000 prompt tokens at 2048 - 64 per step
 
 
 def test_mixed_step_batch_invariance():
