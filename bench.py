@@ -26,8 +26,8 @@ the other workloads of the problem statement (fp32 example, padding ladder,
 rolling cache, decode rows, and the whole mixed token-budget schedule at
 budgets 8192 and 2048), each with its own check.  ``--workload X`` prints X's
 line alone; ``--chunk`` / ``--budget`` sweep the chunk width and the token
-budget.  ``--impl reference`` times the CPU oracle (test infrastructure,
-float64) on a bounded sample of the default workload instead.
+budget.  ``--impl reference`` times the C++ CPU oracle (test infrastructure,
+float64, std::thread) on a bounded sample of the default workload instead.
 """
 from __future__ import annotations
 
@@ -471,12 +471,14 @@ class GqaPrefill:
         return g
 
     def cpu_sample(self, budget_s):
-        """Oracle (as it stands) on whole KV-head groups of the same prompt until
-        the time budget is spent; returns (tokens/s scaled to all heads, sample,
-        seconds, max-abs difference between the oracle's rows and this
-        workload's last GPU output for the groups it ran)."""
+        """The C++ oracle (as it stands, std::thread on every host core) on
+        whole KV-head groups of the same prompt until the time budget is spent.
+        Returns (tokens/s scaled to all heads, sample, seconds, max-abs
+        difference between the oracle's rows and this workload's last GPU
+        output for the groups it ran, query heads compared, threads)."""
         import numpy as np
-        import oracle
+        from oracle import cpp as oracle
+        oracle.set_threads(0)
         q = self.host_q.double().numpy()
         k = self.host_k.double().numpy()
         v = self.host_v.double().numpy()
@@ -494,10 +496,26 @@ class GqaPrefill:
                 break
         t = time.perf_counter() - t0
         full = t * self.HKV / groups
-        sample = (f"oracle.chunked_prefill of the {self.N}-token prompt (chunks {self.sizes[0]}x"
+        sample = (f"C++ oracle chunked_prefill of the {self.N}-token prompt (chunks {self.sizes[0]}x"
                   f"{len(self.sizes) - 1}+{self.sizes[-1]}, unpadded) for {groups} of {self.HKV} KV-head "
                   f"groups ({groups * G} of {self.HQ} query heads), {t:.1f} s, scaled to all heads")
-        return self.N / full, sample, t, diff, groups * G
+        return self.N / full, sample, t, diff, groups * G, oracle.threads()
+
+
+def oracle_single_thread_fp32():
+    """The C++ oracle on one thread over the fp32 example (1000 tokens, 8 heads
+    x 64, chunks of 256): tokens/s and seconds."""
+    from oracle import cpp as oracle
+    import synth_inputs as SI
+    q, k, v = (t.double().numpy() for t in SI.fp32_sdpa_example())
+    oracle.set_threads(1)
+    try:
+        t0 = time.perf_counter()
+        oracle.chunked_prefill(q, k, v, 256)
+        t = time.perf_counter() - t0
+    finally:
+        oracle.set_threads(0)
+    return q.shape[0] / t, t
 
 
 class ChunkLoop:
@@ -1021,13 +1039,16 @@ def run_native(args):
     if rank == 0 and world == 1 and not args.no_extras:
         line["configs"] = other_configs(dev, flush, pk, max(10, min(args.steps, 50)), args.warmup)
     if rank == 0 and world == 1 and not args.skip_cpu:
-        v_cpu, sample, _, diff, heads = wl.cpu_sample(args.cpu_seconds)
+        v_cpu, sample, _, diff, heads, threads = wl.cpu_sample(args.cpu_seconds)
         if not diff < BF16_TOL:
             raise CheckFailed(f"GPU output differs from the oracle by {diff} on the sampled heads")
-        line["cpu_baseline"] = {"value": v_cpu, "unit": "tokens/s", "cores": cpu_cores(), "kind": "oracle",
-                                "sample": sample,
+        v1, t1 = oracle_single_thread_fp32()
+        line["cpu_baseline"] = {"value": v_cpu, "unit": "tokens/s", "cores": threads,
+                                "kind": "oracle (C++ fp64, std::thread)", "sample": sample,
                                 "parity": {"max_abs_err_vs_gpu": diff, "tol": BF16_TOL, "query_heads": heads,
-                                           "rows": wl.N}}
+                                           "rows": wl.N},
+                                "single_thread_fp32_example": {"tokens_per_s": v1, "seconds": t1, "cores": 1,
+                                                               "workload": "fp32_mha8_d64_prompt1000_chunk256"}}
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
@@ -1090,13 +1111,18 @@ def run_single(args, rank, world, dev, pk, pk_src):
 
 
 def run_reference(args):
-    """The CPU oracle as the reference arm (rank 0 only)."""
+    """The C++ CPU oracle as the reference arm (rank 0 only): each step is one
+    KV-head group of the default workload (its 4 query heads over the whole
+    4000-token prompt in chunks of 512), threaded over every host core;
+    tokens/s is scaled to all 8 groups."""
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return
-    import oracle
+    from oracle import cpp as oracle
     import synth_inputs as SI
     N, W, HQ, HKV = 4000, 512, GqaPrefill.HQ, GqaPrefill.HKV
+    oracle.build()
+    oracle.set_threads(0)
     q, k, v = SI.gqa_prompt(N, seed=1)
     qn, kn, vn = (t.double().numpy() for t in (q, k, v))
     G = HQ // HKV
@@ -1118,7 +1144,7 @@ def run_reference(args):
             break
     per_group = sum(times) / len(times)
     value = N / (per_group * HKV)
-    sample = (f"each step: oracle.chunked_prefill of the 4000-token prompt (chunks {sizes}) for one KV-head "
+    sample = (f"each step: C++ oracle chunked_prefill of the 4000-token prompt (chunks {sizes}) for one KV-head "
               f"group ({G} of {HQ} query heads); tokens/s scaled to all {HKV} groups; "
               f"{len(times)} of {args.steps} requested steps timed within a {t_budget:.0f} s budget")
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
@@ -1127,8 +1153,8 @@ def run_reference(args):
             "dtype": "f64", "data": "synthetic (seeded N(0,1) q/k/v)",
             "config": {"workload": "gqa32x8_d128_bf16_prompt4000_chunk512_cap8192", "prompt_tokens": 4000,
                        "chunk": 512, "kv_capacity": 8192, "heads_q": 32, "heads_kv": 8, "head_dim": 128},
-            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cpu_cores(), "kind": "oracle",
-                             "sample": sample},
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": oracle.threads(),
+                             "kind": "oracle (C++ fp64, std::thread)", "sample": sample},
             "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 

@@ -394,6 +394,28 @@ def pin_paged_round_trip():
         assert np.all(np.isnan(pool[unused]))
 
 
+def pin_paged_coordinates():
+    """Each token lands at the (page id, slot) worked out by hand for a
+    scattered block table (tests/golden/paged_layout.json), pages not in the
+    table stay untouched, and the last, partly filled page has only its first
+    slot written."""
+    g = _golden("paged_layout.json")
+    page, hkv, d = g["page"], 2, 3
+    pool = np.full((g["num_pages"], hkv, page, d), np.nan)
+    table = np.array(g["table"], np.int32)
+    for a in range(g["n_tokens"]):
+        O.paged_write(pool, table, a, np.full((hkv, d), float(a + 1)))
+    for a, pid, slot in g["tokens"]:
+        assert np.all(pool[pid, :, slot] == a + 1), (a, pid, slot)
+    for pid in g["untouched_pages"]:
+        assert np.all(np.isnan(pool[pid]))
+    pf = g["partly_filled"]
+    assert not np.isnan(pool[pf["page"], :, pf["written_slots"]]).any()
+    assert np.isnan(pool[pf["page"], :, pf["empty_slots"]]).all()
+    got = O.paged_gather(pool, table, g["n_tokens"])
+    assert np.array_equal(got[:, 0, 0], np.arange(1, g["n_tokens"] + 1, dtype=np.float64))
+
+
 def pin_mixed_step_composition():
     """A mixed step (decode rows + prompt chunks over pages) equals running each
     sequence's rows alone as a chunk over its own gathered cache, and the
@@ -437,5 +459,5 @@ ALL_PINS = [
     pin_identity_values, pin_equal_keys_mean, pin_dominant_key, pin_torch_sdpa_example,
     pin_chunked_equals_one_shot, pin_cache_prefix_bytes, pin_gqa_is_repeated_mha,
     pin_padding_invisible, pin_rolling_mask_examples, pin_rolling_no_overflow_is_plain_prefill,
-    pin_rolling_sliding_window, pin_paged_round_trip, pin_mixed_step_composition,
+    pin_rolling_sliding_window, pin_paged_round_trip, pin_paged_coordinates, pin_mixed_step_composition,
 ]
