@@ -75,6 +75,8 @@ def lib():
                                        c_int32, P, P, c_size_t, P, P]
         L.cp_mixed_step.argtypes = [POINTER(LayerDesc), P, P, P, P, P, P, P, P, c_int32, c_int32,
                                     c_int32, P, P, c_size_t, P, P]
+        L.cp_prefill_varlen.argtypes = [POINTER(LayerDesc), P, P, P, P, P, P, P, c_int32, c_int32, c_int32, P,
+                                        P, c_size_t, P, P]
         L.cp_mixed_step_noalloc.argtypes = [POINTER(LayerDesc), P, P, P, P, P, P, P, P, c_int32, c_int32,
                                             c_int32, P, P, P]
         L.cp_mixed_step_noalloc.restype = c_int32
@@ -91,7 +93,7 @@ def lib():
         L.cp_status_string.argtypes = [c_int32]
         L.cp_status_string.restype = ctypes.c_char_p
         for name in ("cp_kv_append", "cp_pad_chunk", "cp_prefill_chunk_attn", "cp_prefill_chunk",
-                     "cp_mixed_step", "cp_chunk_plan",
+                     "cp_mixed_step", "cp_prefill_varlen", "cp_chunk_plan",
                      "cp_query_ladder", "cp_query_width", "cp_aligned_length", "cp_rolling_mask",
                      "cp_schedule", "cp_abi_version"):
             getattr(L, name).restype = c_int32
@@ -172,6 +174,16 @@ def cp_mixed_step(desc, q, k_new, v_new, k_pages, v_pages, block_table, cu_rows,
                             total_rows, max_ctx, _ptr(out), _ptr(workspace), ws_bytes,
                             _ptr(dev_status), _stream(stream, q))
     _check(s, "cp_mixed_step")
+
+
+def cp_prefill_varlen(desc, q, k_new, v_new, k_cache, v_cache, cu_rows, seqlens_k, num_seqs, total_rows, max_ctx,
+                      out, workspace, dev_status=None, stream=None):
+    """Several sequences with ragged rows over a contiguous cache in one call (see include/cp_api.h)."""
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    s = lib().cp_prefill_varlen(ctypes.byref(desc), _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_cache),
+                                _ptr(v_cache), _ptr(cu_rows), _ptr(seqlens_k), num_seqs, total_rows, max_ctx,
+                                _ptr(out), _ptr(workspace), ws_bytes, _ptr(dev_status), _stream(stream, q))
+    _check(s, "cp_prefill_varlen")
 
 
 def cp_mixed_step_noalloc(desc, q, k_new, v_new, k_pages, v_pages, block_table, cu_rows, past_len,

@@ -242,6 +242,62 @@ int run_fused(const cp_layer_desc* d, AttnArgs a, int64_t rows_total, const void
   return launch_result(launch_attn_tc(a, d->dtype, tq, tk, tv, to, tkn, tvn, (int)pairs, st));
 }
 
+// Append, attention and length advance of a step whose sequences have
+// ragged rows (cu_rows): every row's K/V is appended first (pages through the
+// block table, or the contiguous cache when block_table is NULL), then
+// one-row sequences take the split-KV decode path and the others the
+// tensor-core path, reading the lengths as they were before the step; a last
+// kernel advances each length by its own rows.  Arguments already checked.
+int ragged_step(const cp_layer_desc* desc, const void* q, const void* k_new, const void* v_new, void* k_cache,
+                void* v_cache, const int32_t* block_table, const int32_t* cu_rows, int32_t* past_len,
+                int32_t num_seqs, int32_t total_rows, int32_t max_ctx, void* out, void* workspace,
+                size_t workspace_bytes, int32_t* dev_status, cudaStream_t st) {
+  const SeqRows rows{num_seqs, 0, cu_rows};
+  const CacheView cache = make_cache(desc, block_table);
+
+  AppendArgs ap;
+  ap.hkv = desc->num_kv_heads;
+  ap.d = desc->head_dim;
+  ap.esize = esize_of(desc->dtype);
+  ap.rows = rows;
+  ap.cache = cache;
+  ap.past = past_len;
+  ap.max_ctx = max_ctx;
+  ap.k_new = k_new;
+  ap.v_new = v_new;
+  ap.k_cache = k_cache;
+  ap.v_cache = v_cache;
+  ap.status = dev_status;
+  int r = launch_result(launch_kv_append(ap, total_rows, st));
+  if (r != CP_OK) return r;
+
+  AttnArgs a;
+  std::memset(&a, 0, sizeof(a));
+  a.hq = desc->num_q_heads;
+  a.hkv = desc->num_kv_heads;
+  a.d = desc->head_dim;
+  a.group = a.hq / a.hkv;
+  a.scale_log2 = scale_log2(desc);
+  a.rows = rows;
+  a.cache = cache;
+  a.past = past_len;
+  a.max_ctx = max_ctx;
+  a.q = q;
+  a.k = k_cache;
+  a.v = v_cache;
+  a.out = out;
+  a.status = dev_status;
+  // Every listed sequence has at least one row, so none has more than
+  // total_rows - num_seqs + 1; with one row each the tensor-core path has no
+  // work and is not launched.
+  const int64_t max_rows_per_seq = total_rows >= num_seqs ? (int64_t)total_rows - num_seqs + 1 : total_rows;
+  const bool paged = desc->kind == CP_CACHE_PAGED;
+  r = run_attention(desc, a, total_rows, (int)max_rows_per_seq, k_cache, v_cache, paged ? 0 : desc->batch, workspace,
+                    workspace_bytes, st, paged ? k_new : nullptr, paged ? v_new : nullptr);
+  if (r != CP_OK) return r;
+  return launch_result(launch_commit(past_len, rows, -1, dev_status, st));
+}
+
 }  // namespace
 
 namespace cp {
@@ -477,50 +533,34 @@ int cp_mixed_step(const cp_layer_desc* desc, const void* q, const void* k_new, c
   if (r != CP_OK) return r;
   if (total_rows == 0) return CP_OK;
   if (need > 0 && (workspace == nullptr || workspace_bytes < need || !aligned16(workspace))) return CP_ERR_WORKSPACE;
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
-  const SeqRows rows{num_seqs, 0, cu_rows};
-  const CacheView cache = make_cache(desc, block_table);
+  return ragged_step(desc, q, k_new, v_new, k_pages, v_pages, block_table, cu_rows, past_len, num_seqs, total_rows,
+                     max_ctx, out, workspace, workspace_bytes, dev_status, static_cast<cudaStream_t>(stream));
+}
 
-  AppendArgs ap;
-  ap.hkv = desc->num_kv_heads;
-  ap.d = desc->head_dim;
-  ap.esize = esize_of(desc->dtype);
-  ap.rows = rows;
-  ap.cache = cache;
-  ap.past = past_len;
-  ap.max_ctx = max_ctx;
-  ap.k_new = k_new;
-  ap.v_new = v_new;
-  ap.k_cache = k_pages;
-  ap.v_cache = v_pages;
-  ap.status = dev_status;
-  r = launch_result(launch_kv_append(ap, total_rows, st));
+int cp_prefill_varlen(const cp_layer_desc* desc, const void* q, const void* k_new, const void* v_new, void* k_cache,
+                      void* v_cache, const int32_t* cu_rows, int32_t* seqlens_k, int32_t num_seqs,
+                      int32_t total_rows, int32_t max_ctx, void* out, void* workspace, size_t workspace_bytes,
+                      int32_t* dev_status, void* stream) {
+  int r = check_desc(desc, true);
   if (r != CP_OK) return r;
-
-  AttnArgs a;
-  std::memset(&a, 0, sizeof(a));
-  a.hq = desc->num_q_heads;
-  a.hkv = desc->num_kv_heads;
-  a.d = desc->head_dim;
-  a.group = a.hq / a.hkv;
-  a.scale_log2 = scale_log2(desc);
-  a.rows = rows;
-  a.cache = cache;
-  a.past = past_len;
-  a.max_ctx = max_ctx;
-  a.q = q;
-  a.k = k_pages;
-  a.v = v_pages;
-  a.out = out;
-  a.status = dev_status;
-  // Every listed sequence has at least one row, so none has more than
-  // total_rows - num_seqs + 1; with one row each the tensor-core path has no
-  // work and is not launched.
-  const int64_t max_rows_per_seq = total_rows >= num_seqs ? (int64_t)total_rows - num_seqs + 1 : total_rows;
-  r = run_attention(desc, a, total_rows, (int)max_rows_per_seq, k_pages, v_pages, 0, workspace, workspace_bytes,
-                    st, k_new, v_new);
-  if (r != CP_OK) return r;
-  return launch_result(launch_commit(past_len, rows, -1, dev_status, st));
+  if (desc->kind != CP_CACHE_CONTIG) return CP_ERR_UNSUPPORTED;
+  if (num_seqs <= 0 || num_seqs > desc->batch || total_rows < 0 || max_ctx <= 0) return CP_ERR_INVALID_ARG;
+  if (total_rows == 0) return CP_OK;
+  if (!q || !k_new || !v_new || !k_cache || !v_cache || !cu_rows || !seqlens_k || !out) return CP_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k_new) || !aligned16(v_new) || !aligned16(k_cache) || !aligned16(v_cache) ||
+      !aligned16(out))
+    return CP_ERR_INVALID_ARG;
+  if ((int64_t)max_ctx > layout_limit(desc)) return CP_ERR_CAPACITY;
+  const int G0 = desc->num_q_heads / desc->num_kv_heads;
+  int64_t need = 0;
+  if (desc->dtype != CP_F32) {
+    if (!attn_tc_supported(desc->head_dim, G0, desc->dtype)) return CP_ERR_UNSUPPORTED;
+    if (decode_supported(desc->head_dim, G0, desc->dtype)) need = decode_ws_bytes(desc, max_ctx, num_seqs);
+  }
+  if (need > 0 && (workspace == nullptr || (int64_t)workspace_bytes < need || !aligned16(workspace)))
+    return CP_ERR_WORKSPACE;
+  return ragged_step(desc, q, k_new, v_new, k_cache, v_cache, nullptr, cu_rows, seqlens_k, num_seqs, total_rows,
+                     max_ctx, out, workspace, workspace_bytes, dev_status, static_cast<cudaStream_t>(stream));
 }
 
 }  // extern "C"

@@ -15,7 +15,7 @@
  *     call returns.
  *   - Layouts are dense row-major with the last dimension contiguous:
  *       q, out           [B, R, Hq, D]   (cp_prefill_chunk_attn)
- *                        [T, Hq, D]      (cp_mixed_step)
+ *                        [T, Hq, D]      (cp_mixed_step, cp_prefill_varlen)
  *       k_new, v_new     [B, R, Hkv, D]  (cp_kv_append), [T, Hkv, D] (mixed)
  *       contiguous cache [B, Hkv, capacity, D]
  *       rolling cache    [B, Hkv, capacity, D]
@@ -215,6 +215,37 @@ int cp_mixed_step(const cp_layer_desc* desc, const void* q, const void* k_new,
                   const int32_t* cu_rows, int32_t* past_len, int32_t num_seqs,
                   int32_t total_rows, int32_t max_ctx, void* out, void* workspace,
                   size_t workspace_bytes, int32_t* dev_status, void* stream);
+
+/* cp_prefill_varlen -- one step of several prompts with ragged rows over a
+ * contiguous cache.
+ *
+ * [Glossary] "How chunked prefill works": a step is filled with chunks of
+ * several waiting prompts (and one row per running decode), each sequence
+ * with its own row count and its own cached length.  This is cp_mixed_step
+ * for a cache at fixed physical capacity ([Wiki] 一.3): every row's K/V is
+ * appended at slots seqlens_k[s] .. seqlens_k[s] + rows(s) - 1 of sequence s,
+ * then row i of s attends causally to slots [0, seqlens_k[s] + i] (one-row
+ * sequences on the split-KV decode path, the others on the tensor-core
+ * path), then seqlens_k[s] advances by rows(s).  No query padding: every row
+ * is real.
+ *   desc->kind must be CP_CACHE_CONTIG; sequences 0 .. num_seqs-1 of the
+ *                 cache take part (num_seqs <= desc->batch).
+ *   q, out        device [T, Hq, D];  k_new, v_new device [T, Hkv, D]
+ *   k_cache, v_cache  device [desc->batch, Hkv, capacity, D]
+ *   cu_rows       device int32 [num_seqs + 1] as in cp_mixed_step (every
+ *                 listed sequence has at least one row)
+ *   seqlens_k     device int32 [num_seqs]: valid slots of each sequence
+ *   max_ctx       host bound on seqlens_k[s] + rows(s) (<= capacity; a
+ *                 larger device value sets CP_DEV_BOUNDS and its rows are
+ *                 skipped)
+ *   workspace     device scratch, 16-byte aligned, of at least
+ *                 cp_workspace_size(desc, T, max_ctx, num_seqs) bytes (fp32
+ *                 layers need none) */
+int cp_prefill_varlen(const cp_layer_desc* desc, const void* q, const void* k_new,
+                      const void* v_new, void* k_cache, void* v_cache, const int32_t* cu_rows,
+                      int32_t* seqlens_k, int32_t num_seqs, int32_t total_rows, int32_t max_ctx,
+                      void* out, void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                      void* stream);
 
 /* cp_mixed_step_noalloc -- cp_mixed_step for callers that cannot allocate.
  *

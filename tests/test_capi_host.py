@@ -170,6 +170,31 @@ def test_append_and_mixed_reject_bad_arguments():
                            FAKE, FAKE, need // 4, None, None) == cp.CP_ERR_WORKSPACE
 
 
+def test_varlen_rejects_bad_arguments():
+    """cp_prefill_varlen: contiguous caches only, at most desc->batch sequences,
+    max_ctx within the capacity, 16-byte alignment, a workspace for the
+    decode rows' partials; all refused before anything is enqueued."""
+    L = cp.lib()
+    d = _desc(batch=4)
+
+    def call(desc=d, num_seqs=2, total=10, max_ctx=100, q=FAKE, ws=FAKE, ws_bytes=1 << 20):
+        return L.cp_prefill_varlen(ctypes.byref(desc), q, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, num_seqs, total,
+                                   max_ctx, FAKE, ws, ws_bytes, None, None)
+
+    pd = _desc(kind=cp.CP_CACHE_PAGED, page_size=16, num_pages=64, max_blocks=8)
+    assert call(desc=pd) == cp.CP_ERR_UNSUPPORTED
+    assert call(desc=_desc(kind=cp.CP_CACHE_ROLLING, capacity=1024)) == cp.CP_ERR_UNSUPPORTED
+    assert call(num_seqs=5) == cp.CP_ERR_INVALID_ARG
+    assert call(num_seqs=0) == cp.CP_ERR_INVALID_ARG
+    assert call(max_ctx=8193) == cp.CP_ERR_CAPACITY
+    assert call(q=FAKE + 8) == cp.CP_ERR_INVALID_ARG
+    assert call(q=None) == cp.CP_ERR_INVALID_ARG
+    assert call(ws=None, ws_bytes=0) == cp.CP_ERR_WORKSPACE
+    assert call(ws=FAKE + 4) == cp.CP_ERR_WORKSPACE
+    assert call(desc=_desc(batch=4, num_q_heads=32, num_kv_heads=1)) == cp.CP_ERR_UNSUPPORTED
+    assert call(total=0) == cp.CP_OK  # nothing to do
+
+
 def test_workspace_size_formula():
     d = _desc()
     # a 256-byte control block, a copy of the lengths in 256-byte blocks, then

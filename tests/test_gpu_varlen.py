@@ -1,0 +1,89 @@
+"""GPU parity of cp_prefill_varlen: several sequences with ragged rows and
+different cached lengths over one contiguous cache in a single call (the
+glossary's step filled with chunks of several prompts), against the C++
+oracle, with the cache checked byte for byte and each sequence's rows
+bit-identical to the same sequence run alone."""
+import numpy as np
+import pytest
+import torch
+
+import chunked_prefill_causal_cp_gb300 as cp
+import synth_inputs as SI
+from gpu_util import BF16_TOL, f64
+from oracle import cpp as oracle
+
+pytestmark = pytest.mark.gpu
+
+HQ, HKV, D, CAP = 32, 8, 128, 2048
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a GPU")
+    from chunked_prefill_causal_cp_gb300 import _build
+    _build.build()
+
+
+def _setup(pasts, seed):
+    """Cache [B, HKV, CAP, D] poisoned with NaN, positions [0, past) of each
+    sequence filled with seeded history."""
+    B = len(pasts)
+    kc = torch.full((B, HKV, CAP, D), float("nan"), dtype=torch.bfloat16, device="cuda")
+    vc = torch.full_like(kc, float("nan"))
+    hist = []
+    for s, p in enumerate(pasts):
+        hk = SI.normal((p, HKV, D), seed + 2 * s)
+        hv = SI.normal((p, HKV, D), seed + 2 * s + 1)
+        kc[s, :, :p] = hk.permute(1, 0, 2).cuda()
+        vc[s, :, :p] = hv.permute(1, 0, 2).cuda()
+        hist.append((hk, hv))
+    return kc, vc, hist
+
+
+def _call(kc, vc, pasts, rows, q, kn, vn):
+    B = len(pasts)
+    desc = cp.layer_desc(torch.bfloat16, kc.shape[0], HQ, HKV, D, cp.CP_CACHE_CONTIG, capacity=CAP)
+    cu = torch.tensor(np.concatenate([[0], np.cumsum(rows)]), dtype=torch.int32, device="cuda")
+    lens = torch.tensor(pasts, dtype=torch.int32, device="cuda")
+    T = int(sum(rows))
+    max_ctx = max(p + r for p, r in zip(pasts, rows))
+    out = torch.empty(T, HQ, D, dtype=torch.bfloat16, device="cuda")
+    ws = torch.zeros(cp.cp_workspace_size(desc, T, max_ctx, B), dtype=torch.uint8, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    cp.cp_prefill_varlen(desc, q, kn, vn, kc, vc, cu, lens, B, T, max_ctx, out, ws, dev_status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    return out, lens
+
+
+@pytest.mark.parametrize("pasts,rows", [
+    ([0, 37, 300, 1000, 128], [1, 5, 130, 257, 64]),
+    ([1500, 0, 511], [300, 512, 2]),
+])
+def test_varlen_matches_oracle_and_runs_alone(pasts, rows):
+    kc, vc, hist = _setup(pasts, seed=70)
+    k0, v0 = kc.clone(), vc.clone()
+    T = sum(rows)
+    q, kn, vn = SI.gqa_prompt(T, seed=71)
+    out, lens = _call(kc, vc, pasts, rows, q.cuda(), kn.cuda(), vn.cuda())
+    assert lens.tolist() == [p + r for p, r in zip(pasts, rows)]
+    o = f64(out)
+    t = 0
+    worst = 0.0
+    for s, (p, r) in enumerate(zip(pasts, rows)):
+        # the cache: history, then this call's rows, then the untouched poison
+        got_k = kc[s].permute(1, 0, 2)
+        assert torch.equal(got_k[:p].cpu(), hist[s][0]) and torch.equal(got_k[p:p + r].cpu(), kn[t:t + r])
+        assert torch.equal(vc[s].permute(1, 0, 2)[p:p + r].cpu(), vn[t:t + r])
+        assert torch.isnan(got_k[p + r:].float()).all()
+        keys = np.concatenate([f64(hist[s][0]), f64(kn[t:t + r])])
+        vals = np.concatenate([f64(hist[s][1]), f64(vn[t:t + r])])
+        ref = oracle.chunk_attention(f64(q[t:t + r]), keys, vals, p)
+        worst = max(worst, float(np.abs(o[t:t + r] - ref).max()))
+        # the same sequence alone, from the same starting cache: bit-identical rows
+        ks, vs = k0[s:s + 1].clone(), v0[s:s + 1].clone()
+        alone, _ = _call(ks, vs, [p], [r], q[t:t + r].cuda(), kn[t:t + r].cuda(), vn[t:t + r].cuda())
+        assert torch.equal(alone, out[t:t + r]), s
+        t += r
+    assert worst < BF16_TOL, worst
