@@ -24,9 +24,11 @@ a line.
 The default line also carries, under "configs", one measurement of each of
 the other workloads of the problem statement (fp32 example, padding ladder,
 rolling cache, decode rows, and the whole mixed token-budget schedule at
-budgets 8192 and 2048), each with its own check.  ``--workload X`` prints X's
-line alone; ``--chunk`` / ``--budget`` sweep the chunk width and the token
-budget.  ``--impl reference`` times the C++ CPU oracle (test infrastructure,
+budgets 8192 and 2048, k-row verify chunks at long lengths, and ragged
+prompts in one call), each with its own check.  ``--workload X`` prints X's
+line alone; ``--chunk`` / ``--prompt`` / ``--budget`` set the chunk width, the
+prompt length and the token budget, and ``--sweep`` prints one line per chunk
+width and per token budget.  ``--impl reference`` times the C++ CPU oracle (test infrastructure,
 float64, std::thread) on a bounded sample of the default workload instead.
 """
 from __future__ import annotations
@@ -57,7 +59,9 @@ def parse_args(argv=None):
     p.add_argument("--warmup", type=int, default=20)
     p.add_argument("--impl", default="native", choices=["native", "reference"])
     p.add_argument("--workload", default="gqa_prefill",
-                   choices=["gqa_prefill", "fp32", "ladder", "rolling", "decode", "mixed"])
+                   choices=["gqa_prefill", "fp32", "ladder", "rolling", "decode", "mixed", "verify", "varlen"])
+    p.add_argument("--sweep", action="store_true",
+                   help="one line per chunk width W (gqa_prefill) and per token budget (mixed schedule)")
     p.add_argument("--chunk", type=int, default=512, help="chunk width W of the gqa_prefill workload")
     p.add_argument("--prompt", type=int, default=4000, help="prompt tokens of the gqa_prefill workload")
     p.add_argument("--budget", type=int, default=8192, help="token budget of the mixed workload")
@@ -742,6 +746,11 @@ class MixedSchedule:
         self.cp, self.torch, self.dev = cp, torch, dev
         self.budget, self.decode_only = budget, decode_only
         mb = SI.mixed_batch()
+        if not decode_only:
+            # every sequence that decodes gains one position per step: give each one pages for that
+            n_steps = 1 + max(e[0] for e in cp.cp_schedule(budget, len(mb.decode_ctx), mb.prompt_lens))
+            if n_steps > 64:
+                mb = SI.mixed_batch(decode_tail=n_steps)
         self.mb = mb
         bf = torch.bfloat16
         self.desc = cp.layer_desc(bf, 0, self.HQ, self.HKV, self.D, cp.CP_CACHE_PAGED, page_size=mb.page_size,
@@ -860,6 +869,110 @@ class MixedSchedule:
                 "cuda_graph": True}
 
 
+class ShortChunks:
+    """Short chunks at long cached lengths over a contiguous cache.
+
+    ``verify``: 64 sequences, each with 4000 cached positions, take a 4-row
+    chunk (a speculative-verify step: k = 4 draft tokens checked in one pass;
+    the glossary's related techniques), one cp_prefill_chunk call.
+    ``varlen``: one cp_prefill_varlen call over 8 sequences with ragged rows
+    and different cached lengths (a step filled with chunks of several
+    prompts): rows [2048, 1024, 512, 512, 256, 128, 64, 1] at lengths
+    [0, 1024, 3000, 512, 6000, 7000, 100, 4095].  GQA 32/8 x 128 bf16, cache
+    capacity 8192, N(0,1) history drawn on the device."""
+
+    HQ, HKV, D = 32, 8, 128
+
+    def __init__(self, dev, mode):
+        import torch
+        import chunked_prefill_causal_cp_gb300 as cp
+
+        self.cp, self.torch, self.dev, self.mode = cp, torch, dev, mode
+        bf = torch.bfloat16
+        if mode == "verify":
+            self.B, self.k, self.cap = 64, 4, 4096 + 8
+            self.pasts = [4000] * self.B
+            self.rows = [self.k] * self.B
+        else:
+            self.cap = 8192
+            self.rows = [2048, 1024, 512, 512, 256, 128, 64, 1]
+            self.pasts = [0, 1024, 3000, 512, 6000, 7000, 100, 4095]
+            self.B = len(self.rows)
+        g = torch.Generator(device=dev).manual_seed(9)
+        self.kc = torch.randn(self.B, self.HKV, self.cap, self.D, generator=g, device=dev).to(bf)
+        self.vc = torch.randn(self.B, self.HKV, self.cap, self.D, generator=g, device=dev).to(bf)
+        self.T = sum(self.rows)
+        self.q = torch.randn(self.T, self.HQ, self.D, generator=g, device=dev).to(bf)
+        self.kn = torch.randn(self.T, self.HKV, self.D, generator=g, device=dev).to(bf)
+        self.vn = torch.randn(self.T, self.HKV, self.D, generator=g, device=dev).to(bf)
+        self.out = torch.zeros(self.T, self.HQ, self.D, dtype=bf, device=dev)
+        self.desc = cp.layer_desc(bf, self.B, self.HQ, self.HKV, self.D, cp.CP_CACHE_CONTIG, capacity=self.cap)
+        self.past0 = torch.tensor(self.pasts, dtype=torch.int32, device=dev)
+        self.lens = self.past0.clone()
+        cu = [0]
+        for r in self.rows:
+            cu.append(cu[-1] + r)
+        self.cu_host = cu
+        self.cu = torch.tensor(cu, dtype=torch.int32, device=dev)
+        self.max_ctx = max(p + r for p, r in zip(self.pasts, self.rows))
+        self.status = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.ws = torch.zeros(max(16, cp.cp_workspace_size(self.desc, self.T, self.max_ctx, self.B)),
+                              dtype=torch.uint8, device=dev)
+        kv_row = self.HKV * self.D * 2
+        self.flops = sum(4 * self.D * self.HQ * visible_pairs(p, r) for p, r in zip(self.pasts, self.rows))
+        # algorithmic bytes: cached K/V read once per (sequence, KV head), the new rows' q, k, v and out
+        self.bytes = sum(p * kv_row * 2 for p in self.pasts) + self.T * (2 * self.HQ * self.D * 2 + 2 * kv_row)
+        self.tokens = self.T
+        self.launches = 1 if mode == "verify" else 5
+
+    def step(self):
+        cp = self.cp
+        self.lens.copy_(self.past0)
+        if self.mode == "verify":
+            B, k = self.B, self.k
+            cp.cp_prefill_chunk(self.desc, self.q.view(B, k, self.HQ, self.D), self.kn.view(B, k, self.HKV, self.D),
+                                self.vn.view(B, k, self.HKV, self.D), self.kc, self.vc, self.lens, k, k,
+                                max(self.pasts), self.out.view(B, k, self.HQ, self.D), self.ws,
+                                dev_status=self.status)
+        else:
+            cp.cp_prefill_varlen(self.desc, self.q, self.kn, self.vn, self.kc, self.vc, self.cu, self.lens, self.B,
+                                 self.T, self.max_ctx, self.out, self.ws, dev_status=self.status)
+
+    def self_check(self, n_sample=24, seed=19):
+        """The new rows sit in their slots bit for bit, each length advanced by its
+        rows, sampled rows agree with ref_rows over the sequence's slots [0, pos]."""
+        torch = self.torch
+        torch.cuda.synchronize()
+        slots_ok = True
+        for s, (p, r) in enumerate(zip(self.pasts, self.rows)):
+            t = self.cu_host[s]
+            slots_ok = slots_ok and bits_equal(self.kc[s, :, p:p + r].transpose(0, 1), self.kn[t:t + r]) \
+                and bits_equal(self.vc[s, :, p:p + r].transpose(0, 1), self.vn[t:t + r])
+        lens_ok = self.lens.tolist() == [p + r for p, r in zip(self.pasts, self.rows)]
+        g = torch.Generator().manual_seed(seed)
+        picks = {0, self.T - 1}
+        while len(picks) < n_sample:
+            picks.add(int(torch.randint(0, self.T, (1,), generator=g)))
+        err = 0.0
+        for i in sorted(picks):
+            s = max(j for j in range(self.B) if self.cu_host[j] <= i)
+            pos = self.pasts[s] + (i - self.cu_host[s])
+            ref = ref_rows(self.q[i], self.kc[s, :, :pos + 1].transpose(0, 1), self.vc[s, :, :pos + 1].transpose(0, 1),
+                           self.D ** -0.5)
+            err = max(err, float((self.out[i].float() - ref).abs().max()))
+        status = int(self.status.item())
+        ok = slots_ok and lens_ok and status == 0 and err < BF16_TOL
+        return {"ok": ok, "slots_bit_exact": slots_ok, "lengths_ok": lens_ok, "rows_checked": len(picks),
+                "max_abs_err": err, "tol": BF16_TOL, "status": status}
+
+    def config(self):
+        if self.mode == "verify":
+            return {"workload": "verify_k4_x64_past4000_gqa32x8_d128_bf16", "sequences": self.B, "k": self.k,
+                    "past": self.pasts[0], "l2": L2_NOTE, "cuda_graph": True}
+        return {"workload": "varlen8_gqa32x8_d128_bf16_cap8192", "rows": self.rows, "pasts": self.pasts,
+                "l2": L2_NOTE, "cuda_graph": True}
+
+
 # --------------------------------------------------------------------------- measurement
 
 def measure(wl, graph, flush, reps, warmup, torch, check_kw=None):
@@ -916,6 +1029,17 @@ def other_configs(dev, flush, pk, reps, warmup):
                      "dtype": "bf16", "check": chk, "gpu_launches_per_step": wl.launches}
     del wl
 
+    for mode in ("verify", "varlen"):
+        wl = ShortChunks(dev, mode)
+        ms, chk = measure(wl, capture(wl.step, dev), flush, reps, warmup, torch)
+        gbs = wl.bytes / (ms / 1e3) / 1e9
+        tf = wl.flops / (ms / 1e3) / 1e12
+        res[mode] = {**wl.config(), "rows_per_s": wl.tokens / (ms / 1e3), "ms_per_step": ms, "tflops": tf,
+                     "tensor_frac": tf / tc, "gbs_algorithmic": gbs, "hbm_frac": gbs / hbm,
+                     "roofline_time_us": max(wl.flops / (tc * 1e12), wl.bytes / (hbm * 1e9)) * 1e6,
+                     "dtype": "bf16", "check": chk, "gpu_launches_per_step": wl.launches}
+        del wl
+
     for budget in (8192, 2048):
         wl = MixedSchedule(dev, budget=budget)
         ms, chk = measure(wl, capture(wl.step, dev), flush, max(3, reps // 4), warmup, torch)
@@ -942,6 +1066,8 @@ def run_native(args):
     import chunked_prefill_causal_cp_gb300 as cp
     cp.lib()
     pk, pk_src = peaks()
+    if args.sweep:
+        return run_sweep(args, dev, pk)
     if args.workload != "gqa_prefill":
         return run_single(args, rank, world, dev, pk, pk_src)
 
@@ -1056,6 +1182,35 @@ def run_native(args):
         dist.destroy_process_group()
 
 
+def run_sweep(args, dev, pk):
+    """NEXT-2 of the problem statement: the chunk width W of the GQA prompt and
+    the token budget of the mixed schedule, one line each (each checked first)."""
+    import torch
+    tc, hbm = float(pk["bf16_tflops"]), float(pk["hbm_gbs"])
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    reps = max(5, min(args.steps, 50))
+    for W in (128, 256, 512, 1024, 2048, 4096):
+        wl = GqaPrefill(dev, N=args.prompt, W=W)
+        ms, chk = measure(wl, wl.capture(), flush, reps, args.warmup, torch)
+        print(json.dumps({"sweep": "chunk", "W": W, "prompt": wl.N, "chunks": len(wl.sizes),
+                          "query_widths": sorted(set(wl.widths)),
+                          "padded_rows": sum(w - r for r, w in zip(wl.sizes, wl.widths)),
+                          "tokens_per_s": wl.tokens / (ms / 1e3), "ms_per_step": ms,
+                          "tflops": wl.flops / (ms / 1e3) / 1e12, "check_ok": chk["ok"],
+                          "max_abs_err": chk["max_abs_err"]}), flush=True)
+        del wl
+    for budget in (512, 1024, 2048, 4096, 8192, 16384):
+        wl = MixedSchedule(dev, budget=budget)
+        ms, chk = measure(wl, capture(wl.step, dev), flush, max(3, reps // 5), args.warmup, torch)
+        t_star = sum(max(st["flops"] / (tc * 1e12), st["bytes"] / (hbm * 1e9)) for st in wl.steps) * 1e3
+        print(json.dumps({"sweep": "budget", "budget": budget, "schedule_steps": len(wl.steps),
+                          "rows_per_schedule": wl.R, "rows_per_s": wl.tokens / (ms / 1e3), "ms_per_schedule": ms,
+                          "roofline_time_ms": t_star, "roofline_frac": t_star / ms, "check_ok": chk["ok"],
+                          "max_abs_err": chk["max_abs_err"]}), flush=True)
+        del wl
+        torch.cuda.empty_cache()
+
+
 def run_single(args, rank, world, dev, pk, pk_src):
     """One line for one of the other workloads."""
     import torch
@@ -1064,6 +1219,8 @@ def run_single(args, rank, world, dev, pk, pk_src):
     kw = None
     if args.workload in ("fp32", "rolling"):
         wl = ChunkLoop(dev, args.workload)
+    elif args.workload in ("verify", "varlen"):
+        wl = ShortChunks(dev, args.workload)
     elif args.workload == "ladder":
         unp = LadderRuns(dev, pad=False)
         capture(unp.step, dev).replay()
@@ -1106,6 +1263,14 @@ def run_single(args, rank, world, dev, pk, pk_src):
         line["roofline_frac"] = t_star / ms
     if args.workload == "ladder":
         line["padded_rows_per_step"] = wl.padded_rows
+    if args.workload in ("verify", "varlen"):
+        gbs = wl.bytes / (ms / 1e3) / 1e9
+        line["roofline"] = {"bound": "hbm" if args.workload == "verify" else "tensor",
+                            "achieved": gbs if args.workload == "verify" else wl.flops / (ms / 1e3) / 1e12,
+                            "peak": hbm if args.workload == "verify" else tc,
+                            "unit": "GB/s" if args.workload == "verify" else "TFLOP/s",
+                            "scope": "algorithmic bytes or FLOPs over the whole call"}
+        line["roofline"]["frac"] = line["roofline"]["achieved"] / line["roofline"]["peak"]
     if rank == 0:
         print(json.dumps(line), flush=True)
 
