@@ -418,21 +418,46 @@ class GqaPrefill:
 
     # ---- end to end: host buffers in, result out, through the captured public calls
     def pin(self):
-        self.hq = self.host_q.pin_memory()
-        self.hk = self.host_k.pin_memory()
-        self.hv = self.host_v.pin_memory()
-        self.ho = self.torch.empty(self.N, self.HQ, self.D, dtype=self.torch.bfloat16).pin_memory()
-        self.h2d = (self.hq.numel() + self.hk.numel() + self.hv.numel()) * 2
+        """Pinned host staging in the layout a serving loop would fill: each
+        chunk's q, k and v rows back to back, so one copy per chunk moves all
+        three (each extra copy costs about 2 us of the host link on this part).
+        The device side mirrors it: per chunk one buffer [q | k | v] whose three
+        parts are the call's q, k_new and v_new."""
+        torch = self.torch
+        row = (self.HQ + 2 * self.HKV) * self.D  # elements per token in a packed chunk
+        self.e2e_chunks = []
+        past = 0
+        for r, w in zip(self.sizes, self.widths):
+            hbuf = torch.empty(w * row, dtype=torch.bfloat16).pin_memory()
+            nq, nk = r * self.HQ * self.D, r * self.HKV * self.D
+            dbuf = torch.zeros(w * row, dtype=torch.bfloat16, device=self.dev)
+            qsz, ksz = w * self.HQ * self.D, w * self.HKV * self.D
+            hq = hbuf[:qsz]
+            hk = hbuf[qsz:qsz + ksz]
+            hv = hbuf[qsz + ksz:]
+            hq[:nq].copy_(self.host_q[past:past + r].reshape(-1))
+            hk[:nk].copy_(self.host_k[past:past + r].reshape(-1))
+            hv[:nk].copy_(self.host_v[past:past + r].reshape(-1))
+            self.e2e_chunks.append(dict(
+                h=hbuf, d=dbuf, bytes_in=(nq + 2 * nk) * 2, r=r, w=w, past=past,
+                q=dbuf[:qsz].view(1, w, self.HQ, self.D), k=dbuf[qsz:qsz + ksz].view(1, w, self.HKV, self.D),
+                v=dbuf[qsz + ksz:].view(1, w, self.HKV, self.D),
+                h_in=(hq[:nq], hk[:nk], hv[:nk])))
+            past += r
+        self.ho = torch.empty(self.N, self.HQ, self.D, dtype=torch.bfloat16).pin_memory()
+        self.h2d = sum(c["bytes_in"] for c in self.e2e_chunks)
         self.d2h = self.ho.numel() * 2
 
     def capture_e2e(self):
         """One CUDA graph of a whole step with its host traffic, pipelined the way
-        a serving loop runs chunked prefill: chunk i's q/k/v rows go host ->
-        device on one copy stream ahead of chunk i's compute, and chunk i's
-        output rows go device -> host on another as soon as chunk i is done.
+        a serving loop runs chunked prefill: each chunk's packed q/k/v rows go
+        host -> device in one copy on a copy stream, all queued at once in chunk
+        order; each chunk's call waits for its own rows; its output rows go
+        device -> host on a second copy stream as soon as the chunk is done.
         Every input byte and every output byte of the step crosses the bus inside
         the graph; the step ends when the last output row is on the host."""
         torch = self.torch
+        cp = self.cp
         main = torch.cuda.Stream(self.dev)
         up, down = torch.cuda.Stream(self.dev), torch.cuda.Stream(self.dev)
         n = len(self.sizes)
@@ -443,22 +468,28 @@ class GqaPrefill:
             self.lens.zero_()
             up.wait_stream(main)
             down.wait_stream(main)
-            starts = [sum(self.sizes[:i]) for i in range(n)]
-            with torch.cuda.stream(up):  # all uploads queue at once, in chunk order
-                for i, r in enumerate(self.sizes):
-                    sl = slice(starts[i], starts[i] + r)
-                    self.q[sl].copy_(self.hq[sl], non_blocking=True)
-                    self.k[sl].copy_(self.hk[sl], non_blocking=True)
-                    self.v[sl].copy_(self.hv[sl], non_blocking=True)
+            with torch.cuda.stream(up):
+                for i, c in enumerate(self.e2e_chunks):
+                    if c["w"] == c["r"]:
+                        c["d"].copy_(c["h"], non_blocking=True)
+                    else:  # a short chunk: only its real rows cross the link
+                        qsz, ksz = c["w"] * self.HQ * self.D, c["w"] * self.HKV * self.D
+                        hq, hk, hv = c["h_in"]
+                        c["d"][:hq.numel()].copy_(hq, non_blocking=True)
+                        c["d"][qsz:qsz + hk.numel()].copy_(hk, non_blocking=True)
+                        c["d"][qsz + ksz:qsz + ksz + hv.numel()].copy_(hv, non_blocking=True)
                     ev_in[i].record(up)
-            for i, r in enumerate(self.sizes):
+            for i, c in enumerate(self.e2e_chunks):
                 main.wait_event(ev_in[i])
-                self._chunk(i)
+                r, w, past = c["r"], c["w"], c["past"]
+                if w > r:
+                    cp.cp_pad_chunk(self.desc, c["q"], c["k"], c["v"], r, w)
+                cp.cp_prefill_chunk(self.desc, c["q"], c["k"], c["v"], self.kc, self.vc, self.lens, w, r, past,
+                                    self.out[None, past:past + w], self.ws, dev_status=self.status)
                 ev_done[i].record(main)
                 with torch.cuda.stream(down):
                     down.wait_event(ev_done[i])
-                    sl = slice(starts[i], starts[i] + r)
-                    self.ho[sl].copy_(self.out[sl], non_blocking=True)
+                    self.ho[past:past + r].copy_(self.out[past:past + r], non_blocking=True)
             main.wait_stream(up)
             main.wait_stream(down)
 
@@ -1155,10 +1186,10 @@ def run_native(args):
                      "traffic_note": "mean DRAM bytes per launch over the step's chunk launches (ncu)"},
         "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": wl.h2d,
                 "d2h_bytes_per_step": wl.d2h,
-                "path": ("one captured graph per step of the public calls with its host traffic: all chunks' "
-                         "q/k/v rows pinned host -> device queued in chunk order on a copy stream, each chunk's "
-                         "call waiting for its own rows, and its output rows device -> pinned host on a second "
-                         "copy stream once it is done")},
+                "path": ("one captured graph per step of the public calls with its host traffic: each chunk's "
+                         "q/k/v rows staged back to back in pinned host memory and copied host -> device in one "
+                         "copy, all queued in chunk order on a copy stream; each chunk's call waits for its own "
+                         "rows; its output rows go device -> pinned host on a second copy stream once it is done")},
         "gpu_launches": wl.launches * args.steps,
         "clocks": clk,
     }
