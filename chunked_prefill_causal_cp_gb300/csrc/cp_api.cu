@@ -75,10 +75,19 @@ int64_t max_splits_for(int32_t max_ctx) { return ((int64_t)max_ctx + kDecodeSpli
 constexpr int64_t kControlBytes = 256;
 int64_t snapshot_bytes(int32_t num_seqs) { return ((int64_t)num_seqs * 4 + 255) / 256 * 256; }
 
-// Decode workspace: the split partials (output rows, then max and sum).
-int64_t decode_ws_bytes(const cp_layer_desc* d, int32_t max_ctx, int32_t num_seqs) {
+// Decode workspace: the split partials (output rows, then max and sum) of
+// `rows` query rows on the split-KV path.
+int64_t decode_ws_bytes(const cp_layer_desc* d, int32_t max_ctx, int64_t rows) {
   const int64_t ms = max_splits_for(max_ctx);
-  return (int64_t)num_seqs * d->num_q_heads * ms * (d->head_dim + 2) * (int64_t)sizeof(float);
+  return rows * d->num_q_heads * ms * (d->head_dim + 2) * (int64_t)sizeof(float);
+}
+
+// Rows per sequence a call with `rows_uniform` rows each puts on the split-KV
+// path: all of them when rows_uniform * G <= 16 (a decode row, or a short chunk
+// such as k verified draft tokens), else only one-row sequences (1).
+int decode_rows_for(const cp_layer_desc* d, int rows_uniform) {
+  const int G = d->num_q_heads / d->num_kv_heads;
+  return rows_uniform >= 1 && rows_uniform <= decode_max_rows(G) ? rows_uniform : 1;
 }
 
 // ---- tensor maps (driver entry point fetched through the runtime)
@@ -169,20 +178,25 @@ int run_attention(const cp_layer_desc* d, const AttnArgs& base, int64_t rows_tot
   }
   const bool decode_ok = decode_supported(d->head_dim, G, d->dtype) && d->kind != CP_CACHE_ROLLING;
   if (!attn_tc_supported(d->head_dim, G, d->dtype)) return CP_ERR_UNSUPPORTED;
-  const bool any_multi = rows_max_per_seq > 1;
-  const bool any_single = base.rows.rows_uniform == 0 || base.rows.rows_uniform == 1;
+  // Uniform rows of at most 16 / G per sequence all take the split-KV path;
+  // otherwise it takes the one-row sequences and the tensor-core kernel the rest.
+  const int kdec = decode_rows_for(d, base.rows.rows_uniform);
+  const bool any_multi = rows_max_per_seq > kdec;
+  const bool any_single = base.rows.rows_uniform == 0 || base.rows.rows_uniform == kdec;
   if (decode_ok && any_single) {
-    const int64_t need = decode_ws_bytes(d, a.max_ctx, a.rows.num_seqs);
+    const int64_t need = decode_ws_bytes(d, a.max_ctx, (int64_t)a.rows.num_seqs * kdec);
     if (workspace == nullptr || (int64_t)ws_bytes < need) return CP_ERR_WORKSPACE;
     AttnArgs dec = a;
+    dec.dec_rows = kdec;
     dec.part_o = static_cast<float*>(workspace);
     dec.max_splits = (int)max_splits_for(a.max_ctx);
-    dec.part_ml = dec.part_o + (int64_t)a.rows.num_seqs * d->num_q_heads * dec.max_splits * d->head_dim;
+    dec.part_ml =
+        dec.part_o + (int64_t)a.rows.num_seqs * kdec * d->num_q_heads * dec.max_splits * d->head_dim;
     const int r = launch_result(launch_decode(dec, d->dtype, st));
     if (r != CP_OK) return r;
   }
   if (any_multi || !decode_ok) {
-    a.min_rows = decode_ok ? 2 : 1;
+    a.min_rows = decode_ok ? kdec + 1 : 1;
     CUtensorMap tq, to, tk, tv, tkn, tvn;
     if (!make_tc_maps(d, a.q, a.out, rows_total, k, v, batch_for_maps, &tq, &to, &tk, &tv)) return CP_ERR_CUDA;
     std::memset(&tkn, 0, sizeof(tkn));
@@ -211,7 +225,8 @@ int run_attention(const cp_layer_desc* d, const AttnArgs& base, int64_t rows_tot
 // goes to the tensor-core kernel with the append fused in.
 bool use_fused(const cp_layer_desc* d, int32_t rows_padded) {
   const int G = d->num_q_heads / d->num_kv_heads;
-  return d->kind == CP_CACHE_CONTIG && rows_padded > 1 && d->dtype != CP_F32 &&
+  const bool on_decode_path = decode_supported(d->head_dim, G, d->dtype) && rows_padded <= decode_max_rows(G);
+  return d->kind == CP_CACHE_CONTIG && rows_padded > 1 && !on_decode_path && d->dtype != CP_F32 &&
          attn_tc_supported(d->head_dim, G, d->dtype);
 }
 
@@ -337,8 +352,15 @@ extern "C" {
 
 size_t cp_workspace_size(const cp_layer_desc* desc, int32_t max_rows, int32_t max_ctx, int32_t num_seqs) {
   if (check_desc(desc, false) != CP_OK || max_rows < 0 || max_ctx < 0 || num_seqs < 0) return 0;
-  (void)max_rows;
-  return (size_t)(kControlBytes + snapshot_bytes(num_seqs) + decode_ws_bytes(desc, max_ctx, num_seqs));
+  // Split-KV partials: for each sequence, as many rows as a call of at most
+  // max_rows rows can put on the split-KV path (1, or up to 16 / G rows).
+  int64_t dec_rows = num_seqs;
+  if (num_seqs > 0) {
+    const int G = desc->num_q_heads / desc->num_kv_heads;
+    const int64_t per_seq = std::max<int64_t>(1, ((int64_t)max_rows + num_seqs - 1) / num_seqs);
+    dec_rows = (int64_t)num_seqs * std::min<int64_t>(per_seq, decode_max_rows(G));
+  }
+  return (size_t)(kControlBytes + snapshot_bytes(num_seqs) + decode_ws_bytes(desc, max_ctx, dec_rows));
 }
 
 int cp_kv_append(const cp_layer_desc* desc, const void* k_new, const void* v_new, int32_t rows, void* k_cache,
@@ -453,15 +475,17 @@ int cp_prefill_chunk(const cp_layer_desc* desc, const void* q, void* k_new, void
   }
   const int64_t rows_total = (int64_t)desc->batch * rows_padded;
   if (rows_total > INT32_MAX || (int64_t)max_past + rows_padded > INT32_MAX) return CP_ERR_UNSUPPORTED;
-  // The copy of the lengths always; the split-KV partials only when one-row
-  // chunks take the decode path (checked here, before anything is enqueued).
+  // The copy of the lengths always; the split-KV partials only when the rows
+  // take the split-KV path -- one row, or a short chunk of at most 16 / G rows
+  // (checked here, before anything is enqueued).
   const int G0 = desc->num_q_heads / desc->num_kv_heads;
   if (desc->dtype != CP_F32 && !attn_tc_supported(desc->head_dim, G0, desc->dtype)) return CP_ERR_UNSUPPORTED;
-  const bool decode_rows = rows_padded == 1 && desc->dtype != CP_F32 && desc->kind != CP_CACHE_ROLLING &&
-                           decode_supported(desc->head_dim, G0, desc->dtype);
+  const bool decode_rows = rows_padded <= decode_max_rows(G0) && desc->dtype != CP_F32 &&
+                           desc->kind != CP_CACHE_ROLLING && decode_supported(desc->head_dim, G0, desc->dtype);
   const int64_t snap = snapshot_bytes(desc->batch);
   const int64_t need =
-      kControlBytes + snap + (decode_rows ? decode_ws_bytes(desc, max_past + rows_padded, desc->batch) : 0);
+      kControlBytes + snap +
+      (decode_rows ? decode_ws_bytes(desc, max_past + rows_padded, (int64_t)desc->batch * rows_padded) : 0);
   if (workspace == nullptr || (int64_t)workspace_bytes < need || !aligned16(workspace)) return CP_ERR_WORKSPACE;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   AttnArgs a;
@@ -509,7 +533,8 @@ int cp_prefill_chunk(const cp_layer_desc* desc, const void* q, void* k_new, void
   a.past = past;  // the snapshot: seqlens_k itself may then be advanced by the attention kernel
   // One launch for the attention and the commit when the tensor-core kernel takes every row.
   const int G = desc->num_q_heads / desc->num_kv_heads;
-  const bool tc_only = desc->dtype != CP_F32 && rows_padded > 1 && attn_tc_supported(desc->head_dim, G, desc->dtype);
+  const bool tc_only = desc->dtype != CP_F32 && rows_padded > 1 && !decode_rows &&
+                       attn_tc_supported(desc->head_dim, G, desc->dtype);
   if (tc_only) {
     a.commit_lens = seqlens_k;
     a.commit_add = real_rows;

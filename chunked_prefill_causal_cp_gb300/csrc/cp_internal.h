@@ -56,9 +56,10 @@ struct AttnArgs {
   const void* k;           // cache / pool base (SIMT and decode kernels)
   const void* v;
   void* out;               // [rows_total, hq, d]
-  float* part_o;           // decode split partials [num_seqs, hq, max_splits, d]
-  float* part_ml;          // [num_seqs, hq, max_splits, 2] (max, sum) in log2 domain
+  float* part_o;           // decode split partials [num_seqs * dec_rows, hq, max_splits, d]
+  float* part_ml;          // [num_seqs * dec_rows, hq, max_splits, 2] (max, sum) in log2 domain
   int max_splits;
+  int dec_rows;            // rows per sequence on the split-KV path (1, or k with k * group <= 16)
   int* status;             // optional CP_DEV_* bits
   int kv_direct;           // tensor-core kernel: this call's new K/V rows may be read from
                            // k_new / v_new ([rows_total, hkv, d]) instead of the paged pool
@@ -133,8 +134,11 @@ cudaError_t launch_attn_f32(const AttnArgs& a, int rows_bound, cudaStream_t st);
 cudaError_t launch_attn_tc(const AttnArgs& a, int dtype, const CUtensorMap& tq, const CUtensorMap& tk,
                            const CUtensorMap& tv, const CUtensorMap& to, const CUtensorMap& tkn,
                            const CUtensorMap& tvn, int pairs_bound, cudaStream_t st);
-// Split-KV decode: partials into a.part_o / a.part_ml, then their combine.
+// Split-KV decode: partials into a.part_o / a.part_ml, then their combine.  Takes the
+// sequences with exactly a.dec_rows rows (a.dec_rows * a.group <= 16).
 cudaError_t launch_decode(const AttnArgs& a, int dtype, cudaStream_t st);
+// Most rows per sequence the split-KV path takes for a GQA group of `group` heads.
+constexpr int decode_max_rows(int group) { return group > 0 ? 16 / group : 0; }
 
 // Every check cp_mixed_step makes before enqueueing anything (returns its
 // status); *ws_need is the workspace the step then needs (decode partials).

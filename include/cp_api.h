@@ -139,6 +139,10 @@ int cp_pad_chunk(const cp_layer_desc* desc, void* q, void* k_new, void* v_new, i
  * at least one visible key that weight underflows to exactly 0, so excluding
  * the slot gives the same result.  A row with no visible key -- a left-pad
  * query -- gets output 0.)
+ * Paths: bf16/fp16 chunks of at most 16 / G rows per sequence (a decode row,
+ * or k draft tokens verified in one pass) take the memory-bound split-KV
+ * path, every row of a sequence sharing one read of its K/V (not ROLLING);
+ * longer chunks take the tensor-core path; fp32 a SIMT path.
  *   q, out        device [B, rows_padded, Hq, D]; pad rows' outputs are
  *                 written but unspecified ([Wiki] 四: results are cut back to
  *                 the real rows)
@@ -165,8 +169,9 @@ int cp_prefill_chunk_attn(const cp_layer_desc* desc, const void* q, const void* 
  * seqlens_k by real_rows, with the same arguments and results as those two
  * calls made back to back with commit = 1 ([Glossary] "How chunked prefill
  * works": each chunk's K/V join the cache and its rows attend to the cache).
- * For a contiguous cache with head_dim 128 and more than one row this is one
- * kernel launch: the kernel reads the tiles that hold the chunk's own keys
+ * For a contiguous cache in bf16/fp16 with more rows per sequence than the
+ * split-KV path takes (16 / G) this is one kernel launch: the kernel reads the
+ * tiles that hold the chunk's own keys
  * straight from k_new / v_new, copies those rows into the cache, and the last
  * of its CTAs to have read seqlens_k advances it.  Other layouts take an append
  * launch followed by the attention.
@@ -289,7 +294,10 @@ size_t cp_noalloc_scratch_bytes(void);
  * to `max_rows` query rows, contexts of up to `max_ctx` keys and `num_seqs`
  * sequences: a 256-byte control block and a copy of the sequences' lengths
  * (cp_prefill_chunk; the control block must be zero before first use, see
- * there) and the split-KV partial results. */
+ * there) and the split-KV partial results: for each sequence, one row's, or
+ * up to 16 / G rows' when a call's rows per sequence are that few (short
+ * chunks, e.g. k draft tokens verified in one pass, take the split-KV path
+ * together). */
 size_t cp_workspace_size(const cp_layer_desc* desc, int32_t max_rows, int32_t max_ctx,
                          int32_t num_seqs);
 

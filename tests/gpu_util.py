@@ -27,7 +27,8 @@ class Contig:
         self.status = torch.zeros(1, dtype=torch.int32, device=dev)
         self.cap = cap
         self.fused = fused  # one cp_prefill_chunk call per chunk instead of append + attention
-        self.ws = torch.zeros(max(cp.cp_workspace_size(self.desc, 1, cap, batch), 16), dtype=torch.uint8,
+        # room for the split-KV partials of up to 16 rows per sequence (short chunks take that path)
+        self.ws = torch.zeros(max(cp.cp_workspace_size(self.desc, batch * 16, cap, batch), 16), dtype=torch.uint8,
                               device=dev)
 
     def chunk(self, q, k_new, v_new, real_rows, past, out=None):

@@ -163,11 +163,12 @@ def test_append_and_mixed_reject_bad_arguments():
     pg = _desc(kind=cp.CP_CACHE_PAGED, page_size=16, num_pages=64, max_blocks=8, num_q_heads=32, num_kv_heads=1)
     assert L.cp_mixed_step(ctypes.byref(pg), FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 2, 10, 100,
                            FAKE, FAKE, 1 << 20, None, None) == cp.CP_ERR_UNSUPPORTED
-    need = cp.cp_workspace_size(pd, 10, 100, 2)
+    # a mixed step puts one row per sequence on the split-KV path: 2 rows of partials here
+    need = 2 * 32 * 1 * (128 + 2) * 4
     assert L.cp_mixed_step(ctypes.byref(pd), FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 2, 10, 100,
                            FAKE, None, 0, None, None) == cp.CP_ERR_WORKSPACE
     assert L.cp_mixed_step(ctypes.byref(pd), FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 2, 10, 100,
-                           FAKE, FAKE, need // 4, None, None) == cp.CP_ERR_WORKSPACE
+                           FAKE, FAKE, need - 16, None, None) == cp.CP_ERR_WORKSPACE
 
 
 def test_varlen_rejects_bad_arguments():
@@ -197,6 +198,10 @@ def test_varlen_rejects_bad_arguments():
 
 def test_workspace_size_formula():
     d = _desc()
+    # split-KV partials for up to min(rows per sequence, 16 / G) rows per sequence (G = 4 here)
+    assert cp.cp_workspace_size(d, 8, 1, 2) == 256 + 256 + 2 * 4 * 32 * 1 * 130 * 4
+    assert cp.cp_workspace_size(d, 4, 1, 2) == 256 + 256 + 2 * 2 * 32 * 1 * 130 * 4
+    assert cp.cp_workspace_size(d, 512, 1, 1) == 256 + 256 + 4 * 32 * 1 * 130 * 4
     # a 256-byte control block, a copy of the lengths in 256-byte blocks, then
     # num_seqs * Hq * ceil(ctx / 512) * (D + 2)
     # floats of split partials
