@@ -954,7 +954,8 @@ class ShortChunks:
         # algorithmic bytes: cached K/V read once per (sequence, KV head), the new rows' q, k, v and out
         self.bytes = sum(p * kv_row * 2 for p in self.pasts) + self.T * (2 * self.HQ * self.D * 2 + 2 * kv_row)
         self.tokens = self.T
-        self.launches = 1 if mode == "verify" else 5
+        # verify: append, split-KV kernel, combine, commit; varlen: the same plus the tensor-core kernel
+        self.launches = 4 if mode == "verify" else 5
 
     def step(self):
         cp = self.cp
