@@ -66,6 +66,8 @@ def parse_args(argv=None):
     p.add_argument("--prompt", type=int, default=4000, help="prompt tokens of the gqa_prefill workload")
     p.add_argument("--budget", type=int, default=8192, help="token budget of the mixed workload")
     p.add_argument("--no-pad", action="store_true", help="do not widen chunks to the query-width ladder")
+    p.add_argument("--overlap", action="store_true",
+                   help="mixed workload: cp_mixed_step_overlap (split-KV kernels on a side stream)")
     p.add_argument("--no-extras", action="store_true", help="default line without the other workloads")
     p.add_argument("--cpu-seconds", type=float, default=12.0, help="CPU-baseline sample budget")
     p.add_argument("--skip-cpu", action="store_true")
@@ -765,17 +767,20 @@ class MixedSchedule:
     (seeded page permutation), GQA 32/8 x 128 bf16.  One step of this workload
     is the whole schedule cp_schedule gives for `budget` (10 mixed steps at
     8192, 41 at 2048), each one cp_mixed_step call; ``decode_only`` is instead
-    the 64 decode rows alone, one call."""
+    the 64 decode rows alone, one call.  ``overlap``: each step is one
+    cp_mixed_step_overlap call instead (split-KV kernels on a side stream
+    beside the tensor-core kernel)."""
 
     HQ, HKV, D = 32, 8, 128
 
-    def __init__(self, dev, budget=8192, decode_only=False):
+    def __init__(self, dev, budget=8192, decode_only=False, overlap=False):
         import torch
         import chunked_prefill_causal_cp_gb300 as cp
         import synth_inputs as SI
 
         self.cp, self.torch, self.dev = cp, torch, dev
-        self.budget, self.decode_only = budget, decode_only
+        self.budget, self.decode_only, self.overlap = budget, decode_only, overlap
+        self.handles = (torch.cuda.Stream(dev), torch.cuda.Event(), torch.cuda.Event()) if overlap else None
         mb = SI.mixed_batch()
         if not decode_only:
             # every sequence that decodes gains one position per step: give each one pages for that
@@ -852,9 +857,14 @@ class MixedSchedule:
             st["past_dev"].copy_(st["past0"])
         for st in self.steps:
             sl = slice(st["off"], st["off"] + st["T"])
-            cp.cp_mixed_step(self.desc, self.q[sl], self.kn[sl], self.vn[sl], self.kp, self.vp, st["bt"],
-                             st["cu"], st["past_dev"], st["S"], st["T"], st["max_ctx"], self.out[sl], self.ws,
-                             dev_status=self.status)
+            if self.overlap:
+                cp.cp_mixed_step_overlap(self.desc, self.q[sl], self.kn[sl], self.vn[sl], self.kp, self.vp,
+                                         st["bt"], st["cu"], st["past_dev"], st["S"], st["T"], st["max_ctx"],
+                                         self.out[sl], self.ws, *self.handles, dev_status=self.status)
+            else:
+                cp.cp_mixed_step(self.desc, self.q[sl], self.kn[sl], self.vn[sl], self.kp, self.vp, st["bt"],
+                                 st["cu"], st["past_dev"], st["S"], st["T"], st["max_ctx"], self.out[sl], self.ws,
+                                 dev_status=self.status)
 
     def self_check(self, n_sample=24, seed=17):
         """Every row's K/V lands in its page slot bit for bit (page =
@@ -891,7 +901,7 @@ class MixedSchedule:
                 "max_abs_err": err, "tol": BF16_TOL, "status": status}
 
     def config(self):
-        name = "decode64" if self.decode_only else f"mixed_budget{self.budget}"
+        name = "decode64" if self.decode_only else f"mixed_budget{self.budget}" + ("_overlap" if self.overlap else "")
         return {"workload": f"paged_{name}_gqa32x8_d128_bf16_page16",
                 "schedule_steps": len(self.steps), "rows_per_schedule": self.R,
                 "decode_rows": self.decode_rows, "prefill_rows": self.prefill_rows,
@@ -1072,11 +1082,11 @@ def other_configs(dev, flush, pk, reps, warmup):
                      "dtype": "bf16", "check": chk, "gpu_launches_per_step": wl.launches}
         del wl
 
-    for budget in (8192, 2048):
-        wl = MixedSchedule(dev, budget=budget)
+    for budget, overlap in ((8192, False), (8192, True), (2048, False), (2048, True)):
+        wl = MixedSchedule(dev, budget=budget, overlap=overlap)
         ms, chk = measure(wl, capture(wl.step, dev), flush, max(3, reps // 4), warmup, torch)
         t_star = sum(max(st["flops"] / (tc * 1e12), st["bytes"] / (hbm * 1e9)) for st in wl.steps) * 1e3
-        res[f"mixed_budget{budget}"] = {
+        res[f"mixed_budget{budget}" + ("_overlap" if overlap else "")] = {
             **wl.config(), "rows_per_s": wl.tokens / (ms / 1e3), "ms_per_schedule": ms,
             "flops_per_schedule": wl.flops, "decode_bytes_per_schedule": wl.decode_bytes,
             "roofline_time_ms": t_star, "roofline_frac": t_star / ms, "dtype": "bf16", "check": chk,
@@ -1259,7 +1269,7 @@ def run_single(args, rank, world, dev, pk, pk_src):
         kw = {"unpadded": unp}
         wl = LadderRuns(dev, pad=not args.no_pad)
     else:
-        wl = MixedSchedule(dev, budget=args.budget, decode_only=args.workload == "decode")
+        wl = MixedSchedule(dev, budget=args.budget, decode_only=args.workload == "decode", overlap=args.overlap)
     g = capture(wl.step, dev)
     for _ in range(max(args.warmup, 3)):
         g.replay()

@@ -445,19 +445,21 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_arrive_expect_tx(vf, bytes);
         }
         __syncwarp();
-        for (int pi = 0; pi < npg; ++pi) {
+        // One box per lane: box b < 2 * npg * DB is tensor b / (npg * DB) (K, then V),
+        // page (b / DB) % npg, 64-column half b % DB.
+        const int nbox = npg * DB;
+        for (int b0 = 0; b0 < 2 * nbox; b0 += 32) {
+          const int b = b0 + lane;
+          const int pi = (b / DB) % npg;
           const int page = __shfl_sync(0xffffffffu, my_page, pi);
-          if (lane == 0 && page >= 0)
-            for (int db = 0; db < DB; ++db)
-              tma_load_3d(dk + db * kBlockBytes + pi * ps * 128, &tm_k, kf, db * 64, 0, page * a.hkv + g);
+          if (b < 2 * nbox && page >= 0) {
+            const bool is_v = b >= nbox;
+            const int db = b % DB;
+            tma_load_3d((is_v ? dv : dk) + db * kBlockBytes + pi * ps * 128, is_v ? &tm_v : &tm_k, is_v ? vf : kf,
+                        db * 64, 0, page * a.hkv + g);
+          }
         }
         if (lane == 0 && i == 0 && q1) load_q(1);
-        for (int pi = 0; pi < npg; ++pi) {
-          const int page = __shfl_sync(0xffffffffu, my_page, pi);
-          if (lane == 0 && page >= 0)
-            for (int db = 0; db < DB; ++db)
-              tma_load_3d(dv + db * kBlockBytes + pi * ps * 128, &tm_v, vf, db * 64, 0, page * a.hkv + g);
-        }
       }
       issued = i;
     }

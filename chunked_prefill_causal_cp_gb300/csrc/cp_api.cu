@@ -164,12 +164,26 @@ bool make_tc_maps(const cp_layer_desc* d, const void* q, const void* out, int64_
 
 int launch_result(cudaError_t e) { return e == cudaSuccess ? CP_OK : CP_ERR_CUDA; }
 
+int run_tc_part(const cp_layer_desc* d, AttnArgs a, int64_t rows_total, const void* k, const void* v,
+                int batch_for_maps, cudaStream_t st, const void* k_new, const void* v_new, bool decode_ok, int kdec);
+
+// A caller-provided side stream and two events: when a call launches both the
+// split-KV kernels and the tensor-core kernel, the split-KV ones run on `side`
+// (forked from `st` after what came before, joined back before what follows),
+// so the memory-bound and the tensor-bound work share the GPU.
+struct ForkJoin {
+  cudaStream_t side;
+  cudaEvent_t fork, join;
+};
+
 // Attention over every sequence of `rows`, routed by dtype and row count.
 // k_new / v_new (may be NULL): this call's new K/V rows [rows_total, Hkv, D]; when given with a
 // paged cache, the tensor-core kernel reads the tiles made only of new rows from them.
+// fj (may be NULL): run the split-KV part beside the tensor-core part, as above.
 int run_attention(const cp_layer_desc* d, const AttnArgs& base, int64_t rows_total, int rows_max_per_seq,
                   const void* k, const void* v, int batch_for_maps, void* workspace, size_t ws_bytes,
-                  cudaStream_t st, const void* k_new = nullptr, const void* v_new = nullptr) {
+                  cudaStream_t st, const void* k_new = nullptr, const void* v_new = nullptr,
+                  const ForkJoin* fj = nullptr) {
   const int G = d->num_q_heads / d->num_kv_heads;
   AttnArgs a = base;
   if (d->dtype == CP_F32) {
@@ -183,7 +197,9 @@ int run_attention(const cp_layer_desc* d, const AttnArgs& base, int64_t rows_tot
   const int kdec = decode_rows_for(d, base.rows.rows_uniform);
   const bool any_multi = rows_max_per_seq > kdec;
   const bool any_single = base.rows.rows_uniform == 0 || base.rows.rows_uniform == kdec;
-  if (decode_ok && any_single) {
+  const bool run_dec = decode_ok && any_single, run_tc = any_multi || !decode_ok;
+  const bool forked = fj != nullptr && run_dec && run_tc;
+  if (run_dec) {
     const int64_t need = decode_ws_bytes(d, a.max_ctx, (int64_t)a.rows.num_seqs * kdec);
     if (workspace == nullptr || (int64_t)ws_bytes < need) return CP_ERR_WORKSPACE;
     AttnArgs dec = a;
@@ -192,33 +208,52 @@ int run_attention(const cp_layer_desc* d, const AttnArgs& base, int64_t rows_tot
     dec.max_splits = (int)max_splits_for(a.max_ctx);
     dec.part_ml =
         dec.part_o + (int64_t)a.rows.num_seqs * kdec * d->num_q_heads * dec.max_splits * d->head_dim;
-    const int r = launch_result(launch_decode(dec, d->dtype, st));
-    if (r != CP_OK) return r;
-  }
-  if (any_multi || !decode_ok) {
-    a.min_rows = decode_ok ? kdec + 1 : 1;
-    CUtensorMap tq, to, tk, tv, tkn, tvn;
-    if (!make_tc_maps(d, a.q, a.out, rows_total, k, v, batch_for_maps, &tq, &to, &tk, &tv)) return CP_ERR_CUDA;
-    std::memset(&tkn, 0, sizeof(tkn));
-    std::memset(&tvn, 0, sizeof(tvn));
-    a.kv_direct = 0;
-    if (d->kind == CP_CACHE_PAGED && k_new && v_new) {
-      const uint64_t D = d->head_dim;
-      if (!encode_3d(&tkn, d->dtype, k_new, D, d->num_kv_heads, (uint64_t)rows_total, 64, 1, kTcBlockN) ||
-          !encode_3d(&tvn, d->dtype, v_new, D, d->num_kv_heads, (uint64_t)rows_total, 64, 1, kTcBlockN))
+    cudaStream_t dst = st;
+    if (forked) {
+      if (cudaEventRecord(fj->fork, st) != cudaSuccess || cudaStreamWaitEvent(fj->side, fj->fork, 0) != cudaSuccess)
         return CP_ERR_CUDA;
-      a.kv_direct = 1;
+      dst = fj->side;
     }
-    const int ppt = 2 * (kTcBlockM / G);  // tokens per pair of 128-row Q tiles
-    int64_t pairs;
-    if (a.rows.rows_uniform > 0)
-      pairs = (int64_t)a.rows.num_seqs * ((a.rows.rows_uniform + ppt - 1) / ppt);
-    else
-      pairs = (rows_total + ppt - 1) / ppt + a.rows.num_seqs;
-    if (2 * pairs > INT32_MAX) return CP_ERR_UNSUPPORTED;
-    return launch_result(launch_attn_tc(a, d->dtype, tq, tk, tv, to, tkn, tvn, (int)pairs, st));
+    int r = launch_result(launch_decode(dec, d->dtype, dst));
+    if (forked && cudaEventRecord(fj->join, fj->side) != cudaSuccess && r == CP_OK) r = CP_ERR_CUDA;
+    if (r != CP_OK) {
+      if (forked) cudaStreamWaitEvent(st, fj->join, 0);
+      return r;
+    }
+  }
+  if (run_tc) {
+    const int r = run_tc_part(d, a, rows_total, k, v, batch_for_maps, st, k_new, v_new, decode_ok, kdec);
+    if (forked && cudaStreamWaitEvent(st, fj->join, 0) != cudaSuccess && r == CP_OK) return CP_ERR_CUDA;
+    return r;
   }
   return CP_OK;
+}
+
+// The tensor-core part of run_attention.
+int run_tc_part(const cp_layer_desc* d, AttnArgs a, int64_t rows_total, const void* k, const void* v,
+                int batch_for_maps, cudaStream_t st, const void* k_new, const void* v_new, bool decode_ok, int kdec) {
+  const int G = d->num_q_heads / d->num_kv_heads;
+  a.min_rows = decode_ok ? kdec + 1 : 1;
+  CUtensorMap tq, to, tk, tv, tkn, tvn;
+  if (!make_tc_maps(d, a.q, a.out, rows_total, k, v, batch_for_maps, &tq, &to, &tk, &tv)) return CP_ERR_CUDA;
+  std::memset(&tkn, 0, sizeof(tkn));
+  std::memset(&tvn, 0, sizeof(tvn));
+  a.kv_direct = 0;
+  if (d->kind == CP_CACHE_PAGED && k_new && v_new) {
+    const uint64_t D = d->head_dim;
+    if (!encode_3d(&tkn, d->dtype, k_new, D, d->num_kv_heads, (uint64_t)rows_total, 64, 1, kTcBlockN) ||
+        !encode_3d(&tvn, d->dtype, v_new, D, d->num_kv_heads, (uint64_t)rows_total, 64, 1, kTcBlockN))
+      return CP_ERR_CUDA;
+    a.kv_direct = 1;
+  }
+  const int ppt = 2 * (kTcBlockM / G);  // tokens per pair of 128-row Q tiles
+  int64_t pairs;
+  if (a.rows.rows_uniform > 0)
+    pairs = (int64_t)a.rows.num_seqs * ((a.rows.rows_uniform + ppt - 1) / ppt);
+  else
+    pairs = (rows_total + ppt - 1) / ppt + a.rows.num_seqs;
+  if (2 * pairs > INT32_MAX) return CP_ERR_UNSUPPORTED;
+  return launch_result(launch_attn_tc(a, d->dtype, tq, tk, tv, to, tkn, tvn, (int)pairs, st));
 }
 
 // A contiguous-cache chunk of uniform rows (more than one) in half precision
@@ -266,7 +301,7 @@ int run_fused(const cp_layer_desc* d, AttnArgs a, int64_t rows_total, const void
 int ragged_step(const cp_layer_desc* desc, const void* q, const void* k_new, const void* v_new, void* k_cache,
                 void* v_cache, const int32_t* block_table, const int32_t* cu_rows, int32_t* past_len,
                 int32_t num_seqs, int32_t total_rows, int32_t max_ctx, void* out, void* workspace,
-                size_t workspace_bytes, int32_t* dev_status, cudaStream_t st) {
+                size_t workspace_bytes, int32_t* dev_status, cudaStream_t st, const ForkJoin* fj = nullptr) {
   const SeqRows rows{num_seqs, 0, cu_rows};
   const CacheView cache = make_cache(desc, block_table);
 
@@ -308,7 +343,7 @@ int ragged_step(const cp_layer_desc* desc, const void* q, const void* k_new, con
   const int64_t max_rows_per_seq = total_rows >= num_seqs ? (int64_t)total_rows - num_seqs + 1 : total_rows;
   const bool paged = desc->kind == CP_CACHE_PAGED;
   r = run_attention(desc, a, total_rows, (int)max_rows_per_seq, k_cache, v_cache, paged ? 0 : desc->batch, workspace,
-                    workspace_bytes, st, paged ? k_new : nullptr, paged ? v_new : nullptr);
+                    workspace_bytes, st, paged ? k_new : nullptr, paged ? v_new : nullptr, fj);
   if (r != CP_OK) return r;
   return launch_result(launch_commit(past_len, rows, -1, dev_status, st));
 }
@@ -560,6 +595,24 @@ int cp_mixed_step(const cp_layer_desc* desc, const void* q, const void* k_new, c
   if (need > 0 && (workspace == nullptr || workspace_bytes < need || !aligned16(workspace))) return CP_ERR_WORKSPACE;
   return ragged_step(desc, q, k_new, v_new, k_pages, v_pages, block_table, cu_rows, past_len, num_seqs, total_rows,
                      max_ctx, out, workspace, workspace_bytes, dev_status, static_cast<cudaStream_t>(stream));
+}
+
+int cp_mixed_step_overlap(const cp_layer_desc* desc, const void* q, const void* k_new, const void* v_new,
+                          void* k_pages, void* v_pages, const int32_t* block_table, const int32_t* cu_rows,
+                          int32_t* past_len, int32_t num_seqs, int32_t total_rows, int32_t max_ctx, void* out,
+                          void* workspace, size_t workspace_bytes, int32_t* dev_status, void* stream,
+                          void* side_stream, void* fork_event, void* join_event) {
+  size_t need = 0;
+  int r = cp::mixed_step_check(desc, q, k_new, v_new, k_pages, v_pages, block_table, cu_rows, past_len, num_seqs,
+                               total_rows, max_ctx, out, &need);
+  if (r != CP_OK) return r;
+  if (!side_stream || !fork_event || !join_event || side_stream == stream) return CP_ERR_INVALID_ARG;
+  if (total_rows == 0) return CP_OK;
+  if (need > 0 && (workspace == nullptr || workspace_bytes < need || !aligned16(workspace))) return CP_ERR_WORKSPACE;
+  const ForkJoin fj{static_cast<cudaStream_t>(side_stream), static_cast<cudaEvent_t>(fork_event),
+                    static_cast<cudaEvent_t>(join_event)};
+  return ragged_step(desc, q, k_new, v_new, k_pages, v_pages, block_table, cu_rows, past_len, num_seqs, total_rows,
+                     max_ctx, out, workspace, workspace_bytes, dev_status, static_cast<cudaStream_t>(stream), &fj);
 }
 
 int cp_prefill_varlen(const cp_layer_desc* desc, const void* q, const void* k_new, const void* v_new, void* k_cache,

@@ -221,6 +221,34 @@ int cp_mixed_step(const cp_layer_desc* desc, const void* q, const void* k_new,
                   int32_t total_rows, int32_t max_ctx, void* out, void* workspace,
                   size_t workspace_bytes, int32_t* dev_status, void* stream);
 
+/* cp_mixed_step_overlap -- cp_mixed_step with its two attention paths running
+ * side by side.
+ *
+ * [Glossary] "How chunked prefill works": the decode rows of a mixed step are
+ * memory-bound and the prompt chunks compute-bound, so the GPU can serve both
+ * at once.  This call does what cp_mixed_step does, with the same arguments,
+ * checks, status codes and results (bit for bit), but when a step has both
+ * decode rows and prompt chunks it launches the split-KV kernels on
+ * `side_stream` and the tensor-core kernel on `stream` in between:
+ *   stream:      append -> record(fork_event) -> tensor-core attention
+ *                -> wait(join_event) -> length advance
+ *   side_stream: wait(fork_event) -> split-KV + combine -> record(join_event)
+ * A step with only one kind of row runs everything on `stream`.
+ *   side_stream   a CUDA stream of the same device, not `stream` (caller-owned;
+ *                 work the caller queued there before the call runs first)
+ *   fork_event, join_event  caller-owned cudaEvent_t handles (created with
+ *                 cudaEventDisableTiming is best); the call records them, so
+ *                 they must not be waited on by other work until it returns.
+ * Under stream capture both streams join back into `stream` before the call
+ * returns, so the step captures as one graph.  NULL side_stream or events, or
+ * side_stream == stream, return CP_ERR_INVALID_ARG. */
+int cp_mixed_step_overlap(const cp_layer_desc* desc, const void* q, const void* k_new,
+                          const void* v_new, void* k_pages, void* v_pages,
+                          const int32_t* block_table, const int32_t* cu_rows, int32_t* past_len,
+                          int32_t num_seqs, int32_t total_rows, int32_t max_ctx, void* out,
+                          void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                          void* stream, void* side_stream, void* fork_event, void* join_event);
+
 /* cp_prefill_varlen -- one step of several prompts with ragged rows over a
  * contiguous cache.
  *

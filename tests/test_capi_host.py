@@ -254,6 +254,34 @@ def test_noalloc_status_codes_match_mixed_step():
         assert a == want and b == want, (kw, a, b, want)
 
 
+def test_overlap_status_codes_match_mixed_step():
+    """cp_mixed_step_overlap makes cp_mixed_step's argument checks first and
+    returns the same status; then it refuses a missing side stream or event and
+    a side stream equal to the main one (handles here are never used: every
+    case stops before anything is enqueued)."""
+    L = cp.lib()
+    pd = dict(kind=cp.CP_CACHE_PAGED, page_size=16, num_pages=64, max_blocks=8)
+    SIDE, EV1, EV2 = 0x2000, 0x3000, 0x4000
+
+    def ov(desc, num_seqs=2, total_rows=10, max_ctx=100, q=FAKE, out=FAKE, stream=None, side=SIDE, ev1=EV1,
+           ev2=EV2):
+        return L.cp_mixed_step_overlap(ctypes.byref(desc) if desc is not None else None, q, FAKE, FAKE, FAKE, FAKE,
+                                       FAKE, FAKE, FAKE, num_seqs, total_rows, max_ctx, out, FAKE, 1 << 30, None,
+                                       stream, side, ev1, ev2)
+
+    for desc, kw in [(_desc(head_dim=96, **pd), {}), (_desc(), {}), (_desc(num_q_heads=30, **pd), {}),
+                     (_desc(**pd), dict(num_seqs=0)), (_desc(**pd), dict(q=None)),
+                     (_desc(**pd), dict(max_ctx=8 * 16 + 1)), (None, {})]:
+        want, _ = _mixed_pair(desc, **kw)
+        assert want != cp.CP_OK and ov(desc, **kw) == want, kw
+    d = _desc(**pd)
+    assert ov(d, total_rows=0) == cp.CP_OK
+    assert ov(d, side=None) == cp.CP_ERR_INVALID_ARG
+    assert ov(d, ev1=None) == cp.CP_ERR_INVALID_ARG
+    assert ov(d, ev2=None) == cp.CP_ERR_INVALID_ARG
+    assert ov(d, stream=SIDE) == cp.CP_ERR_INVALID_ARG
+
+
 def test_noalloc_refuses_a_step_whose_partials_exceed_the_scratch():
     """The fixed scratch is compared with the split-KV partials cp_mixed_step
     would use for the step: one sequence more than fits is refused with

@@ -49,7 +49,8 @@ class Paged:
             self.ok[pages.numpy(), :, (a % PAGE).numpy()] = f64(kv_k.to(self.dtype))
             self.ov[pages.numpy(), :, (a % PAGE).numpy()] = f64(kv_v.to(self.dtype))
 
-    def step(self, seqs, rows, past, q, kn, vn, max_ctx):
+    def args(self, seqs, rows, past, max_ctx):
+        """Device buffers of one step: cu_rows, past lengths, block table, output, workspace."""
         S = len(seqs)
         cu = torch.tensor(np.concatenate([[0], np.cumsum(rows)]), dtype=torch.int32, device="cuda")
         pl = torch.tensor(past, dtype=torch.int32, device="cuda")
@@ -57,8 +58,21 @@ class Paged:
         T = int(sum(rows))
         out = torch.empty(T, HQ, D, dtype=self.dtype, device="cuda")
         ws = torch.zeros(cp.cp_workspace_size(self.desc, T, max_ctx, S), dtype=torch.uint8, device="cuda")
-        cp.cp_mixed_step(self.desc, q, kn, vn, self.k, self.v, bt, cu, pl, S, T, max_ctx, out, ws,
-                         dev_status=self.status)
+        return cu, pl, bt, out, ws
+
+    def launch(self, q, kn, vn, cu, pl, bt, out, ws, max_ctx, overlap=None):
+        """One step on the current stream; `overlap` = (side stream, fork event, join event)."""
+        S, T = pl.numel(), q.shape[0]
+        if overlap is None:
+            cp.cp_mixed_step(self.desc, q, kn, vn, self.k, self.v, bt, cu, pl, S, T, max_ctx, out, ws,
+                             dev_status=self.status)
+        else:
+            cp.cp_mixed_step_overlap(self.desc, q, kn, vn, self.k, self.v, bt, cu, pl, S, T, max_ctx, out, ws,
+                                     *overlap, dev_status=self.status)
+
+    def step(self, seqs, rows, past, q, kn, vn, max_ctx, overlap=None):
+        cu, pl, bt, out, ws = self.args(seqs, rows, past, max_ctx)
+        self.launch(q, kn, vn, cu, pl, bt, out, ws, max_ctx, overlap)
         return out, pl
 
 
@@ -87,7 +101,16 @@ def _layout(ctx, prompts, seed):
     return mb
 
 
-def _run_schedule(budget, ctx, prompts, seed):
+def _same_bits(a, b):
+    """Equal bit patterns (pool slots never written hold NaN)."""
+    return torch.equal(a.view(torch.int16), b.view(torch.int16))
+
+
+def _overlap_handles():
+    return torch.cuda.Stream(), torch.cuda.Event(), torch.cuda.Event()
+
+
+def _run_schedule(budget, ctx, prompts, seed, overlap=False):
     """Every step cp_schedule gives for `budget`, on the GPU and in the oracle:
     each step's every row within tolerance, past lengths advanced by the rows,
     and at the end the pools equal the oracle's bit for bit (slots never
@@ -101,6 +124,7 @@ def _run_schedule(budget, ctx, prompts, seed):
     pq = [SI.gqa_prompt(n, seed=30 + i) for i, n in enumerate(prompts)]
     nd = len(ctx)
     plan = _schedule_steps(budget, nd, prompts)
+    handles = _overlap_handles() if overlap else None
     for si, entries in enumerate(plan):
         assert sum(r for _, _, r in entries) <= budget
         seqs, rows, qs, ks, vs = [], [], [], [], []
@@ -116,7 +140,7 @@ def _run_schedule(budget, ctx, prompts, seed):
         q = torch.cat(qs); kn = torch.cat(ks); vn = torch.cat(vs)
         past = [pos[s] for s in seqs]
         max_ctx = max(p + r for p, r in zip(past, rows))
-        out, pl = P.step(seqs, rows, past, q.cuda(), kn.cuda(), vn.cuda(), max_ctx)
+        out, pl = P.step(seqs, rows, past, q.cuda(), kn.cuda(), vn.cuda(), max_ctx, handles)
         torch.cuda.synchronize()
         ref, P.ok, P.ov, newp = oracle.mixed_step(f64(q), f64(kn), f64(vn), P.ok, P.ov,
                                                   mb.block_table[seqs].numpy(), rows, past)
@@ -138,6 +162,53 @@ def test_mixed_steps_reduced_full_check():
     """8 decodes with contexts at page and split edges plus 2 prompts, budget 256."""
     n = _run_schedule(256, [1, 2, 16, 17, 511, 512, 513, 700], [600, 450], seed=21)
     assert n >= 5
+
+
+def test_overlap_schedule_reduced_full_check():
+    """The same schedule through cp_mixed_step_overlap (split-KV kernels on a
+    side stream): every row against the oracle, then the pools."""
+    n = _run_schedule(256, [1, 2, 16, 17, 511, 512, 513, 700], [600, 450], seed=21, overlap=True)
+    assert n >= 5
+
+
+def test_overlap_is_bit_identical_to_mixed_step():
+    """64 decodes (contexts U{1..3000}) beside a 1500-row prompt chunk:
+    cp_mixed_step_overlap gives cp_mixed_step's output, pools and lengths bit
+    for bit, launched eagerly and replayed from a captured CUDA graph."""
+    ctx = torch.randint(1, 3001, (64,), generator=torch.Generator().manual_seed(31)).tolist()
+    mb = _layout(ctx, [1500], seed=31)
+    P = Paged(mb, with_oracle=False)
+    for s, c in enumerate(ctx):
+        if c > 1:
+            P.prefill_history(s, SI.normal((c - 1, HKV, D), 700 + s), SI.normal((c - 1, HKV, D), 800 + s))
+    dq, dk, dv = SI.gqa_prompt(64, seed=52)
+    qp, kp, vp = SI.gqa_prompt(1500, seed=53)
+    q = torch.cat([dq, qp]).cuda(); kn = torch.cat([dk, kp]).cuda(); vn = torch.cat([dv, vp]).cuda()
+    seqs, rows, past = list(range(65)), [1] * 64 + [1500], [c - 1 for c in ctx] + [0]
+    max_ctx = max(p + r for p, r in zip(past, rows))
+    k0, v0 = P.k.clone(), P.v.clone()
+    want, pl_want = P.step(seqs, rows, past, q, kn, vn, max_ctx)
+    torch.cuda.synchronize()
+    kw, vw = P.k.clone(), P.v.clone()
+    handles = _overlap_handles()
+    P.k.copy_(k0); P.v.copy_(v0)
+    got, pl_got = P.step(seqs, rows, past, q, kn, vn, max_ctx, handles)
+    torch.cuda.synchronize()
+    assert torch.equal(got, want) and torch.equal(pl_got, pl_want)
+    assert _same_bits(P.k, kw) and _same_bits(P.v, vw)
+    # Captured: both streams join back into the capture stream.
+    cu, pl, bt, out, ws = P.args(seqs, rows, past, max_ctx)
+    past_dev = pl.clone()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        P.launch(q, kn, vn, cu, pl, bt, out, ws, max_ctx, handles)
+    for _ in range(2):
+        P.k.copy_(k0); P.v.copy_(v0); pl.copy_(past_dev); out.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(out, want) and torch.equal(pl, pl_want)
+        assert _same_bits(P.k, kw) and _same_bits(P.v, vw)
+    assert int(P.status.item()) == 0
 
 
 def test_mixed_schedule_budget_2048():
