@@ -149,13 +149,19 @@ __device__ __forceinline__ uint32_t pack2<__half>(float lo, float hi) {
 }
 
 // Which (sequence, first token) a cluster owns; a pair covers 2*rpt tokens.
-// Within a sequence the pairs are handed out last-first, so the pairs with
-// the most keys start earliest.  Every warp of the CTA calls this with all
+// With a work list it is entry w; otherwise, within a sequence the pairs are
+// handed out last-first, so the pairs with the most keys start earliest.  Every warp of the CTA calls this with all
 // lanes: for ragged rows each warp scans the sequences 32 at a time (one
 // coalesced round of loads per 32 sequences, a shuffle prefix sum of their
 // pair counts), so the lookup costs a few memory latencies, not one per
 // sequence.
 __device__ __forceinline__ bool find_pair(const AttnArgs& a, int ppt, int w, int& s, int& t0) {
+  if (a.pair_order) {
+    const int2 e = a.pair_order[w];
+    s = e.x;
+    t0 = e.y;
+    return e.x >= 0;
+  }
   if (a.rows.rows_uniform > 0) {
     const int np = (a.rows.rows_uniform + ppt - 1) / ppt;
     const int pair = np - 1 - w / a.rows.num_seqs;
@@ -276,7 +282,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = a.group;
   const int rpt = kTcBlockM / G;  // tokens per Q tile
-  const int g = blockIdx.y;
+  // The cluster's work: with a work list, pair L / hkv of KV head L % hkv for
+  // the cluster's linear index L (so the heaviest pairs of every head start
+  // first); else pair blockIdx.x / 2 of KV head blockIdx.y.
+  const int cl = (int)blockIdx.y * (int)(gridDim.x >> 1) + (int)(blockIdx.x >> 1);
+  const int g = a.pair_order ? cl % a.hkv : (int)blockIdx.y;
+  const int w_pair = a.pair_order ? cl / a.hkv : (int)(blockIdx.x >> 1);
   const int rank = (int)cluster_ctarank();
 
   // ---- set-up that reads no global memory: it may overlap the previous kernel
@@ -321,7 +332,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   // ---- this cluster's pair (the same for both CTAs, so both leave together)
   int s = 0, t0 = 0, rows = 0, past = 0;
-  bool have_pair = find_pair(a, 2 * rpt, blockIdx.x >> 1, s, t0);
+  bool have_pair = find_pair(a, 2 * rpt, w_pair, s, t0);
   if (have_pair) {
     rows = seq_rows(a.rows, s);
     past = a.past[s];

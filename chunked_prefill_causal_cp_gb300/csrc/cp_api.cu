@@ -298,6 +298,37 @@ int run_fused(const cp_layer_desc* d, AttnArgs a, int64_t rows_total, const void
 // one-row sequences take the split-KV decode path and the others the
 // tensor-core path, reading the lengths as they were before the step; a last
 // kernel advances each length by its own rows.  Arguments already checked.
+// Where a ragged call's work list goes: after the split-KV partials, 16-byte
+// aligned, one int2 per pair the tensor-core grid has room for.  `use` is false
+// when the tensor-core kernel will not run (fp32 layers, or one row per
+// sequence on the split-KV path).
+struct PairOrderPlan {
+  bool use;
+  int64_t offset, bytes;
+  int pair_tokens, min_rows, pairs_bound;
+};
+
+PairOrderPlan pair_order_plan(const cp_layer_desc* d, int64_t total_rows, int32_t max_ctx, int32_t num_seqs,
+                              int64_t max_rows_per_seq) {
+  PairOrderPlan p{false, 0, 0, 0, 0, 0};
+  const int G = d->num_q_heads / d->num_kv_heads;
+  if (d->dtype == CP_F32 || !attn_tc_supported(d->head_dim, G, d->dtype)) return p;
+  const bool decode_ok = decode_supported(d->head_dim, G, d->dtype) && d->kind != CP_CACHE_ROLLING;
+  const int kdec = decode_rows_for(d, 0);
+  if (decode_ok && max_rows_per_seq <= kdec) return p;
+  const int64_t dec_need = decode_ok ? decode_ws_bytes(d, max_ctx, num_seqs) : 0;
+  const int ppt = 2 * (kTcBlockM / G);
+  const int64_t pairs = (total_rows + ppt - 1) / ppt + num_seqs;  // the tensor-core grid's pair bound
+  if (2 * pairs > INT32_MAX) return p;
+  p.use = true;
+  p.offset = (dec_need + 15) / 16 * 16;
+  p.bytes = pairs * 8;
+  p.pair_tokens = ppt;
+  p.min_rows = decode_ok ? kdec + 1 : 1;
+  p.pairs_bound = (int)pairs;
+  return p;
+}
+
 int ragged_step(const cp_layer_desc* desc, const void* q, const void* k_new, const void* v_new, void* k_cache,
                 void* v_cache, const int32_t* block_table, const int32_t* cu_rows, int32_t* past_len,
                 int32_t num_seqs, int32_t total_rows, int32_t max_ctx, void* out, void* workspace,
@@ -318,6 +349,19 @@ int ragged_step(const cp_layer_desc* desc, const void* q, const void* k_new, con
   ap.k_cache = k_cache;
   ap.v_cache = v_cache;
   ap.status = dev_status;
+  // Every listed sequence has at least one row, so none has more than
+  // total_rows - num_seqs + 1; with one row each the tensor-core path has no
+  // work and is not launched.
+  const int64_t max_rows_per_seq = total_rows >= num_seqs ? (int64_t)total_rows - num_seqs + 1 : total_rows;
+  // The tensor-core kernel's heaviest-first work list, built by the append
+  // kernel, when the workspace has room for it after the split-KV partials.
+  const PairOrderPlan plan = pair_order_plan(desc, total_rows, max_ctx, num_seqs, max_rows_per_seq);
+  if (plan.use && workspace && aligned16(workspace) && (int64_t)workspace_bytes >= plan.offset + plan.bytes) {
+    ap.pair_order = reinterpret_cast<int2*>(static_cast<char*>(workspace) + plan.offset);
+    ap.pair_tokens = plan.pair_tokens;
+    ap.pair_min_rows = plan.min_rows;
+    ap.pairs_bound = plan.pairs_bound;
+  }
   int r = launch_result(launch_kv_append(ap, total_rows, st));
   if (r != CP_OK) return r;
 
@@ -337,10 +381,7 @@ int ragged_step(const cp_layer_desc* desc, const void* q, const void* k_new, con
   a.v = v_cache;
   a.out = out;
   a.status = dev_status;
-  // Every listed sequence has at least one row, so none has more than
-  // total_rows - num_seqs + 1; with one row each the tensor-core path has no
-  // work and is not launched.
-  const int64_t max_rows_per_seq = total_rows >= num_seqs ? (int64_t)total_rows - num_seqs + 1 : total_rows;
+  a.pair_order = ap.pair_order;
   const bool paged = desc->kind == CP_CACHE_PAGED;
   r = run_attention(desc, a, total_rows, (int)max_rows_per_seq, k_cache, v_cache, paged ? 0 : desc->batch, workspace,
                     workspace_bytes, st, paged ? k_new : nullptr, paged ? v_new : nullptr, fj);
@@ -395,7 +436,15 @@ size_t cp_workspace_size(const cp_layer_desc* desc, int32_t max_rows, int32_t ma
     const int64_t per_seq = std::max<int64_t>(1, ((int64_t)max_rows + num_seqs - 1) / num_seqs);
     dec_rows = (int64_t)num_seqs * std::min<int64_t>(per_seq, decode_max_rows(G));
   }
-  return (size_t)(kControlBytes + snapshot_bytes(num_seqs) + decode_ws_bytes(desc, max_ctx, dec_rows));
+  // A ragged call's work list for the tensor-core kernel (one int2 per pair),
+  // placed after its split-KV partials (which the terms above cover).
+  int64_t order = 0;
+  const int G = desc->num_q_heads / desc->num_kv_heads;
+  if (desc->dtype != CP_F32 && attn_tc_supported(desc->head_dim, G, desc->dtype)) {
+    const int ppt = 2 * (kTcBlockM / G);
+    order = ((int64_t)(max_rows + ppt - 1) / ppt + num_seqs) * 8 + 16;
+  }
+  return (size_t)(kControlBytes + snapshot_bytes(num_seqs) + decode_ws_bytes(desc, max_ctx, dec_rows) + order);
 }
 
 int cp_kv_append(const cp_layer_desc* desc, const void* k_new, const void* v_new, int32_t rows, void* k_cache,

@@ -75,6 +75,12 @@ struct AttnArgs {
   const void* v_new = nullptr;
   void* k_cache = nullptr;
   void* v_cache = nullptr;
+  // Tensor-core kernel, ragged rows: if set, the work of cluster L (linear
+  // index over the grid) is pair_order[L / hkv] for KV head L % hkv, a list the
+  // append kernel wrote with the pairs that see the most keys first (entries
+  // with a negative sequence are empty).  Else pair blockIdx.x / 2 of KV head
+  // blockIdx.y, found by scanning the sequences.
+  const int2* pair_order = nullptr;
 };
 
 struct AppendArgs {
@@ -89,6 +95,15 @@ struct AppendArgs {
   void* v_cache;
   int* status;
   int* past_snapshot = nullptr;  // optional [num_seqs]: CTA 0 copies past[] here
+  // Optional work list for the tensor-core kernel that follows (ragged rows):
+  // one extra CTA writes pairs_bound entries (sequence, first token) -- every
+  // pair of pair_tokens tokens of the sequences with at least pair_min_rows
+  // rows, ordered by the keys the pair's last token sees, most first (equal
+  // counts in any order), then (-1, 0) entries up to pairs_bound.
+  int2* pair_order = nullptr;
+  int pair_tokens = 0;
+  int pair_min_rows = 0;
+  int pairs_bound = 0;
 };
 
 // Launches `kernel` with programmatic dependent launch allowed: the grid may

@@ -43,9 +43,121 @@ __device__ __forceinline__ long long slot_offset(const CacheView& c, int hkv, in
   return ((long long)(page * hkv + g) * c.page_size + pos % c.page_size) * d;
 }
 
-__global__ void kv_append_kernel(const AppendArgs a, int rows_total) {
+// Buckets of the work list's counting sort: 128 keys each; pairs that see
+// more keys than the last bucket holds share it.
+constexpr int kOrderBuckets = 4096;
+constexpr int kAppendBlock = 256;
+
+__device__ __forceinline__ int order_bucket(int keys) {
+  return min(max((keys + 127) >> 7, 0), kOrderBuckets - 1);
+}
+
+// Exclusive prefix sum of v over the kAppendBlock threads; *total gets the sum.
+__device__ __forceinline__ int block_exclusive_scan(int v, int* wsum, int* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) wsum[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    int w = lane < kAppendBlock / 32 ? wsum[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < kAppendBlock / 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= o) w += y;
+    }
+    if (lane < kAppendBlock / 32) wsum[lane] = w;
+  }
+  __syncthreads();
+  const int res = (warp > 0 ? wsum[warp - 1] : 0) + x - v;
+  *total = wsum[kAppendBlock / 32 - 1];
+  __syncthreads();  // wsum may be reused
+  return res;
+}
+
+// The tensor-core kernel's work list, heaviest pairs first (see AppendArgs):
+// a histogram of the pairs' key counts, a descending exclusive scan of it, and
+// a second pass that places each pair at its bucket's cursor.  The sequences
+// go kAppendBlock at a time: a scan of their pair counts gives each pair an
+// index, and each thread takes pairs by index.  Entries past pairs_bound (only
+// from malformed row offsets) are dropped and reported.
+__device__ void build_pair_order(const AppendArgs& a) {
+  __shared__ int hist[kOrderBuckets];
+  __shared__ int s_off[kAppendBlock + 1], s_r[kAppendBlock], s_p[kAppendBlock];
+  __shared__ int wsum[kAppendBlock / 32];
+  const int tid = threadIdx.x;
+  const int ppt = a.pair_tokens;
+  for (int b = tid; b < kOrderBuckets; b += kAppendBlock) hist[b] = 0;
+  __syncthreads();
+  int total = 0;
+  for (int pass = 0; pass < 2; ++pass) {
+    for (int s0 = 0; s0 < a.rows.num_seqs; s0 += kAppendBlock) {
+      const int s = s0 + tid;
+      int r = 0, p = 0, np = 0;
+      if (s < a.rows.num_seqs) {
+        r = seq_rows(a.rows, s);
+        p = a.past[s];
+        if (r >= a.pair_min_rows && r > 0) np = min((r + ppt - 1) / ppt, a.pairs_bound);
+      }
+      int chunk = 0;
+      const int off = block_exclusive_scan(np, wsum, &chunk);
+      s_off[tid] = off;
+      s_r[tid] = r;
+      s_p[tid] = p;
+      if (tid == 0) s_off[kAppendBlock] = chunk;
+      __syncthreads();
+      for (int i = tid; i < chunk; i += kAppendBlock) {
+        int lo = 0, hi = kAppendBlock - 1;  // last j with s_off[j] <= i
+        while (lo < hi) {
+          const int mid = (lo + hi + 1) >> 1;
+          if (s_off[mid] <= i) lo = mid; else hi = mid - 1;
+        }
+        const int k = i - s_off[lo];
+        const int b = order_bucket(s_p[lo] + min((k + 1) * ppt, s_r[lo]));
+        if (pass == 0) {
+          atomicAdd(&hist[b], 1);
+        } else {
+          const int pos = atomicAdd(&hist[b], 1);
+          if (pos < a.pairs_bound)
+            a.pair_order[pos] = make_int2(s0 + lo, k * ppt);
+          else if (a.status)
+            atomicOr(a.status, CP_DEV_BOUNDS);
+        }
+      }
+      __syncthreads();
+    }
+    if (pass == 0) {
+      // Thread t owns the buckets that come t-th from the top, per at a time;
+      // each bucket becomes the index of its first entry.
+      constexpr int per = kOrderBuckets / kAppendBlock;
+      const int top = kOrderBuckets - 1 - tid * per;
+      int sum = 0;
+#pragma unroll
+      for (int i = 0; i < per; ++i) sum += hist[top - i];
+      int before = block_exclusive_scan(sum, wsum, &total);
+#pragma unroll
+      for (int i = 0; i < per; ++i) {
+        const int c = hist[top - i];
+        hist[top - i] = before;
+        before += c;
+      }
+      __syncthreads();
+    }
+  }
+  for (int i = min(total, a.pairs_bound) + tid; i < a.pairs_bound; i += kAppendBlock) a.pair_order[i] = make_int2(-1, 0);
+}
+
+__global__ void __launch_bounds__(kAppendBlock) kv_append_kernel(const AppendArgs a, int rows_total) {
   pdl_launch_dependents();
   pdl_wait();
+  if (a.pair_order && blockIdx.x == gridDim.x - 1) {  // the extra CTA
+    build_pair_order(a);
+    return;
+  }
   if (a.past_snapshot && blockIdx.x == 0)
     for (int s = threadIdx.x; s < a.rows.num_seqs; s += blockDim.x) a.past_snapshot[s] = a.past[s];
   const int vec_per_row = a.d * a.esize / 16;           // 16-byte vectors per row
@@ -116,8 +228,8 @@ cudaError_t launch_kv_append(const AppendArgs& a, int rows_total, cudaStream_t s
   const long long vec_per_row = a.d * a.esize / 16;
   const long long threads = (long long)rows_total * a.hkv * vec_per_row;
   if (threads == 0) return cudaSuccess;
-  const int block = 256;
-  const long long grid = (threads + block - 1) / block;
+  const int block = kAppendBlock;
+  const long long grid = (threads + block - 1) / block + (a.pair_order ? 1 : 0);
   return launch_pdl(kv_append_kernel, dim3((unsigned)grid), dim3(block), 0, st, a, rows_total);
 }
 

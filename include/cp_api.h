@@ -325,7 +325,12 @@ size_t cp_noalloc_scratch_bytes(void);
  * there) and the split-KV partial results: for each sequence, one row's, or
  * up to 16 / G rows' when a call's rows per sequence are that few (short
  * chunks, e.g. k draft tokens verified in one pass, take the split-KV path
- * together). */
+ * together); for 16-bit layers, also room for the work list of a ragged call
+ * (cp_mixed_step, cp_mixed_step_overlap, cp_prefill_varlen): 8 bytes per pair
+ * of 2 * 128 / G query tokens plus 8 per sequence.  A ragged call keeps the
+ * list after its split-KV partials and uses it only when the workspace has
+ * room: it then hands the tensor-core kernel's clusters the pairs that see
+ * the most keys first (results are the same bit for bit either way). */
 size_t cp_workspace_size(const cp_layer_desc* desc, int32_t max_rows, int32_t max_ctx,
                          int32_t num_seqs);
 

@@ -137,7 +137,7 @@ def test_fused_chunk_rejects_bad_arguments_before_launch():
     # the copy of the lengths always needs the workspace; one-row chunks (decode) need the partials too
     assert _chunk(_desc(), ws=None) == cp.CP_ERR_WORKSPACE
     assert _chunk(_desc(), ws_bytes=511) == cp.CP_ERR_WORKSPACE
-    need = cp.cp_workspace_size(_desc(), 1, 101, 1)
+    need = 256 + 256 + 32 * 1 * 130 * 4  # control block, lengths copy, one row's split partials
     assert _chunk(_desc(), rows=1, real=1, max_past=100, ws_bytes=need - 1) == cp.CP_ERR_WORKSPACE
     assert _chunk(_desc(), ws=FAKE + 4) == cp.CP_ERR_WORKSPACE
     # the same layout rules as the separate calls
@@ -196,18 +196,26 @@ def test_varlen_rejects_bad_arguments():
     assert call(total=0) == cp.CP_OK  # nothing to do
 
 
+def _order(max_rows, num_seqs, ppt=64):
+    """The ragged calls' work list: one 8-byte entry per pair of ppt tokens
+    (2 * 128 / G; G = 4 here), one more per sequence, plus 16 bytes of alignment."""
+    return (-(-max_rows // ppt) + num_seqs) * 8 + 16
+
+
 def test_workspace_size_formula():
     d = _desc()
     # split-KV partials for up to min(rows per sequence, 16 / G) rows per sequence (G = 4 here)
-    assert cp.cp_workspace_size(d, 8, 1, 2) == 256 + 256 + 2 * 4 * 32 * 1 * 130 * 4
-    assert cp.cp_workspace_size(d, 4, 1, 2) == 256 + 256 + 2 * 2 * 32 * 1 * 130 * 4
-    assert cp.cp_workspace_size(d, 512, 1, 1) == 256 + 256 + 4 * 32 * 1 * 130 * 4
+    assert cp.cp_workspace_size(d, 8, 1, 2) == 256 + 256 + 2 * 4 * 32 * 1 * 130 * 4 + _order(8, 2)
+    assert cp.cp_workspace_size(d, 4, 1, 2) == 256 + 256 + 2 * 2 * 32 * 1 * 130 * 4 + _order(4, 2)
+    assert cp.cp_workspace_size(d, 512, 1, 1) == 256 + 256 + 4 * 32 * 1 * 130 * 4 + _order(512, 1)
     # a 256-byte control block, a copy of the lengths in 256-byte blocks, then
-    # num_seqs * Hq * ceil(ctx / 512) * (D + 2)
-    # floats of split partials
-    assert cp.cp_workspace_size(d, 64, 8192, 64) == 256 + 256 + 64 * 32 * 16 * 130 * 4
-    assert cp.cp_workspace_size(d, 1, 1, 1) == 256 + 256 + 32 * 1 * 130 * 4
-    assert cp.cp_workspace_size(d, 1, 1, 65) == 256 + 512 + 65 * 32 * 1 * 130 * 4
+    # num_seqs * Hq * ceil(ctx / 512) * (D + 2) floats of split partials, then
+    # the work list
+    assert cp.cp_workspace_size(d, 64, 8192, 64) == 256 + 256 + 64 * 32 * 16 * 130 * 4 + _order(64, 64)
+    assert cp.cp_workspace_size(d, 1, 1, 1) == 256 + 256 + 32 * 1 * 130 * 4 + _order(1, 1)
+    assert cp.cp_workspace_size(d, 1, 1, 65) == 256 + 512 + 65 * 32 * 1 * 130 * 4 + _order(1, 65)
+    # fp32 layers run no tensor-core kernel: no work list
+    assert cp.cp_workspace_size(_desc(dtype=torch.float32), 1, 1, 1) == 256 + 256 + 32 * 1 * 130 * 4
 
 
 def test_mixed_step_rejects_misaligned_workspace():

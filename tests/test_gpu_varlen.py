@@ -41,7 +41,12 @@ def _setup(pasts, seed):
     return kc, vc, hist
 
 
-def _call(kc, vc, pasts, rows, q, kn, vn):
+def _partials_bytes(B, max_ctx):
+    """The split-KV partials a ragged call keeps at the start of its workspace."""
+    return B * HQ * (-(-max_ctx // 512)) * (D + 2) * 4
+
+
+def _call(kc, vc, pasts, rows, q, kn, vn, ws_bytes=None, keep_ws=False):
     B = len(pasts)
     desc = cp.layer_desc(torch.bfloat16, kc.shape[0], HQ, HKV, D, cp.CP_CACHE_CONTIG, capacity=CAP)
     cu = torch.tensor(np.concatenate([[0], np.cumsum(rows)]), dtype=torch.int32, device="cuda")
@@ -49,12 +54,14 @@ def _call(kc, vc, pasts, rows, q, kn, vn):
     T = int(sum(rows))
     max_ctx = max(p + r for p, r in zip(pasts, rows))
     out = torch.empty(T, HQ, D, dtype=torch.bfloat16, device="cuda")
-    ws = torch.zeros(cp.cp_workspace_size(desc, T, max_ctx, B), dtype=torch.uint8, device="cuda")
+    if ws_bytes is None:
+        ws_bytes = cp.cp_workspace_size(desc, T, max_ctx, B)
+    ws = torch.zeros(ws_bytes, dtype=torch.uint8, device="cuda")
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
     cp.cp_prefill_varlen(desc, q, kn, vn, kc, vc, cu, lens, B, T, max_ctx, out, ws, dev_status=status)
     torch.cuda.synchronize()
     assert int(status.item()) == 0
-    return out, lens
+    return (out, lens, ws) if keep_ws else (out, lens)
 
 
 @pytest.mark.parametrize("pasts,rows", [
@@ -87,3 +94,38 @@ def test_varlen_matches_oracle_and_runs_alone(pasts, rows):
         assert torch.equal(alone, out[t:t + r]), s
         t += r
     assert worst < BF16_TOL, worst
+
+
+def test_work_list_is_heaviest_first_and_changes_no_bit():
+    """The append kernel's work list for the tensor-core kernel holds every
+    pair (64 tokens at G = 4) of every sequence with more than one row exactly
+    once, ordered by the 128-key tiles its last token sees, most first, then
+    empty entries.  A workspace with no room for the list (the split-KV
+    partials only) takes the sequence-order scan instead, with bit-identical
+    output: the list only changes which cluster computes which pair."""
+    pasts, rows = [0, 1024, 1800, 512, 1900, 1, 100], [700, 300, 130, 257, 64, 1, 2]
+    kc, vc, _ = _setup(pasts, seed=80)
+    k0, v0 = kc.clone(), vc.clone()
+    T, B = sum(rows), len(pasts)
+    q, kn, vn = SI.gqa_prompt(T, seed=81)
+    out, _, ws = _call(kc, vc, pasts, rows, q.cuda(), kn.cuda(), vn.cuda(), keep_ws=True)
+    max_ctx = max(p + r for p, r in zip(pasts, rows))
+    off = -(-_partials_bytes(B, max_ctx) // 16) * 16
+    bound = -(-T // 64) + B
+    lst = ws[off:off + 8 * bound].cpu().view(torch.int32).view(bound, 2).tolist()
+    n_valid = sum(1 for s, _ in lst if s >= 0)
+    assert all(s >= 0 for s, _ in lst[:n_valid]) and all(e == [-1, 0] for e in lst[n_valid:])
+    want = sorted((s, k * 64) for s, r in enumerate(rows) if r > 1 for k in range(-(-r // 64)))
+    got = [tuple(e) for e in lst[:n_valid]]
+    assert sorted(got) == want
+
+    def tiles(e):
+        s, t0 = e
+        return -(-(pasts[s] + min(t0 + 64, rows[s])) // 128)
+
+    assert all(tiles(a) >= tiles(b) for a, b in zip(got, got[1:]))
+    # no room for the list: the same rows, bit for bit
+    kc.copy_(k0)
+    vc.copy_(v0)
+    plain, _ = _call(kc, vc, pasts, rows, q.cuda(), kn.cuda(), vn.cuda(), ws_bytes=_partials_bytes(B, max_ctx))
+    assert torch.equal(plain, out)
