@@ -59,7 +59,8 @@ def parse_args(argv=None):
     p.add_argument("--warmup", type=int, default=20)
     p.add_argument("--impl", default="native", choices=["native", "reference"])
     p.add_argument("--workload", default="gqa_prefill",
-                   choices=["gqa_prefill", "fp32", "ladder", "rolling", "decode", "mixed", "verify", "varlen"])
+                   choices=["gqa_prefill", "fp32", "ladder", "rolling", "decode", "mixed", "verify", "varlen", "append",
+                            "append_paged"])
     p.add_argument("--sweep", action="store_true",
                    help="one line per chunk width W (gqa_prefill) and per token budget (mixed schedule)")
     p.add_argument("--chunk", type=int, default=512, help="chunk width W of the gqa_prefill workload")
@@ -1015,6 +1016,86 @@ class ShortChunks:
                 "l2": L2_NOTE, "cuda_graph": True}
 
 
+class AppendRows:
+    """The KV append alone ([Wiki] 一.1: chunk k writes its own slots): 64
+    sequences each append a 512-row chunk after 4000 cached positions, GQA 8
+    KV heads x 128 bf16, one cp_kv_append call.  ``contig``: a contiguous cache
+    of capacity 4608; ``paged``: 16-token pages from a seeded permutation of
+    the pool.  Algorithmic bytes: the rows' K and V read once and written once
+    (268 MB per call)."""
+
+    HKV, D, B, R, PAST = 8, 128, 64, 512, 4000
+
+    def __init__(self, dev, mode):
+        import torch
+        import chunked_prefill_causal_cp_gb300 as cp
+
+        self.cp, self.torch, self.dev, self.mode = cp, torch, dev, mode
+        bf = torch.bfloat16
+        B, R, H, D = self.B, self.R, self.HKV, self.D
+        g = torch.Generator(device=dev).manual_seed(13)
+        self.kn = torch.randn(B, R, H, D, generator=g, device=dev).to(bf)
+        self.vn = torch.randn(B, R, H, D, generator=g, device=dev).to(bf)
+        self.lens = torch.full((B,), self.PAST, dtype=torch.int32, device=dev)
+        self.status = torch.zeros(1, dtype=torch.int32, device=dev)
+        n = self.PAST + R
+        if mode == "contig":
+            self.cap = 4608
+            self.desc = cp.layer_desc(bf, B, 4 * H, H, D, cp.CP_CACHE_CONTIG, capacity=self.cap)
+            self.kc = torch.full((B, H, self.cap, D), -7.0, dtype=bf, device=dev)
+            self.vc = torch.full_like(self.kc, -7.0)
+            self.table = None
+        else:
+            self.page = 16
+            nb = -(-n // self.page)
+            perm = torch.randperm(B * nb, generator=torch.Generator().manual_seed(14))
+            self.table = perm.view(B, nb).to(torch.int32).to(dev)
+            self.desc = cp.layer_desc(bf, B, 4 * H, H, D, cp.CP_CACHE_PAGED, page_size=self.page,
+                                      num_pages=B * nb, max_blocks=nb)
+            self.kc = torch.full((B * nb, H, self.page, D), -7.0, dtype=bf, device=dev)
+            self.vc = torch.full_like(self.kc, -7.0)
+        self.bytes = 2 * 2 * B * R * H * D * 2
+        self.tokens = B * R
+        self.flops = 0
+        self.launches = 1
+
+    def step(self):
+        self.cp.cp_kv_append(self.desc, self.kn, self.vn, self.R, self.kc, self.vc, self.lens, self.PAST,
+                             block_table=self.table, dev_status=self.status)
+
+    def _slots(self, cache):
+        """[B, R, H, D] view of the slots of positions [PAST, PAST + R)."""
+        torch = self.torch
+        pos = torch.arange(self.PAST, self.PAST + self.R, device=self.dev)
+        if self.mode == "contig":
+            return cache[:, :, self.PAST:self.PAST + self.R].transpose(1, 2)
+        pages = self.table[:, pos // self.page].long()  # [B, R]
+        return cache[pages, :, (pos % self.page).expand(self.B, -1)]
+
+    def self_check(self):
+        """Every appended row sits in its slot bit for bit; every other slot still
+        holds the fill value; the lengths are not modified."""
+        torch = self.torch
+        torch.cuda.synchronize()
+        rows_ok = bits_equal(self._slots(self.kc), self.kn) and bits_equal(self._slots(self.vc), self.vn)
+        written = self.B * self.R * self.HKV * self.D
+        rest_ok = all(int((c == -7.0).sum()) == c.numel() - written for c in (self.kc, self.vc))
+        lens_ok = bool((self.lens == self.PAST).all())
+        status = int(self.status.item())
+        ok = rows_ok and rest_ok and lens_ok and status == 0
+        return {"ok": ok, "rows_bit_exact": rows_ok, "other_slots_untouched": rest_ok, "lengths_untouched": lens_ok,
+                "status": status}
+
+    def config(self):
+        c = {"workload": f"append_{self.mode}_x64_r512_past4000_kv8_d128_bf16", "sequences": self.B, "rows": self.R,
+             "past": self.PAST, "bytes_per_call": self.bytes, "l2": L2_NOTE, "cuda_graph": True}
+        if self.mode == "contig":
+            c["capacity"] = self.cap
+        else:
+            c["page_size"] = self.page
+        return c
+
+
 # --------------------------------------------------------------------------- measurement
 
 def measure(wl, graph, flush, reps, warmup, torch, check_kw=None):
@@ -1080,6 +1161,16 @@ def other_configs(dev, flush, pk, reps, warmup):
                      "tensor_frac": tf / tc, "gbs_algorithmic": gbs, "hbm_frac": gbs / hbm,
                      "roofline_time_us": max(wl.flops / (tc * 1e12), wl.bytes / (hbm * 1e9)) * 1e6,
                      "dtype": "bf16", "check": chk, "gpu_launches_per_step": wl.launches}
+        del wl
+
+    for mode in ("contig", "paged"):
+        wl = AppendRows(dev, mode)
+        ms, chk = measure(wl, capture(wl.step, dev), flush, reps, warmup, torch)
+        gbs = wl.bytes / (ms / 1e3) / 1e9
+        res[f"append_{mode}"] = {**wl.config(), "rows_per_s": wl.tokens / (ms / 1e3), "ms_per_step": ms,
+                                 "gbs_algorithmic": gbs, "hbm_frac": gbs / hbm,
+                                 "traffic": kernel_traffic(f"kv_append_{mode}.json"), "dtype": "bf16", "check": chk,
+                                 "gpu_launches_per_step": wl.launches}
         del wl
 
     for budget, overlap in ((8192, False), (8192, True), (2048, False), (2048, True)):
@@ -1263,6 +1354,8 @@ def run_single(args, rank, world, dev, pk, pk_src):
         wl = ChunkLoop(dev, args.workload)
     elif args.workload in ("verify", "varlen"):
         wl = ShortChunks(dev, args.workload)
+    elif args.workload in ("append", "append_paged"):
+        wl = AppendRows(dev, "paged" if args.workload == "append_paged" else "contig")
     elif args.workload == "ladder":
         unp = LadderRuns(dev, pad=False)
         capture(unp.step, dev).replay()
@@ -1313,6 +1406,11 @@ def run_single(args, rank, world, dev, pk, pk_src):
                             "unit": "GB/s" if args.workload == "verify" else "TFLOP/s",
                             "scope": "algorithmic bytes or FLOPs over the whole call"}
         line["roofline"]["frac"] = line["roofline"]["achieved"] / line["roofline"]["peak"]
+    if args.workload in ("append", "append_paged"):
+        gbs = wl.bytes / (ms / 1e3) / 1e9
+        line["roofline"] = {"bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s", "frac": gbs / hbm,
+                            "traffic": kernel_traffic(f"kv_append_{wl.mode}.json"), "kernel": "kv_append_kernel",
+                            "scope": "the rows' K/V read and written once, over the call (one launch)"}
     if rank == 0:
         print(json.dumps(line), flush=True)
 
