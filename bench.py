@@ -200,6 +200,13 @@ def kernel_traffic(profile_name):
     return float(rec["dram_bytes_per_launch"])
 
 
+def fp32_alu_peak_tflops(dev):
+    """FP32 FMA peak of the SIMT path: SMs x 128 FMA lanes x 2 FLOP x the part's
+    maximum SM clock (2070 MHz)."""
+    import torch
+    return torch.cuda.get_device_properties(dev).multi_processor_count * 128 * 2 * 2.07e9 / 1e12
+
+
 def cpu_cores():
     return os.cpu_count() or 1
 
@@ -1117,8 +1124,10 @@ def other_configs(dev, flush, pk, reps, warmup):
 
     wl = ChunkLoop(dev, "fp32")
     ms, chk = measure(wl, capture(wl.step, dev), flush, reps, warmup, torch)
+    alu = fp32_alu_peak_tflops(dev)
     res["fp32_example"] = {**wl.config(), "tokens_per_s": wl.tokens / (ms / 1e3), "ms_per_step": ms,
-                           "tflops": wl.flops / (ms / 1e3) / 1e12, "dtype": "f32", "check": chk,
+                           "tflops": wl.flops / (ms / 1e3) / 1e12, "alu_peak_tflops": alu,
+                           "alu_frac_whole_step": wl.flops / (ms / 1e3) / 1e12 / alu, "dtype": "f32", "check": chk,
                            "gpu_launches_per_step": wl.launches}
     del wl
 
@@ -1384,6 +1393,11 @@ def run_single(args, rank, world, dev, pk, pk_src):
             "check": check, "gpu_launches": wl.launches * args.steps, "clocks": clk, "peaks": pk_src}
     if args.workload == "fp32":
         line["dtype"] = "f32"
+        alu = fp32_alu_peak_tflops(dev)
+        line["roofline"] = {"bound": "alu", "achieved": wl.flops / (ms / 1e3) / 1e12, "peak": alu, "unit": "TFLOP/s",
+                            "frac": wl.flops / (ms / 1e3) / 1e12 / alu, "kernel": "attn_f32_kernel",
+                            "peak_source": "SMs x 128 FP32 FMA lanes x 2 x 2070 MHz",
+                            "scope": "algorithmic FLOPs over the whole step (append, attention and commit launches)"}
     else:
         line["dtype"] = "f16" if args.workload == "rolling" else "bf16"
         line["tensor_frac_whole_step"] = wl.flops / (ms / 1e3) / 1e12 / tc
