@@ -233,7 +233,10 @@ int cp_mixed_step(const cp_layer_desc* desc, const void* q, const void* k_new,
  *   stream:      append -> record(fork_event) -> tensor-core attention
  *                -> wait(join_event) -> length advance
  *   side_stream: wait(fork_event) -> split-KV + combine -> record(join_event)
- * A step with only one kind of row runs everything on `stream`.
+ * A step with only one kind of row runs everything on `stream`.  On this GPU a
+ * tensor-core CTA takes its SM's whole register file, so the two kinds of kernel
+ * share the GPU only where one grid drains and the other fills: the step may
+ * come out a little shorter or a little longer than with cp_mixed_step.
  *   side_stream   a CUDA stream of the same device, not `stream` (caller-owned;
  *                 work the caller queued there before the call runs first)
  *   fork_event, join_event  caller-owned cudaEvent_t handles (created with
