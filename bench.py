@@ -604,9 +604,9 @@ class ChunkLoop:
                                   device=dev)
         self.tokens = sum(r["L"] - r["lp"] for r in self.runs)
         self.flops = sum(4 * r["d"] * r["H"] * r["pairs"] for r in self.runs)
-        # one cp_prefill_chunk call per chunk: the append and the attention (the tensor-core kernel
-        # advances seqlens_k itself; the fp32 path takes a separate advance)
-        self.launches = sum((2 if r["dtype"] != torch.float32 else 3) * len(r["sizes"]) for r in self.runs)
+        # one cp_prefill_chunk call per chunk: the append, then the attention kernel (tensor-core or
+        # fp32), which also advances seqlens_k
+        self.launches = sum(2 * len(r["sizes"]) for r in self.runs)
 
     def step(self):
         cp = self.cp

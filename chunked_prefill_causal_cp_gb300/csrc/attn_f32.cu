@@ -5,22 +5,26 @@
 // x 64 dims, fp32).  TF32 tensor-core products would not meet that bound, so
 // this kernel multiplies in full fp32.  Its roofline is the FP32 FMA rate.
 //
-// A CTA of 4 warps owns 16 consecutive query rows of one query head; warp w
-// owns rows 4w .. 4w+3 outright (their scores, softmax state and output), so
-// only the K/V tiles are shared across warps.  (Two rows per warp in 8 warps,
-// or one in 16, measured slower: the extra warps do not hide more latency
-// than the lost register reuse costs in instructions.)  64-key K/V tiles stream through
-// a two-stage shared-memory ring with cp.async (16-byte copies, zero-filled
-// past the keys), one tile ahead of the arithmetic.  Per tile and warp:
-//   scores  lane l computes keys l and l + 32 of its 4 rows: a float4 of each
-//           row of Q (a broadcast) and of each of its two K rows per 4 dims;
+// A CTA owns 16 consecutive query rows of one query head and splits their key
+// walk over kSplits warp groups (4 for D = 64, 2 for D = 128): group `sp` takes
+// the 32-key tiles sp, sp + kSplits, ...  The example's chunks hold only 2048
+// query rows in all, so the split is what puts several warps on each SM
+// sub-partition.  Within a group, warp w owns rows 4w .. 4w+3 outright (scores,
+// online softmax state and output).  Each group streams its tiles through its
+// own two-stage shared-memory ring with cp.async (16-byte copies, zero-filled
+// past the keys), one tile ahead.  Per tile and warp:
+//   scores  lane l computes key l of its 4 rows from a float4 of each Q row (a
+//           broadcast) and of its K row per 4 dimensions;
 //   softmax online, in the log2 domain: the row max by a warp reduction, the
 //           row sum kept per lane and reduced once at the end;
-//   output  P goes to the warp's rows of a shared tile, and lane l
-//           accumulates D/32 consecutive output dimensions of its 4 rows from
-//           a float4 of P (4 keys, a broadcast) and V rows read as vectors.
-// Every dot product runs over dimensions, and every output sum over keys, in
-// ascending order.  Works on all three cache layouts through cp_kv.cuh.
+//   output  P goes to the warp's rows of its group's P tile, and lane l
+//           accumulates D/32 consecutive output dimensions of its 4 rows from a
+//           float4 of P (4 keys, a broadcast) and vectors of V rows.
+// At the end the groups' partial results (max, sum, output) meet in shared
+// memory and are merged in group order.  Every dot product runs over
+// dimensions in ascending order, and every output sum over a group's keys in
+// ascending order, so the result depends only on the inputs.  Works on all
+// three cache layouts through cp_kv.cuh.
 #include <atomic>
 #include <cmath>
 #include <cstdint>
@@ -33,18 +37,32 @@ namespace cp {
 namespace {
 
 constexpr int kRows = 16;     // query rows per CTA
-constexpr int kKeys = 64;     // keys per tile
-constexpr int kWarps = 4;     // warps per CTA; warp w owns rows 4w .. 4w+3
-constexpr int kThreads = kWarps * 32;
-static_assert(kRows == 4 * kWarps, "each warp owns four rows");
+constexpr int kKeys = 32;     // keys per tile
+constexpr int kRowWarps = 4;  // warps per group; warp w owns rows 4w .. 4w+3
+
+template <int D>
+struct F32Cfg {
+  static constexpr int kSplits = D == 64 ? 4 : 2;  // warp groups splitting the key walk
+  static constexpr int kThreads = kSplits * kRowWarps * 32;
+  static constexpr int KS = D + 4;  // K row stride in floats: float4 reads by 8 lanes hit 8 distinct 16-byte slots
+};
 
 template <int D>
 struct F32Smem {
-  static constexpr int KS = D + 4;  // K row stride in floats: float4 reads by 8 lanes hit 8 distinct 16-byte slots
+  static constexpr int S = F32Cfg<D>::kSplits;
   float q[kRows][D];
-  float k[2][kKeys][KS];
-  float v[2][kKeys][D];
-  float p[kRows][kKeys];
+  union {
+    struct {
+      float k[S][2][kKeys][F32Cfg<D>::KS];
+      float v[S][2][kKeys][D];
+    } ring;
+    struct {  // the groups' partial results, after the walk
+      float o[S][kRows][D];
+      float m[S][kRows];
+      float l[S][kRows];
+    } part;
+  };
+  float p[S][kRows][kKeys];
 };
 
 __device__ __forceinline__ void cp_async16(void* dst, const void* src, bool fill) {
@@ -56,14 +74,26 @@ __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commi
 template <int N>
 __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
 
+// A named barrier for the 128 threads of warp group `sp` (ids 1 .. kSplits;
+// 0 is __syncthreads).
+__device__ __forceinline__ void group_sync(int sp) {
+  asm volatile("bar.sync %0, %1;" ::"r"(sp + 1), "n"(kRowWarps * 32) : "memory");
+}
+
 template <int D>
-__global__ void __launch_bounds__(kThreads) attn_f32_kernel(const AttnArgs a) {
+__global__ void __launch_bounds__(F32Cfg<D>::kThreads) attn_f32_kernel(const AttnArgs a) {
+  using C = F32Cfg<D>;
+  constexpr int S = C::kSplits;
+  constexpr int DV = D / 32;  // output dimensions per lane
   extern __shared__ __align__(16) uint8_t f32_smem_raw[];
   F32Smem<D>& sm = *reinterpret_cast<F32Smem<D>*>(f32_smem_raw);
-  constexpr int DV = D / 32;  // output dimensions per lane
 
   pdl_launch_dependents();
   pdl_wait();
+  // The length advance of a one-call chunk: `past` is then a copy of the
+  // lengths taken by the append, so CTA (0, 0, 0) may advance them at once.
+  if (a.commit_lens && blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0)
+    for (int i = threadIdx.x; i < a.rows.num_seqs; i += C::kThreads) a.commit_lens[i] += a.commit_add;
   const int s = blockIdx.z;
   const int h = blockIdx.y;
   const int g = h / a.group;
@@ -71,6 +101,9 @@ __global__ void __launch_bounds__(kThreads) attn_f32_kernel(const AttnArgs a) {
   const int t0 = blockIdx.x * kRows;
   if (t0 >= rows || rows < a.min_rows) return;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int sp = warp / kRowWarps;                   // this warp's group
+  const int rw = warp % kRowWarps;                   // its rows: 4 rw .. 4 rw + 3
+  const int gtid = threadIdx.x % (kRowWarps * 32);  // thread index within the group
   const int past = a.past[s];
   const int n = past + rows;
   if (n > a.max_ctx || past < 0) {
@@ -85,13 +118,14 @@ __global__ void __launch_bounds__(kThreads) attn_f32_kernel(const AttnArgs a) {
   const float* kc = static_cast<const float*>(a.k);
   const float* vc = static_cast<const float*>(a.v);
 
-  // K/V tile j0 .. j0+63 into stage `st`: 16-byte chunks, keys past the walk
-  // (or on an out-of-range page) zero-filled.
-  auto load_tile = [&](int j0, int st) {
+  // K/V tile `tile` (keys 32 tile ..) into this group's stage `st`, by the
+  // group's threads: 16-byte chunks, keys past the walk (or on an
+  // out-of-range page) zero-filled.
+  auto load_tile = [&](int tile, int st) {
     constexpr int kChunks = D / 4;  // 16-byte chunks per row
-    for (int c = threadIdx.x; c < kKeys * kChunks; c += kThreads) {
+    for (int c = gtid; c < kKeys * kChunks; c += kRowWarps * 32) {
       const int r = c / kChunks, c4 = c % kChunks;
-      const int j = j0 + r;
+      const int j = tile * kKeys + r;
       long long off = -1;
       if (j < keys.nkeys) {
         off = key_offset(a.cache, a.hkv, D, s, g, j);
@@ -99,24 +133,27 @@ __global__ void __launch_bounds__(kThreads) attn_f32_kernel(const AttnArgs a) {
       }
       const bool ok = off >= 0;
       const long long e = ok ? off + 4 * c4 : 0;
-      cp_async16(&sm.k[st][r][4 * c4], kc + e, ok);
-      cp_async16(&sm.v[st][r][4 * c4], vc + e, ok);
+      cp_async16(&sm.ring.k[sp][st][r][4 * c4], kc + e, ok);
+      cp_async16(&sm.ring.v[sp][st][r][4 * c4], vc + e, ok);
     }
   };
 
-  load_tile(0, 0);
+  const int ntiles = (keys.nkeys + kKeys - 1) / kKeys;
+  const int nmine = ntiles > sp ? (ntiles - sp + S - 1) / S : 0;  // this group's tiles: sp + S i
+  if (nmine > 0) load_tile(sp, 0);
   cp_async_commit();
-  for (int e = threadIdx.x; e < kRows * D; e += kThreads) {
+  for (int e = threadIdx.x; e < kRows * D; e += C::kThreads) {
     const int r = e / D, d = e % D;
     const int t = t0 + r;
     sm.q[r][d] = t < rows ? q[((row0 + t) * a.hq + h) * D + d] : 0.f;
   }
+  __syncthreads();  // Q is in shared memory for every group
 
   int p_row[4];
   float m[4], l[4], o[4][DV];
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    const int t = t0 + 4 * warp + i;
+    const int t = t0 + 4 * rw + i;
     p_row[i] = t < rows ? past + t : -1;  // absolute position; -1: no row (sees nothing)
     m[i] = -INFINITY;
     l[i] = 0.f;
@@ -124,90 +161,71 @@ __global__ void __launch_bounds__(kThreads) attn_f32_kernel(const AttnArgs a) {
     for (int u = 0; u < DV; ++u) o[i][u] = 0.f;
   }
 
-  const int ntiles = (keys.nkeys + kKeys - 1) / kKeys;
-  for (int tile = 0; tile < ntiles; ++tile) {
-    const int st = tile & 1;
-    if (tile + 1 < ntiles) {
-      load_tile((tile + 1) * kKeys, st ^ 1);
+  for (int it = 0; it < nmine; ++it) {
+    const int st = it & 1;
+    const int tile = sp + S * it;
+    if (it + 1 < nmine) {
+      load_tile(tile + S, st ^ 1);
       cp_async_commit();
       cp_async_wait<1>();
     } else {
       cp_async_wait<0>();
     }
-    __syncthreads();  // tile `tile` (and, the first time, Q) is in shared memory for every warp
+    group_sync(sp);  // the group's tile is in shared memory for all its warps
 
-    // ---- scores of keys j0 + lane and j0 + lane + 32 for rows 4w .. 4w+3
-    const int j0 = tile * kKeys;
-    float sc[4][2];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) sc[i][0] = sc[i][1] = 0.f;
+    // ---- scores of key 32 tile + lane for rows 4 rw .. 4 rw + 3
+    float sc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll 4
     for (int d4 = 0; d4 < D / 4; ++d4) {
-      const float4 k0 = *reinterpret_cast<const float4*>(&sm.k[st][lane][4 * d4]);
-      const float4 k1 = *reinterpret_cast<const float4*>(&sm.k[st][lane + 32][4 * d4]);
+      const float4 kv = *reinterpret_cast<const float4*>(&sm.ring.k[sp][st][lane][4 * d4]);
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
-        const float4 qv = *reinterpret_cast<const float4*>(&sm.q[4 * warp + i][4 * d4]);
-        sc[i][0] = fmaf(qv.x, k0.x, sc[i][0]);
-        sc[i][0] = fmaf(qv.y, k0.y, sc[i][0]);
-        sc[i][0] = fmaf(qv.z, k0.z, sc[i][0]);
-        sc[i][0] = fmaf(qv.w, k0.w, sc[i][0]);
-        sc[i][1] = fmaf(qv.x, k1.x, sc[i][1]);
-        sc[i][1] = fmaf(qv.y, k1.y, sc[i][1]);
-        sc[i][1] = fmaf(qv.z, k1.z, sc[i][1]);
-        sc[i][1] = fmaf(qv.w, k1.w, sc[i][1]);
+        const float4 qv = *reinterpret_cast<const float4*>(&sm.q[4 * rw + i][4 * d4]);
+        sc[i] = fmaf(qv.x, kv.x, sc[i]);
+        sc[i] = fmaf(qv.y, kv.y, sc[i]);
+        sc[i] = fmaf(qv.z, kv.z, sc[i]);
+        sc[i] = fmaf(qv.w, kv.w, sc[i]);
       }
     }
     // ---- visibility and the online softmax, row by row
-    int pos[2];
-    bool in[2];
-#pragma unroll
-    for (int c = 0; c < 2; ++c) {
-      const int j = j0 + lane + 32 * c;
-      in[c] = j < keys.nkeys;
-      pos[c] = in[c] ? key_pos(a.cache, keys, j) : 0;
-    }
+    const int j = tile * kKeys + lane;
+    const bool in = j < keys.nkeys;
+    const int pos = in ? key_pos(a.cache, keys, j) : 0;
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      float x[2];
-#pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        const bool vis = in[c] && pos[c] <= p_row[i] && pos[c] >= keys.lo;
-        x[c] = vis ? sc[i][c] * a.scale_log2 : -INFINITY;
-      }
-      float mt = fmaxf(x[0], x[1]);
+      const bool vis = in && pos <= p_row[i] && pos >= keys.lo;
+      const float x = vis ? sc[i] * a.scale_log2 : -INFINITY;
+      float mt = x;
 #pragma unroll
       for (int off = 16; off; off >>= 1) mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, off));
       const float m_new = fmaxf(m[i], mt);
-      float p0 = 0.f, p1 = 0.f;
+      float pr = 0.f;
       if (m_new != -INFINITY) {  // else nothing visible yet: the row's state stays as it is
         const float alpha = (m[i] == -INFINITY) ? 0.f : ex2_approx(m[i] - m_new);
-        p0 = x[0] == -INFINITY ? 0.f : ex2_approx(x[0] - m_new);
-        p1 = x[1] == -INFINITY ? 0.f : ex2_approx(x[1] - m_new);
-        l[i] = l[i] * alpha + (p0 + p1);
+        pr = x == -INFINITY ? 0.f : ex2_approx(x - m_new);
+        l[i] = l[i] * alpha + pr;
         m[i] = m_new;
 #pragma unroll
         for (int u = 0; u < DV; ++u) o[i][u] *= alpha;
       }
-      sm.p[4 * warp + i][lane] = p0;
-      sm.p[4 * warp + i][lane + 32] = p1;
+      sm.p[sp][4 * rw + i][lane] = pr;
     }
     __syncwarp();  // the warp's own rows of P are written (no other warp reads them)
 
-    // ---- O[rows][lane * DV ..] += P V, keys in ascending order
+    // ---- O[rows][lane * DV ..] += P V over the tile's keys in ascending order
 #pragma unroll 2
     for (int k4 = 0; k4 < kKeys / 4; ++k4) {
       float4 pv[4];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) pv[i] = *reinterpret_cast<const float4*>(&sm.p[4 * warp + i][4 * k4]);
+      for (int i = 0; i < 4; ++i) pv[i] = *reinterpret_cast<const float4*>(&sm.p[sp][4 * rw + i][4 * k4]);
 #pragma unroll
       for (int kk = 0; kk < 4; ++kk) {
         float vv[DV];
         if constexpr (DV == 4) {
-          const float4 t = *reinterpret_cast<const float4*>(&sm.v[st][4 * k4 + kk][4 * lane]);
+          const float4 t = *reinterpret_cast<const float4*>(&sm.ring.v[sp][st][4 * k4 + kk][4 * lane]);
           vv[0] = t.x; vv[1] = t.y; vv[2] = t.z; vv[3] = t.w;
         } else {
-          const float2 t = *reinterpret_cast<const float2*>(&sm.v[st][4 * k4 + kk][2 * lane]);
+          const float2 t = *reinterpret_cast<const float2*>(&sm.ring.v[sp][st][4 * k4 + kk][2 * lane]);
           vv[0] = t.x; vv[1] = t.y;
         }
 #pragma unroll
@@ -218,22 +236,43 @@ __global__ void __launch_bounds__(kThreads) attn_f32_kernel(const AttnArgs a) {
         }
       }
     }
-    __syncthreads();  // every warp is done with stage `st` before the next loads overwrite it
+    group_sync(sp);  // the group is done with stage `st` before its next loads overwrite it
   }
-  cp_async_wait<0>();  // no copy into shared memory outlives the loop
+  cp_async_wait<0>();  // no copy into shared memory outlives the walk
+  __syncthreads();     // every group is done with the ring: it now holds the partial results
 
-  float* out = static_cast<float*>(a.out);
+  // ---- the groups' partials, then their merge in group order
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     float lt = l[i];
 #pragma unroll
     for (int off = 16; off; off >>= 1) lt += __shfl_xor_sync(0xffffffffu, lt, off);
-    const int t = t0 + 4 * warp + i;
-    if (t >= rows) continue;
-    const float inv = lt > 0.f ? 1.f / lt : 0.f;
-    float* dst = out + ((row0 + t) * a.hq + h) * D + DV * lane;
+    const int r = 4 * rw + i;
+    if (lane == 0) {
+      sm.part.m[sp][r] = m[i];
+      sm.part.l[sp][r] = lt;
+    }
 #pragma unroll
-    for (int u = 0; u < DV; ++u) dst[u] = o[i][u] * inv;
+    for (int u = 0; u < DV; ++u) sm.part.o[sp][r][DV * lane + u] = o[i][u];
+  }
+  __syncthreads();
+  float* out = static_cast<float*>(a.out);
+  for (int e = threadIdx.x; e < kRows * D; e += C::kThreads) {
+    const int r = e / D, d = e % D;
+    const int t = t0 + r;
+    if (t >= rows) continue;
+    float mm = -INFINITY;
+#pragma unroll
+    for (int k = 0; k < S; ++k) mm = fmaxf(mm, sm.part.m[k][r]);
+    float acc = 0.f, lsum = 0.f;
+#pragma unroll
+    for (int k = 0; k < S; ++k) {
+      const float mk = sm.part.m[k][r];
+      const float w = mk == -INFINITY ? 0.f : ex2_approx(mk - mm);
+      acc = fmaf(w, sm.part.o[k][r][d], acc);
+      lsum = fmaf(w, sm.part.l[k][r], lsum);
+    }
+    out[((row0 + t) * a.hq + h) * D + d] = lsum > 0.f ? acc * (1.f / lsum) : 0.f;
   }
 }
 
@@ -251,7 +290,7 @@ cudaError_t launch_f32_t(const AttnArgs& a, dim3 grid, cudaStream_t st) {
     if (e != cudaSuccess) return e;
     ready_mask.fetch_or(bit);
   }
-  return launch_pdl(attn_f32_kernel<D>, grid, dim3(kThreads), (size_t)smem, st, a);
+  return launch_pdl(attn_f32_kernel<D>, grid, dim3(F32Cfg<D>::kThreads), (size_t)smem, st, a);
 }
 
 }  // namespace

@@ -615,10 +615,11 @@ int cp_prefill_chunk(const cp_layer_desc* desc, const void* q, void* k_new, void
   if (r != CP_OK) return r;
 
   a.past = past;  // the snapshot: seqlens_k itself may then be advanced by the attention kernel
-  // One launch for the attention and the commit when the tensor-core kernel takes every row.
+  // One launch for the attention and the commit when a single kernel takes
+  // every row: the tensor-core kernel, or the fp32 one.
   const int G = desc->num_q_heads / desc->num_kv_heads;
-  const bool tc_only = desc->dtype != CP_F32 && rows_padded > 1 && !decode_rows &&
-                       attn_tc_supported(desc->head_dim, G, desc->dtype);
+  const bool tc_only = (desc->dtype == CP_F32 ||
+                        (rows_padded > 1 && !decode_rows && attn_tc_supported(desc->head_dim, G, desc->dtype)));
   if (tc_only) {
     a.commit_lens = seqlens_k;
     a.commit_add = real_rows;

@@ -63,7 +63,7 @@ struct AttnArgs {
   int* status;             // optional CP_DEV_* bits
   int kv_direct;           // tensor-core kernel: this call's new K/V rows may be read from
                            // k_new / v_new ([rows_total, hkv, d]) instead of the paged pool
-  int* commit_lens = nullptr;  // tensor-core kernel: if set, lengths advanced by commit_add after the
+  int* commit_lens = nullptr;  // tensor-core and fp32 kernels: if set, lengths advanced by commit_add after the
   int commit_add = 0;          // attention reads them: by CTA (0, 0) right after the dependency wait
                                // when `past` is a copy (it must not alias commit_lens), else through
   unsigned* ticket = nullptr;  // the ticket counter (zero before the launch, left zero)
