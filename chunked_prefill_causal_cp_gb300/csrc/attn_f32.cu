@@ -25,6 +25,13 @@
 // dimensions in ascending order, and every output sum over a group's keys in
 // ascending order, so the result depends only on the inputs.  Works on all
 // three cache layouts through cp_kv.cuh.
+//
+// One-call chunk on a contiguous cache (`fused`): the keys at or past the
+// cached length are this call's rows, read from k_new / v_new; the CTAs of the
+// first query head of each KV group copy their 16 rows' K and V into the
+// cache (no CTA of the launch reads those slots from the cache), and the last
+// CTA to take a ticket, after every CTA has read the lengths, advances them
+// ([Wiki] 一.1 and 四).
 #include <atomic>
 #include <cmath>
 #include <cstdint>
@@ -80,6 +87,24 @@ __device__ __forceinline__ void group_sync(int sp) {
   asm volatile("bar.sync %0, %1;" ::"r"(sp + 1), "n"(kRowWarps * 32) : "memory");
 }
 
+// The ticket of a one-call chunk: every CTA takes one after all its threads
+// have read the lengths; the last one advances them by commit_add and resets
+// the counter.  A counter found above the grid size was not zero before the
+// launch: reported as CP_DEV_BOUNDS.
+__device__ __forceinline__ void take_ticket(const AttnArgs& a) {
+  __threadfence();
+  const unsigned total = gridDim.x * gridDim.y * gridDim.z;
+  const unsigned t = atomicAdd(a.ticket, 1u);
+  if (t == total - 1) {
+    __threadfence();
+    for (int i = 0; i < a.rows.num_seqs; ++i) a.commit_lens[i] += a.commit_add;
+    __threadfence();
+    atomicExch(a.ticket, 0u);
+  } else if (t >= total && a.status) {
+    atomicOr(a.status, CP_DEV_BOUNDS);
+  }
+}
+
 template <int D>
 __global__ void __launch_bounds__(F32Cfg<D>::kThreads) attn_f32_kernel(const AttnArgs a) {
   using C = F32Cfg<D>;
@@ -90,26 +115,34 @@ __global__ void __launch_bounds__(F32Cfg<D>::kThreads) attn_f32_kernel(const Att
 
   pdl_launch_dependents();
   pdl_wait();
-  // The length advance of a one-call chunk: `past` is then a copy of the
-  // lengths taken by the append, so CTA (0, 0, 0) may advance them at once.
-  if (a.commit_lens && blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0)
+  // The length advance of a one-call chunk with a separate append: `past` is
+  // then a copy of the lengths, so CTA (0, 0, 0) may advance them at once.
+  if (a.commit_lens && !a.ticket && blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0)
     for (int i = threadIdx.x; i < a.rows.num_seqs; i += C::kThreads) a.commit_lens[i] += a.commit_add;
   const int s = blockIdx.z;
   const int h = blockIdx.y;
   const int g = h / a.group;
   const int rows = seq_rows(a.rows, s);
   const int t0 = blockIdx.x * kRows;
-  if (t0 >= rows || rows < a.min_rows) return;
+  bool work = t0 < rows && rows >= a.min_rows;
+  int past = 0;
+  if (work) {
+    past = a.past[s];
+    if (past < 0 || past + rows > a.max_ctx) {
+      if (a.status && threadIdx.x == 0) atomicOr(a.status, CP_DEV_BOUNDS);
+      work = false;
+    }
+  }
+  if (a.ticket) {
+    __syncthreads();  // every thread has read its length before this CTA takes a ticket
+    if (threadIdx.x == 0) take_ticket(a);
+  }
+  if (!work) return;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int sp = warp / kRowWarps;                   // this warp's group
   const int rw = warp % kRowWarps;                   // its rows: 4 rw .. 4 rw + 3
   const int gtid = threadIdx.x % (kRowWarps * 32);  // thread index within the group
-  const int past = a.past[s];
   const int n = past + rows;
-  if (n > a.max_ctx || past < 0) {
-    if (a.status && threadIdx.x == 0) atomicOr(a.status, CP_DEV_BOUNDS);
-    return;
-  }
   const int t_last = min(t0 + kRows, rows) - 1;
   const SeqKeys keys = seq_keys(a, s, n, past + t_last);
   const long long row0 = seq_row0(a.rows, s);
@@ -117,6 +150,9 @@ __global__ void __launch_bounds__(F32Cfg<D>::kThreads) attn_f32_kernel(const Att
   const float* q = static_cast<const float*>(a.q);
   const float* kc = static_cast<const float*>(a.k);
   const float* vc = static_cast<const float*>(a.v);
+  const float* kn = static_cast<const float*>(a.k_new);
+  const float* vn = static_cast<const float*>(a.v_new);
+  const bool fused = a.fused != 0;
 
   // K/V tile `tile` (keys 32 tile ..) into this group's stage `st`, by the
   // group's threads: 16-byte chunks, keys past the walk (or on an
@@ -126,17 +162,33 @@ __global__ void __launch_bounds__(F32Cfg<D>::kThreads) attn_f32_kernel(const Att
     for (int c = gtid; c < kKeys * kChunks; c += kRowWarps * 32) {
       const int r = c / kChunks, c4 = c % kChunks;
       const int j = tile * kKeys + r;
+      const bool from_new = fused && j >= past;  // this call's row j - past of sequence s
       long long off = -1;
       if (j < keys.nkeys) {
-        off = key_offset(a.cache, a.hkv, D, s, g, j);
+        off = from_new ? (((long long)s * rows + (j - past)) * a.hkv + g) * D : key_offset(a.cache, a.hkv, D, s, g, j);
         if (off < 0 && a.status && c4 == 0) atomicOr(a.status, CP_DEV_BOUNDS);
       }
       const bool ok = off >= 0;
       const long long e = ok ? off + 4 * c4 : 0;
-      cp_async16(&sm.ring.k[sp][st][r][4 * c4], kc + e, ok);
-      cp_async16(&sm.ring.v[sp][st][r][4 * c4], vc + e, ok);
+      cp_async16(&sm.ring.k[sp][st][r][4 * c4], (from_new ? kn : kc) + e, ok);
+      cp_async16(&sm.ring.v[sp][st][r][4 * c4], (from_new ? vn : vc) + e, ok);
     }
   };
+
+  if (fused && h % a.group == 0) {
+    // This CTA's rows of KV head g into their cache slots, 16 bytes at a time.
+    float* kdst = static_cast<float*>(a.k_cache);
+    float* vdst = static_cast<float*>(a.v_cache);
+    for (int e = threadIdx.x; e < kRows * (D / 4); e += C::kThreads) {
+      const int r = e / (D / 4), c4 = e % (D / 4);
+      const int t = t0 + r;
+      if (t >= rows) continue;
+      const long long src = (((long long)s * rows + t) * a.hkv + g) * D + 4 * c4;
+      const long long dst = (((long long)s * a.hkv + g) * a.cache.capacity + past + t) * D + 4 * c4;
+      *reinterpret_cast<float4*>(kdst + dst) = *reinterpret_cast<const float4*>(kn + src);
+      *reinterpret_cast<float4*>(vdst + dst) = *reinterpret_cast<const float4*>(vn + src);
+    }
+  }
 
   const int ntiles = (keys.nkeys + kKeys - 1) / kKeys;
   const int nmine = ntiles > sp ? (ntiles - sp + S - 1) / S : 0;  // this group's tiles: sp + S i

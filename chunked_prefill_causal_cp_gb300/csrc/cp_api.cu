@@ -595,6 +595,20 @@ int cp_prefill_chunk(const cp_layer_desc* desc, const void* q, void* k_new, void
     a.commit_add = real_rows;
     return run_fused(desc, a, rows_total, k_new, v_new, st);
   }
+  if (desc->dtype == CP_F32 && desc->kind == CP_CACHE_CONTIG) {
+    // fp32, contiguous: the fp32 kernel appends, attends and advances in one launch.
+    a.past = seqlens_k;
+    a.ticket = static_cast<unsigned*>(workspace);
+    a.commit_lens = seqlens_k;
+    a.commit_add = real_rows;
+    a.min_rows = 1;
+    a.fused = 1;
+    a.k_new = k_new;
+    a.v_new = v_new;
+    a.k_cache = k_cache;
+    a.v_cache = v_cache;
+    return launch_result(launch_attn_f32(a, rows_padded, st));
+  }
   int* past = reinterpret_cast<int*>(static_cast<char*>(workspace) + kControlBytes);
 
   AppendArgs ap;
