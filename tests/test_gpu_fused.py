@@ -108,7 +108,7 @@ def test_fused_decode_row(n, hq, hkv, d, dtype):
 
 
 def test_fused_fp32_glossary_example():
-    """fp32 (the SIMT path, then a separate advance): 1e-4 of the oracle."""
+    """fp32 (the SIMT path, one launch per chunk): 1e-4 of the oracle."""
     q, k, v = SI.fp32_sdpa_example()
     cache = Contig(torch.float32, 8, 8, 64, cap=1024, fused=True)
     out, _ = prefill(cache, q.cuda(), k.cuda(), v.cuda(), 256)
@@ -116,6 +116,70 @@ def test_fused_fp32_glossary_example():
     ref = oracle.causal_attention(f64(q), f64(k), f64(v))
     assert np.abs(f64(out) - ref).max() < F32_TOL
     assert int(cache.lens.item()) == 1000 and int(cache.status.item()) == 0
+
+
+@pytest.mark.parametrize("n,W,hq,hkv,d", [
+    (700, 256, 8, 2, 64),    # GQA 4, head_dim 64 (four warp groups split the keys)
+    (389, 128, 4, 2, 128),   # GQA 2, head_dim 128 (two warp groups)
+    (301, 96, 4, 4, 64),     # MHA, chunk not a multiple of the 32-key tile
+    (5, 2, 8, 4, 128),       # tiny chunks, first chunk of 2 rows
+])
+def test_fused_fp32_chunks_match_oracle_and_separate_calls(n, W, hq, hkv, d):
+    """fp32 on a contiguous cache is one launch per chunk (the kernel reads the
+    chunk's keys from k_new, copies its rows into the cache and advances
+    seqlens_k by ticket): within 1e-4 of the oracle, bit-identical to the
+    separate append + attention calls, and the cache byte for byte."""
+    q, k, v = SI.gqa_prompt(n, seed=n + 1, hq=hq, hkv=hkv, dim=d, dtype=torch.float32)
+    qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
+    cap = ((n + 127) // 128 + 1) * 128
+    fused = Contig(torch.float32, hq, hkv, d, cap=cap, fused=True)
+    split = Contig(torch.float32, hq, hkv, d, cap=cap)
+    out_f, _ = prefill(fused, qd, kd, vd, W)
+    out_s, _ = prefill(split, qd, kd, vd, W)
+    torch.cuda.synchronize()
+    ref, _, _ = oracle.chunked_prefill(f64(q), f64(k), f64(v), W)
+    assert np.abs(f64(out_f) - ref).max() < F32_TOL
+    assert torch.equal(out_f, out_s)
+    assert torch.equal(fused.k[0, :, :n].cpu(), k.permute(1, 0, 2))
+    assert torch.equal(fused.v[0, :, :n].cpu(), v.permute(1, 0, 2))
+    assert torch.isnan(fused.k[0, :, n:]).all()
+    assert int(fused.lens.item()) == n and int(fused.status.item()) == 0
+    assert int(fused.ws[:4].view(torch.int32).item()) == 0  # the ticket counter is left zero
+
+
+def test_fused_fp32_batch_padded_chunk():
+    """fp32, B = 3 sequences at their own lengths, one chunk widened from 90 to
+    100 rows (the pad rows repeat the last real row): every sequence's real rows
+    within 1e-4 of the oracle, its 100 rows appended, each length advanced by
+    the 90 real rows."""
+    B, R, real, hq, hkv, d = 3, 100, 90, 8, 2, 64
+    pasts = [0, 37, 300]
+    cache = Contig(torch.float32, hq, hkv, d, cap=512, batch=B, fused=True)
+    seqs = [SI.gqa_prompt(p + real, seed=80 + i, hq=hq, hkv=hkv, dim=d, dtype=torch.float32)
+            for i, p in enumerate(pasts)]
+    for b, p in enumerate(pasts):
+        _, k, v = seqs[b]
+        cache.k[b, :, :p] = k[:p].permute(1, 0, 2).cuda()
+        cache.v[b, :, :p] = v[:p].permute(1, 0, 2).cuda()
+    cache.lens.copy_(torch.tensor(pasts, dtype=torch.int32))
+
+    def widened(t, p):
+        idx = torch.cat([torch.arange(p, p + real), torch.full((R - real,), p + real - 1)])
+        return t[idx]
+
+    qb = torch.stack([widened(s[0], p) for s, p in zip(seqs, pasts)]).cuda()
+    kb = torch.stack([widened(s[1], p) for s, p in zip(seqs, pasts)]).cuda()
+    vb = torch.stack([widened(s[2], p) for s, p in zip(seqs, pasts)]).cuda()
+    out = cache.chunk(qb, kb, vb, real, max(pasts))
+    torch.cuda.synchronize()
+    for b, p in enumerate(pasts):
+        q, k, v = seqs[b]
+        ref = oracle.chunk_attention(f64(q[p:p + real]), f64(k), f64(v), p)
+        assert np.abs(f64(out[b, :real]) - ref).max() < F32_TOL
+        assert torch.equal(cache.k[b, :, p:p + R].cpu(), kb[b].cpu().permute(1, 0, 2))
+        assert torch.equal(cache.v[b, :, p:p + R].cpu(), vb[b].cpu().permute(1, 0, 2))
+    assert cache.lens.tolist() == [p + real for p in pasts]
+    assert int(cache.status.item()) == 0
 
 
 def test_fused_paged_prompt():
