@@ -200,6 +200,17 @@ def kernel_traffic(profile_name):
     return float(rec["dram_bytes_per_launch"])
 
 
+def mixed_rooflines(steps, tc, hbm):
+    """Two roofline times of a mixed schedule, in ms: T* = sum over steps of
+    max(FLOPs / tensor peak, decode bytes / copy rate), which assumes the decode
+    rows' bytes stream entirely beside the tensor-core work, and the serial
+    time = sum of the two, which holds when an SM's shared-memory intake is
+    about its share of the HBM rate (so an SM cannot do both at once)."""
+    t_star = sum(max(st["flops"] / (tc * 1e12), st["bytes"] / (hbm * 1e9)) for st in steps) * 1e3
+    t_serial = sum(st["flops"] / (tc * 1e12) + st["bytes"] / (hbm * 1e9) for st in steps) * 1e3
+    return t_star, t_serial
+
+
 def fp32_alu_peak_tflops(dev):
     """FP32 FMA peak of the SIMT path: SMs x 128 FMA lanes x 2 FLOP x the part's
     maximum SM clock (2070 MHz)."""
@@ -1186,12 +1197,13 @@ def other_configs(dev, flush, pk, reps, warmup):
     for budget, overlap in ((8192, False), (8192, True), (2048, False), (2048, True)):
         wl = MixedSchedule(dev, budget=budget, overlap=overlap)
         ms, chk = measure(wl, capture(wl.step, dev), flush, max(3, reps // 4), warmup, torch)
-        t_star = sum(max(st["flops"] / (tc * 1e12), st["bytes"] / (hbm * 1e9)) for st in wl.steps) * 1e3
+        t_star, t_serial = mixed_rooflines(wl.steps, tc, hbm)
         res[f"mixed_budget{budget}" + ("_overlap" if overlap else "")] = {
             **wl.config(), "rows_per_s": wl.tokens / (ms / 1e3), "ms_per_schedule": ms,
             "flops_per_schedule": wl.flops, "decode_bytes_per_schedule": wl.decode_bytes,
-            "roofline_time_ms": t_star, "roofline_frac": t_star / ms, "dtype": "bf16", "check": chk,
-            "gpu_launches_per_step": wl.launches}
+            "roofline_time_ms": t_star, "roofline_frac": t_star / ms,
+            "roofline_serial_time_ms": t_serial, "roofline_serial_frac": t_serial / ms, "dtype": "bf16",
+            "check": chk, "gpu_launches_per_step": wl.launches}
         del wl
     torch.cuda.synchronize()
     return res
@@ -1345,11 +1357,12 @@ def run_sweep(args, dev, pk):
     for budget in (512, 1024, 2048, 4096, 8192, 16384):
         wl = MixedSchedule(dev, budget=budget)
         ms, chk = measure(wl, capture(wl.step, dev), flush, max(3, reps // 5), args.warmup, torch)
-        t_star = sum(max(st["flops"] / (tc * 1e12), st["bytes"] / (hbm * 1e9)) for st in wl.steps) * 1e3
+        t_star, t_serial = mixed_rooflines(wl.steps, tc, hbm)
         print(json.dumps({"sweep": "budget", "budget": budget, "schedule_steps": len(wl.steps),
                           "rows_per_schedule": wl.R, "rows_per_s": wl.tokens / (ms / 1e3), "ms_per_schedule": ms,
-                          "roofline_time_ms": t_star, "roofline_frac": t_star / ms, "check_ok": chk["ok"],
-                          "max_abs_err": chk["max_abs_err"]}), flush=True)
+                          "roofline_time_ms": t_star, "roofline_frac": t_star / ms,
+                          "roofline_serial_time_ms": t_serial, "roofline_serial_frac": t_serial / ms,
+                          "check_ok": chk["ok"], "max_abs_err": chk["max_abs_err"]}), flush=True)
         del wl
         torch.cuda.empty_cache()
 
@@ -1408,9 +1421,11 @@ def run_single(args, rank, world, dev, pk, pk_src):
                             "traffic": kernel_traffic("decode_split_paged.json"), "kernel": "decode_split_kernel",
                             "scope": "decode rows' bytes over the whole call: a lower bound on the kernel's rate"}
     if args.workload == "mixed":
-        t_star = sum(max(st["flops"] / (tc * 1e12), st["bytes"] / (hbm * 1e9)) for st in wl.steps) * 1e3
+        t_star, t_serial = mixed_rooflines(wl.steps, tc, hbm)
         line["roofline_time_ms"] = t_star
         line["roofline_frac"] = t_star / ms
+        line["roofline_serial_time_ms"] = t_serial
+        line["roofline_serial_frac"] = t_serial / ms
     if args.workload == "ladder":
         line["padded_rows_per_step"] = wl.padded_rows
     if args.workload in ("verify", "varlen"):

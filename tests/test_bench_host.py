@@ -61,3 +61,14 @@ def test_rolling_visible_pairs_match_the_oracle_mask():
             m = oracle.rolling_mask(c, C, k, lp)
             total += int((m == 0).sum())
         assert bench.rolling_visible_pairs(L, c, C, lp) == total, (L, c, C, lp)
+
+
+def test_mixed_rooflines_bracket_each_step():
+    """T* takes each step's larger term and the serial time their sum, so
+    T* <= serial <= 2 T*, with equality cases at the ends."""
+    steps = [{"flops": 2e12, "bytes": 1e9}, {"flops": 0.0, "bytes": 5e9}, {"flops": 4e12, "bytes": 0.0}]
+    tc, hbm = 2000.0, 5000.0  # TFLOP/s, GB/s
+    t_star, t_serial = bench.mixed_rooflines(steps, tc, hbm)
+    assert abs(t_star - (1.0 + 1.0 + 2.0)) < 1e-9          # ms: max(1, 0.2), max(0, 1), max(2, 0)
+    assert abs(t_serial - (1.2 + 1.0 + 2.0)) < 1e-9
+    assert t_star <= t_serial <= 2 * t_star
