@@ -574,6 +574,86 @@ def oracle_single_thread_fp32():
     return q.shape[0] / t, t
 
 
+def oracle_config_samples(budget_s=3.0):
+    """The C++ oracle (as it stands, std::thread on every host core) on bounded
+    samples of the other workloads, each scaled to its workload's unit; every
+    entry says what ran and how it was scaled."""
+    import numpy as np
+    import torch
+    from oracle import cpp as oracle
+    import synth_inputs as SI
+
+    oracle.set_threads(0)
+    res = {}
+    # config 1: the fp32 example, whole
+    q, k, v = (t.double().numpy() for t in SI.fp32_sdpa_example())
+    t0 = time.perf_counter()
+    oracle.chunked_prefill(q, k, v, 256)
+    t = time.perf_counter() - t0
+    res["fp32_example"] = {"tokens_per_s": q.shape[0] / t, "seconds": t,
+                           "sample": "the whole example: 1000 tokens, 8 heads x 64, chunks of 256"}
+    # config 3: the ladder prompts, KV-head group 0 of each until the budget is spent, scaled to 8 groups
+    toks, t_sum, done = 0, 0.0, 0
+    for idx in range(len(SI.LADDER_PROMPT_LENGTHS)):
+        q, k, v = (t.double().numpy() for t in SI.ladder_prompt(idx))
+        t0 = time.perf_counter()
+        oracle.chunked_prefill(q[:, :4], k[:, :1], v[:, :1], 512)
+        t_sum += time.perf_counter() - t0
+        toks += q.shape[0]
+        done += 1
+        if t_sum > budget_s:
+            break
+    res["padding_ladder"] = {"tokens_per_s": toks / (t_sum * 8), "seconds": t_sum,
+                             "sample": f"{done} of the 6 prompts, KV-head group 0 (4 of 32 query heads), chunks of "
+                                       "512 (the real rows, which padding leaves unchanged), scaled to 8 groups"}
+    # config 4: the rolling runs, whole, the shorter first
+    toks, t_sum, runs = 0, 0.0, []
+    for L, n_real in ((768, 700), (2048, 2000)):
+        q, k, v = (t.double().numpy() for t in SI.rolling_prompt(L))
+        t0 = time.perf_counter()
+        oracle.rolling_prefill(q, k, v, 256, 1024, L - n_real)
+        t_sum += time.perf_counter() - t0
+        toks += n_real
+        runs.append(L)
+        if t_sum > budget_s:
+            break
+    res["rolling"] = {"tokens_per_s": toks / t_sum, "seconds": t_sum,
+                      "sample": f"the whole rolling run(s) of aligned length {runs}, 16 heads x 128, C = 1024, c = 256"}
+    # config 5: step 1 at budget 8192 (64 decode rows, then the first 8128 rows of a prompt), sampled
+    mb = SI.mixed_batch()
+    ctx = mb.decode_ctx
+    g = torch.Generator().manual_seed(29)
+    t_dec, keys_dec = 0.0, 0
+    for i in range(8):
+        c = ctx[i]
+        kk = torch.randn(c, 8, 128, generator=g, dtype=torch.float64).numpy()
+        vv = torch.randn(c, 8, 128, generator=g, dtype=torch.float64).numpy()
+        qq = torch.randn(32, 128, generator=g, dtype=torch.float64).numpy()
+        t0 = time.perf_counter()
+        oracle.attention_row(qq, kk, vv, c - 1)
+        t_dec += time.perf_counter() - t0
+        keys_dec += c
+    dec_all = t_dec * sum(ctx) / keys_dec
+    n_pre = 8128
+    kk = torch.randn(n_pre, 8, 128, generator=g, dtype=torch.float64).numpy()
+    vv = torch.randn(n_pre, 8, 128, generator=g, dtype=torch.float64).numpy()
+    t_pre, pairs = 0.0, 0
+    for p in np.linspace(0, n_pre - 1, 16).astype(int):
+        qq = torch.randn(32, 128, generator=g, dtype=torch.float64).numpy()
+        t0 = time.perf_counter()
+        oracle.attention_row(qq, kk, vv, int(p))
+        t_pre += time.perf_counter() - t0
+        pairs += int(p) + 1
+    pre_all = t_pre * (n_pre * (n_pre + 1) // 2) / pairs
+    res["mixed_budget8192_step1"] = {
+        "rows_per_s": (64 + n_pre) / (dec_all + pre_all), "seconds_estimated": dec_all + pre_all,
+        "seconds_run": t_dec + t_pre,
+        "sample": "8 of the 64 decode rows over their whole contexts, scaled by context length to all 64; "
+                  "16 of the 8128 prompt rows at evenly spread positions, scaled by visible keys to the chunk"}
+    res["threads"] = oracle.threads()
+    return res
+
+
 class ChunkLoop:
     """Chunk-by-chunk prefill of one prompt through the public calls, for the
     rolling-cache workload (fp16 MHA 16 x 128, window 1024, chunk 256, aligned
@@ -1329,7 +1409,8 @@ def run_native(args):
                                 "parity": {"max_abs_err_vs_gpu": diff, "tol": BF16_TOL, "query_heads": heads,
                                            "rows": wl.N},
                                 "single_thread_fp32_example": {"tokens_per_s": v1, "seconds": t1, "cores": 1,
-                                                               "workload": "fp32_mha8_d64_prompt1000_chunk256"}}
+                                                               "workload": "fp32_mha8_d64_prompt1000_chunk256"},
+                                "configs": oracle_config_samples()}
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:

@@ -72,3 +72,16 @@ def test_mixed_rooflines_bracket_each_step():
     assert abs(t_star - (1.0 + 1.0 + 2.0)) < 1e-9          # ms: max(1, 0.2), max(0, 1), max(2, 0)
     assert abs(t_serial - (1.2 + 1.0 + 2.0)) < 1e-9
     assert t_star <= t_serial <= 2 * t_star
+
+
+def test_oracle_config_samples_cover_every_other_workload():
+    """The CPU baseline's bounded oracle samples name the configs they stand for
+    and return positive rates (a tiny budget: one prompt, one rolling run)."""
+    from oracle import cpp
+    cpp.build()
+    r = bench.oracle_config_samples(budget_s=0.01)
+    assert set(r) == {"fp32_example", "padding_ladder", "rolling", "mixed_budget8192_step1", "threads"}
+    for name in ("fp32_example", "padding_ladder", "rolling"):
+        assert r[name]["tokens_per_s"] > 0 and r[name]["sample"]
+    assert r["mixed_budget8192_step1"]["rows_per_s"] > 0
+    assert r["threads"] >= 1
