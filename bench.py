@@ -585,14 +585,14 @@ def oracle_config_samples(budget_s=3.0):
 
     oracle.set_threads(0)
     res = {}
-    # config 1: the fp32 example, whole
+    # the fp32 example, whole
     q, k, v = (t.double().numpy() for t in SI.fp32_sdpa_example())
     t0 = time.perf_counter()
     oracle.chunked_prefill(q, k, v, 256)
     t = time.perf_counter() - t0
     res["fp32_example"] = {"tokens_per_s": q.shape[0] / t, "seconds": t,
                            "sample": "the whole example: 1000 tokens, 8 heads x 64, chunks of 256"}
-    # config 3: the ladder prompts, KV-head group 0 of each until the budget is spent, scaled to 8 groups
+    # the ladder prompts, KV-head group 0 of each until the budget is spent, scaled to 8 groups
     toks, t_sum, done = 0, 0.0, 0
     for idx in range(len(SI.LADDER_PROMPT_LENGTHS)):
         q, k, v = (t.double().numpy() for t in SI.ladder_prompt(idx))
@@ -606,7 +606,7 @@ def oracle_config_samples(budget_s=3.0):
     res["padding_ladder"] = {"tokens_per_s": toks / (t_sum * 8), "seconds": t_sum,
                              "sample": f"{done} of the 6 prompts, KV-head group 0 (4 of 32 query heads), chunks of "
                                        "512 (the real rows, which padding leaves unchanged), scaled to 8 groups"}
-    # config 4: the rolling runs, whole, the shorter first
+    # the rolling runs, whole, the shorter first
     toks, t_sum, runs = 0, 0.0, []
     for L, n_real in ((768, 700), (2048, 2000)):
         q, k, v = (t.double().numpy() for t in SI.rolling_prompt(L))
@@ -619,7 +619,7 @@ def oracle_config_samples(budget_s=3.0):
             break
     res["rolling"] = {"tokens_per_s": toks / t_sum, "seconds": t_sum,
                       "sample": f"the whole rolling run(s) of aligned length {runs}, 16 heads x 128, C = 1024, c = 256"}
-    # config 5: step 1 at budget 8192 (64 decode rows, then the first 8128 rows of a prompt), sampled
+    # the mixed schedule's step 1 at budget 8192 (64 decode rows, then the first 8128 rows of a prompt), sampled
     mb = SI.mixed_batch()
     ctx = mb.decode_ctx
     g = torch.Generator().manual_seed(29)
@@ -1419,8 +1419,8 @@ def run_native(args):
 
 
 def run_sweep(args, dev, pk):
-    """NEXT-2 of the problem statement: the chunk width W of the GQA prompt and
-    the token budget of the mixed schedule, one line each (each checked first)."""
+    """Sweeps of the chunk width W of the GQA prompt and of the token budget of
+    the mixed schedule, one line each (each checked first)."""
     import torch
     tc, hbm = float(pk["bf16_tflops"]), float(pk["hbm_gbs"])
     flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
