@@ -2,8 +2,8 @@
 """Benchmark of the chunked-prefill causal attention hot path on one GB300.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
-                    [--workload gqa_prefill|fp32|ladder|rolling|decode|mixed]
-                    [--chunk W] [--prompt N] [--budget B] [--no-pad] [--no-extras]
+                    [--workload gqa_prefill|fp32|ladder|rolling|decode|mixed|verify|varlen|append|append_paged]
+                    [--chunk W] [--prompt N] [--budget B] [--overlap] [--no-pad] [--no-extras] [--sweep]
 
 Default workload (the one the headline metric is quoted on): one GQA layer,
 32 query / 8 KV heads, head_dim 128, bf16, a 4000-token prompt prefilled in
@@ -22,10 +22,12 @@ evaluation of the attention definition); a failed check ends the run without
 a line.
 
 The default line also carries, under "configs", one measurement of each of
-the other workloads of the problem statement (fp32 example, padding ladder,
-rolling cache, decode rows, and the whole mixed token-budget schedule at
-budgets 8192 and 2048, k-row verify chunks at long lengths, and ragged
-prompts in one call), each with its own check.  ``--workload X`` prints X's
+the other workloads (fp32 example, padding ladder, rolling cache, decode
+rows, k-row verify chunks at long lengths, ragged prompts in one call, the
+KV append alone on a contiguous and a paged cache, and the whole mixed
+token-budget schedule at budgets 8192 and 2048, serial and with the decode
+rows on a side stream), each with its own check, and under "cpu_baseline" the
+C++ oracle on bounded samples of the default and the other workloads.  ``--workload X`` prints X's
 line alone; ``--chunk`` / ``--prompt`` / ``--budget`` set the chunk width, the
 prompt length and the token budget, and ``--sweep`` prints one line per chunk
 width and per token budget.  ``--impl reference`` times the C++ CPU oracle (test infrastructure,
