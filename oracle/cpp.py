@@ -40,50 +40,56 @@ def build(force: bool = False) -> str:
     return LIB
 
 
+def load(path: str):
+    """The oracle library at `path` with every function's signature set (the
+    tests also load variant builds of the same source through this)."""
+    L = ctypes.CDLL(path)
+    sig = {
+        "cpo_set_threads": (None, [ctypes.c_int]),
+        "cpo_threads": (ctypes.c_int, []),
+        "cpo_chunk_plan": (ctypes.c_int, [ctypes.c_int, ctypes.c_int, _I, ctypes.c_int]),
+        "cpo_query_ladder": (ctypes.c_int, [ctypes.c_int, _I]),
+        "cpo_query_width": (ctypes.c_int, [ctypes.c_int, ctypes.c_int]),
+        "cpo_left_pad_length": (ctypes.c_int, [ctypes.c_int, ctypes.c_int]),
+        "cpo_schedule": (ctypes.c_int, [ctypes.c_int, ctypes.c_int, _I, ctypes.c_int, _I, ctypes.c_int]),
+        "cpo_pad_rows": (ctypes.c_int, [_D, ctypes.c_int, ctypes.c_int64, ctypes.c_int, _D]),
+        "cpo_chunk_attention": (None, [_D, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, _D, _D,
+                                       ctypes.c_int, ctypes.c_double, _D]),
+        "cpo_causal_attention": (None, [_D, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, _D, _D,
+                                        ctypes.c_double, _D]),
+        "cpo_chunked_prefill": (ctypes.c_int, [_D, _D, _D, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                               ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_double, _D,
+                                               _D, _D, _D]),
+        "cpo_kv_append": (ctypes.c_int, [_D, _D, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                         ctypes.c_int, _I]),
+        "cpo_padded_chunk": (ctypes.c_int, [_D, _D, _D, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                            ctypes.c_int, _D, _D, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                            ctypes.c_double, _D]),
+        "cpo_rolling_update": (None, [_D, _D, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, _D]),
+        "cpo_rolling_mask": (None, [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, _D]),
+        "cpo_rolling_prefill": (ctypes.c_int, [_D, _D, _D, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                               ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_double,
+                                               _D, _D]),
+        "cpo_paged_write": (ctypes.c_int, [_D, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, _I,
+                                           ctypes.c_int, _D]),
+        "cpo_paged_gather": (ctypes.c_int, [_D, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, _I,
+                                            ctypes.c_int, _D]),
+        "cpo_mixed_step": (ctypes.c_int, [_D, _D, _D, _D, _D, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                          ctypes.c_int, ctypes.c_int, _I, ctypes.c_int, _I, _I, ctypes.c_int,
+                                          ctypes.c_double, _D]),
+    }
+    for name, (res, args) in sig.items():
+        fn = getattr(L, name)
+        fn.restype = res
+        fn.argtypes = args
+    return L
+
+
 def lib():
     global _lib
     with _lock:
         if _lib is None:
-            L = ctypes.CDLL(build())
-            sig = {
-                "cpo_set_threads": (None, [ctypes.c_int]),
-                "cpo_threads": (ctypes.c_int, []),
-                "cpo_chunk_plan": (ctypes.c_int, [ctypes.c_int, ctypes.c_int, _I, ctypes.c_int]),
-                "cpo_query_ladder": (ctypes.c_int, [ctypes.c_int, _I]),
-                "cpo_query_width": (ctypes.c_int, [ctypes.c_int, ctypes.c_int]),
-                "cpo_left_pad_length": (ctypes.c_int, [ctypes.c_int, ctypes.c_int]),
-                "cpo_schedule": (ctypes.c_int, [ctypes.c_int, ctypes.c_int, _I, ctypes.c_int, _I, ctypes.c_int]),
-                "cpo_pad_rows": (ctypes.c_int, [_D, ctypes.c_int, ctypes.c_int64, ctypes.c_int, _D]),
-                "cpo_chunk_attention": (None, [_D, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, _D, _D,
-                                               ctypes.c_int, ctypes.c_double, _D]),
-                "cpo_causal_attention": (None, [_D, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, _D, _D,
-                                                ctypes.c_double, _D]),
-                "cpo_chunked_prefill": (ctypes.c_int, [_D, _D, _D, ctypes.c_int, ctypes.c_int, ctypes.c_int,
-                                                       ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_double, _D,
-                                                       _D, _D, _D]),
-                "cpo_kv_append": (ctypes.c_int, [_D, _D, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
-                                                 ctypes.c_int, _I]),
-                "cpo_padded_chunk": (ctypes.c_int, [_D, _D, _D, ctypes.c_int, ctypes.c_int, ctypes.c_int,
-                                                    ctypes.c_int, _D, _D, ctypes.c_int, ctypes.c_int, ctypes.c_int,
-                                                    ctypes.c_double, _D]),
-                "cpo_rolling_update": (None, [_D, _D, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, _D]),
-                "cpo_rolling_mask": (None, [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, _D]),
-                "cpo_rolling_prefill": (ctypes.c_int, [_D, _D, _D, ctypes.c_int, ctypes.c_int, ctypes.c_int,
-                                                       ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_double,
-                                                       _D, _D]),
-                "cpo_paged_write": (ctypes.c_int, [_D, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, _I,
-                                                   ctypes.c_int, _D]),
-                "cpo_paged_gather": (ctypes.c_int, [_D, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, _I,
-                                                    ctypes.c_int, _D]),
-                "cpo_mixed_step": (ctypes.c_int, [_D, _D, _D, _D, _D, ctypes.c_int, ctypes.c_int, ctypes.c_int,
-                                                  ctypes.c_int, ctypes.c_int, _I, ctypes.c_int, _I, _I, ctypes.c_int,
-                                                  ctypes.c_double, _D]),
-            }
-            for name, (res, args) in sig.items():
-                fn = getattr(L, name)
-                fn.restype = res
-                fn.argtypes = args
-            _lib = L
+            _lib = load(build())
     return _lib
 
 
