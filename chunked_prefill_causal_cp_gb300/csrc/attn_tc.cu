@@ -259,7 +259,7 @@ __device__ __forceinline__ void take_ticket(const AttnArgs& a) {
   }
 }
 
-template <typename T, int D>
+template <typename T, int D, bool kRing>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
@@ -356,7 +356,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int n = past + rows;  // positions written, including this call's rows
   const int row0 = seq_row0(a.rows, s);
   const int t_end = min(t0 + 2 * rpt, rows);
-  const bool rolling = a.cache.kind == CP_CACHE_ROLLING;
+  // A ring cache: the launcher picks the kRing instantiation for it (compiled
+  // for the ring alone); the other instantiation keeps the run-time test.
+  const bool rolling = kRing || a.cache.kind == CP_CACHE_ROLLING;
   const bool paged = a.cache.kind == CP_CACHE_PAGED;
   const int cap = a.cache.capacity;
   // Key indices walked: absolute positions [0, nkeys) (contiguous / paged) or
@@ -827,7 +829,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <typename T, int D>
+template <typename T, int D, bool kRing>
 cudaError_t launch_t(const AttnArgs& a, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                      const CUtensorMap& to, const CUtensorMap& tkn, const CUtensorMap& tvn, int pairs_bound,
                      cudaStream_t st) {
@@ -846,10 +848,10 @@ cudaError_t launch_t(const AttnArgs& a, const CUtensorMap& tq, const CUtensorMap
     // The register split is only sound at the per-thread count it was sized
     // for: refuse to launch a build that came out at another count.
     cudaFuncAttributes fa;
-    e = cudaFuncGetAttributes(&fa, attn_tc_kernel<T, D>);
+    e = cudaFuncGetAttributes(&fa, attn_tc_kernel<T, D, kRing>);
     if (e != cudaSuccess) return e;
     if (fa.numRegs != kRegsLaunch) return cudaErrorInvalidDeviceFunction;
-    e = cudaFuncSetAttribute(attn_tc_kernel<T, D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    e = cudaFuncSetAttribute(attn_tc_kernel<T, D, kRing>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     ready_mask.fetch_or(bit, std::memory_order_release);
   }
@@ -868,7 +870,7 @@ cudaError_t launch_t(const AttnArgs& a, const CUtensorMap& tq, const CUtensorMap
   cfg.stream = st;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  e = cudaLaunchKernelEx(&cfg, attn_tc_kernel<T, D>, tq, tk, tv, to, tkn, tvn, a);
+  e = cudaLaunchKernelEx(&cfg, attn_tc_kernel<T, D, kRing>, tq, tk, tv, to, tkn, tvn, a);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
@@ -888,11 +890,19 @@ cudaError_t launch_attn_tc(const AttnArgs& a, int dtype, const CUtensorMap& tq, 
                            const CUtensorMap& tv, const CUtensorMap& to, const CUtensorMap& tkn,
                            const CUtensorMap& tvn, int pairs_bound, cudaStream_t st) {
   if (pairs_bound <= 0) return cudaSuccess;
-  if (dtype == CP_BF16)
-    return a.d == 64 ? launch_t<__nv_bfloat16, 64>(a, tq, tk, tv, to, tkn, tvn, pairs_bound, st)
-                     : launch_t<__nv_bfloat16, 128>(a, tq, tk, tv, to, tkn, tvn, pairs_bound, st);
-  return a.d == 64 ? launch_t<__half, 64>(a, tq, tk, tv, to, tkn, tvn, pairs_bound, st)
-                   : launch_t<__half, 128>(a, tq, tk, tv, to, tkn, tvn, pairs_bound, st);
+  const bool ring = a.cache.kind == CP_CACHE_ROLLING;
+  if (dtype == CP_BF16) {
+    if (ring)
+      return a.d == 64 ? launch_t<__nv_bfloat16, 64, true>(a, tq, tk, tv, to, tkn, tvn, pairs_bound, st)
+                       : launch_t<__nv_bfloat16, 128, true>(a, tq, tk, tv, to, tkn, tvn, pairs_bound, st);
+    return a.d == 64 ? launch_t<__nv_bfloat16, 64, false>(a, tq, tk, tv, to, tkn, tvn, pairs_bound, st)
+                     : launch_t<__nv_bfloat16, 128, false>(a, tq, tk, tv, to, tkn, tvn, pairs_bound, st);
+  }
+  if (ring)
+    return a.d == 64 ? launch_t<__half, 64, true>(a, tq, tk, tv, to, tkn, tvn, pairs_bound, st)
+                     : launch_t<__half, 128, true>(a, tq, tk, tv, to, tkn, tvn, pairs_bound, st);
+  return a.d == 64 ? launch_t<__half, 64, false>(a, tq, tk, tv, to, tkn, tvn, pairs_bound, st)
+                   : launch_t<__half, 128, false>(a, tq, tk, tv, to, tkn, tvn, pairs_bound, st);
 }
 
 }  // namespace cp
