@@ -697,10 +697,10 @@ class ChunkLoop:
                                   device=dev)
         self.tokens = sum(r["L"] - r["lp"] for r in self.runs)
         self.flops = sum(4 * r["d"] * r["H"] * r["pairs"] for r in self.runs)
-        # one cp_prefill_chunk call per chunk: fp32 on a contiguous cache is one launch (the kernel
-        # appends, attends and advances seqlens_k); the rolling cache takes the append, then the
-        # attention kernel, which advances seqlens_k
-        self.launches = sum((1 if r["dtype"] == torch.float32 else 2) * len(r["sizes"]) for r in self.runs)
+        # one cp_prefill_chunk call per chunk, one launch each: the fp32 kernel on the contiguous
+        # cache, the tensor-core kernel on the ring (256-row chunks on a 1024-slot ring), each
+        # appending the chunk, attending and advancing seqlens_k
+        self.launches = sum(len(r["sizes"]) for r in self.runs)
 
     def step(self):
         cp = self.cp

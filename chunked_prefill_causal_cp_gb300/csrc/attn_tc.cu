@@ -241,6 +241,95 @@ struct Walk {
   }
 };
 
+// The walks of a ring cache's physical slots [0, nkeys).  The call's rows are
+// positions [past, past + rows), in slots (past + t) mod cap: one range of
+// slots that wraps only at the ring's end.  When the ring is wider than a tile
+// and rows <= cap - 128 (so no tile holds both ends of a wrapped range), a tile
+// that holds cached and new slots is walked twice, its cached slots and then
+// its new ones, whether or not the append is fused (so both paths do the same
+// arithmetic), and every tile's new slots form one contiguous span; else
+// (`split` false) every tile is walked once, as on an unfused ring.  Virtual
+// tile j goes to CTA rank j % 2.
+struct RingWalk {
+  bool split = false;
+  int cap = 1, nkeys = 0, rows = 0, s0 = 0, count = 0;
+  int dbl0 = -1, dbl1 = -1;  // the tiles walked twice, ascending (-1: none)
+  __device__ __forceinline__ RingWalk() {}
+  __device__ __forceinline__ RingWalk(int cap_, int nkeys_, int past, int rows_, int ntiles) {
+    cap = cap_;
+    nkeys = nkeys_;
+    rows = rows_;
+    s0 = past % cap_;
+    split = cap_ > kTcBlockN && rows_ <= cap_ - kTcBlockN;
+    dbl0 = dbl1 = -1;
+    count = ntiles;
+    if (split) {
+      const int ca = s0 / kTcBlockN, cb = ((s0 + rows - 1) % cap) / kTcBlockN;
+      const int c0 = min(ca, cb), c1 = max(ca, cb);
+      if (both(c0)) dbl0 = c0;
+      if (c1 != c0 && both(c1)) {
+        if (dbl0 < 0) dbl0 = c1; else dbl1 = c1;
+      }
+      count = ntiles + (dbl0 >= 0) + (dbl1 >= 0);
+    }
+  }
+  // The new slots [a, b) of tile t (a == b: none).
+  __device__ __forceinline__ void new_span(int t, int& a, int& b) const {
+    const int j0 = t * kTcBlockN, j1 = min(j0 + kTcBlockN, nkeys);
+    int lo = max(j0, s0), hi = min(j1, min(s0 + rows, cap));
+    if (lo < hi) { a = lo; b = hi; return; }
+    lo = j0;
+    hi = min(j1, s0 + rows - cap);
+    if (lo < hi) { a = lo; b = hi; return; }
+    a = b = j0;
+  }
+  __device__ __forceinline__ bool both(int t) const {
+    int a, b;
+    new_span(t, a, b);
+    return a < b && (b - a) < min(t * kTcBlockN + kTcBlockN, nkeys) - t * kTcBlockN;
+  }
+  __device__ __forceinline__ void at(int w, int& tile, bool& is_new) const {
+    int base = 0;  // tiles walked twice before the candidate
+    const int d[2] = {dbl0, dbl1};
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      if (d[k] < 0) break;
+      const int first = d[k] + base;  // walk index of tile d[k]'s cached walk
+      if (w < first) break;
+      if (w == first || w == first + 1) {
+        tile = d[k];
+        is_new = w == first + 1;
+        return;
+      }
+      ++base;
+    }
+    tile = w - base;
+    int a, b;
+    new_span(tile, a, b);
+    is_new = split && a < b;  // a tile walked once holds only new slots or only cached ones
+  }
+  // Slots [lo, hi) of the tile that hold written data (the interface of Walk;
+  // the ring's masks come from the slot-to-position map instead).
+  __device__ __forceinline__ void range(int tile, bool, int& lo, int& hi) const {
+    lo = tile * kTcBlockN;
+    hi = min(lo + kTcBlockN, nkeys);
+  }
+  // Row of k_new / v_new that slot tile * 128 maps to in a new walk (rows
+  // outside [0, rows) are not new slots and read as zero).
+  __device__ __forceinline__ int new_row(int tile) const {
+    const int j0 = tile * kTcBlockN;
+    return j0 - s0 + (j0 + kTcBlockN <= s0 ? cap : 0);
+  }
+};
+
+// The walk a kernel instantiation uses: the ring's on a ring cache, else the plain one.
+template <bool kRing>
+__device__ __forceinline__ const std::conditional_t<kRing, RingWalk, Walk>& pick_walk(const Walk& plain,
+                                                                                      const RingWalk& ring) {
+  if constexpr (kRing) return ring;
+  else return plain;
+}
+
 // The last CTA of the grid to take a ticket -- every CTA takes one after all its
 // threads have read their sequence's length -- adds commit_add to every length
 // and resets the counter for the next launch.  A counter found above the grid
@@ -366,7 +455,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int nkeys = rolling ? min(n, cap) : past + t_end;
   const int n_valid = rolling ? nkeys : n;  // key indices holding written data
   const int ntiles = (nkeys + kTcBlockN - 1) / kTcBlockN;
-  const Walk walk(!rolling && !paged, past, n_valid, ntiles);
+  const Walk walk_plain(!rolling && !paged, past, n_valid, ntiles);
+  const RingWalk walk_ring = kRing ? RingWalk(cap, nkeys, past, rows, ntiles) : RingWalk();
+  const auto& walk = pick_walk<kRing>(walk_plain, walk_ring);
   const int nmine = walk.count > rank ? (walk.count - rank + 1) / 2 : 0;  // this CTA's walks: rank + 2i
   const bool q1 = t0 + rpt < rows;  // Q tile 1 holds at least one row (else it is skipped)
   const bool own_tile = rank == 0 || q1;   // Q tile `rank` (finished here) has rows
@@ -429,12 +520,24 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (from_new) {
         // Fused append: keys [j0, j0 + 128) are rows j0 - past ... of this
         // sequence's k_new / v_new (4-D maps: rows outside [0, rows) read as zero).
+        if constexpr (kRing) {
+          // On a ring, slot j0 maps to row walk.new_row(tile).
+          if (lane == 0) {
+            const int nr = walk.new_row(tile);
+            mbar_arrive_expect_tx(kf, DB * kBlockBytes);
+            for (int db = 0; db < DB; ++db) tma_load_4d(dk + db * kBlockBytes, &tm_kn, kf, db * 64, g, nr, s);
+            if (i == 0 && q1) load_q(1);
+            mbar_arrive_expect_tx(vf, DB * kBlockBytes);
+            for (int db = 0; db < DB; ++db) tma_load_4d(dv + db * kBlockBytes, &tm_vn, vf, db * 64, g, nr, s);
+          }
+        } else {
         if (lane == 0) {
           mbar_arrive_expect_tx(kf, DB * kBlockBytes);
           for (int db = 0; db < DB; ++db) tma_load_4d(dk + db * kBlockBytes, &tm_kn, kf, db * 64, g, j0 - past, s);
           if (i == 0 && q1) load_q(1);
           mbar_arrive_expect_tx(vf, DB * kBlockBytes);
           for (int db = 0; db < DB; ++db) tma_load_4d(dv + db * kBlockBytes, &tm_vn, vf, db * 64, g, j0 - past, s);
+        }
         }
       } else if (!paged || direct) {
         // Contiguous: keys [j0, j0 + 128) of KV head g.  Direct: they are rows
@@ -535,6 +638,33 @@ __global__ void __launch_bounds__(kThreads, 1)
         int ztile;
         bool znew;
         walk.at(rank + 2 * i, ztile, znew);
+        if constexpr (kRing) {
+          if (!(a.fused && znew)) {  // read from the ring: zero V rows that hold no slot of this walk
+            uint8_t* v_stage = sV + (i & 1) * DB * kBlockBytes;
+            auto zero_rows = [&](int lo, int hi) {  // rows [lo, hi) of the tile
+              const int nvec = max(hi - lo, 0) * 128 / 16;
+              for (int db = 0; db < DB; ++db) {
+                uint4* p = reinterpret_cast<uint4*>(v_stage + db * kBlockBytes + lo * 128);
+                for (int e = lane; e < nvec; e += 32) p[e] = make_uint4(0, 0, 0, 0);
+              }
+            };
+            const int jz = ztile * kTcBlockN;
+            const int valid = min(jz + kTcBlockN, walk.nkeys) - jz;  // rows holding written slots
+            int na, nb;
+            walk.new_span(ztile, na, nb);
+            if (!walk.split) {
+              zero_rows(valid, kTcBlockN);
+            } else if (znew) {  // keep the new span only
+              zero_rows(0, na - jz);
+              zero_rows(nb - jz, kTcBlockN);
+            } else {  // keep the cached slots: zero the new span and the unwritten tail
+              zero_rows(na - jz, nb - jz);
+              zero_rows(valid, kTcBlockN);
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+          }
+        } else {
         if (!(a.fused && znew)) {  // read from the cache: zero V rows that hold no key of this walk
           int zlo, zhi;
           walk.range(ztile, znew, zlo, zhi);
@@ -549,6 +679,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             fence_proxy_async_smem();
             __syncwarp();
           }
+        }
         }
         tc_fence_after();
         issue_pv(0, i);
@@ -582,6 +713,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr int kVec = D * 2 / 16;  // 16-byte vectors per row
       const long long src_row = (long long)row0 + tk0;
       const long long dst_row = ((long long)(s * a.hkv + g)) * cap + past + tk0;
+      if constexpr (kRing) {
+        for (int e = lane; e < nrow * kVec; e += 32) {  // position past + t lives in slot (past + t) mod cap
+          const int r = e / kVec, c = e % kVec;
+          const long long so = ((src_row + r) * a.hkv + g) * kVec + c;
+          const long long dof = (((long long)(s * a.hkv + g)) * cap + (past + tk0 + r) % cap) * kVec + c;
+          const uint4 kv = reinterpret_cast<const uint4*>(a.k_new)[so];
+          const uint4 vv = reinterpret_cast<const uint4*>(a.v_new)[so];
+          reinterpret_cast<uint4*>(a.k_cache)[dof] = kv;
+          reinterpret_cast<uint4*>(a.v_cache)[dof] = vv;
+        }
+      } else {
       for (int e = lane; e < nrow * kVec; e += 32) {
         const int r = e / kVec, c = e % kVec;
         const long long so = ((src_row + r) * a.hkv + g) * kVec + c;
@@ -590,6 +732,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint4 vv = reinterpret_cast<const uint4*>(a.v_new)[so];
         reinterpret_cast<uint4*>(a.k_cache)[dof] = kv;
         reinterpret_cast<uint4*>(a.v_cache)[dof] = vv;
+      }
       }
     }
   } else if (warp == 3) {
@@ -655,6 +798,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int pos = key + base_hi - (key > r_slot ? cap : 0);
           const bool vis = key < nkeys && pos >= lo && pos <= p_row;
           if (!vis) sv[c] = __float_as_uint(-INFINITY);
+        }
+        if constexpr (kRing) {
+          if (tile == walk.dbl0 || tile == walk.dbl1) {  // walked twice: this walk's slots only
+            int na, nb;
+            walk.new_span(tile, na, nb);
+            const int ca = na - j0, cb = nb - j0;
+#pragma unroll
+            for (int c = 0; c < 128; ++c)
+              if ((c >= ca && c < cb) != is_new) sv[c] = __float_as_uint(-INFINITY);
+          }
         }
       }
       {

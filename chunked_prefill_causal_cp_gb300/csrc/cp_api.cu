@@ -256,13 +256,17 @@ int run_tc_part(const cp_layer_desc* d, AttnArgs a, int64_t rows_total, const vo
   return launch_result(launch_attn_tc(a, d->dtype, tq, tk, tv, to, tkn, tvn, (int)pairs, st));
 }
 
-// A contiguous-cache chunk of uniform rows (more than one) in half precision
-// goes to the tensor-core kernel with the append fused in.
+// A chunk of uniform rows in half precision goes to the tensor-core kernel
+// with the append fused in: on a contiguous cache when it has more rows than
+// the split-KV path takes; on a ring wider than one tile when rows <= capacity
+// - 128 (the geometry in which the kernel walks a ring's cached and new slots
+// apart, as it then also does for an unfused ring call).
 bool use_fused(const cp_layer_desc* d, int32_t rows_padded) {
   const int G = d->num_q_heads / d->num_kv_heads;
+  if (d->dtype == CP_F32 || !attn_tc_supported(d->head_dim, G, d->dtype)) return false;
+  if (d->kind == CP_CACHE_ROLLING) return d->capacity > kTcBlockN && rows_padded <= d->capacity - kTcBlockN;
   const bool on_decode_path = decode_supported(d->head_dim, G, d->dtype) && rows_padded <= decode_max_rows(G);
-  return d->kind == CP_CACHE_CONTIG && rows_padded > 1 && !on_decode_path && d->dtype != CP_F32 &&
-         attn_tc_supported(d->head_dim, G, d->dtype);
+  return d->kind == CP_CACHE_CONTIG && rows_padded > 1 && !on_decode_path;
 }
 
 // One launch for append, attention and the advance of the lengths: the tiles

@@ -170,11 +170,12 @@ int cp_prefill_chunk_attn(const cp_layer_desc* desc, const void* q, const void* 
  * calls made back to back with commit = 1 ([Glossary] "How chunked prefill
  * works": each chunk's K/V join the cache and its rows attend to the cache).
  * For a contiguous cache in bf16/fp16 with more rows per sequence than the
- * split-KV path takes (16 / G), and for a contiguous cache in fp32, this is one
- * kernel launch: the kernel reads the chunk's own keys straight from
- * k_new / v_new, copies those rows into the cache, and the last of its CTAs to
- * have read seqlens_k advances it.  Other layouts take an append launch
- * followed by the attention.
+ * split-KV path takes (16 / G), for a contiguous cache in fp32, and for a
+ * rolling cache in bf16/fp16 wider than 128 slots with rows <= capacity - 128,
+ * this is one kernel launch: the kernel reads the chunk's own keys straight
+ * from k_new / v_new, copies those rows into the cache (ring: slot position
+ * mod capacity), and the last of its CTAs to have read seqlens_k advances it.
+ * Other cases take an append launch followed by the attention.
  *   q, out        device [B, rows_padded, Hq, D]
  *   k_new, v_new  device [B, rows_padded, Hkv, D] (rows [real_rows,
  *                 rows_padded) are appended too: cp_pad_chunk fills them); they

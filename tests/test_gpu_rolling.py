@@ -90,6 +90,21 @@ def test_rolling_small_ragged():
     _run_rolling(300, 48, 176, 4, 64, torch.bfloat16, seed=11)
 
 
+@pytest.mark.parametrize("n_real,c,C,H,d,dtype,seed", [
+    (300, 48, 176, 4, 64, torch.bfloat16, 11),    # ring not a multiple of the tile, chunks of 48
+    (700, 96, 384, 8, 128, torch.float16, 12),    # chunks of 96: the new slots straddle 128-slot tiles
+    (1100, 256, 384, 4, 128, torch.bfloat16, 13), # chunks of 256 = capacity - 128: the widest split
+])
+def test_rolling_fused_equals_separate_at_straddling_chunks(n_real, c, C, H, d, dtype, seed):
+    """One-call chunks on a ring (the kernel reads the chunk's slots from k_new,
+    walks a tile that holds cached and new slots twice, and copies the rows
+    into the ring): the oracle's outputs and ring contents, and the separate
+    append + attention calls bit for bit."""
+    got, _, lp, _, _, _ = _run_rolling(n_real, c, C, H, d, dtype, seed=seed, fused=True)
+    ref, _, _, _, _, _ = _run_rolling(n_real, c, C, H, d, dtype, seed=seed)
+    assert np.array_equal(got, ref)
+
+
 def test_rolling_gqa():
     """Rolling window with grouped-query heads (8 query / 2 KV heads, bf16):
     compared with the oracle's rolling prefill on the K/V heads repeated per
