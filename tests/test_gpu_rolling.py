@@ -105,11 +105,8 @@ def test_rolling_fused_equals_separate_at_straddling_chunks(n_real, c, C, H, d, 
     assert np.array_equal(got, ref)
 
 
-def test_rolling_gqa():
-    """Rolling window with grouped-query heads (8 query / 2 KV heads, bf16):
-    compared with the oracle's rolling prefill on the K/V heads repeated per
-    query head (grouped-query attention equals that multi-head attention)."""
-    n_real, c, C, hq, hkv, d = 500, 128, 384, 8, 2, 128
+def _run_gqa(c, fused):
+    n_real, C, hq, hkv, d = 500, 384, 8, 2, 128
     G = hq // hkv
     L = cp.cp_aligned_length(n_real, c)
     lp = L - n_real
@@ -123,11 +120,16 @@ def test_rolling_gqa():
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
     out = torch.empty(L, hq, d, dtype=torch.bfloat16, device="cuda")
     qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
+    ws = torch.zeros(cp.cp_workspace_size(desc, c, C, 1), dtype=torch.uint8, device="cuda")
     for ci in range(L // c):
         sl = slice(ci * c, (ci + 1) * c)
-        cp.cp_kv_append(desc, kd[None, sl], vd[None, sl], c, kc, vc, lens, ci * c, dev_status=status)
-        cp.cp_prefill_chunk_attn(desc, qd[None, sl], kc, vc, lens, c, c, ci * c, out[None, sl], None,
-                                 commit=True, left_pad=left, dev_status=status)
+        if fused:
+            cp.cp_prefill_chunk(desc, qd[None, sl], kd[None, sl], vd[None, sl], kc, vc, lens, c, c, ci * c,
+                                out[None, sl], ws, left_pad=left, dev_status=status)
+        else:
+            cp.cp_kv_append(desc, kd[None, sl], vd[None, sl], c, kc, vc, lens, ci * c, dev_status=status)
+            cp.cp_prefill_chunk_attn(desc, qd[None, sl], kc, vc, lens, c, c, ci * c, out[None, sl], None,
+                                     commit=True, left_pad=left, dev_status=status)
     torch.cuda.synchronize()
     assert int(status.item()) == 0 and int(lens.item()) == L
     k_rep = np.repeat(f64(k), G, axis=1)
@@ -144,3 +146,19 @@ def test_rolling_gqa():
     phys = torch.from_numpy(a[keep] % C)
     assert torch.equal(kc[0, :, phys].cpu().double(), torch.from_numpy(ok_k[::G][:, keep]))
     assert torch.equal(vc[0, :, phys].cpu().double(), torch.from_numpy(ok_v[::G][:, keep]))
+    return got
+
+
+def test_rolling_gqa():
+    """Rolling window with grouped-query heads (8 query / 2 KV heads, bf16):
+    compared with the oracle's rolling prefill on the K/V heads repeated per
+    query head (grouped-query attention equals that multi-head attention)."""
+    _run_gqa(128, fused=False)
+
+
+@pytest.mark.parametrize("c", [128, 96])
+def test_rolling_gqa_fused_call(c):
+    """The same grouped-query window through the one-call chunk entry point
+    (chunks of 96 put the new slots across 128-slot tiles): the oracle, and
+    the separate append + attention calls bit for bit."""
+    assert np.array_equal(_run_gqa(c, fused=True), _run_gqa(c, fused=False))
