@@ -162,3 +162,74 @@ def test_rolling_gqa_fused_call(c):
     (chunks of 96 put the new slots across 128-slot tiles): the oracle, and
     the separate append + attention calls bit for bit."""
     assert np.array_equal(_run_gqa(c, fused=True), _run_gqa(c, fused=False))
+
+
+def _run_ring_batch(n_reals, c, C, hq, hkv, d, dtype, seed, fused):
+    """A batch of left-padded sequences of one aligned length on a ring cache,
+    chunk by chunk; returns (out [B, L, hq, d] float64, k ring, v ring, L)."""
+    L = max(cp.cp_aligned_length(n, c) for n in n_reals)
+    B = len(n_reals)
+    G = hq // hkv
+    qs, ks, vs = [], [], []
+    for b in range(B):
+        q, _, _ = SI.rolling_prompt(L, seed=seed + 2 * b, heads=hq, dim=d, dtype=dtype)
+        _, k, v = SI.rolling_prompt(L, seed=seed + 2 * b + 1, heads=hkv, dim=d, dtype=dtype)
+        qs.append(q)
+        ks.append(k)
+        vs.append(v)
+    qd, kd, vd = (torch.stack(t).cuda() for t in (qs, ks, vs))
+    desc = cp.layer_desc(dtype, B, hq, hkv, d, cp.CP_CACHE_ROLLING, capacity=C)
+    kc = torch.full((B, hkv, C, d), float("nan"), dtype=dtype, device="cuda")
+    vc = torch.full_like(kc, float("nan"))
+    lens = torch.zeros(B, dtype=torch.int32, device="cuda")
+    left = torch.tensor([L - n for n in n_reals], dtype=torch.int32, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = torch.empty(B, L, hq, d, dtype=dtype, device="cuda")
+    ws = torch.zeros(cp.cp_workspace_size(desc, B * c, C, B), dtype=torch.uint8, device="cuda")
+    for ci in range(L // c):
+        sl = slice(ci * c, (ci + 1) * c)
+        q_, k_, v_ = qd[:, sl].contiguous(), kd[:, sl].contiguous(), vd[:, sl].contiguous()
+        o_ = torch.empty_like(q_)
+        if fused:
+            cp.cp_prefill_chunk(desc, q_, k_, v_, kc, vc, lens, c, c, ci * c, o_, ws, left_pad=left,
+                                dev_status=status)
+        else:
+            cp.cp_kv_append(desc, k_, v_, c, kc, vc, lens, ci * c, dev_status=status)
+            cp.cp_prefill_chunk_attn(desc, q_, kc, vc, lens, c, c, ci * c, o_, None, commit=True,
+                                     left_pad=left, dev_status=status)
+        out[:, sl] = o_
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0 and torch.equal(lens.cpu(), torch.full((B,), L, dtype=torch.int32))
+    got = f64(out)
+    assert np.isfinite(got).all()
+    j = np.arange(C)
+    a = L - C + j
+    keep = a >= 0
+    phys = torch.from_numpy(a[keep] % C)
+    for b, n in enumerate(n_reals):
+        lp = L - n
+        k_rep = np.repeat(f64(ks[b]), G, axis=1)
+        v_rep = np.repeat(f64(vs[b]), G, axis=1)
+        ref, snaps = oracle.rolling_prefill(f64(qs[b]), k_rep, v_rep, c, C, lp)
+        err = np.abs(got[b, lp:] - ref[lp:]).max()
+        assert err < BF16_TOL, (b, err)
+        ok_k, ok_v = snaps[-1]
+        assert torch.equal(kc[b, :, phys].cpu().double(), torch.from_numpy(ok_k[::G][:, keep])), b
+        assert torch.equal(vc[b, :, phys].cpu().double(), torch.from_numpy(ok_v[::G][:, keep])), b
+    return got
+
+
+@pytest.mark.parametrize("n_reals,c,C,hq,hkv,d,dtype", [
+    ((700, 650), 128, 384, 8, 2, 128, torch.bfloat16),   # two sequences, left pads 68 and 118
+    ((500, 333, 480), 96, 352, 4, 4, 64, torch.float16),  # three sequences, MHA, head_dim 64
+    ((450,), 64, 256, 16, 2, 64, torch.bfloat16),        # GQA 8, head_dim 64
+    ((300,), 64, 320, 16, 1, 128, torch.float16),        # GQA 16 (one KV head)
+])
+def test_rolling_batches_and_groups(n_reals, c, C, hq, hkv, d, dtype):
+    """Ring caches for a batch of left-padded sequences and for large query
+    groups: each sequence against the oracle's rolling prefill (K/V heads
+    repeated per query head) with its ring de-rotated byte for byte, through
+    the one-call entry point and the separate calls, bit for bit."""
+    fused = _run_ring_batch(n_reals, c, C, hq, hkv, d, dtype, seed=40, fused=True)
+    split = _run_ring_batch(n_reals, c, C, hq, hkv, d, dtype, seed=40, fused=False)
+    assert np.array_equal(fused, split)
