@@ -32,7 +32,10 @@
 // Warp roles (384 threads per CTA, three warpgroups):
 //   warp 0      TMA producer: both Q tiles once, then this CTA's K and V tiles
 //               in a 2-stage ring, one stage = one K tile + one V tile, each
-//               with its own barrier (paged caches: one box per page).  The
+//               with its own barrier (paged caches: one box per page and lane;
+//               at head_dim 128 a box holds both 64-column halves of a page and
+//               the stage takes the page layout, 8-row groups [half][8][128 B],
+//               which the MMA descriptors of that instantiation follow).  The
 //               first stage is issued as Q0, K, Q1, V, so the first MMA waits
 //               for a quarter of the start-up bytes.
 //   warp 1      TMEM allocator and MMA issuer (one elected lane).  Per KV tile:
@@ -322,6 +325,16 @@ struct RingWalk {
   }
 };
 
+// Paged instantiation: whether walk w's K/V stage holds whole pages (the page
+// layout) rather than two 128-row boxes read from k_new / v_new.
+template <typename W>
+__device__ __forceinline__ bool stage_has_pages(const W& walk, int w, int kv_direct, int past) {
+  int t;
+  bool nw;
+  walk.at(w, t, nw);
+  return !(kv_direct && t * kTcBlockN >= past);
+}
+
 // The walk a kernel instantiation uses: the ring's on a ring cache, else the plain one.
 template <bool kRing>
 __device__ __forceinline__ const std::conditional_t<kRing, RingWalk, Walk>& pick_walk(const Walk& plain,
@@ -348,7 +361,7 @@ __device__ __forceinline__ void take_ticket(const AttnArgs& a) {
   }
 }
 
-template <typename T, int D, bool kRing>
+template <typename T, int D, bool kRing, bool kPageBox>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
@@ -561,6 +574,18 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_arrive_expect_tx(vf, bytes);
         }
         __syncwarp();
+        if constexpr (kPageBox) {
+          // One box per page and lane, both 64-column halves: page pi lands at
+          // pi * ps * 256 as 8-row groups [ps / 8][half][8 rows][128 B] (the
+          // page layout); lanes npg .. 2 npg - 1 load V.
+          const int pi = lane % npg;
+          const int page = __shfl_sync(0xffffffffu, my_page, pi);
+          if (lane < 2 * npg && page >= 0) {
+            const bool is_v = lane >= npg;
+            tma_load_4d((is_v ? dv : dk) + pi * ps * 256, is_v ? &tm_v : &tm_k, is_v ? vf : kf, 0, 0, 0,
+                        (page * a.hkv + g) * (ps / 8));
+          }
+        } else {
         // One box per lane: box b < 2 * npg * DB is tensor b / (npg * DB) (K, then V),
         // page (b / DB) % npg, 64-column half b % DB.
         const int nbox = npg * DB;
@@ -574,6 +599,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tma_load_3d((is_v ? dv : dk) + db * kBlockBytes + pi * ps * 128, is_v ? &tm_v : &tm_k, is_v ? vf : kf,
                         db * 64, 0, page * a.hkv + g);
           }
+        }
         }
         if (lane == 0 && i == 0 && q1) load_q(1);
       }
@@ -602,7 +628,23 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t q_desc0 = make_sdesc_sw128(smem_u32(sQ), 16, 1024);
       const uint64_t k_desc0 = make_sdesc_sw128(smem_u32(sK), 16, 1024);
       const uint64_t v_desc0 = make_sdesc_sw128(smem_u32(sV), kBlockBytes, 1024);
+      // Page layout (the paged instantiation's page boxes): K's 8-row groups
+      // 2048 B apart with the second 64-column half 1024 B in; V's 16-key steps
+      // 4096 B apart, its 8-key groups 2048 B and its halves (the MMA's N
+      // blocks) 1024 B apart.  Tiles read from k_new keep the two-box layout.
       auto issue_qk = [&](int w, int i) {  // S_w = Q_w K_i^T
+        if constexpr (kPageBox) {
+          const bool pg = stage_has_pages(walk, rank + 2 * i, a.kv_direct, past);
+          const uint64_t q_desc = q_desc0 + w * kTileStep;
+          const uint64_t k_desc = (pg ? make_sdesc_sw128(smem_u32(sK), 16, 2048) : k_desc0) + (i & 1) * kTileStep;
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint64_t off = ((kk >> 2) * kBlockBytes + (kk & 3) * 32) >> 4;
+            const uint64_t koff = pg ? ((kk >> 2) * 1024 + (kk & 3) * 32) >> 4 : off;
+            mma_ss_elect(tmem + 256u * w, q_desc + off, k_desc + koff, kIdescQK, kk > 0);
+          }
+          mma_commit_elect(&bar->s_full[w]);
+        } else {
         const uint64_t q_desc = q_desc0 + w * kTileStep;
         const uint64_t k_desc = k_desc0 + (i & 1) * kTileStep;
 #pragma unroll
@@ -611,13 +653,24 @@ __global__ void __launch_bounds__(kThreads, 1)
           mma_ss_elect(tmem + 256u * w, q_desc + off, k_desc + off, kIdescQK, kk > 0);
         }
         mma_commit_elect(&bar->s_full[w]);
+        }
       };
       auto issue_pv = [&](int w, int i) {  // O_w += P_w V_i
+        if constexpr (kPageBox) {
+          const bool pg = stage_has_pages(walk, rank + 2 * i, a.kv_direct, past);
+          const uint64_t v_desc = (pg ? make_sdesc_sw128(smem_u32(sV), 1024, 2048) : v_desc0) + (i & 1) * kTileStep;
+          const int step = pg ? 4096 : 2048;
+#pragma unroll
+          for (int kk = 0; kk < kTcBlockN / 16; ++kk)
+            mma_ts_elect(tmem + 256u * w + 128u, tmem + 256u * w + kk * 8, v_desc + ((kk * step) >> 4), kIdescPV,
+                         (i > 0 || kk > 0) ? 1u : 0u);
+        } else {
         const uint64_t v_desc = v_desc0 + (i & 1) * kTileStep;
 #pragma unroll
         for (int kk = 0; kk < kTcBlockN / 16; ++kk)
           mma_ts_elect(tmem + 256u * w + 128u, tmem + 256u * w + kk * 8, v_desc + ((kk * 2048) >> 4), kIdescPV,
                        (i > 0 || kk > 0) ? 1u : 0u);
+        }
       };
       bool ok = nmine > 0 && wait(&bar->q_full[0], 0) && wait(&bar->k_full[0], 0);
       if (ok) {
@@ -672,9 +725,25 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (tail < kTcBlockN) {
             uint8_t* v_stage = sV + (i & 1) * DB * kBlockBytes;
             const int nvec = (kTcBlockN - tail) * 128 / 16;
+            if constexpr (kPageBox) {
+              // Page layout: row r of half db at (r / 8) * 2048 + db * 1024 + (r % 8) * 128.
+              if (stage_has_pages(walk, rank + 2 * i, a.kv_direct, past)) {
+                for (int e = lane; e < nvec * DB; e += 32) {
+                  const int r = tail + e / (8 * DB), db = (e / 8) % DB;
+                  *reinterpret_cast<uint4*>(v_stage + (r >> 3) * 2048 + db * 1024 + (r & 7) * 128 + (e & 7) * 16) =
+                      make_uint4(0, 0, 0, 0);
+                }
+              } else {
+                for (int db = 0; db < DB; ++db) {
+                  uint4* p = reinterpret_cast<uint4*>(v_stage + db * kBlockBytes + tail * 128);
+                  for (int e = lane; e < nvec; e += 32) p[e] = make_uint4(0, 0, 0, 0);
+                }
+              }
+            } else {
             for (int db = 0; db < DB; ++db) {
               uint4* p = reinterpret_cast<uint4*>(v_stage + db * kBlockBytes + tail * 128);
               for (int e = lane; e < nvec; e += 32) p[e] = make_uint4(0, 0, 0, 0);
+            }
             }
             fence_proxy_async_smem();
             __syncwarp();
@@ -982,7 +1051,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <typename T, int D, bool kRing>
+template <typename T, int D, bool kRing, bool kPageBox = false>
 cudaError_t launch_t(const AttnArgs& a, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                      const CUtensorMap& to, const CUtensorMap& tkn, const CUtensorMap& tvn, int pairs_bound,
                      cudaStream_t st) {
@@ -1001,10 +1070,10 @@ cudaError_t launch_t(const AttnArgs& a, const CUtensorMap& tq, const CUtensorMap
     // The register split is only sound at the per-thread count it was sized
     // for: refuse to launch a build that came out at another count.
     cudaFuncAttributes fa;
-    e = cudaFuncGetAttributes(&fa, attn_tc_kernel<T, D, kRing>);
+    e = cudaFuncGetAttributes(&fa, attn_tc_kernel<T, D, kRing, kPageBox>);
     if (e != cudaSuccess) return e;
     if (fa.numRegs != kRegsLaunch) return cudaErrorInvalidDeviceFunction;
-    e = cudaFuncSetAttribute(attn_tc_kernel<T, D, kRing>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    e = cudaFuncSetAttribute(attn_tc_kernel<T, D, kRing, kPageBox>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     ready_mask.fetch_or(bit, std::memory_order_release);
   }
@@ -1023,7 +1092,7 @@ cudaError_t launch_t(const AttnArgs& a, const CUtensorMap& tq, const CUtensorMap
   cfg.stream = st;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  e = cudaLaunchKernelEx(&cfg, attn_tc_kernel<T, D, kRing>, tq, tk, tv, to, tkn, tvn, a);
+  e = cudaLaunchKernelEx(&cfg, attn_tc_kernel<T, D, kRing, kPageBox>, tq, tk, tv, to, tkn, tvn, a);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
@@ -1037,6 +1106,7 @@ bool attn_tc_supported(int d, int group, int dtype) {
 
 // pairs_bound: number of 2*128-row Q-tile pairs to cover (one 2-CTA cluster each).
 // to: the output [rows, Hq, D] with the same box as tq (finished tiles are TMA-stored).
+// tk, tv on a paged cache with D = 128: page-row maps (make_tc_maps), one box per page.
 // tkn, tvn: this call's new K/V rows: [rows, Hkv, D] with box {64, 1, 128} when a.kv_direct
 // (paged), [num_seqs, rows_uniform, Hkv, D] with box {64, 1, 128, 1} when a.fused (contiguous).
 cudaError_t launch_attn_tc(const AttnArgs& a, int dtype, const CUtensorMap& tq, const CUtensorMap& tk,
@@ -1044,6 +1114,9 @@ cudaError_t launch_attn_tc(const AttnArgs& a, int dtype, const CUtensorMap& tq, 
                            const CUtensorMap& tvn, int pairs_bound, cudaStream_t st) {
   if (pairs_bound <= 0) return cudaSuccess;
   const bool ring = a.cache.kind == CP_CACHE_ROLLING;
+  if (a.cache.kind == CP_CACHE_PAGED && a.d == 128)  // page-layout stages (tk, tv: page-row maps)
+    return dtype == CP_BF16 ? launch_t<__nv_bfloat16, 128, false, true>(a, tq, tk, tv, to, tkn, tvn, pairs_bound, st)
+                            : launch_t<__half, 128, false, true>(a, tq, tk, tv, to, tkn, tvn, pairs_bound, st);
   if (dtype == CP_BF16) {
     if (ring)
       return a.d == 64 ? launch_t<__nv_bfloat16, 64, true>(a, tq, tk, tv, to, tkn, tvn, pairs_bound, st)

@@ -143,9 +143,28 @@ bool encode_4d(CUtensorMap* m, int dtype, const void* base, uint64_t d0, uint64_
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Page-row map of a [rows, 128] 16-bit pool (rows a multiple of 8): the 4-D
+// view {64 columns, 8 rows (256 B apart), 2 halves (128 B apart), rows / 8
+// groups (2048 B apart)} with one page per box, so a box lands as
+// [page / 8][half][8 rows][128 B] (128-byte swizzle).
+bool encode_page_rows(CUtensorMap* m, int dtype, const void* base, uint64_t rows, uint32_t page) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn || rows % 8 || page % 8 || page / 8 > 256) return false;
+  const cuuint64_t dims[4] = {64, 8, 2, rows / 8};
+  const cuuint64_t strides[3] = {256, 128, 2048};
+  const cuuint32_t box[4] = {64, 8, 2, page / 8};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  const CUtensorMapDataType ty =
+      dtype == CP_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  return fn(m, ty, 4, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // Tensor maps of the tensor-core path: Q/out rows [rows_total, Hq, D] in
 // boxes of (64 dims, G heads, 128/G tokens); K/V in boxes of 128 keys
-// (contiguous / rolling) or one page (paged) by 64 dims.
+// (contiguous / rolling) or one page (paged) by 64 dims, or on a paged cache
+// with D = 128 page-row maps (one box per page, both halves).
 bool make_tc_maps(const cp_layer_desc* d, const void* q, const void* out, int64_t rows_total, const void* k,
                   const void* v, int batch, CUtensorMap* tq, CUtensorMap* to, CUtensorMap* tk, CUtensorMap* tv) {
   const int G = d->num_q_heads / d->num_kv_heads;
@@ -154,6 +173,9 @@ bool make_tc_maps(const cp_layer_desc* d, const void* q, const void* out, int64_
   if (!encode_3d(to, d->dtype, out, D, d->num_q_heads, (uint64_t)rows_total, 64, G, kTcBlockM / G)) return false;
   if (d->kind == CP_CACHE_PAGED) {
     const uint64_t planes = (uint64_t)d->num_pages * d->num_kv_heads;
+    if (D == 128)
+      return encode_page_rows(tk, d->dtype, k, planes * d->page_size, d->page_size) &&
+             encode_page_rows(tv, d->dtype, v, planes * d->page_size, d->page_size);
     return encode_3d(tk, d->dtype, k, D, d->page_size, planes, 64, d->page_size, 1) &&
            encode_3d(tv, d->dtype, v, D, d->page_size, planes, 64, d->page_size, 1);
   }
