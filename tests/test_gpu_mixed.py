@@ -416,3 +416,68 @@ def test_mixed_step_page_sizes(page):
     got_k, got_v = f64(kp), f64(vp)
     mask = ~np.isnan(ok)
     assert np.array_equal(got_k[mask], ok[mask]) and np.array_equal(got_v[mask], ov[mask])
+
+
+@pytest.mark.parametrize("page,dtype,hq,hkv,d", [
+    (16, torch.bfloat16, 32, 8, 128),
+    (32, torch.float16, 32, 8, 128),
+    (64, torch.bfloat16, 16, 2, 128),
+    (128, torch.float16, 8, 8, 128),
+    (16, torch.float16, 16, 16, 128),
+    (16, torch.bfloat16, 32, 8, 64),
+])
+def test_prompt_chunk_over_cached_pages(page, dtype, hq, hkv, d):
+    """A prompt chunk whose keys are mostly cached pages (the tensor-core path
+    reads them page by page; at head_dim 128 one box per page in the page
+    layout), beside two decode rows: a first prompt of 700 tokens is already in
+    the pool, the step brings its next 200 rows.  Every row against the oracle,
+    the pools bit for bit."""
+    ctx = [301, 1030]
+    past_p, R = 700, 200
+    lens = ctx + [past_p + R]
+    need = [-(-(n + 64) // page) for n in lens]
+    max_blocks, num_pages = max(need), sum(need)
+    perm = torch.randperm(num_pages, generator=torch.Generator().manual_seed(page + hq))
+    table = torch.full((len(need), max_blocks), -1, dtype=torch.int32)
+    off = 0
+    for s, nb in enumerate(need):
+        table[s, :nb] = perm[off:off + nb].to(torch.int32)
+        off += nb
+    desc = cp.layer_desc(dtype, 0, hq, hkv, d, cp.CP_CACHE_PAGED, page_size=page, num_pages=num_pages,
+                         max_blocks=max_blocks)
+    kp = torch.full((num_pages, hkv, page, d), float("nan"), dtype=dtype, device="cuda")
+    vp = torch.full_like(kp, float("nan"))
+    ok = np.full(tuple(kp.shape), np.nan)
+    ov = np.full(tuple(kp.shape), np.nan)
+    hist = [c - 1 for c in ctx] + [past_p]
+    for s, n in enumerate(hist):  # positions [0, n) already in the pool
+        hk, hv = SI.normal((n, hkv, d), 1400 + s).to(dtype), SI.normal((n, hkv, d), 1500 + s).to(dtype)
+        a = torch.arange(n)
+        pg = table[s, a // page].long()
+        kp[pg, :, a % page] = hk.cuda()
+        vp[pg, :, a % page] = hv.cuda()
+        ok[pg.numpy(), :, (a % page).numpy()] = f64(hk)
+        ov[pg.numpy(), :, (a % page).numpy()] = f64(hv)
+    dq, dk, dv = SI.gqa_prompt(2, seed=80 + page, hq=hq, hkv=hkv, dim=d, dtype=dtype)
+    pq, pk, pv = SI.gqa_prompt(R, seed=81 + page, hq=hq, hkv=hkv, dim=d, dtype=dtype)
+    q = torch.cat([dq, pq]); kn = torch.cat([dk, pk]); vn = torch.cat([dv, pv])
+    rows = [1, 1, R]
+    S, T = len(rows), sum(rows)
+    max_ctx = max(p + r for p, r in zip(hist, rows))
+    cu = torch.tensor(np.concatenate([[0], np.cumsum(rows)]), dtype=torch.int32, device="cuda")
+    pl = torch.tensor(hist, dtype=torch.int32, device="cuda")
+    out = torch.empty(T, hq, d, dtype=dtype, device="cuda")
+    ws = torch.zeros(cp.cp_workspace_size(desc, T, max_ctx, S), dtype=torch.uint8, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    cp.cp_mixed_step(desc, q.cuda(), kn.cuda(), vn.cuda(), kp, vp, table.cuda(), cu, pl, S, T, max_ctx, out, ws,
+                     dev_status=status)
+    torch.cuda.synchronize()
+    ref, ok, ov, newp = oracle.mixed_step(f64(q), f64(kn), f64(vn), ok, ov, table.numpy(), rows, hist)
+    assert int(status.item()) == 0
+    err = np.abs(f64(out) - ref).max()
+    assert err < BF16_TOL, err
+    assert pl.tolist() == newp
+    got_k, got_v = f64(kp), f64(vp)
+    mask = ~np.isnan(ok)
+    assert np.array_equal(got_k[mask], ok[mask]) and np.array_equal(got_v[mask], ov[mask])
+    assert np.isnan(got_k[~mask]).all() and np.isnan(got_v[~mask]).all()
