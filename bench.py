@@ -49,6 +49,7 @@ sys.path.insert(0, ROOT)
 
 METRIC = "chunked-prefill attn tokens/s & effective TFLOP/s; % of GB300 BF16/HBM roofline"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+HBM_NOMINAL_GBS = 7900.0  # the part's nominal HBM3e rate, reported beside the measured copy rate
 BF16_TOL = 2e-2   # max-abs error bound for 16-bit inputs with fp32 accumulation
 FP32_TOL = 1e-4   # max-abs error bound for the fp32 path
 L2_NOTE = "flushed between timed steps (512 MiB write)"
@@ -1249,6 +1250,7 @@ def other_configs(dev, flush, pk, reps, warmup):
     gbs = wl.decode_bytes / (ms / 1e3) / 1e9
     res["decode"] = {**wl.config(), "rows_per_s": wl.tokens / (ms / 1e3), "ms_per_step": ms,
                      "decode_bytes_per_step": wl.decode_bytes, "gbs_whole_step": gbs, "hbm_frac_whole_step": gbs / hbm,
+                     "hbm_frac_nominal": gbs / HBM_NOMINAL_GBS,
                      "traffic": kernel_traffic("decode_split_paged.json"),
                      "scope": ("K/V, q and out bytes of the 64 decode rows over the whole cp_mixed_step call "
                                "(append, split-KV kernel, combine, commit): a lower bound on the kernel's rate"),
@@ -1262,6 +1264,7 @@ def other_configs(dev, flush, pk, reps, warmup):
         tf = wl.flops / (ms / 1e3) / 1e12
         res[mode] = {**wl.config(), "rows_per_s": wl.tokens / (ms / 1e3), "ms_per_step": ms, "tflops": tf,
                      "tensor_frac": tf / tc, "gbs_algorithmic": gbs, "hbm_frac": gbs / hbm,
+                     "hbm_frac_nominal": gbs / HBM_NOMINAL_GBS,
                      "roofline_time_us": max(wl.flops / (tc * 1e12), wl.bytes / (hbm * 1e9)) * 1e6,
                      "dtype": "bf16", "check": chk, "gpu_launches_per_step": wl.launches}
         del wl
@@ -1272,6 +1275,7 @@ def other_configs(dev, flush, pk, reps, warmup):
         gbs = wl.bytes / (ms / 1e3) / 1e9
         res[f"append_{mode}"] = {**wl.config(), "rows_per_s": wl.tokens / (ms / 1e3), "ms_per_step": ms,
                                  "gbs_algorithmic": gbs, "hbm_frac": gbs / hbm,
+                                 "hbm_frac_nominal": gbs / HBM_NOMINAL_GBS,
                                  "traffic": kernel_traffic(f"kv_append_{mode}.json"), "dtype": "bf16", "check": chk,
                                  "gpu_launches_per_step": wl.launches}
         del wl
@@ -1501,6 +1505,7 @@ def run_single(args, rank, world, dev, pk, pk_src):
     if args.workload == "decode":
         gbs = wl.decode_bytes / (ms / 1e3) / 1e9
         line["roofline"] = {"bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s", "frac": gbs / hbm,
+                            "frac_of_nominal": gbs / HBM_NOMINAL_GBS,
                             "traffic": kernel_traffic("decode_split_paged.json"), "kernel": "decode_split_kernel",
                             "scope": "decode rows' bytes over the whole call: a lower bound on the kernel's rate"}
     if args.workload == "mixed":
@@ -1519,9 +1524,12 @@ def run_single(args, rank, world, dev, pk, pk_src):
                             "unit": "GB/s" if args.workload == "verify" else "TFLOP/s",
                             "scope": "algorithmic bytes or FLOPs over the whole call"}
         line["roofline"]["frac"] = line["roofline"]["achieved"] / line["roofline"]["peak"]
+        if args.workload == "verify":
+            line["roofline"]["frac_of_nominal"] = gbs / HBM_NOMINAL_GBS
     if args.workload in ("append", "append_paged"):
         gbs = wl.bytes / (ms / 1e3) / 1e9
         line["roofline"] = {"bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s", "frac": gbs / hbm,
+                            "frac_of_nominal": gbs / HBM_NOMINAL_GBS,
                             "traffic": kernel_traffic(f"kv_append_{wl.mode}.json"), "kernel": "kv_append_kernel",
                             "scope": "the rows' K/V read and written once, over the call (one launch)"}
     if rank == 0:
