@@ -93,11 +93,13 @@ def lib():
         L.cp_rolling_mask.argtypes = [c_int32, c_int32, c_int32, c_int32, POINTER(c_float)]
         L.cp_schedule.argtypes = [c_int32, c_int32, POINTER(c_int32), c_int32, POINTER(SchedEntry), c_int32]
         L.cp_status_string.argtypes = [c_int32]
+        L.cp_selftest_bounded_wait.argtypes = [P, P, P]
+        L.cp_abi_version.argtypes = []
         L.cp_status_string.restype = ctypes.c_char_p
         for name in ("cp_kv_append", "cp_pad_chunk", "cp_prefill_chunk_attn", "cp_prefill_chunk",
                      "cp_mixed_step", "cp_mixed_step_overlap", "cp_prefill_varlen", "cp_chunk_plan",
                      "cp_query_ladder", "cp_query_width", "cp_aligned_length", "cp_rolling_mask",
-                     "cp_schedule", "cp_abi_version"):
+                     "cp_schedule", "cp_abi_version", "cp_selftest_bounded_wait"):
             getattr(L, name).restype = c_int32
         _lib = L
     return _lib
@@ -279,3 +281,7 @@ def cp_status_string(status) -> str:
 
 def cp_abi_version() -> int:
     return lib().cp_abi_version()
+
+
+def cp_selftest_bounded_wait(dev_status, dev_out, stream=None) -> int:
+    return lib().cp_selftest_bounded_wait(_ptr(dev_status), _ptr(dev_out), _stream(stream, dev_out))

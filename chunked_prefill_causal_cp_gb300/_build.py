@@ -17,7 +17,8 @@ BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libcp.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr"]
-SOURCES = ["cp_api.cu", "plan.cpp", "kv_append.cu", "attn_f32.cu", "attn_tc.cu", "decode.cu", "noalloc.cu"]
+SOURCES = ["cp_api.cu", "plan.cpp", "kv_append.cu", "attn_f32.cu", "attn_tc.cu", "decode.cu", "noalloc.cu",
+           "selftest.cu"]
 
 
 def _nvcc():

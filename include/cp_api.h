@@ -391,6 +391,21 @@ int32_t cp_schedule(int32_t budget, int32_t n_running, const int32_t* prompt_len
 /* cp_status_string -- static text for a cp_status value. */
 const char* cp_status_string(int32_t status);
 
+/* cp_selftest_bounded_wait -- checks, on the device, the bounded wait that
+ * every kernel of this library uses for its barriers (no page defines it:
+ * it is this library's failure-detection path).  One warp waits on a
+ * barrier that nothing completes; the wait gives up after the library's wait
+ * limit (4 s), ORs CP_DEV_TIMEOUT into *dev_status and raises the CTA's abort
+ * flag, and a second wait returns at once.  No fault, no trap: the context
+ * stays usable.  Asynchronous on `stream`; takes the wait limit to finish.
+ *   dev_status  device int32, OR-ed with CP_DEV_TIMEOUT
+ *   dev_out     device uint64[5], 8-byte aligned: first wait succeeded (0/1),
+ *               its duration in ns, second wait succeeded (0/1), its
+ *               duration in ns, the abort flag at the end (0/1)
+ * Returns CP_ERR_INVALID_ARG for a null or misaligned pointer, CP_ERR_CUDA if
+ * the launch fails, else CP_OK. */
+int cp_selftest_bounded_wait(int32_t* dev_status, uint64_t* dev_out, void* stream);
+
 /* cp_abi_version -- CP_ABI_VERSION of the built library. */
 int32_t cp_abi_version(void);
 

@@ -301,3 +301,23 @@ def test_noalloc_refuses_a_step_whose_partials_exceed_the_scratch():
     st = L.cp_mixed_step_noalloc(ctypes.byref(d), FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, fits + 1,
                                  fits + 1, 8192, FAKE, None, None)
     assert st == cp.CP_ERR_WORKSPACE
+
+
+def test_selftest_rejects_bad_pointers_before_launch():
+    """The bounded-wait self-test checks its pointers on the host (no launch)."""
+    L = cp.lib()
+    f = L.cp_selftest_bounded_wait
+    assert f(None, None, None) == cp.CP_ERR_INVALID_ARG
+    assert f(ctypes.c_void_p(16), None, None) == cp.CP_ERR_INVALID_ARG
+    assert f(ctypes.c_void_p(16), ctypes.c_void_p(20), None) == cp.CP_ERR_INVALID_ARG  # not 8-byte aligned
+
+
+def test_every_bound_entry_point_declares_its_argument_types():
+    """Every C function the binding calls has ctypes argtypes, so no 64-bit
+    pointer or stream handle is passed as a 32-bit int."""
+    import re
+    src = open(cp.__file__).read()
+    called = set(re.findall(r"lib\(\)\.(cp_\w+)\(", src))
+    L = cp.lib()
+    missing = [name for name in sorted(called) if getattr(L, name).argtypes is None]
+    assert not missing, missing
