@@ -2,7 +2,7 @@
 """Benchmark of the chunked-prefill causal attention hot path on one GB300.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
-                    [--workload gqa_prefill|fp32|ladder|rolling|decode|mixed|verify|varlen|append|append_paged]
+                    [--workload gqa_prefill|fp32|ladder|rolling|decode|mixed|verify|varlen|deep|append|append_paged]
                     [--chunk W] [--prompt N] [--budget B] [--overlap] [--no-pad] [--no-extras] [--sweep]
 
 Default workload (the one the headline metric is quoted on): one GQA layer,
@@ -23,8 +23,9 @@ a line.
 
 The default line also carries, under "configs", one measurement of each of
 the other workloads (fp32 example, padding ladder, rolling cache, decode
-rows, k-row verify chunks at long lengths, ragged prompts in one call, the
-KV append alone on a contiguous and a paged cache, and the whole mixed
+rows, k-row verify chunks at long lengths, ragged prompts in one call, one
+8128-row chunk at 8128 cached positions (the attention kernel's steady state),
+the KV append alone on a contiguous and a paged cache, and the whole mixed
 token-budget schedule at budgets 8192 and 2048, serial and with the decode
 rows on a side stream), each with its own check, and under "cpu_baseline" the
 C++ oracle on bounded samples of the default and the other workloads.  ``--workload X`` prints X's
@@ -62,8 +63,8 @@ def parse_args(argv=None):
     p.add_argument("--warmup", type=int, default=20)
     p.add_argument("--impl", default="native", choices=["native", "reference"])
     p.add_argument("--workload", default="gqa_prefill",
-                   choices=["gqa_prefill", "fp32", "ladder", "rolling", "decode", "mixed", "verify", "varlen", "append",
-                            "append_paged"])
+                   choices=["gqa_prefill", "fp32", "ladder", "rolling", "decode", "mixed", "verify", "varlen", "deep",
+                            "append", "append_paged"])
     p.add_argument("--sweep", action="store_true",
                    help="one line per chunk width W (gqa_prefill) and per token budget (mixed schedule)")
     p.add_argument("--chunk", type=int, default=512, help="chunk width W of the gqa_prefill workload")
@@ -1023,7 +1024,11 @@ class ShortChunks:
     and different cached lengths (a step filled with chunks of several
     prompts): rows [2048, 1024, 512, 512, 256, 128, 64, 1] at lengths
     [0, 1024, 3000, 512, 6000, 7000, 100, 4095].  GQA 32/8 x 128 bf16, cache
-    capacity 8192, N(0,1) history drawn on the device."""
+    capacity 8192, N(0,1) history drawn on the device.
+    ``deep``: one 8128-row chunk of one sequence at 8128 cached positions (the
+    size of a budget-8192 step's prompt chunk), one cp_prefill_chunk call (one
+    launch): the kernel's steady state, with its per-launch fixed cost spread
+    over a long key walk."""
 
     HQ, HKV, D = 32, 8, 128
 
@@ -1037,6 +1042,9 @@ class ShortChunks:
             self.B, self.k, self.cap = 64, 4, 4096 + 8
             self.pasts = [4000] * self.B
             self.rows = [self.k] * self.B
+        elif mode == "deep":
+            self.B, self.cap = 1, 16384
+            self.pasts, self.rows = [8128], [8128]
         else:
             self.cap = 8192
             self.rows = [2048, 1024, 512, 512, 256, 128, 64, 1]
@@ -1067,14 +1075,15 @@ class ShortChunks:
         # algorithmic bytes: cached K/V read once per (sequence, KV head), the new rows' q, k, v and out
         self.bytes = sum(p * kv_row * 2 for p in self.pasts) + self.T * (2 * self.HQ * self.D * 2 + 2 * kv_row)
         self.tokens = self.T
-        # verify: append, split-KV kernel, combine, commit; varlen: the same plus the tensor-core kernel
-        self.launches = 4 if mode == "verify" else 5
+        # verify: append, split-KV kernel, combine, commit; varlen: the same plus the tensor-core kernel;
+        # deep: one tensor-core launch (append and length advance fused in)
+        self.launches = {"verify": 4, "varlen": 5, "deep": 1}[mode]
 
     def step(self):
         cp = self.cp
         self.lens.copy_(self.past0)
-        if self.mode == "verify":
-            B, k = self.B, self.k
+        if self.mode in ("verify", "deep"):
+            B, k = self.B, self.rows[0]
             cp.cp_prefill_chunk(self.desc, self.q.view(B, k, self.HQ, self.D), self.kn.view(B, k, self.HKV, self.D),
                                 self.vn.view(B, k, self.HKV, self.D), self.kc, self.vc, self.lens, k, k,
                                 max(self.pasts), self.out.view(B, k, self.HQ, self.D), self.ws,
@@ -1114,6 +1123,9 @@ class ShortChunks:
         if self.mode == "verify":
             return {"workload": "verify_k4_x64_past4000_gqa32x8_d128_bf16", "sequences": self.B, "k": self.k,
                     "past": self.pasts[0], "l2": L2_NOTE, "cuda_graph": True}
+        if self.mode == "deep":
+            return {"workload": "deep_chunk_rows8128_past8128_gqa32x8_d128_bf16", "rows": self.rows[0],
+                    "past": self.pasts[0], "capacity": self.cap, "l2": L2_NOTE, "cuda_graph": True}
         return {"workload": "varlen8_gqa32x8_d128_bf16_cap8192", "rows": self.rows, "pasts": self.pasts,
                 "l2": L2_NOTE, "cuda_graph": True}
 
@@ -1257,7 +1269,7 @@ def other_configs(dev, flush, pk, reps, warmup):
                      "dtype": "bf16", "check": chk, "gpu_launches_per_step": wl.launches}
     del wl
 
-    for mode in ("verify", "varlen"):
+    for mode in ("verify", "varlen", "deep"):
         wl = ShortChunks(dev, mode)
         ms, chk = measure(wl, capture(wl.step, dev), flush, reps, warmup, torch)
         gbs = wl.bytes / (ms / 1e3) / 1e9
@@ -1267,6 +1279,8 @@ def other_configs(dev, flush, pk, reps, warmup):
                      "hbm_frac_nominal": gbs / HBM_NOMINAL_GBS,
                      "roofline_time_us": max(wl.flops / (tc * 1e12), wl.bytes / (hbm * 1e9)) * 1e6,
                      "dtype": "bf16", "check": chk, "gpu_launches_per_step": wl.launches}
+        if mode == "deep":
+            res[mode]["tensor_frac_sustained"] = tf / float(pk.get("bf16_tflops_sustained", tc))
         del wl
 
     for mode in ("contig", "paged"):
@@ -1462,7 +1476,7 @@ def run_single(args, rank, world, dev, pk, pk_src):
     kw = None
     if args.workload in ("fp32", "rolling"):
         wl = ChunkLoop(dev, args.workload)
-    elif args.workload in ("verify", "varlen"):
+    elif args.workload in ("verify", "varlen", "deep"):
         wl = ShortChunks(dev, args.workload)
     elif args.workload in ("append", "append_paged"):
         wl = AppendRows(dev, "paged" if args.workload == "append_paged" else "contig")
@@ -1516,7 +1530,7 @@ def run_single(args, rank, world, dev, pk, pk_src):
         line["roofline_serial_frac"] = t_serial / ms
     if args.workload == "ladder":
         line["padded_rows_per_step"] = wl.padded_rows
-    if args.workload in ("verify", "varlen"):
+    if args.workload in ("verify", "varlen", "deep"):
         gbs = wl.bytes / (ms / 1e3) / 1e9
         line["roofline"] = {"bound": "hbm" if args.workload == "verify" else "tensor",
                             "achieved": gbs if args.workload == "verify" else wl.flops / (ms / 1e3) / 1e12,
