@@ -1,0 +1,31 @@
+"""The C ABI from C: tests/capi_example.c, built with gcc against
+include/cp_api.h and libcp.so, calls the host-side helpers (no GPU) and
+prints results the pages fix (the 7 x 512 + 416 plan, the {171, 342, 512}
+ladder, the 10-step budget-8192 schedule whose first step is 64 decodes plus
+8128 prompt rows)."""
+import os
+import subprocess
+
+import chunked_prefill_causal_cp_gb300 as cp
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+ROOT = os.path.dirname(HERE)
+
+
+def test_c_program_links_and_calls_the_host_helpers(tmp_path):
+    cp.lib()  # the library is built
+    libdir = os.path.dirname(os.path.abspath(cp.LIB_PATH))
+    exe = os.path.join(tmp_path, "capi_example")
+    subprocess.check_call(["gcc", "-std=c99", "-Wall", "-Werror", "-I", os.path.join(ROOT, "include"),
+                           os.path.join(HERE, "capi_example.c"), "-L", libdir, "-l:libcp.so",
+                           "-Wl,-rpath," + libdir, "-o", exe])
+    out = subprocess.run([exe], capture_output=True, text=True, check=True).stdout.splitlines()
+    assert out[0] == f"abi {cp.cp_abi_version()}"
+    assert out[1] == "plan 8: 512 512 512 512 512 512 512 416"
+    assert out[2] == "ladder 3: 171 342 512"
+    assert out[3] == "width416 512"
+    assert out[4] == "aligned 2048"
+    assert out[5].startswith("schedule ") and out[5].endswith(", 10 steps, step 0 rows 8192")
+    ws = cp.cp_workspace_size(cp.layer_desc(1, 1, 32, 8, 128, cp.CP_CACHE_CONTIG, capacity=8192), 512, 8192, 1)
+    assert out[6] == f"workspace {ws}"
+    assert out[7] == f"rows past the chunk: {cp.lib().cp_status_string(cp.CP_ERR_INVALID_ARG).decode()}"
