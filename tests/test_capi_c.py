@@ -29,3 +29,27 @@ def test_c_program_links_and_calls_the_host_helpers(tmp_path):
     ws = cp.cp_workspace_size(cp.layer_desc(1, 1, 32, 8, 128, cp.CP_CACHE_CONTIG, capacity=8192), 512, 8192, 1)
     assert out[6] == f"workspace {ws}"
     assert out[7] == f"rows past the chunk: {cp.lib().cp_status_string(cp.CP_ERR_INVALID_ARG).decode()}"
+
+
+import pytest  # noqa: E402
+import torch  # noqa: E402
+
+
+@pytest.mark.gpu
+def test_c_program_runs_a_chunked_prefill_on_the_gpu(tmp_path):
+    """tests/capi_gpu_example.c: cudaMalloc, cp_prefill_chunk per chunk,
+    every output row against its own double-precision causal attention."""
+    if not torch.cuda.is_available():
+        pytest.skip("needs a GPU")
+    from chunked_prefill_causal_cp_gb300 import _build
+    _build.build()
+    libdir = os.path.dirname(os.path.abspath(cp.LIB_PATH))
+    cuda = os.environ.get("CUDA_HOME", "/usr/local/cuda")
+    exe = os.path.join(tmp_path, "capi_gpu_example")
+    subprocess.check_call(["gcc", "-std=c99", "-O2", "-Wall", "-Werror", "-I", os.path.join(ROOT, "include"),
+                           "-I", os.path.join(cuda, "include"), os.path.join(HERE, "capi_gpu_example.c"),
+                           "-L", libdir, "-l:libcp.so", "-L", os.path.join(cuda, "lib64"), "-lcudart", "-lm",
+                           "-Wl,-rpath," + libdir, "-Wl,-rpath," + os.path.join(cuda, "lib64"), "-o", exe])
+    r = subprocess.run([exe], capture_output=True, text=True)
+    assert r.returncode == 0, r.stdout + r.stderr
+    assert r.stdout.startswith("chunks 3 seqlens_k 300 status 0")
