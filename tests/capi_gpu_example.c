@@ -1,9 +1,9 @@
 /* A C program driving a chunked prefill through include/cp_api.h with the
  * CUDA runtime alone (no Python, no PyTorch): a 300-token GQA prompt (8 query
- * / 2 KV heads x 64, bf16) in chunks of 128 through cp_prefill_chunk, then
- * every output row checked against a double-precision evaluation of causal
- * attention written here.  tests/test_capi_c.py builds and runs it. */
-#include <math.h>
+ * / 2 KV heads x 64, bf16) in chunks of 128 through cp_prefill_chunk.  It
+ * writes q, k, v and the output (raw bf16, in that order) to the file named
+ * by its argument; tests/test_capi_c.py builds and runs it and compares the
+ * output with the oracle. */
 #include <stdint.h>
 #include <stdio.h>
 #include <stdlib.h>
@@ -21,12 +21,6 @@ static uint16_t to_bf16(float x) {  /* round to nearest even */
   u += 0x7FFFu + ((u >> 16) & 1u);
   return (uint16_t)(u >> 16);
 }
-static double from_bf16(uint16_t h) {
-  uint32_t u = (uint32_t)h << 16;
-  float x;
-  memcpy(&x, &u, 4);
-  return x;
-}
 static double uniform(uint64_t* s) {  /* xorshift64*, in [-1, 1) */
   *s ^= *s >> 12; *s ^= *s << 25; *s ^= *s >> 27;
   return (double)((*s * 2685821657736338717ull) >> 11) / 4503599627370496.0 - 1.0;
@@ -35,7 +29,8 @@ static double uniform(uint64_t* s) {  /* xorshift64*, in [-1, 1) */
 #define CHECK(x) do { cudaError_t e_ = (x); if (e_ != cudaSuccess) { \
   printf("cuda error %s at %d\n", cudaGetErrorString(e_), __LINE__); return 1; } } while (0)
 
-int main(void) {
+int main(int argc, char** argv) {
+  if (argc != 2) return 1;
   static uint16_t q[N * HQ * D], k[N * HKV * D], v[N * HKV * D], o[N * HQ * D];
   uint64_t seed = 0x9E3779B97F4A7C15ull;
   for (int i = 0; i < N * HQ * D; ++i) q[i] = to_bf16((float)uniform(&seed));
@@ -70,27 +65,12 @@ int main(void) {
   CHECK(cudaMemcpy(o, dout, sizeof o, cudaMemcpyDeviceToHost));
   CHECK(cudaMemcpy(&hlens, lens, 4, cudaMemcpyDeviceToHost));
   CHECK(cudaMemcpy(&hstatus, status, 4, cudaMemcpyDeviceToHost));
-  double worst = 0.0;
-  static double s[N];
-  for (int p = 0; p < N; ++p)
-    for (int h = 0; h < HQ; ++h) {
-      const int g = h / (HQ / HKV);
-      double m = -1e300, z = 0.0;
-      for (int j = 0; j <= p; ++j) {  /* causal: keys 0 .. p */
-        double dot = 0.0;
-        for (int t = 0; t < D; ++t)
-          dot += from_bf16(q[(p * HQ + h) * D + t]) * from_bf16(k[(j * HKV + g) * D + t]);
-        s[j] = dot / sqrt((double)D);
-        if (s[j] > m) m = s[j];
-      }
-      for (int j = 0; j <= p; ++j) { s[j] = exp(s[j] - m); z += s[j]; }
-      for (int t = 0; t < D; ++t) {
-        double acc = 0.0;
-        for (int j = 0; j <= p; ++j) acc += s[j] * from_bf16(v[(j * HKV + g) * D + t]);
-        const double err = fabs(acc / z - from_bf16(o[(p * HQ + h) * D + t]));
-        if (err > worst) worst = err;
-      }
-    }
-  printf("chunks %d seqlens_k %d status %d max_abs_err %.3e\n", (int)nc, (int)hlens, (int)hstatus, worst);
-  return (hlens == N && hstatus == 0 && worst < 2e-2) ? 0 : 2;
+  FILE* f = fopen(argv[1], "wb");
+  if (!f || fwrite(q, sizeof q, 1, f) != 1 || fwrite(k, sizeof k, 1, f) != 1 || fwrite(v, sizeof v, 1, f) != 1 ||
+      fwrite(o, sizeof o, 1, f) != 1 || fclose(f) != 0) {
+    printf("cannot write %s\n", argv[1]);
+    return 1;
+  }
+  printf("chunks %d seqlens_k %d status %d\n", (int)nc, (int)hlens, (int)hstatus);
+  return (hlens == N && hstatus == 0) ? 0 : 2;
 }

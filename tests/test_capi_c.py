@@ -6,7 +6,12 @@ ladder, the 10-step budget-8192 schedule whose first step is 64 decodes plus
 import os
 import subprocess
 
+import numpy as np
+import pytest
+import torch
+
 import chunked_prefill_causal_cp_gb300 as cp
+import oracle
 
 HERE = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(HERE)
@@ -31,14 +36,11 @@ def test_c_program_links_and_calls_the_host_helpers(tmp_path):
     assert out[7] == f"rows past the chunk: {cp.lib().cp_status_string(cp.CP_ERR_INVALID_ARG).decode()}"
 
 
-import pytest  # noqa: E402
-import torch  # noqa: E402
-
 
 @pytest.mark.gpu
 def test_c_program_runs_a_chunked_prefill_on_the_gpu(tmp_path):
-    """tests/capi_gpu_example.c: cudaMalloc, cp_prefill_chunk per chunk,
-    every output row against its own double-precision causal attention."""
+    """tests/capi_gpu_example.c: cudaMalloc, cp_prefill_chunk per chunk; the
+    inputs and outputs it writes out are compared with the oracle."""
     if not torch.cuda.is_available():
         pytest.skip("needs a GPU")
     from chunked_prefill_causal_cp_gb300 import _build
@@ -48,8 +50,17 @@ def test_c_program_runs_a_chunked_prefill_on_the_gpu(tmp_path):
     exe = os.path.join(tmp_path, "capi_gpu_example")
     subprocess.check_call(["gcc", "-std=c99", "-O2", "-Wall", "-Werror", "-I", os.path.join(ROOT, "include"),
                            "-I", os.path.join(cuda, "include"), os.path.join(HERE, "capi_gpu_example.c"),
-                           "-L", libdir, "-l:libcp.so", "-L", os.path.join(cuda, "lib64"), "-lcudart", "-lm",
+                           "-L", libdir, "-l:libcp.so", "-L", os.path.join(cuda, "lib64"), "-lcudart",
                            "-Wl,-rpath," + libdir, "-Wl,-rpath," + os.path.join(cuda, "lib64"), "-o", exe])
-    r = subprocess.run([exe], capture_output=True, text=True)
+    dump = os.path.join(tmp_path, "tensors.bin")
+    r = subprocess.run([exe, dump], capture_output=True, text=True)
     assert r.returncode == 0, r.stdout + r.stderr
     assert r.stdout.startswith("chunks 3 seqlens_k 300 status 0")
+    n, hq, hkv, d = 300, 8, 2, 64
+    raw = np.fromfile(dump, dtype=np.uint16)
+    sizes = [n * hq * d, n * hkv * d, n * hkv * d, n * hq * d]
+    parts = np.split(raw, np.cumsum(sizes)[:-1])
+    q, k, v, out = (torch.from_numpy(p.astype(np.int16)).view(torch.bfloat16).double().numpy()
+                    .reshape(n, -1, d) for p in parts)
+    ref, _, _ = oracle.chunked_prefill(q, k, v, 128)
+    assert np.abs(out - ref).max() < 2e-2
