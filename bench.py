@@ -434,7 +434,6 @@ class GqaPrefill:
 
     def config(self):
         return {"workload": f"gqa32x8_d128_bf16_prompt{self.N}_chunk{self.W}_cap{self.CAP}",
-                "model": "single GQA attention layer (synthetic N(0,1) q/k/v)",
                 "prompt_tokens": self.N, "chunk": self.W, "chunks": self.sizes,
                 "query_widths": self.widths, "kv_capacity": self.CAP, "heads_q": self.HQ,
                 "heads_kv": self.HKV, "head_dim": self.D, "global_batch": 1, "seq_len": self.N,
