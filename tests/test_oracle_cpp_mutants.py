@@ -45,6 +45,13 @@ MUTANTS = {
     # the remainder chunk put first
     "remainder_first": ("if (count < cap) sizes[count] = std::min(w, n - start);",
                         "if (count < cap) sizes[count] = (count == 0 && n % w) ? n % w : w;"),
+    # the scores taken against V instead of K
+    "scores_from_v": ("    if (!visible[j]) continue;\n    double dot = 0.0;\n    for (int t = 0; t < d; ++t) dot += q[t] * k[j * stride + t];",
+                      "    if (!visible[j]) continue;\n    double dot = 0.0;\n    for (int t = 0; t < d; ++t) dot += q[t] * v[j * stride + t];"),
+    # the additive rolling mask left out of the scores
+    "additive_mask_dropped": ("    s[j] = scale * dot + mask[j];\n", "    s[j] = scale * dot;\n"),
+    # the token budget not charged for the decode rows
+    "budget_ignores_decodes": ("    int left = budget - (int)decodes.size();\n", "    int left = budget;\n"),
     # pad rows filled with zeros instead of the last real row
     "pad_with_zeros": ("  for (int t = r; t < rp; ++t) std::memcpy(out + t * e, x + (int64_t)(r - 1) * e, "
                        "sizeof(double) * e);\n",

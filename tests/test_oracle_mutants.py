@@ -2,8 +2,9 @@
 one pin fails for each: a dropped or shifted causal diagonal, a wrong GQA
 head map, a wrong scale, a transposed softmax axis, an off-by-one append, a
 rolling cache that drops the newest rows, a wrong mask sign or pad bound, a
-floor-rounded ladder step, a remainder chunk put first, and swapped page
-indices."""
+floor-rounded ladder step, a remainder chunk put first, scores taken against
+V, the additive mask left out, a token budget that does not charge the decode
+rows, and swapped page indices."""
 import math
 
 import numpy as np
@@ -73,6 +74,40 @@ def _paged_gather_swapped(pool, table_row, n):
     return np.stack([pool[int(table_row[a % page]), :, a // page % page, :] for a in range(n)])
 
 
+def _attend_scores_from_v(q, k, v, visible, scale):
+    s = scale * (np.asarray(q, np.float64) @ np.asarray(v, np.float64).T)
+    s = np.where(visible, s, -np.inf)
+    w = np.exp(s - s.max(axis=1, keepdims=True))
+    return (w @ np.asarray(v, np.float64)) / w.sum(axis=1, keepdims=True)
+
+
+def _attend_additive_mask_dropped(q, k, v, mask, scale):
+    s = scale * (np.asarray(q, np.float64) @ np.asarray(k, np.float64).T)
+    w = np.exp(s - s.max(axis=1, keepdims=True))
+    return (w @ np.asarray(v, np.float64)) / w.sum(axis=1, keepdims=True)
+
+
+def _schedule_budget_ignores_decodes(budget, n_running, prompt_lens):
+    decodes = list(range(n_running))
+    done = [0] * len(prompt_lens)
+    steps = []
+    while any(d < n for d, n in zip(done, prompt_lens)):
+        left = budget  # the mistake: decode rows not charged
+        chunks, finished = [], []
+        for i, n in enumerate(prompt_lens):
+            if done[i] >= n or left == 0:
+                continue
+            take = min(left, n - done[i])
+            chunks.append((n_running + i, done[i], take))
+            done[i] += take
+            left -= take
+            if done[i] == n:
+                finished.append(n_running + i)
+        steps.append((list(decodes), chunks))
+        decodes += finished
+    return steps
+
+
 MUTANTS = {
     "diag_dropped": ("causal_visible", lambda pq, pk: pk[None, :] < pq[:, None]),
     "future_leak": ("causal_visible", lambda pq, pk: pk[None, :] <= pq[:, None] + 1),
@@ -87,6 +122,9 @@ MUTANTS = {
     "rolling_mask_pad": ("rolling_mask", _rolling_mask_pad_inclusive),
     "ladder_floor": ("query_ladder", _ladder_floor),
     "remainder_first": ("chunk_plan", _chunk_plan_remainder_first),
+    "scores_from_v": ("attend", _attend_scores_from_v),
+    "additive_mask_dropped": ("attend_additive", _attend_additive_mask_dropped),
+    "budget_ignores_decodes": ("schedule", _schedule_budget_ignores_decodes),
     "pad_with_zeros": ("pad_rows", lambda x, rp: np.concatenate(
         [x, np.zeros((rp - x.shape[0],) + x.shape[1:], x.dtype)])),
 }
