@@ -72,7 +72,8 @@ def parse_args(argv=None):
     p.add_argument("--budget", type=int, default=8192, help="token budget of the mixed workload")
     p.add_argument("--no-pad", action="store_true", help="do not widen chunks to the query-width ladder")
     p.add_argument("--overlap", action="store_true",
-                   help="mixed workload: cp_mixed_step_overlap (split-KV kernels on a side stream)")
+                   help="mixed / varlen workloads: cp_mixed_step_overlap / cp_prefill_varlen_overlap "
+                        "(split-KV kernels on a side stream)")
     p.add_argument("--no-extras", action="store_true", help="default line without the other workloads")
     p.add_argument("--cpu-seconds", type=float, default=12.0, help="CPU-baseline sample budget")
     p.add_argument("--skip-cpu", action="store_true")
@@ -1033,11 +1034,16 @@ class ShortChunks:
 
     HQ, HKV, D = 32, 8, 128
 
-    def __init__(self, dev, mode):
+    def __init__(self, dev, mode, overlap=False):
         import torch
         import chunked_prefill_causal_cp_gb300 as cp
 
         self.cp, self.torch, self.dev, self.mode = cp, torch, dev, mode
+        # varlen: the one-row sequence's split-KV kernels on a side stream (cp_prefill_varlen_overlap)
+        self.overlap = overlap and mode == "varlen"
+        if self.overlap:
+            self.side = torch.cuda.Stream(dev)
+            self.fork, self.join = torch.cuda.Event(), torch.cuda.Event()
         bf = torch.bfloat16
         if mode == "verify":
             self.B, self.k, self.cap = 64, 4, 4096 + 8
@@ -1089,6 +1095,10 @@ class ShortChunks:
                                 self.vn.view(B, k, self.HKV, self.D), self.kc, self.vc, self.lens, k, k,
                                 max(self.pasts), self.out.view(B, k, self.HQ, self.D), self.ws,
                                 dev_status=self.status)
+        elif self.overlap:
+            cp.cp_prefill_varlen_overlap(self.desc, self.q, self.kn, self.vn, self.kc, self.vc, self.cu, self.lens,
+                                         self.B, self.T, self.max_ctx, self.out, self.ws, self.side, self.fork,
+                                         self.join, dev_status=self.status)
         else:
             cp.cp_prefill_varlen(self.desc, self.q, self.kn, self.vn, self.kc, self.vc, self.cu, self.lens, self.B,
                                  self.T, self.max_ctx, self.out, self.ws, dev_status=self.status)
@@ -1127,8 +1137,8 @@ class ShortChunks:
         if self.mode == "deep":
             return {"workload": "deep_chunk_rows8128_past8128_gqa32x8_d128_bf16", "rows": self.rows[0],
                     "past": self.pasts[0], "capacity": self.cap, "l2": L2_NOTE, "cuda_graph": True}
-        return {"workload": "varlen8_gqa32x8_d128_bf16_cap8192", "rows": self.rows, "pasts": self.pasts,
-                "l2": L2_NOTE, "cuda_graph": True}
+        name = "varlen8_overlap_gqa32x8_d128_bf16_cap8192" if self.overlap else "varlen8_gqa32x8_d128_bf16_cap8192"
+        return {"workload": name, "rows": self.rows, "pasts": self.pasts, "l2": L2_NOTE, "cuda_graph": True}
 
 
 class AppendRows:
@@ -1270,8 +1280,8 @@ def other_configs(dev, flush, pk, reps, warmup):
                      "dtype": "bf16", "check": chk, "gpu_launches_per_step": wl.launches}
     del wl
 
-    for mode in ("verify", "varlen", "deep"):
-        wl = ShortChunks(dev, mode)
+    for mode in ("verify", "varlen", "varlen_overlap", "deep"):
+        wl = ShortChunks(dev, mode.replace("_overlap", ""), overlap=mode.endswith("_overlap"))
         ms, chk = measure(wl, capture(wl.step, dev), flush, reps, warmup, torch)
         gbs = wl.bytes / (ms / 1e3) / 1e9
         tf = wl.flops / (ms / 1e3) / 1e12
@@ -1478,7 +1488,7 @@ def run_single(args, rank, world, dev, pk, pk_src):
     if args.workload in ("fp32", "rolling"):
         wl = ChunkLoop(dev, args.workload)
     elif args.workload in ("verify", "varlen", "deep"):
-        wl = ShortChunks(dev, args.workload)
+        wl = ShortChunks(dev, args.workload, overlap=args.overlap)
     elif args.workload in ("append", "append_paged"):
         wl = AppendRows(dev, "paged" if args.workload == "append_paged" else "contig")
     elif args.workload == "ladder":

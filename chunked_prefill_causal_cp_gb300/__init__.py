@@ -79,6 +79,8 @@ def lib():
                                             c_int32, P, P, c_size_t, P, P, P, P, P]
         L.cp_prefill_varlen.argtypes = [POINTER(LayerDesc), P, P, P, P, P, P, P, c_int32, c_int32, c_int32, P,
                                         P, c_size_t, P, P]
+        L.cp_prefill_varlen_overlap.argtypes = [POINTER(LayerDesc), P, P, P, P, P, P, P, c_int32, c_int32,
+                                                c_int32, P, P, c_size_t, P, P, P, P, P]
         L.cp_mixed_step_noalloc.argtypes = [POINTER(LayerDesc), P, P, P, P, P, P, P, P, c_int32, c_int32,
                                             c_int32, P, P, P]
         L.cp_mixed_step_noalloc.restype = c_int32
@@ -97,7 +99,8 @@ def lib():
         L.cp_abi_version.argtypes = []
         L.cp_status_string.restype = ctypes.c_char_p
         for name in ("cp_kv_append", "cp_pad_chunk", "cp_prefill_chunk_attn", "cp_prefill_chunk",
-                     "cp_mixed_step", "cp_mixed_step_overlap", "cp_prefill_varlen", "cp_chunk_plan",
+                     "cp_mixed_step", "cp_mixed_step_overlap", "cp_prefill_varlen", "cp_prefill_varlen_overlap",
+                     "cp_chunk_plan",
                      "cp_query_ladder", "cp_query_width", "cp_aligned_length", "cp_rolling_mask",
                      "cp_schedule", "cp_abi_version", "cp_selftest_bounded_wait"):
             getattr(L, name).restype = c_int32
@@ -180,14 +183,8 @@ def cp_mixed_step(desc, q, k_new, v_new, k_pages, v_pages, block_table, cu_rows,
     _check(s, "cp_mixed_step")
 
 
-def cp_mixed_step_overlap(desc, q, k_new, v_new, k_pages, v_pages, block_table, cu_rows, past_len,
-                          num_seqs, total_rows, max_ctx, out, workspace, side_stream, fork_event, join_event,
-                          dev_status=None, stream=None):
-    """cp_mixed_step with the split-KV kernels on `side_stream` beside the
-    tensor-core kernel (see include/cp_api.h).  `side_stream` is a
-    torch.cuda.Stream (or a raw handle); the events are torch.cuda.Event
-    objects (or raw handles)."""
-    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+def _side_handles(side_stream, fork_event, join_event):
+    """Raw handles of a side stream and two events (torch objects or raw handles)."""
     side = side_stream if isinstance(side_stream, int) else side_stream.cuda_stream
     evs = []
     for ev in (fork_event, join_event):
@@ -197,6 +194,18 @@ def cp_mixed_step_overlap(desc, q, k_new, v_new, k_pages, v_pages, block_table, 
         if not ev.cuda_event:  # torch creates the event on its first record
             ev.record(side_stream if not isinstance(side_stream, int) else None)
         evs.append(ev.cuda_event)
+    return side, evs
+
+
+def cp_mixed_step_overlap(desc, q, k_new, v_new, k_pages, v_pages, block_table, cu_rows, past_len,
+                          num_seqs, total_rows, max_ctx, out, workspace, side_stream, fork_event, join_event,
+                          dev_status=None, stream=None):
+    """cp_mixed_step with the split-KV kernels on `side_stream` beside the
+    tensor-core kernel (see include/cp_api.h).  `side_stream` is a
+    torch.cuda.Stream (or a raw handle); the events are torch.cuda.Event
+    objects (or raw handles)."""
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    side, evs = _side_handles(side_stream, fork_event, join_event)
     s = lib().cp_mixed_step_overlap(ctypes.byref(desc), _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_pages),
                                     _ptr(v_pages), _ptr(block_table), _ptr(cu_rows), _ptr(past_len), num_seqs,
                                     total_rows, max_ctx, _ptr(out), _ptr(workspace), ws_bytes,
@@ -212,6 +221,20 @@ def cp_prefill_varlen(desc, q, k_new, v_new, k_cache, v_cache, cu_rows, seqlens_
                                 _ptr(v_cache), _ptr(cu_rows), _ptr(seqlens_k), num_seqs, total_rows, max_ctx,
                                 _ptr(out), _ptr(workspace), ws_bytes, _ptr(dev_status), _stream(stream, q))
     _check(s, "cp_prefill_varlen")
+
+
+def cp_prefill_varlen_overlap(desc, q, k_new, v_new, k_cache, v_cache, cu_rows, seqlens_k, num_seqs, total_rows,
+                              max_ctx, out, workspace, side_stream, fork_event, join_event, dev_status=None,
+                              stream=None):
+    """cp_prefill_varlen with the one-row sequences' split-KV kernels on
+    `side_stream` (see include/cp_api.h); handles as in cp_mixed_step_overlap."""
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    side, evs = _side_handles(side_stream, fork_event, join_event)
+    s = lib().cp_prefill_varlen_overlap(ctypes.byref(desc), _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_cache),
+                                        _ptr(v_cache), _ptr(cu_rows), _ptr(seqlens_k), num_seqs, total_rows,
+                                        max_ctx, _ptr(out), _ptr(workspace), ws_bytes, _ptr(dev_status),
+                                        _stream(stream, q), side, evs[0], evs[1])
+    _check(s, "cp_prefill_varlen_overlap")
 
 
 def cp_mixed_step_noalloc(desc, q, k_new, v_new, k_pages, v_pages, block_table, cu_rows, past_len,

@@ -705,10 +705,15 @@ int cp_mixed_step_overlap(const cp_layer_desc* desc, const void* q, const void* 
                      max_ctx, out, workspace, workspace_bytes, dev_status, static_cast<cudaStream_t>(stream), &fj);
 }
 
-int cp_prefill_varlen(const cp_layer_desc* desc, const void* q, const void* k_new, const void* v_new, void* k_cache,
-                      void* v_cache, const int32_t* cu_rows, int32_t* seqlens_k, int32_t num_seqs,
-                      int32_t total_rows, int32_t max_ctx, void* out, void* workspace, size_t workspace_bytes,
-                      int32_t* dev_status, void* stream) {
+}  // extern "C"
+
+namespace cp {
+// The checks of cp_prefill_varlen (and its overlap form), in order; *need
+// receives the workspace bytes the call needs.
+int varlen_check(const cp_layer_desc* desc, const void* q, const void* k_new, const void* v_new, void* k_cache,
+                 void* v_cache, const int32_t* cu_rows, int32_t* seqlens_k, int32_t num_seqs, int32_t total_rows,
+                 int32_t max_ctx, void* out, int64_t* need) {
+  *need = 0;
   int r = check_desc(desc, true);
   if (r != CP_OK) return r;
   if (desc->kind != CP_CACHE_CONTIG) return CP_ERR_UNSUPPORTED;
@@ -720,15 +725,47 @@ int cp_prefill_varlen(const cp_layer_desc* desc, const void* q, const void* k_ne
     return CP_ERR_INVALID_ARG;
   if ((int64_t)max_ctx > layout_limit(desc)) return CP_ERR_CAPACITY;
   const int G0 = desc->num_q_heads / desc->num_kv_heads;
-  int64_t need = 0;
   if (desc->dtype != CP_F32) {
     if (!attn_tc_supported(desc->head_dim, G0, desc->dtype)) return CP_ERR_UNSUPPORTED;
-    if (decode_supported(desc->head_dim, G0, desc->dtype)) need = decode_ws_bytes(desc, max_ctx, num_seqs);
+    if (decode_supported(desc->head_dim, G0, desc->dtype)) *need = decode_ws_bytes(desc, max_ctx, num_seqs);
   }
+  return CP_OK;
+}
+}  // namespace cp
+
+extern "C" {
+
+int cp_prefill_varlen(const cp_layer_desc* desc, const void* q, const void* k_new, const void* v_new, void* k_cache,
+                      void* v_cache, const int32_t* cu_rows, int32_t* seqlens_k, int32_t num_seqs,
+                      int32_t total_rows, int32_t max_ctx, void* out, void* workspace, size_t workspace_bytes,
+                      int32_t* dev_status, void* stream) {
+  int64_t need = 0;
+  const int r = cp::varlen_check(desc, q, k_new, v_new, k_cache, v_cache, cu_rows, seqlens_k, num_seqs, total_rows,
+                                 max_ctx, out, &need);
+  if (r != CP_OK || total_rows == 0) return r;
   if (need > 0 && (workspace == nullptr || (int64_t)workspace_bytes < need || !aligned16(workspace)))
     return CP_ERR_WORKSPACE;
   return ragged_step(desc, q, k_new, v_new, k_cache, v_cache, nullptr, cu_rows, seqlens_k, num_seqs, total_rows,
                      max_ctx, out, workspace, workspace_bytes, dev_status, static_cast<cudaStream_t>(stream));
+}
+
+int cp_prefill_varlen_overlap(const cp_layer_desc* desc, const void* q, const void* k_new, const void* v_new,
+                              void* k_cache, void* v_cache, const int32_t* cu_rows, int32_t* seqlens_k,
+                              int32_t num_seqs, int32_t total_rows, int32_t max_ctx, void* out, void* workspace,
+                              size_t workspace_bytes, int32_t* dev_status, void* stream, void* side_stream,
+                              void* fork_event, void* join_event) {
+  int64_t need = 0;
+  const int r = cp::varlen_check(desc, q, k_new, v_new, k_cache, v_cache, cu_rows, seqlens_k, num_seqs, total_rows,
+                                 max_ctx, out, &need);
+  if (r != CP_OK) return r;
+  if (!side_stream || !fork_event || !join_event || side_stream == stream) return CP_ERR_INVALID_ARG;
+  if (total_rows == 0) return CP_OK;
+  if (need > 0 && (workspace == nullptr || (int64_t)workspace_bytes < need || !aligned16(workspace)))
+    return CP_ERR_WORKSPACE;
+  const ForkJoin fj{static_cast<cudaStream_t>(side_stream), static_cast<cudaEvent_t>(fork_event),
+                    static_cast<cudaEvent_t>(join_event)};
+  return ragged_step(desc, q, k_new, v_new, k_cache, v_cache, nullptr, cu_rows, seqlens_k, num_seqs, total_rows,
+                     max_ctx, out, workspace, workspace_bytes, dev_status, static_cast<cudaStream_t>(stream), &fj);
 }
 
 }  // extern "C"

@@ -284,6 +284,22 @@ int cp_prefill_varlen(const cp_layer_desc* desc, const void* q, const void* k_ne
                       void* out, void* workspace, size_t workspace_bytes, int32_t* dev_status,
                       void* stream);
 
+/* cp_prefill_varlen_overlap -- cp_prefill_varlen with its one-row sequences
+ * on a side stream.
+ *
+ * The same call as cp_prefill_varlen (same arguments, checks, status codes
+ * and results, bit for bit), but when a step has both one-row sequences
+ * (split-KV path) and longer ones (tensor-core path), the split-KV kernels run
+ * on `side_stream` beside the tensor-core kernel, forked after the append and
+ * joined before the length advance, exactly as cp_mixed_step_overlap does.
+ * side_stream, fork_event and join_event as in cp_mixed_step_overlap (NULL,
+ * or side_stream == stream, returns CP_ERR_INVALID_ARG). */
+int cp_prefill_varlen_overlap(const cp_layer_desc* desc, const void* q, const void* k_new,
+                              const void* v_new, void* k_cache, void* v_cache, const int32_t* cu_rows,
+                              int32_t* seqlens_k, int32_t num_seqs, int32_t total_rows, int32_t max_ctx,
+                              void* out, void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                              void* stream, void* side_stream, void* fork_event, void* join_event);
+
 /* cp_mixed_step_noalloc -- cp_mixed_step for callers that cannot allocate.
  *
  * The pages have no counterpart to this entry point; it is a convenience of

@@ -321,3 +321,40 @@ def test_every_bound_entry_point_declares_its_argument_types():
     L = cp.lib()
     missing = [name for name in sorted(called) if getattr(L, name).argtypes is None]
     assert not missing, missing
+
+
+def test_varlen_overlap_status_codes_match_varlen():
+    """cp_prefill_varlen_overlap makes cp_prefill_varlen's checks first, with
+    the same status codes, then refuses a missing side stream or event and a
+    side stream equal to the main one (no case enqueues anything)."""
+    L = cp.lib()
+    SIDE, EV1, EV2 = 0x2000, 0x3000, 0x4000
+
+    def both(desc, num_seqs=2, total_rows=10, max_ctx=100, q=FAKE, ws=FAKE, ws_bytes=1 << 30):
+        d = ctypes.byref(desc) if desc is not None else None
+        plain = L.cp_prefill_varlen(d, q, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, num_seqs, total_rows, max_ctx, FAKE,
+                                    ws, ws_bytes, None, None)
+        over = L.cp_prefill_varlen_overlap(d, q, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, num_seqs, total_rows, max_ctx,
+                                           FAKE, ws, ws_bytes, None, None, SIDE, EV1, EV2)
+        return plain, over
+
+    cases = [(_desc(batch=4, head_dim=96), {}), (_desc(batch=4, kind=cp.CP_CACHE_PAGED, page_size=16,
+                                                     num_pages=8, max_blocks=4), {}),
+             (_desc(batch=4, num_q_heads=30), {}), (_desc(batch=4), dict(num_seqs=5)),
+             (_desc(batch=4), dict(q=None)), (_desc(batch=4), dict(q=FAKE + 8)),
+             (_desc(batch=4), dict(max_ctx=8193)), (_desc(batch=4), dict(ws=None)), (None, {})]
+    for desc, kw in cases:
+        plain, over = both(desc, **kw)
+        assert plain != cp.CP_OK and over == plain, (kw, plain, over)
+    d = _desc(batch=4)
+    assert both(d, total_rows=0) == (cp.CP_OK, cp.CP_OK)
+
+    def ov(**kw):
+        a = dict(side=SIDE, ev1=EV1, ev2=EV2, stream=None)
+        a.update(kw)
+        return L.cp_prefill_varlen_overlap(ctypes.byref(d), FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 2, 10, 100,
+                                           FAKE, FAKE, 1 << 30, None, a["stream"], a["side"], a["ev1"], a["ev2"])
+    assert ov(side=None) == cp.CP_ERR_INVALID_ARG
+    assert ov(ev1=None) == cp.CP_ERR_INVALID_ARG
+    assert ov(ev2=None) == cp.CP_ERR_INVALID_ARG
+    assert ov(stream=SIDE) == cp.CP_ERR_INVALID_ARG

@@ -129,3 +129,65 @@ def test_work_list_is_heaviest_first_and_changes_no_bit():
     vc.copy_(v0)
     plain, _ = _call(kc, vc, pasts, rows, q.cuda(), kn.cuda(), vn.cuda(), ws_bytes=_partials_bytes(B, max_ctx))
     assert torch.equal(plain, out)
+
+
+def test_overlap_form_is_bit_identical_eager_and_captured():
+    """cp_prefill_varlen_overlap (one-row sequences' split-KV kernels on a side
+    stream beside the tensor-core kernel) gives cp_prefill_varlen's outputs,
+    cache and lengths bit for bit, launched eagerly and replayed from a
+    captured CUDA graph."""
+    pasts, rows = [0, 37, 300, 1000, 128, 1500], [1, 5, 130, 257, 64, 1]
+    T = sum(rows)
+    q, kn, vn = (t.cuda() for t in SI.gqa_prompt(T, seed=81))
+    desc = cp.layer_desc(torch.bfloat16, len(pasts), HQ, HKV, D, cp.CP_CACHE_CONTIG, capacity=CAP)
+    cu = torch.tensor(np.concatenate([[0], np.cumsum(rows)]), dtype=torch.int32, device="cuda")
+    max_ctx = max(p + r for p, r in zip(pasts, rows))
+    base_k, base_v, _ = _setup(pasts, seed=80)
+
+    def run(overlap, graph=False):
+        kc, vc = base_k.clone(), base_v.clone()
+        lens = torch.tensor(pasts, dtype=torch.int32, device="cuda")
+        lens0 = lens.clone()
+        out = torch.zeros(T, HQ, D, dtype=torch.bfloat16, device="cuda")
+        ws = torch.zeros(cp.cp_workspace_size(desc, T, max_ctx, len(pasts)), dtype=torch.uint8, device="cuda")
+        status = torch.zeros(1, dtype=torch.int32, device="cuda")
+        side, ev1, ev2 = torch.cuda.Stream(), torch.cuda.Event(), torch.cuda.Event()
+
+        def reset():
+            kc.copy_(base_k)
+            vc.copy_(base_v)
+            lens.copy_(lens0)
+            out.zero_()
+
+        def call():
+            if overlap:
+                cp.cp_prefill_varlen_overlap(desc, q, kn, vn, kc, vc, cu, lens, len(pasts), T, max_ctx, out, ws,
+                                             side, ev1, ev2, dev_status=status)
+            else:
+                cp.cp_prefill_varlen(desc, q, kn, vn, kc, vc, cu, lens, len(pasts), T, max_ctx, out, ws,
+                                     dev_status=status)
+        if graph:
+            s = torch.cuda.Stream()
+            s.wait_stream(torch.cuda.current_stream())
+            with torch.cuda.stream(s):
+                call()  # warm-up outside the capture
+            torch.cuda.current_stream().wait_stream(s)
+            torch.cuda.synchronize()
+            reset()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                call()
+            reset()
+            g.replay()
+        else:
+            call()
+        torch.cuda.synchronize()
+        assert int(status.item()) == 0
+        return out, kc, vc, lens
+
+    ref = run(False)
+    for graph in (False, True):
+        got = run(True, graph)
+        assert torch.equal(got[0], ref[0]) and torch.equal(got[3], ref[3]), graph
+        assert torch.equal(got[1].view(torch.int16), ref[1].view(torch.int16))
+        assert torch.equal(got[2].view(torch.int16), ref[2].view(torch.int16))
