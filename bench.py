@@ -1082,9 +1082,10 @@ class ShortChunks:
         # algorithmic bytes: cached K/V read once per (sequence, KV head), the new rows' q, k, v and out
         self.bytes = sum(p * kv_row * 2 for p in self.pasts) + self.T * (2 * self.HQ * self.D * 2 + 2 * kv_row)
         self.tokens = self.T
-        # verify: append, split-KV kernel, combine, commit; varlen: the same plus the tensor-core kernel;
-        # deep: one tensor-core launch (append and length advance fused in)
-        self.launches = {"verify": 4, "varlen": 5, "deep": 1}[mode]
+        # verify: append, split-KV kernel (which also advances the lengths), combine; varlen: append,
+        # split-KV kernel, combine, tensor-core kernel, commit; deep: one tensor-core launch (append and
+        # length advance fused in)
+        self.launches = {"verify": 3, "varlen": 5, "deep": 1}[mode]
 
     def step(self):
         cp = self.cp

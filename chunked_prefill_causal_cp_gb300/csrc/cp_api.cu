@@ -226,6 +226,7 @@ int run_attention(const cp_layer_desc* d, const AttnArgs& base, int64_t rows_tot
     if (workspace == nullptr || (int64_t)ws_bytes < need) return CP_ERR_WORKSPACE;
     AttnArgs dec = a;
     dec.dec_rows = kdec;
+    if (run_tc) dec.commit_lens = nullptr;  // the tensor-core kernel advances the lengths
     dec.part_o = static_cast<float*>(workspace);
     dec.max_splits = (int)max_splits_for(a.max_ctx);
     dec.part_ml =
@@ -660,7 +661,10 @@ int cp_prefill_chunk(const cp_layer_desc* desc, const void* q, void* k_new, void
   const int G = desc->num_q_heads / desc->num_kv_heads;
   const bool tc_only = (desc->dtype == CP_F32 ||
                         (rows_padded > 1 && !decode_rows && attn_tc_supported(desc->head_dim, G, desc->dtype)));
-  if (tc_only) {
+  // Every row on one path (the tensor-core kernel, the fp32 one, or the
+  // split-KV kernels of a short chunk): that path's kernel advances the lengths.
+  const bool one_path = tc_only || decode_rows;
+  if (one_path) {
     a.commit_lens = seqlens_k;
     a.commit_add = real_rows;
   }
@@ -669,7 +673,7 @@ int cp_prefill_chunk(const cp_layer_desc* desc, const void* q, void* k_new, void
                     (size_t)(workspace_bytes - kControlBytes - snap), st,
                     desc->kind == CP_CACHE_PAGED ? k_new : nullptr, desc->kind == CP_CACHE_PAGED ? v_new : nullptr);
   if (r != CP_OK) return r;
-  if (!tc_only) return launch_result(launch_commit(seqlens_k, a.rows, real_rows, nullptr, st));
+  if (!one_path) return launch_result(launch_commit(seqlens_k, a.rows, real_rows, nullptr, st));
   return CP_OK;
 }
 

@@ -63,9 +63,12 @@ struct AttnArgs {
   int* status;             // optional CP_DEV_* bits
   int kv_direct;           // tensor-core kernel: this call's new K/V rows may be read from
                            // k_new / v_new ([rows_total, hkv, d]) instead of the paged pool
-  int* commit_lens = nullptr;  // tensor-core and fp32 kernels: if set, lengths advanced by commit_add after the
-  int commit_add = 0;          // attention reads them: by CTA (0, 0) right after the dependency wait
-                               // when `past` is a copy (it must not alias commit_lens), else through
+  // If set, the lengths are advanced by commit_add once the attention has read
+  // them: by CTA (0, 0) right after the dependency wait when `past` is a copy
+  // (it must not alias commit_lens; tensor-core, fp32 and split-KV kernels),
+  // else through the ticket (tensor-core and fp32 kernels).
+  int* commit_lens = nullptr;
+  int commit_add = 0;
   unsigned* ticket = nullptr;  // the ticket counter (zero before the launch, left zero)
   // Tensor-core kernel, contiguous cache, fused append: the tiles that hold this
   // call's keys are read from k_new / v_new [num_seqs, rows_uniform, hkv, d] and

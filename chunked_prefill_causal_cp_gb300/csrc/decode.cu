@@ -112,6 +112,9 @@ __global__ void __launch_bounds__(kDecWarps * 32, 4) decode_split_kernel(const A
   pdl_launch_dependents();
   const int split = blockIdx.x % a.max_splits, s = blockIdx.x / a.max_splits, gk = blockIdx.y;
   pdl_wait();  // everything below reads what earlier kernels wrote
+  // One-call chunk: `past` is a copy of the lengths, so one CTA may advance them at once.
+  if (a.commit_lens && !a.ticket && blockIdx.x == 0 && blockIdx.y == 0)
+    for (int i = threadIdx.x; i < a.rows.num_seqs; i += blockDim.x) a.commit_lens[i] += a.commit_add;
   if (seq_rows(a.rows, s) != 1) return;
   const int past = a.past[s];
   const int n = past + 1;
@@ -326,6 +329,9 @@ __global__ void __launch_bounds__(kDecWarps * 32, NF == 1 ? 4 : 3) decode_rows_k
   pdl_launch_dependents();
   const int split = blockIdx.x % a.max_splits, s = blockIdx.x / a.max_splits, gk = blockIdx.y;
   pdl_wait();  // everything below reads what earlier kernels wrote
+  // One-call chunk: `past` is a copy of the lengths, so one CTA may advance them at once.
+  if (a.commit_lens && !a.ticket && blockIdx.x == 0 && blockIdx.y == 0)
+    for (int i = threadIdx.x; i < a.rows.num_seqs; i += blockDim.x) a.commit_lens[i] += a.commit_add;
   const int kr = a.dec_rows;  // rows per sequence on this path
   if (seq_rows(a.rows, s) != kr) return;
   const int past = a.past[s];
